@@ -1,0 +1,501 @@
+// Host side of the GB300 angular-correlation library: the C ABI declared in include/acf.h.
+//
+// One acf_histogram call = catalog conversion (one or two launches) -> pair kernel (persistent
+// blocks, one resident set per SM) -> merge kernel, all on the context's stream with no host
+// synchronisation. See acf_kernels.cuh for the device side.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/acf.h"
+#include "acf_kernels.cuh"
+
+using namespace acf;
+
+namespace {
+
+// theta'^2 = q * f(q) for a chord q on [0, 2]; f fitted by fit_arcsin2.py (degree 7,
+// absolute theta' error <= 2.5e-8 rad after rounding the scaled coefficients to fp32)
+const double kArcsin2Coef[8] = {0.99999959294652097,   0.083342611628085594,  0.011049794431887118,
+                                0.0019657095570993176, 4.2347086002697957e-05, 0.00029099553526503564,
+                                -9.1427792701640403e-05, 2.3068911858269848e-05};
+
+constexpr int kK = 8;                          // i-galaxies per thread
+constexpr int kMaxEntries = 49152;             // histogram entries a block can hold (192 KB)
+constexpr size_t kTileBytes = 2 * kJT * sizeof(float4);
+constexpr int kMaxTimed = 4096;
+
+struct Plan {
+  BinParams bp;
+  int map = kMirror;
+  int method = kChordPoly;
+  int layout = kLane;
+  int threads = 256;
+  size_t smem = 0;
+};
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace
+
+struct acf_ctx {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int num_sms = 0;
+  std::string err;
+  Workspace ws;     // vectors + per-block partial rows
+  Workspace io;     // device staging for acf_correlate_host
+  // options
+  int opt_threads = 0, opt_ctas = 0, opt_method = kChordPoly, opt_layout = 0, opt_timing = 0;
+  // info about the last histogram
+  long long info_grid = 0, info_threads = 0, info_ctas = 0, info_chunks = 0, info_layout = 0, info_map = 0,
+            info_entries = 0, info_smem = 0, info_pairs = 0, info_flush = 0;
+  // kernel timing
+  std::vector<cudaEvent_t> ev;  // pairs (start, stop)
+  int ev_used = 0;
+};
+
+namespace {
+
+int fail(acf_ctx* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf;
+  return code;
+}
+
+int cuda_fail(acf_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, ACF_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+#define ACF_CUDA(c, call)                                  \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail((c), e_, #call); \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int ensure(acf_ctx* c, Workspace& w, size_t bytes) {
+  if (bytes <= w.bytes) return ACF_OK;
+  size_t want = std::max(bytes, w.bytes + w.bytes / 2);
+  if (w.ptr) {
+    ACF_CUDA(c, cudaStreamSynchronize(c->stream));
+    ACF_CUDA(c, cudaFree(w.ptr));
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  cudaError_t e = cudaMalloc(&w.ptr, want);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    w.ptr = nullptr;
+    return fail(c, ACF_ERR_NOMEM, "cudaMalloc of %zu bytes failed: %s", want, cudaGetErrorString(e));
+  }
+  w.bytes = want;
+  return ACF_OK;
+}
+
+// Work out the bin map, the shared-memory layout and the polynomial for one binning.
+int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
+  if (!(w_deg > 0.0) || !std::isfinite(w_deg)) return fail(c, ACF_ERR_ARG, "bin_width_deg must be finite and > 0");
+  if (nbins <= 0) return fail(c, ACF_ERR_ARG, "nbins must be > 0");
+  const double pi = 3.14159265358979323846;
+  const double w_rad = w_deg * pi / 180.0;
+  const double P = 180.0 / w_deg;  // bins in half a turn
+  BinParams& bp = pl.bp;
+  std::memset(&bp, 0, sizeof bp);
+  for (int k = 0; k < 8; ++k) bp.c[k] = (float)(kArcsin2Coef[k] / (w_rad * w_rad));
+  bp.nbins = nbins;
+  bp.inv_w = (float)(1.0 / w_rad);
+  bp.half_p = (float)(P / 2.0);
+  pl.method = c->opt_method;
+  const double pr = std::rint(P);
+  const bool integral = std::fabs(P - pr) <= 1e-9 * std::max(1.0, P) && pr >= 4.0;
+  long long mirror_entries = integral ? 2 * (long long)std::ceil(pr / 2.0) + 4 : -1;
+  if (pl.method == kChordPoly && integral && mirror_entries <= kMaxEntries) {
+    pl.map = kMirror;
+    bp.off = (int)std::ceil(pr / 2.0) + 2;
+    bp.p_int = (int)pr;
+    bp.entries = (int)mirror_entries;
+    bp.magic = (float)(8388608.0 + bp.off);
+    bp.clamp_c = (float)(bp.entries - 1);
+  } else {
+    pl.map = kClamp;
+    const double fp = std::floor(P * (1.0 + 1e-6)) + 1.0;  // indices the clamp-free range can reach
+    const long long entries = (long long)std::min<double>((double)nbins, fp);
+    if (entries > kMaxEntries)
+      return fail(c, ACF_ERR_UNSUPPORTED, "histogram of %lld entries exceeds the %d-entry shared-memory plan",
+                  entries, kMaxEntries);
+    bp.entries = (int)entries;
+    bp.magic = 8388608.0f;
+    bp.clamp_c = (float)(entries - 1);
+  }
+  // layout: 32 lane-private copies when they fit comfortably, else one block-shared copy
+  const size_t lane_bytes = kTileBytes + (size_t)bp.entries * 32 * 4;
+  int layout = c->opt_layout;
+  if (layout == 0) layout = (lane_bytes <= 200 * 1024) ? kLane : kBlock;
+  if (layout == kLane && lane_bytes > 227 * 1024)
+    return fail(c, ACF_ERR_UNSUPPORTED, "lane-private layout needs %zu bytes of shared memory", lane_bytes);
+  pl.layout = layout;
+  pl.smem = (layout == kLane) ? lane_bytes : kTileBytes + (size_t)((bp.entries * 4 + 15) & ~15);
+  // threads: 256 when two blocks fit on an SM, else 512 so one block still fills 16 warps
+  pl.threads = c->opt_threads ? c->opt_threads : (pl.smem * 2 + 2048 <= 233472 ? 256 : 512);
+  if (pl.threads != 256 && pl.threads != 512) return fail(c, ACF_ERR_ARG, "threads must be 256 or 512");
+  return ACF_OK;
+}
+
+typedef void (*PairKernelFn)(const PairParams);
+
+PairKernelFn pick_kernel(const Plan& pl) {
+#define ACF_PICK(T, L, M, X) \
+  if (pl.threads == T && pl.layout == L && pl.map == M && pl.method == X) return pair_kernel<kK, T, L, M, X>;
+  ACF_PICK(256, kLane, kMirror, kChordPoly)
+  ACF_PICK(256, kLane, kClamp, kChordPoly)
+  ACF_PICK(256, kBlock, kMirror, kChordPoly)
+  ACF_PICK(256, kBlock, kClamp, kChordPoly)
+  ACF_PICK(512, kLane, kMirror, kChordPoly)
+  ACF_PICK(512, kLane, kClamp, kChordPoly)
+  ACF_PICK(512, kBlock, kMirror, kChordPoly)
+  ACF_PICK(512, kBlock, kClamp, kChordPoly)
+  ACF_PICK(256, kLane, kClamp, kDotAcos)
+  ACF_PICK(256, kBlock, kClamp, kDotAcos)
+  ACF_PICK(512, kLane, kClamp, kDotAcos)
+  ACF_PICK(512, kBlock, kClamp, kDotAcos)
+#undef ACF_PICK
+  return nullptr;
+}
+
+int launch_convert(acf_ctx* c, const float* ra, const float* dec, long long n, float4* v) {
+  if (n <= 0) return ACF_OK;
+  const int threads = 256;
+  const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 16);
+  convert_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, v);
+  ACF_CUDA(c, cudaGetLastError());
+  return ACF_OK;
+}
+
+struct Launch {
+  PairKernelFn fn = nullptr;
+  int ctas = 0;
+  long long grid = 0, chunks = 0, rows = 0, cj = 0, step = 0;
+};
+
+// Persistent grid: every SM gets as many blocks as can be resident, never more blocks than chunks.
+int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym, Launch& L) {
+  L.fn = pick_kernel(pl);
+  if (!L.fn) return fail(c, ACF_ERR_UNSUPPORTED, "no kernel for this plan");
+  ACF_CUDA(c, cudaFuncSetAttribute(L.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
+  int occ = 0;
+  ACF_CUDA(c, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, L.fn, pl.threads, pl.smem));
+  if (occ <= 0) return fail(c, ACF_ERR_UNSUPPORTED, "pair kernel cannot be resident (smem %zu)", pl.smem);
+  L.ctas = c->opt_ctas > 0 ? std::min(c->opt_ctas, occ) : occ;
+  const long long bi = (long long)pl.threads * kK;
+  L.rows = (ni + bi - 1) / bi;
+  L.cj = (nj + kJT - 1) / kJT;
+  L.step = bi / kJT;
+  L.chunks = sym ? L.rows * L.cj - L.step * L.rows * (L.rows - 1) / 2 : L.rows * L.cj;
+  L.grid = std::min<long long>((long long)c->num_sms * L.ctas, std::max<long long>(L.chunks, 1));
+  return ACF_OK;
+}
+
+// The pair kernel and merge for vectors already on the device. partial holds L.grid rows.
+int histogram_vectors(acf_ctx* c, const float4* vi, long long ni, const float4* vj, long long nj, bool sym,
+                      const Plan& pl, const Launch& L, unsigned long long* partial, uint64_t* out) {
+  PairParams p;
+  p.vi = vi;
+  p.vj = vj;
+  p.ni = ni;
+  p.nj = nj;
+  p.total_chunks = L.chunks;
+  p.chunks_per_row = L.cj;
+  p.rows = L.rows;
+  p.sym = sym ? 1 : 0;
+  p.row_step = (int)L.step;
+  p.inc = sym ? 2u : 1u;
+  // the largest number of increments one shared 32-bit word can take per chunk
+  const double per_chunk = (pl.layout == kLane ? (double)(pl.threads / 32) : (double)pl.threads) * kK * kJT * p.inc;
+  p.flush_every = (unsigned)std::max(1.0, std::floor(4294967295.0 / per_chunk));
+  p.partial = partial;
+  p.bp = pl.bp;
+  const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
+  if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
+  L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
+  ACF_CUDA(c, cudaGetLastError());
+  if (timed) {
+    ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
+    c->ev_used += 2;
+  }
+#ifdef ACF_DEBUG_BOUNDS
+  {
+    DebugRecord r;
+    ACF_CUDA(c, cudaStreamSynchronize(c->stream));
+    ACF_CUDA(c, cudaMemcpyFromSymbol(&r, g_debug, sizeof r));
+    if (r.count) {
+      DebugRecord z{};
+      ACF_CUDA(c, cudaMemcpyToSymbol(g_debug, &z, sizeof z));
+      return fail(c, ACF_ERR_CUDA,
+                  "bounds check: %u violations; first kind %d a=%lld b=%lld f=[%.9g %.9g %.9g %.9g %.9g %.9g %.9g %.9g]",
+                  r.count, r.kind, r.a, r.b, r.f[0], r.f[1], r.f[2], r.f[3], r.f[4], r.f[5], r.f[6], r.f[7]);
+    }
+  }
+#endif
+  const unsigned long long self = sym ? (unsigned long long)ni : 0ull;
+  const int mthreads = 256;
+  const int mblocks = (int)std::min<long long>((pl.bp.nbins + mthreads - 1) / mthreads, 4096);
+  merge_kernel<<<mblocks, mthreads, 0, c->stream>>>(partial, (int)L.grid, pl.bp.nbins, self,
+                                                     reinterpret_cast<unsigned long long*>(out));
+  ACF_CUDA(c, cudaGetLastError());
+  c->info_grid = L.grid;
+  c->info_threads = pl.threads;
+  c->info_ctas = L.ctas;
+  c->info_chunks = L.chunks;
+  c->info_layout = pl.layout;
+  c->info_map = pl.map;
+  c->info_entries = pl.bp.entries;
+  c->info_smem = (long long)pl.smem;
+  c->info_pairs = sym ? ni * (ni - 1) / 2 : ni * nj;
+  c->info_flush = p.flush_every;
+  return ACF_OK;
+}
+
+int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2, const float* dec2,
+                   int64_t n2, double w_deg, int32_t nbins, uint64_t* out) {
+  if (!c) return ACF_ERR_ARG;
+  if (n < 0) return fail(c, ACF_ERR_ARG, "n must be >= 0");
+  if (!out) return fail(c, ACF_ERR_ARG, "out is NULL");
+  const bool sym = (ra2 == nullptr && dec2 == nullptr) || (ra2 == ra && dec2 == dec && n2 == n);
+  if (!sym && n2 < 0) return fail(c, ACF_ERR_ARG, "n2 must be >= 0");
+  if (!sym && ((ra2 == nullptr) != (dec2 == nullptr))) return fail(c, ACF_ERR_ARG, "ra2 and dec2 must both be set");
+  const int64_t nj = sym ? n : n2;
+  Plan pl;
+  int rc = make_plan(c, w_deg, nbins, pl);
+  if (rc) return rc;
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  if (n == 0 || nj == 0) {
+    ACF_CUDA(c, cudaMemsetAsync(out, 0, sizeof(uint64_t) * (size_t)nbins, c->stream));
+    return ACF_OK;
+  }
+  if (!ra || !dec || (!sym && (!ra2 || !dec2))) return fail(c, ACF_ERR_ARG, "catalog pointer is NULL");
+  Launch L;
+  rc = plan_launch(c, pl, n, nj, sym, L);
+  if (rc) return rc;
+  const size_t b_vi = align256((size_t)n * sizeof(float4));
+  const size_t b_vj = sym ? 0 : align256((size_t)nj * sizeof(float4));
+  const size_t b_part = align256((size_t)L.grid * (size_t)nbins * sizeof(unsigned long long));
+  rc = ensure(c, c->ws, b_vi + b_vj + b_part);
+  if (rc) return rc;
+  char* base = static_cast<char*>(c->ws.ptr);
+  float4* vi = reinterpret_cast<float4*>(base);
+  float4* vj = sym ? vi : reinterpret_cast<float4*>(base + b_vi);
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(base + b_vi + b_vj);
+  rc = launch_convert(c, ra, dec, n, vi);
+  if (rc) return rc;
+  if (!sym) {
+    rc = launch_convert(c, ra2, dec2, nj, vj);
+    if (rc) return rc;
+  }
+  return histogram_vectors(c, vi, n, vj, nj, sym, pl, L, part, out);
+}
+
+}  // namespace
+
+extern "C" {
+
+#ifdef ACF_DEBUG_BOUNDS
+const char* acf_version(void) { return "acf 0.1 sm_103a bounds-checked"; }
+#else
+const char* acf_version(void) { return "acf 0.1 sm_103a"; }
+#endif
+
+int acf_create(acf_ctx** out, int device, void* cuda_stream) {
+  if (!out) return ACF_ERR_ARG;
+  *out = nullptr;
+  acf_ctx* c = new (std::nothrow) acf_ctx();
+  if (!c) return ACF_ERR_NOMEM;
+  c->device = device;
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = cudaSetDevice(device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) {
+    delete c;
+    return ACF_ERR_CUDA;
+  }
+  *out = c;
+  return ACF_OK;
+}
+
+void acf_destroy(acf_ctx* c) {
+  if (!c) return;
+  cudaSetDevice(c->device);
+  cudaStreamSynchronize(c->stream);
+  if (c->ws.ptr) cudaFree(c->ws.ptr);
+  if (c->io.ptr) cudaFree(c->io.ptr);
+  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+  delete c;
+}
+
+const char* acf_last_error(const acf_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+int acf_set_stream(acf_ctx* c, void* s) {
+  if (!c) return ACF_ERR_ARG;
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  ACF_CUDA(c, cudaStreamSynchronize(c->stream));
+  c->stream = static_cast<cudaStream_t>(s);
+  return ACF_OK;
+}
+
+int acf_histogram(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2, const float* dec2,
+                  int64_t n2, double w_deg, int32_t nbins, uint64_t* out) {
+  return histogram_impl(c, ra, dec, n, ra2, dec2, n2, w_deg, nbins, out);
+}
+
+int acf_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t* rr, int32_t nbins, int64_t n_d,
+              int64_t n_r, double* omega) {
+  if (!c) return ACF_ERR_ARG;
+  if (!dd || !dr || !rr || !omega) return fail(c, ACF_ERR_ARG, "omega: NULL pointer");
+  if (nbins <= 0 || n_d <= 0 || n_r <= 0) return fail(c, ACF_ERR_ARG, "omega: nbins, n_d, n_r must be > 0");
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  const double nd = (double)n_d, nr = (double)n_r;
+  const double f_dd = (nr * nr) / (nd * nd), f_dr = (nr * nr) / (nd * nr);
+  const int threads = 256;
+  const int blocks = std::min((nbins + threads - 1) / threads, 4096);
+  omega_kernel<<<blocks, threads, 0, c->stream>>>(reinterpret_cast<const unsigned long long*>(dd),
+                                                   reinterpret_cast<const unsigned long long*>(dr),
+                                                   reinterpret_cast<const unsigned long long*>(rr), nbins, f_dd, f_dr,
+                                                   omega);
+  ACF_CUDA(c, cudaGetLastError());
+  return ACF_OK;
+}
+
+int acf_correlate_host(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_d, const float* ra_r,
+                       const float* dec_r, int64_t n_r, double w_deg, int32_t nbins, uint64_t* dd, uint64_t* dr,
+                       uint64_t* rr, double* omega) {
+  if (!c) return ACF_ERR_ARG;
+  if (!ra_d || !dec_d || !ra_r || !dec_r || !dd || !dr || !rr || !omega)
+    return fail(c, ACF_ERR_ARG, "correlate: NULL pointer");
+  if (n_d <= 0 || n_r <= 0) return fail(c, ACF_ERR_ARG, "correlate: n_d and n_r must be > 0");
+  if (nbins <= 0) return fail(c, ACF_ERR_ARG, "nbins must be > 0");
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  const size_t bd = align256((size_t)n_d * 4), br = align256((size_t)n_r * 4), bh = align256((size_t)nbins * 8);
+  int rc = ensure(c, c->io, 2 * bd + 2 * br + 4 * bh);
+  if (rc) return rc;
+  char* p = static_cast<char*>(c->io.ptr);
+  float* d_ra_d = reinterpret_cast<float*>(p);
+  float* d_dec_d = reinterpret_cast<float*>(p + bd);
+  float* d_ra_r = reinterpret_cast<float*>(p + 2 * bd);
+  float* d_dec_r = reinterpret_cast<float*>(p + 2 * bd + br);
+  char* h = p + 2 * bd + 2 * br;
+  uint64_t* d_dd = reinterpret_cast<uint64_t*>(h);
+  uint64_t* d_dr = reinterpret_cast<uint64_t*>(h + bh);
+  uint64_t* d_rr = reinterpret_cast<uint64_t*>(h + 2 * bh);
+  double* d_om = reinterpret_cast<double*>(h + 3 * bh);
+  ACF_CUDA(c, cudaMemcpyAsync(d_ra_d, ra_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
+  ACF_CUDA(c, cudaMemcpyAsync(d_dec_d, dec_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
+  ACF_CUDA(c, cudaMemcpyAsync(d_ra_r, ra_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
+  ACF_CUDA(c, cudaMemcpyAsync(d_dec_r, dec_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
+  if ((rc = histogram_impl(c, d_ra_d, d_dec_d, n_d, nullptr, nullptr, 0, w_deg, nbins, d_dd))) return rc;
+  if ((rc = histogram_impl(c, d_ra_d, d_dec_d, n_d, d_ra_r, d_dec_r, n_r, w_deg, nbins, d_dr))) return rc;
+  if ((rc = histogram_impl(c, d_ra_r, d_dec_r, n_r, nullptr, nullptr, 0, w_deg, nbins, d_rr))) return rc;
+  if ((rc = acf_omega(c, d_dd, d_dr, d_rr, nbins, n_d, n_r, d_om))) return rc;
+  ACF_CUDA(c, cudaMemcpyAsync(dd, d_dd, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+  ACF_CUDA(c, cudaMemcpyAsync(dr, d_dr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+  ACF_CUDA(c, cudaMemcpyAsync(rr, d_rr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+  ACF_CUDA(c, cudaMemcpyAsync(omega, d_om, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+  ACF_CUDA(c, cudaStreamSynchronize(c->stream));
+  return ACF_OK;
+}
+
+int acf_pair_bins(acf_ctx* c, const float* ra1, const float* dec1, const float* ra2, const float* dec2, int64_t n,
+                  double w_deg, int32_t nbins, int32_t* bins) {
+  if (!c) return ACF_ERR_ARG;
+  if (n < 0) return fail(c, ACF_ERR_ARG, "n must be >= 0");
+  Plan pl;
+  int rc = make_plan(c, w_deg, nbins, pl);
+  if (rc) return rc;
+  if (n == 0) return ACF_OK;
+  if (!ra1 || !dec1 || !ra2 || !dec2 || !bins) return fail(c, ACF_ERR_ARG, "pair_bins: NULL pointer");
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  const int threads = 256;
+  const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 32);
+  if (pl.method == kDotAcos)
+    pair_bins_kernel<kClamp, kDotAcos><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
+  else if (pl.map == kMirror)
+    pair_bins_kernel<kMirror, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
+  else
+    pair_bins_kernel<kClamp, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
+  ACF_CUDA(c, cudaGetLastError());
+  return ACF_OK;
+}
+
+int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
+  if (!c || !key) return ACF_ERR_ARG;
+  if (!strcmp(key, "threads")) {
+    if (v != 0 && v != 256 && v != 512) return fail(c, ACF_ERR_ARG, "threads must be 0, 256 or 512");
+    c->opt_threads = (int)v;
+  } else if (!strcmp(key, "ctas_per_sm")) {
+    if (v < 0 || v > 8) return fail(c, ACF_ERR_ARG, "ctas_per_sm must be 0..8");
+    c->opt_ctas = (int)v;
+  } else if (!strcmp(key, "bin_method")) {
+    if (v != kChordPoly && v != kDotAcos) return fail(c, ACF_ERR_ARG, "bin_method must be 0 or 1");
+    c->opt_method = (int)v;
+  } else if (!strcmp(key, "layout")) {
+    if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "layout must be 0, 1 or 2");
+    c->opt_layout = (int)v;
+  } else if (!strcmp(key, "kernel_timing")) {
+    c->opt_timing = v ? 1 : 0;
+    if (c->opt_timing && c->ev.empty()) {
+      ACF_CUDA(c, cudaSetDevice(c->device));
+      c->ev.resize(2 * kMaxTimed);
+      for (auto& e : c->ev) ACF_CUDA(c, cudaEventCreate(&e));
+    }
+    c->ev_used = 0;
+  } else {
+    return fail(c, ACF_ERR_ARG, "unknown option '%s'", key);
+  }
+  return ACF_OK;
+}
+
+int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
+  if (!c || !key || !v) return ACF_ERR_ARG;
+  struct {
+    const char* k;
+    long long val;
+  } t[] = {{"grid", c->info_grid},       {"threads", c->info_threads},   {"ctas_per_sm", c->info_ctas},
+           {"chunks", c->info_chunks},   {"layout", c->info_layout},     {"bin_map", c->info_map},
+           {"hist_entries", c->info_entries}, {"smem_bytes", c->info_smem}, {"pairs_evaluated", c->info_pairs},
+           {"flush_every", c->info_flush}};
+  for (auto& e : t)
+    if (!strcmp(e.k, key)) {
+      *v = e.val;
+      return ACF_OK;
+    }
+  return ACF_ERR_ARG;
+}
+
+int acf_kernel_times(acf_ctx* c, float* ms, int32_t cap, int32_t* count) {
+  if (!c || !count || (cap > 0 && !ms)) return ACF_ERR_ARG;
+  *count = 0;
+  if (!c->opt_timing) return fail(c, ACF_ERR_ARG, "kernel_timing is off");
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  ACF_CUDA(c, cudaStreamSynchronize(c->stream));
+  const int pairs = c->ev_used / 2;
+  int k = 0;
+  for (; k < pairs && k < cap; ++k) ACF_CUDA(c, cudaEventElapsedTime(&ms[k], c->ev[2 * k], c->ev[2 * k + 1]));
+  *count = k;
+  c->ev_used = 0;
+  return ACF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+"""Derive the polynomial the pair kernel uses to turn a squared chord into a squared angle.
+
+For two unit vectors at angle theta' <= 90 degrees, the squared chord is q = |u - v|^2 =
+4 sin^2(theta'/2), so theta'^2 = 4 asin^2(sqrt(q)/2) = q * f(q) with f analytic on [0, 2]
+(f(0) = 1). We fit P(q) ~ f(q) with degree-7 coefficients, minimising the largest ABSOLUTE error
+in theta' (relative error of f times theta'/2), by Lawson's iteratively reweighted least squares
+on a Chebyshev grid, with f evaluated in 40-digit arithmetic. Prints the coefficients (highest
+degree last) and the worst theta' error before and after rounding them to fp32.
+
+Run: python fit_arcsin2.py
+"""
+import mpmath as mp
+import numpy as np
+
+mp.mp.dps = 40
+DEG = 7
+N = 6000
+
+
+def f_exact(q):
+    q = mp.mpf(q)
+    if q == 0:
+        return mp.mpf(1)
+    th = 2 * mp.asin(mp.sqrt(q) / 2)
+    return th * th / q
+
+
+def main():
+    xs = [mp.mpf(1) - mp.cos(mp.pi * (k + mp.mpf("0.5")) / N) for k in range(N)]
+    fx = np.array([float(f_exact(x)) for x in xs])
+    th = np.array([float(2 * mp.asin(mp.sqrt(x) / 2)) for x in xs])
+    xf = np.array([float(x) for x in xs])
+    V = np.vander(xf, DEG + 1, increasing=True)
+    w = np.ones(N) / N
+    for _ in range(2000):
+        W = np.sqrt(w) * th / fx
+        c, *_ = np.linalg.lstsq(V * W[:, None], fx * W, rcond=None)
+        err = np.abs(V @ c - fx) / fx * th / 2
+        w = w * (err / err.max()) ** 0.5
+        w /= w.sum()
+    print("degree", DEG, "max |d theta'| (rad) %.3e" % err.max())
+    c32 = c.astype(np.float32).astype(np.float64)
+    err32 = np.abs(V @ c32 - fx) / fx * th / 2
+    print("after fp32 rounding of the coefficients: %.3e" % err32.max())
+    for k, v in enumerate(c):
+        print("  c%d = %.17g" % (k, v))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * acf.h — C ABI of the GB300 angular-correlation library (libacf.so).
+ *
+ * What it computes ("CUDA Deep Dive: 10B Galaxy Pairs on an RTX 5080", section "The problem"):
+ * for galaxies given by right ascension alpha and declination delta in ARCMINUTES, the angular
+ * separation of a pair is
+ *     theta = arccos( sin d1 sin d2 + cos d1 cos d2 cos(a1 - a2) ),
+ * every ordered pair of two catalogs is binned by theta into bins of equal width, giving the
+ * histograms DD (real-real), DR (real-random) and RR (random-random), and the Landy-Szalay
+ * estimator is omega = (DD - 2 DR + RR) / RR.
+ *
+ * Binning (Appendix A of the same page, the bin-index helper): bin k holds theta in
+ * [k w, (k+1) w); separations beyond nbins * w are clamped into the last bin, so every pair is
+ * counted and a histogram always sums to n1 * n2.
+ *
+ * Precision contract: the kernels work in fp32 on unit vectors built in fp64. The computed
+ * separation of every pair is within 1e-6 rad of the fp64 value of the formula above, so a pair
+ * can land in a neighbouring bin only if its fp64 theta lies within 1e-6 rad of that bin edge.
+ *
+ * Conventions for every entry point:
+ *   - Array arguments marked "device" are caller-owned CUDA device pointers on the context's
+ *     device. The library never frees them and never keeps them after the call returns.
+ *   - Work is enqueued on the context's stream and is asynchronous unless stated otherwise;
+ *     synchronise that stream before reading outputs. Calls on one context must be ordered on
+ *     that stream (the context owns one workspace that consecutive calls reuse).
+ *   - Every function returns ACF_OK (0) or a negative ACF_ERR_* code and never exits the
+ *     process. acf_last_error() gives a message for the last failure on that context.
+ *     Launch errors are detected at once; faults inside a kernel surface on a later call or sync.
+ *   - Non-finite RA/Dec inputs are treated as (0, 0) so no kernel can index out of bounds; their
+ *     pairs are therefore binned as if the galaxy sat at RA = Dec = 0.
+ */
+#ifndef ACF_H
+#define ACF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ACF_OK 0
+#define ACF_ERR_ARG (-1)         /* NULL pointer where data is required, n < 0, nbins <= 0, bad width */
+#define ACF_ERR_UNSUPPORTED (-2) /* histogram too large for the shared-memory plan (see acf_histogram) */
+#define ACF_ERR_NOMEM (-3)       /* device or pinned host allocation failed */
+#define ACF_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
+
+typedef struct acf_ctx acf_ctx;
+
+/* Library version string, e.g. "acf 0.1 sm_103a". Static storage. */
+const char *acf_version(void);
+
+/*
+ * Create a context on CUDA device `device` that enqueues work on `cuda_stream` (a cudaStream_t;
+ * NULL means the legacy default stream). The context owns a device workspace that grows on
+ * demand and is freed by acf_destroy. *out receives the handle (NULL on failure).
+ */
+int acf_create(acf_ctx **out, int device, void *cuda_stream);
+
+/* Free the context and its workspace (synchronises its stream first). NULL is a no-op. */
+void acf_destroy(acf_ctx *ctx);
+
+/* Message describing the last failure on this context ("" if none). Valid until the next call. */
+const char *acf_last_error(const acf_ctx *ctx);
+
+/* Switch the context to another stream. Synchronises the old stream first. */
+int acf_set_stream(acf_ctx *ctx, void *cuda_stream);
+
+/*
+ * One histogram of angular separations (the DD, DR or RR of section "The problem").
+ *
+ *   ra, dec      device float[n]  first catalog, arcminutes
+ *   ra2, dec2    device float[n2] second catalog, arcminutes; pass NULL/NULL (n2 ignored), or the
+ *                same pointers and n2 == n, for an auto-correlation (DD or RR)
+ *   bin_width_deg  bin width w in degrees, finite and > 0
+ *   nbins        number of bins, > 0
+ *   out          device uint64[nbins], OVERWRITTEN with the counts
+ *
+ * Cross-correlation counts all n * n2 ordered pairs. Auto-correlation counts all n^2 ordered
+ * pairs: each unordered pair i != j is evaluated once and counted twice, and the n self-pairs
+ * (theta = 0) are added to bin 0, as in the symmetric scheme of the page's section "L1: DD/RR
+ * symmetry". Either way sum(out) == n * n2 exactly.
+ * n == 0 or n2 == 0 gives an all-zero histogram. Returns ACF_ERR_UNSUPPORTED when the
+ * per-block shared-memory histogram does not fit: that needs min(nbins, 180/w + 1) <= 49152
+ * (or, when 180/w is an integer, 180/w + 4 <= 49152).
+ */
+int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, const float *ra2, const float *dec2,
+                  int64_t n2, double bin_width_deg, int32_t nbins, uint64_t *out);
+
+/*
+ * Landy-Szalay estimator per bin (section "The problem"), computed in fp64 on the device:
+ *     omega_k = (DD_k/N_dd - 2 DR_k/N_dr + RR_k/N_rr) / (RR_k/N_rr),
+ * N_dd = n_d^2, N_dr = n_d n_r, N_rr = n_r^2 (with n_d == n_r this is (DD - 2DR + RR)/RR).
+ * Bins with RR_k = 0 get NaN (the page writes only bins with RR > 0).
+ *   dd, dr, rr   device uint64[nbins]
+ *   n_d, n_r     catalog sizes, > 0
+ *   omega        device double[nbins], overwritten
+ */
+int acf_omega(acf_ctx *ctx, const uint64_t *dd, const uint64_t *dr, const uint64_t *rr, int32_t nbins, int64_t n_d,
+              int64_t n_r, double *omega);
+
+/*
+ * The whole job from HOST memory: copies the two catalogs to the device, computes DD, DR, RR and
+ * omega, copies the four results back and synchronises the stream before returning.
+ *   ra_d, dec_d  host float[n_d];  ra_r, dec_r  host float[n_r]  (arcminutes; pinned memory
+ *                gives asynchronous copies, pageable memory works too)
+ *   dd, dr, rr   host uint64[nbins], overwritten;  omega  host double[nbins], overwritten
+ * Same binning rules as acf_histogram; n_d and n_r must be > 0.
+ */
+int acf_correlate_host(acf_ctx *ctx, const float *ra_d, const float *dec_d, int64_t n_d, const float *ra_r,
+                       const float *dec_r, int64_t n_r, double bin_width_deg, int32_t nbins, uint64_t *dd,
+                       uint64_t *dr, uint64_t *rr, double *omega);
+
+/*
+ * Diagnostic: the bin that the histogram kernels assign to each of n individual pairs
+ * (ra1[k], dec1[k]) - (ra2[k], dec2[k]), computed by the same device code path.
+ *   ra1, dec1, ra2, dec2  device float[n];  bins  device int32[n], overwritten
+ */
+int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float *ra2, const float *dec2, int64_t n,
+                  double bin_width_deg, int32_t nbins, int32_t *bins);
+
+/*
+ * Tuning and measurement switches (all optional). Keys:
+ *   "threads"        threads per block of the pair kernel: 256 or 512 (default: chosen)
+ *   "ctas_per_sm"    resident blocks per SM to launch (default: occupancy maximum)
+ *   "bin_method"     0 = chord + arcsin^2 polynomial (default, meets the precision contract);
+ *                    1 = dot product + acosf (the page's exact-acos form; measured alternative,
+ *                        does NOT meet the precision contract at small or near-180 separations)
+ *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram
+ *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
+ */
+int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
+
+/*
+ * Read back facts about the last acf_histogram call. Keys: "grid", "threads", "ctas_per_sm",
+ * "chunks", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
+ * "pairs_evaluated", "flush_every".
+ */
+int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
+
+/*
+ * With "kernel_timing" on: synchronise, write up to `cap` per-launch durations of the pair
+ * kernel (milliseconds, CUDA events on the context stream) recorded since the last call into
+ * ms[], set *count, and clear the record. At most 4096 launches are kept.
+ */
+int acf_kernel_times(acf_ctx *ctx, float *ms, int32_t cap, int32_t *count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ACF_H */

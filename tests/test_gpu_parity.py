@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA library through its C ABI against the fp64 oracle.
+
+The rule (from the fp64 definition of "CUDA Deep Dive: 10B Galaxy Pairs on an RTX 5080", section
+"The problem"): every histogram sums to exactly n1*n2; every bin equals the oracle's except that
+pairs whose fp64 theta is within 1e-6 rad of a bin edge may sit in the bin on the other side of
+that edge (checked through cumulative counts by oracle.check.edge_flux); omega computed on the GPU
+from the GPU counts equals the oracle's omega of the same counts to 1e-12 relative.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import check
+
+pytestmark = pytest.mark.gpu
+
+TOL = oracle.EDGE_TOL_RAD
+
+
+@pytest.fixture(scope="module")
+def ctx(acf):
+    c = acf.Context(0)
+    yield c
+    c.close()
+
+
+def _compare(acf, ctx, ra1, dec1, ra2, dec2, w, nb, threads=0):
+    g = ctx.histogram(ra1, dec1, ra2, dec2, bin_width_deg=w, nbins=nb)
+    torch.cuda.synchronize()
+    gh = acf.as_uint64(g)
+    o = oracle.histogram(ra1, dec1, ra2, dec2, w, nb, threads=threads)
+    rep = check.edge_flux(gh, o.hist, o.near_below, o.near_above)
+    n1 = len(ra1)
+    n2 = n1 if ra2 is None else len(ra2)
+    assert int(gh.sum()) == n1 * n2
+    assert rep.ok, str(rep)
+    return gh, o, rep
+
+
+def test_tiny_workload_full_parity_and_omega(acf, ctx):
+    c = synth.config(0)
+    w, nb = c.bin_width_deg, c.nbins
+    dd, _, r1 = _compare(acf, ctx, c.ra_d, c.dec_d, None, None, w, nb)
+    dr, _, r2 = _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
+    rr, _, r3 = _compare(acf, ctx, c.ra_r, c.dec_r, None, None, w, nb)
+    tdd, tdr, trr = (torch.from_numpy(x.view(np.int64)).cuda() for x in (dd, dr, rr))
+    om = ctx.omega(tdd, tdr, trr, c.n_d, c.n_r).cpu().numpy()
+    assert check.omega_close(om, oracle.omega(dd, dr, rr, c.n_d, c.n_r), rel=1e-12)
+
+
+# sizes spanning several i-rows (2048 per row) and j-chunks (128) with ragged tails
+@pytest.mark.parametrize("n1,n2", [(1, 1), (1, 5), (7, 1), (129, 127), (2047, 2049), (4097, 300), (5000, 4099)])
+def test_ragged_cross_and_auto(acf, ctx, n1, n2):
+    c = synth.catalogs(n1, n2, 3 if n1 >= 6 else 0, 30.0, seed=1000 + n1 + n2)
+    _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+    _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+    _compare(acf, ctx, c.ra_r, c.dec_r, None, None, 0.25, 720)
+
+
+@pytest.mark.parametrize("w,nb,layout", [
+    (0.25, 720, 0),     # mirror map, lane-private copies
+    (0.25, 720, 2),     # mirror map, forced block-shared histogram
+    (0.25, 1440, 0),    # the page's 1440 bins: bins beyond 180 degrees stay empty
+    (0.25, 100, 0),     # bins stop at 25 degrees: the rest is clamped into bin 99
+    (0.35, 515, 0),     # 180/w not an integer: clamp map
+    (0.35, 40, 0),      # clamp map with heavy clamping
+    (1.0, 180, 0),
+    (10.0, 18, 0),
+    (45.0, 4, 0),       # tiny P: still the mirror map
+    (60.0, 3, 0),       # P = 3 < 4: clamp map
+    (0.01, 18000, 0),   # fine binning: block-shared layout
+    (0.03, 2000, 0),    # 6000 half-turn bins, 2000 used: mirror map, block layout
+    (7.0, 1, 0),        # one bin
+])
+def test_binnings(acf, ctx, w, nb, layout):
+    c = synth.catalogs(1500, 1200, 8, 60.0, seed=77)
+    ctx.set_option("layout", layout)
+    try:
+        _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
+        _compare(acf, ctx, c.ra_d, c.dec_d, None, None, w, nb)
+    finally:
+        ctx.set_option("layout", 0)
+
+
+@pytest.mark.parametrize("threads", [256, 512])
+def test_thread_counts(acf, ctx, threads):
+    c = synth.catalogs(3000, 2500, 10, 30.0, seed=5)
+    ctx.set_option("threads", threads)
+    try:
+        _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+        _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+        assert ctx.info("threads") == threads
+    finally:
+        ctx.set_option("threads", 0)
+
+
+def test_small_field_contention(acf, ctx):
+    c = synth.catalogs(3000, 3000, 40, 3.0, seed=3, patch_arcmin=300.0)
+    dd, _, _ = _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+    assert dd[40:].sum() == 0  # a 5x5 degree patch has no pair beyond ~7.1 degrees
+    _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+
+
+def test_special_pairs(acf, ctx):
+    # duplicates, exact antipodes, poles, equator, RA wrap: all land where the oracle puts them
+    ra = np.array([0.0, 0.0, 10800.0, 21599.99, 5.0, 1234.5, 1234.5, 77.25, 300.0, 300.0], np.float32)
+    dec = np.array([0.0, 0.0, 0.0, 0.0, 5400.0, -5400.0, 5400.0, 0.0, 100.0, -100.0], np.float32)
+    _compare(acf, ctx, ra, dec, None, None, 0.25, 720)
+    ra2 = np.where(ra < 10800, ra + 10800, ra - 10800).astype(np.float32)
+    g = acf.as_uint64(ctx.histogram(ra, dec, ra2, -dec, bin_width_deg=0.25, nbins=720))
+    torch.cuda.synchronize()
+    o = oracle.histogram(ra, dec, ra2, -dec, 0.25, 720)
+    assert check.edge_flux(g, o.hist, o.near_below, o.near_above).ok
+    pb = ctx.pair_bins(ra, dec, ra2, -dec, 0.25, 720).cpu().numpy()
+    assert np.all(pb == 719)  # exact antipodes: the last bin
+
+
+def test_empty_inputs_give_zero_histograms(acf, ctx):
+    e = np.zeros(0, np.float32)
+    one = np.ones(3, np.float32)
+    for args in ((e, e, None, None), (e, e, one, one), (one, one, e, e)):
+        g = ctx.histogram(*args, bin_width_deg=0.25, nbins=720)
+        torch.cuda.synchronize()
+        assert int(acf.as_uint64(g).sum()) == 0
+
+
+def test_argument_errors_return_codes(acf, ctx):
+    d = torch.zeros(4, device="cuda")
+    out = torch.empty(720, dtype=torch.int64, device="cuda")
+    h = ctx.handle
+    lib = acf.load()
+    P = lambda t: t.data_ptr()
+    assert lib.acf_histogram(h, P(d), P(d), -1, None, None, 0, 0.25, 720, P(out)) == acf.ACF_ERR_ARG
+    assert lib.acf_histogram(h, P(d), P(d), 4, None, None, 0, 0.0, 720, P(out)) == acf.ACF_ERR_ARG
+    assert lib.acf_histogram(h, P(d), P(d), 4, None, None, 0, float("nan"), 720, P(out)) == acf.ACF_ERR_ARG
+    assert lib.acf_histogram(h, P(d), P(d), 4, None, None, 0, 0.25, 0, P(out)) == acf.ACF_ERR_ARG
+    assert lib.acf_histogram(h, P(d), P(d), 4, None, None, 0, 0.25, 720, None) == acf.ACF_ERR_ARG
+    assert lib.acf_histogram(h, P(d), P(d), 4, P(d), None, 4, 0.25, 720, P(out)) == acf.ACF_ERR_ARG
+    assert lib.acf_histogram(h, P(d), P(d), 4, None, None, 0, 1e-4, 10**6, P(out)) == acf.ACF_ERR_UNSUPPORTED
+    assert "exceeds" in acf.acf_last_error(h)
+    assert lib.acf_omega(h, P(out), P(out), P(out), 0, 1, 1, P(out)) == acf.ACF_ERR_ARG
+    assert lib.acf_set_option(h, b"no_such_option", 1) == acf.ACF_ERR_ARG
+    assert lib.acf_set_option(h, b"threads", 300) == acf.ACF_ERR_ARG
+    # the context still works afterwards
+    c = synth.catalogs(100, 100, 0, 0.0, seed=1)
+    _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+
+
+def test_correlate_host_matches_device_path(acf, ctx):
+    c = synth.catalogs(2500, 2200, 10, 30.0, seed=9)
+    dd, dr, rr, om = ctx.correlate_host(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+    tdd = ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)
+    tdr = ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+    trr = ctx.histogram(c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+    tom = ctx.omega(tdd, tdr, trr, c.n_d, c.n_r)
+    torch.cuda.synchronize()
+    assert np.array_equal(dd, acf.as_uint64(tdd))
+    assert np.array_equal(dr, acf.as_uint64(tdr))
+    assert np.array_equal(rr, acf.as_uint64(trr))
+    assert check.omega_close(om, tom.cpu().numpy(), rel=0.0)
+    assert check.omega_close(om, oracle.omega(dd, dr, rr, c.n_d, c.n_r), rel=1e-12)
+
+
+def _pair_sets(n, seed):
+    """Random pairs over the whole sphere, tight pairs (< 1 deg), near-antipodal pairs and pairs
+    near 90 degrees, where the kernel switches between the difference and the sum chord."""
+    rng = np.random.default_rng(seed)
+    ra1, dec1 = synth.uniform_sphere(n, seed)
+    ra2, dec2 = synth.uniform_sphere(n, seed + 1)
+    sets = [(ra1, dec1, ra2, dec2)]
+    # tight: offsets up to 1 degree
+    sets.append((ra1, dec1, (ra1 + rng.uniform(-60, 60, n)).astype(np.float32) % np.float32(21600),
+                 np.clip(dec1 + rng.uniform(-60, 60, n), -5400, 5400).astype(np.float32)))
+    # near antipodal
+    ra_a = np.where(ra1 < 10800, ra1 + 10800, ra1 - 10800) + rng.uniform(-60, 60, n)
+    sets.append((ra1, dec1, (ra_a % 21600).astype(np.float32),
+                 np.clip(-dec1 + rng.uniform(-60, 60, n), -5400, 5400).astype(np.float32)))
+    # near 90 degrees: the pole against the equator band, plus equator pairs 90 degrees apart
+    sets.append((ra1, np.full(n, 5400.0, np.float32) - rng.uniform(0, 30, n).astype(np.float32), ra2,
+                 rng.uniform(-30, 30, n).astype(np.float32)))
+    sets.append((ra1, np.zeros(n, np.float32), ((ra1 + 5400 + rng.uniform(-30, 30, n)) % 21600).astype(np.float32),
+                 rng.uniform(-30, 30, n).astype(np.float32)))
+    return sets
+
+
+@pytest.mark.parametrize("w,nb", [(0.25, 720), (0.01, 18000), (0.35, 515)])
+def test_per_pair_bins_only_move_within_tolerance_of_an_edge(acf, ctx, w, nb):
+    w_rad = math.radians(w)
+    worst = 0.0
+    for s in _pair_sets(400_000, seed=123):
+        ra1, dec1, ra2, dec2 = (np.ascontiguousarray(a, dtype=np.float32) for a in s)
+        gb = ctx.pair_bins(ra1, dec1, ra2, dec2, w, nb).cpu().numpy()
+        ob = oracle.pair_bin(ra1, dec1, ra2, dec2, w, nb)
+        th = oracle.pair_theta(ra1, dec1, ra2, dec2)
+        bad = np.nonzero(gb != ob)[0]
+        if len(bad):
+            assert np.all(np.abs(gb[bad] - ob[bad]) == 1)
+            edge = np.maximum(gb[bad], ob[bad]) * w_rad
+            dist = np.abs(th[bad] - edge)
+            worst = max(worst, float(dist.max()))
+            assert np.all(dist < TOL), f"moved pair {float(dist.max()):.3e} rad from its edge"
+    print(f"w={w}: largest distance from the edge of a moved pair {worst:.3e} rad")
+
+
+def test_auto_correlation_decomposes_into_parts(acf, ctx):
+    # DD(A u B) = DD(A) + DD(B) + 2 X(A, B) exactly: the symmetric path and the cross path bin
+    # every pair identically
+    c = synth.catalogs(9000, 0, 20, 30.0, seed=8)
+    a, b = slice(0, 4100), slice(4100, 9000)
+    full = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)).astype(object)
+    da = acf.as_uint64(ctx.histogram(c.ra_d[a], c.dec_d[a], bin_width_deg=0.25, nbins=720)).astype(object)
+    db = acf.as_uint64(ctx.histogram(c.ra_d[b], c.dec_d[b], bin_width_deg=0.25, nbins=720)).astype(object)
+    x = acf.as_uint64(ctx.histogram(c.ra_d[a], c.dec_d[a], c.ra_d[b], c.dec_d[b], bin_width_deg=0.25,
+                                    nbins=720)).astype(object)
+    torch.cuda.synchronize()
+    assert list(full) == list(da + db + 2 * x)
+
+
+def test_acos_method_keeps_totals(acf, ctx):
+    # the page's dot + acos route: a measured alternative. Its totals are exact; its bins are
+    # not held to the 1e-6 rad rule (fp32 arccos near 0 and 180 degrees is too coarse).
+    c = synth.catalogs(3000, 2000, 10, 30.0, seed=10)
+    ctx.set_option("bin_method", 1)
+    try:
+        g = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720))
+        s = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720))
+        torch.cuda.synchronize()
+        assert int(g.sum()) == 3000 * 2000 and int(s.sum()) == 3000 * 3000
+        o = oracle.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+        assert np.abs(g.astype(np.int64) - o.hist.astype(np.int64)).sum() < 0.01 * g.sum()
+    finally:
+        ctx.set_option("bin_method", 0)
+
+
+def test_kernel_timing_records_launches(acf, ctx):
+    c = synth.catalogs(2000, 2000, 0, 0.0, seed=2)
+    ctx.set_option("kernel_timing", 1)
+    try:
+        ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)
+        ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+        t = ctx.kernel_times()
+        assert len(t) == 2 and all(x > 0 for x in t)
+    finally:
+        ctx.set_option("kernel_timing", 0)
