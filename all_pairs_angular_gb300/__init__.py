@@ -46,7 +46,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     if _lib is not None:
         return _lib
     debug = os.environ.get("ACF_DEBUG_BOUNDS", "") == "1"
-    if build_if_missing:
+    if os.environ.get("ACF_LIB"):
+        path = os.environ["ACF_LIB"]  # a prebuilt variant (tuning experiments)
+    elif build_if_missing:
         path = _build.build(debug=debug)
     else:
         path = _build.DEBUG_LIB_PATH if debug else _build.LIB_PATH

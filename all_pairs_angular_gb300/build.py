@@ -22,10 +22,12 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libacf.so")
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, debug: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, debug: bool = False,
+          out: str | None = None) -> str:
     """Compile (if stale) and return the path of libacf.so (libacf_debug.so with ``debug``: every
-    shared-memory and global index checked, violations reported instead of accessed)."""
-    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    shared-memory and global index checked, violations reported instead of accessed). ``extra``
+    adds nvcc flags (e.g. -DACF_K=6) and ``out`` names another output file for such variants."""
+    path = out or (DEBUG_LIB_PATH if debug else LIB_PATH)
     newest = max(os.path.getmtime(p) for p in DEPENDS)
     if not force and not extra and os.path.exists(path) and os.path.getmtime(path) >= newest:
         return path

@@ -20,13 +20,10 @@ using namespace acf;
 
 namespace {
 
-// theta'^2 = q * f(q) for a chord q on [0, 2]; f fitted by fit_arcsin2.py (degree 7,
-// absolute theta' error <= 2.5e-8 rad after rounding the scaled coefficients to fp32)
-const double kArcsin2Coef[8] = {0.99999959294652097,   0.083342611628085594,  0.011049794431887118,
-                                0.0019657095570993176, 4.2347086002697957e-05, 0.00029099553526503564,
-                                -9.1427792701640403e-05, 2.3068911858269848e-05};
-
-constexpr int kK = 8;                          // i-galaxies per thread
+#ifndef ACF_K
+#define ACF_K 5
+#endif
+constexpr int kK = ACF_K;                      // i-galaxies per thread
 constexpr int kMaxEntries = 49152;             // histogram entries a block can hold (192 KB)
 constexpr size_t kTileBytes = 2 * kJT * sizeof(float4);
 constexpr int kMaxTimed = 4096;
@@ -116,10 +113,8 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   const double P = 180.0 / w_deg;  // bins in half a turn
   BinParams& bp = pl.bp;
   std::memset(&bp, 0, sizeof bp);
-  for (int k = 0; k < 8; ++k) bp.c[k] = (float)(kArcsin2Coef[k] / (w_rad * w_rad));
   bp.nbins = nbins;
   bp.inv_w = (float)(1.0 / w_rad);
-  bp.half_p = (float)(P / 2.0);
   pl.method = c->opt_method;
   const double pr = std::rint(P);
   const bool integral = std::fabs(P - pr) <= 1e-9 * std::max(1.0, P) && pr >= 4.0;
@@ -150,8 +145,8 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     return fail(c, ACF_ERR_UNSUPPORTED, "lane-private layout needs %zu bytes of shared memory", lane_bytes);
   pl.layout = layout;
   pl.smem = (layout == kLane) ? lane_bytes : kTileBytes + (size_t)((bp.entries * 4 + 15) & ~15);
-  // threads: 256 when two blocks fit on an SM, else 512 so one block still fills 16 warps
-  pl.threads = c->opt_threads ? c->opt_threads : (pl.smem * 2 + 2048 <= 233472 ? 256 : 512);
+  // 512 threads at <= 64 registers: two resident blocks give 32 warps per SM
+  pl.threads = c->opt_threads ? c->opt_threads : 512;
   if (pl.threads != 256 && pl.threads != 512) return fail(c, ACF_ERR_ARG, "threads must be 256 or 512");
   return ACF_OK;
 }
@@ -177,11 +172,11 @@ PairKernelFn pick_kernel(const Plan& pl) {
   return nullptr;
 }
 
-int launch_convert(acf_ctx* c, const float* ra, const float* dec, long long n, float4* v) {
+int launch_convert(acf_ctx* c, const float* ra, const float* dec, long long n, float4* v, unsigned int* ticket) {
   if (n <= 0) return ACF_OK;
   const int threads = 256;
   const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 16);
-  convert_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, v);
+  convert_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, v, ticket);
   ACF_CUDA(c, cudaGetLastError());
   return ACF_OK;
 }
@@ -207,12 +202,16 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
   L.step = bi / kJT;
   L.chunks = sym ? L.rows * L.cj - L.step * L.rows * (L.rows - 1) / 2 : L.rows * L.cj;
   L.grid = std::min<long long>((long long)c->num_sms * L.ctas, std::max<long long>(L.chunks, 1));
+  // the kernel hands out chunks with a 32-bit ticket that may run past the end by 2 per block
+  if (L.chunks + 2 * L.grid + 2 >= 4294967295ll)
+    return fail(c, ACF_ERR_UNSUPPORTED, "%lld chunks exceed the 32-bit chunk dispenser", L.chunks);
   return ACF_OK;
 }
 
 // The pair kernel and merge for vectors already on the device. partial holds L.grid rows.
 int histogram_vectors(acf_ctx* c, const float4* vi, long long ni, const float4* vj, long long nj, bool sym,
-                      const Plan& pl, const Launch& L, unsigned long long* partial, uint64_t* out) {
+                      const Plan& pl, const Launch& L, unsigned long long* partial, unsigned int* ticket,
+                      uint64_t* out) {
   PairParams p;
   p.vi = vi;
   p.vj = vj;
@@ -228,6 +227,7 @@ int histogram_vectors(acf_ctx* c, const float4* vi, long long ni, const float4* 
   const double per_chunk = (pl.layout == kLane ? (double)(pl.threads / 32) : (double)pl.threads) * kK * kJT * p.inc;
   p.flush_every = (unsigned)std::max(1.0, std::floor(4294967295.0 / per_chunk));
   p.partial = partial;
+  p.ticket = ticket;
   p.bp = pl.bp;
   const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
   if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
@@ -252,10 +252,9 @@ int histogram_vectors(acf_ctx* c, const float4* vi, long long ni, const float4* 
   }
 #endif
   const unsigned long long self = sym ? (unsigned long long)ni : 0ull;
-  const int mthreads = 256;
-  const int mblocks = (int)std::min<long long>((pl.bp.nbins + mthreads - 1) / mthreads, 4096);
-  merge_kernel<<<mblocks, mthreads, 0, c->stream>>>(partial, (int)L.grid, pl.bp.nbins, self,
-                                                     reinterpret_cast<unsigned long long*>(out));
+  const int mblocks = (pl.bp.nbins + 31) / 32;
+  merge_kernel<<<mblocks, 32 * kMergeWarps, 0, c->stream>>>(partial, (int)L.grid, pl.bp.nbins, self,
+                                                             reinterpret_cast<unsigned long long*>(out));
   ACF_CUDA(c, cudaGetLastError());
   c->info_grid = L.grid;
   c->info_threads = pl.threads;
@@ -274,6 +273,7 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
                    int64_t n2, double w_deg, int32_t nbins, uint64_t* out) {
   if (!c) return ACF_ERR_ARG;
   if (n < 0) return fail(c, ACF_ERR_ARG, "n must be >= 0");
+  if (n > 2147483647ll || n2 > 2147483647ll) return fail(c, ACF_ERR_UNSUPPORTED, "catalogs are limited to 2^31-1 galaxies");
   if (!out) return fail(c, ACF_ERR_ARG, "out is NULL");
   const bool sym = (ra2 == nullptr && dec2 == nullptr) || (ra2 == ra && dec2 == dec && n2 == n);
   if (!sym && n2 < 0) return fail(c, ACF_ERR_ARG, "n2 must be >= 0");
@@ -294,19 +294,20 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   const size_t b_vi = align256((size_t)n * sizeof(float4));
   const size_t b_vj = sym ? 0 : align256((size_t)nj * sizeof(float4));
   const size_t b_part = align256((size_t)L.grid * (size_t)nbins * sizeof(unsigned long long));
-  rc = ensure(c, c->ws, b_vi + b_vj + b_part);
+  rc = ensure(c, c->ws, 256 + b_vi + b_vj + b_part);
   if (rc) return rc;
   char* base = static_cast<char*>(c->ws.ptr);
-  float4* vi = reinterpret_cast<float4*>(base);
-  float4* vj = sym ? vi : reinterpret_cast<float4*>(base + b_vi);
-  unsigned long long* part = reinterpret_cast<unsigned long long*>(base + b_vi + b_vj);
-  rc = launch_convert(c, ra, dec, n, vi);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(base);
+  float4* vi = reinterpret_cast<float4*>(base + 256);
+  float4* vj = sym ? vi : reinterpret_cast<float4*>(base + 256 + b_vi);
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(base + 256 + b_vi + b_vj);
+  rc = launch_convert(c, ra, dec, n, vi, ticket);
   if (rc) return rc;
   if (!sym) {
-    rc = launch_convert(c, ra2, dec2, nj, vj);
+    rc = launch_convert(c, ra2, dec2, nj, vj, nullptr);
     if (rc) return rc;
   }
-  return histogram_vectors(c, vi, n, vj, nj, sym, pl, L, part, out);
+  return histogram_vectors(c, vi, n, vj, nj, sym, pl, L, part, ticket, out);
 }
 
 }  // namespace

@@ -28,16 +28,28 @@
 namespace acf {
 
 constexpr int kJT = 128;  // j-galaxies per shared-memory chunk
+#ifndef ACF_JJ_UNROLL
+#define ACF_JJ_UNROLL 4
+#endif
+constexpr int kJJUnroll = ACF_JJ_UNROLL;
+#ifndef ACF_ASM_LOP3
+#define ACF_ASM_LOP3 1  // write the two sign-bit logic ops as explicit lop3 (2 ops, not 3)
+#endif  // j-loop unroll of the full-chunk path
 constexpr float kMagic = 8388608.0f;  // 2^23: adding it with round-toward-zero floors into the mantissa
 
 enum Layout { kLane = 1, kBlock = 2 };
 enum BinMap { kMirror = 0, kClamp = 1 };
 enum Method { kChordPoly = 0, kDotAcos = 1 };
 
+// theta'^2 = q * P(q) for a chord q = |u - v|^2 on [0, 2] (theta' <= 90 degrees), P of degree 7
+// fitted by fit_arcsin2.py: absolute theta' error <= 1.8e-8 rad (2.5e-8 after fp32 rounding).
+__device__ constexpr float kP0 = 0.99999959294652097f, kP1 = 0.083342611628085594f, kP2 = 0.011049794431887118f,
+                           kP3 = 0.0019657095570993176f, kP4 = 4.2347086002697957e-05f,
+                           kP5 = 0.00029099553526503564f, kP6 = -9.1427792701640403e-05f,
+                           kP7 = 2.3068911858269848e-05f;
+
 struct BinParams {
-  float c[8];      // coefficients of q * P(q) = (theta'/w)^2, lowest degree first
   float magic;     // 2^23 + off (mirror) or 2^23 (clamp)
-  float half_p;    // P/2 with P = pi / w (clamp map)
   float clamp_c;   // largest index (clamp map)
   float inv_w;     // 1 / w in radians (acos method)
   int off;         // mirror: index of theta' = 0 on the near side
@@ -58,6 +70,7 @@ struct PairParams {
   unsigned int inc;            // 2 (sym) or 1 (cross)
   unsigned int flush_every;    // chunks between flushes of the 32-bit shared counters
   unsigned long long* partial; // [gridDim.x][nbins]
+  unsigned int* ticket;        // chunk dispenser; zero before the launch
   BinParams bp;
 };
 
@@ -90,15 +103,32 @@ __device__ __noinline__ void debug_note(int kind, long long a, long long b, floa
 
 // ------------------------------------------------------------------ small PTX helpers
 
+// Callers pass arguments >= 1e-26 (never subnormal), so flushing subnormals changes nothing and
+// spares the input range check that the non-ftz form carries.
 __device__ __forceinline__ float sqrt_approx(float x) {
   float y;
-  asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
 __device__ __forceinline__ float add_rz(float a, float b) {
   float y;
   asm("add.rz.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
+// three-input logic op; lut is the truth table over (a=0xF0, b=0xCC, c=0xAA)
+template <int LUT>
+__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t y;
+  asm("lop3.b32 %0, %1, %2, %3, %4;" : "=r"(y) : "r"(a), "r"(b), "r"(c), "n"(LUT));
+  return y;
+}
+
+// a * b + c with one rounding, toward zero
+__device__ __forceinline__ float fma_rz(float a, float b, float c) {
+  float y;
+  asm("fma.rz.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
   return y;
 }
 
@@ -130,8 +160,10 @@ __device__ __forceinline__ float4 radec_to_unit(float ra_arcmin, float dec_arcmi
   return make_float4((float)(cd * ca), (float)(cd * sa), (float)sd, 0.0f);
 }
 
+// Also zeroes the pair kernel's chunk dispenser, which the next pair launch on the stream uses.
 __global__ void convert_kernel(const float* __restrict__ ra, const float* __restrict__ dec, long long n,
-                               float4* __restrict__ v) {
+                               float4* __restrict__ v, unsigned int* __restrict__ ticket) {
+  if (blockIdx.x == 0 && threadIdx.x == 0 && ticket) *ticket = 0u;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     v[i] = radec_to_unit(ra[i], dec[i]);
 }
@@ -149,29 +181,39 @@ __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float x
     const float t = acosf(fminf(fmaxf(d, -1.0f), 1.0f)) * bp.inv_w;
     return add_rz(fminf(t, bp.clamp_c), kMagic);
   } else {
-    const uint32_t sbit = __float_as_uint(d) & 0x80000000u;
-    const float s = __uint_as_float(sbit | 0x3f800000u);  // +1 or -1
-    const float dx = fmaf(-s, xj, xi);
-    const float dy = fmaf(-s, yj, yi);
-    const float dz = fmaf(-s, zj, zi);
+    const uint32_t db = __float_as_uint(d);
+    // ns = -sign(d) as +-1.0: (d & signmask) ^ bits(-1.0), one logic op
+#if ACF_ASM_LOP3
+    const float ns = __uint_as_float(lop3<0x6A>(db, 0x80000000u, 0xbf800000u));
+#else
+    const float ns = __uint_as_float((db & 0x80000000u) ^ 0xbf800000u);
+#endif
+    const float dx = fmaf(ns, xj, xi);
+    const float dy = fmaf(ns, yj, yi);
+    const float dz = fmaf(ns, zj, zi);
     // 1e-30 keeps t' > 0 for identical or exactly antipodal vectors (see the mirror map)
     const float q = fmaf(dz, dz, fmaf(dy, dy, fmaf(dx, dx, 1e-30f)));
-    float p = bp.c[7];
-    p = fmaf(p, q, bp.c[6]);
-    p = fmaf(p, q, bp.c[5]);
-    p = fmaf(p, q, bp.c[4]);
-    p = fmaf(p, q, bp.c[3]);
-    p = fmaf(p, q, bp.c[2]);
-    p = fmaf(p, q, bp.c[1]);
-    p = fmaf(p, q, bp.c[0]);
-    const float tp = sqrt_approx(p * q);  // theta' / w
+    float p = fmaf(kP7, q, kP6);
+    p = fmaf(p, q, kP5);
+    p = fmaf(p, q, kP4);
+    p = fmaf(p, q, kP3);
+    p = fmaf(p, q, kP2);
+    p = fmaf(p, q, kP1);
+    p = fmaf(p, q, kP0);
+    const float th = sqrt_approx(p * q);  // theta' in radians
     if (MAP == kMirror) {
-      // near side (s = +1): index off + floor(t'); far side: round-toward-zero of (2^23 + off - t')
-      // gives off - ceil(t'), and bin P - ceil(t') is exactly floor(P - t') when P is an integer.
-      return add_rz(__uint_as_float(__float_as_uint(tp) | sbit), bp.magic);
+      // near side (s = +1): floor(theta'/w) exactly, by one fma rounded toward zero onto 2^23 + off;
+      // far side: the same fma of -theta' gives off - ceil(theta'/w), and bin P - ceil(theta'/w)
+      // is exactly floor((pi - theta')/w) when P = pi/w is an integer.
+      // theta' carrying the sign of d: th | (d & signmask), one logic op
+#if ACF_ASM_LOP3
+      return fma_rz(__uint_as_float(lop3<0xF8>(__float_as_uint(th), db, 0x80000000u)), bp.inv_w, bp.magic);
+#else
+      return fma_rz(__uint_as_float(__float_as_uint(th) | (db & 0x80000000u)), bp.inv_w, bp.magic);
+#endif
     } else {
-      const float h = fmaf(s, -bp.half_p, bp.half_p);  // 0 or P
-      const float t = fmaf(s, tp, h);                   // t' or P - t'
+      const float h = fmaf(ns, 1.57079632679489662f, 1.57079632679489662f);  // 0 or pi
+      const float t = fmaf(-ns, th, h) * bp.inv_w;                             // theta / w
       return add_rz(fminf(t, bp.clamp_c), kMagic);
     }
   }
@@ -188,23 +230,25 @@ __device__ __forceinline__ int entry_to_bin(int e, const BinParams& bp) {
 
 // ------------------------------------------------------------------ pair kernel
 
-// Map chunk q to (row ib, chunk column jc).
-__device__ __forceinline__ void chunk_coords(const PairParams& p, long long q, long long& ib, long long& jc) {
+// Map chunk q to (row ib, chunk column jc). The host guarantees chunk counts below 2^32 and
+// catalogs below 2^31 galaxies, so 32-bit indices suffice.
+__device__ __forceinline__ void chunk_coords(const PairParams& p, unsigned int q, int& ib, int& jc) {
+  const long long cj = p.chunks_per_row;
   if (!p.sym) {
-    ib = q / p.chunks_per_row;
-    jc = q - ib * p.chunks_per_row;
+    ib = (int)(q / (unsigned long long)cj);
+    jc = (int)(q - (unsigned long long)ib * cj);
     return;
   }
   // row r starts at S(r) = r*CJ - R*r*(r-1)/2; largest r with S(r) <= q
   long long lo = 0, hi = p.rows - 1;
   while (lo < hi) {
     const long long mid = (lo + hi + 1) >> 1;
-    const long long s = mid * p.chunks_per_row - (long long)p.row_step * mid * (mid - 1) / 2;
-    if (s <= q) lo = mid;
+    const long long s = mid * cj - (long long)p.row_step * mid * (mid - 1) / 2;
+    if (s <= (long long)q) lo = mid;
     else hi = mid - 1;
   }
-  ib = lo;
-  jc = ib * p.row_step + (q - (ib * p.chunks_per_row - (long long)p.row_step * ib * (ib - 1) / 2));
+  ib = (int)lo;
+  jc = (int)(lo * p.row_step + ((long long)q - (lo * cj - (long long)p.row_step * lo * (lo - 1) / 2)));
 }
 
 template <int K, int THREADS, int LAYOUT, int MAP, int METHOD>
@@ -230,12 +274,17 @@ __device__ __forceinline__ void flush_hist(const PairParams& p, uint32_t* hist, 
   }
 }
 
+// One chunk = the block's BI = THREADS*K i-galaxies (K per thread, in registers) against kJT
+// j-galaxies (in shared memory). Chunks are handed out by an atomic ticket so that uneven chunk
+// costs (ragged tails, diagonal chunks of DD/RR) spread over all blocks; the ticket two chunks
+// ahead is fetched while the current chunk is computed.
 template <int K, int THREADS, int LAYOUT, int MAP, int METHOD>
-__global__ void __launch_bounds__(THREADS) pair_kernel(const PairParams p) {
+__global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) pair_kernel(const PairParams p) {
   constexpr int BI = THREADS * K;
   extern __shared__ __align__(16) unsigned char smem[];
   float4* tiles = reinterpret_cast<float4*>(smem);                    // [2][kJT]
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + 2 * kJT * sizeof(float4));
+  __shared__ unsigned int s_ticket[2];
   const int tid = threadIdx.x, lane = tid & 31;
 
   // zero this block's histogram and its partial row
@@ -243,6 +292,10 @@ __global__ void __launch_bounds__(THREADS) pair_kernel(const PairParams p) {
   for (int w = tid; w < words; w += THREADS) hist[w] = 0;
   unsigned long long* row = p.partial + (size_t)blockIdx.x * p.bp.nbins;
   for (int k = tid; k < p.bp.nbins; k += THREADS) row[k] = 0ull;
+  if (tid == 0) {
+    s_ticket[0] = atomicAdd(p.ticket, 1u);
+    s_ticket[1] = atomicAdd(p.ticket, 1u);
+  }
 
   const uint32_t hist_addr = (uint32_t)__cvta_generic_to_shared(hist);
   const uint32_t tiles_addr = (uint32_t)__cvta_generic_to_shared(tiles);
@@ -251,68 +304,70 @@ __global__ void __launch_bounds__(THREADS) pair_kernel(const PairParams p) {
   // address of entry e in this lane's copy = (code bits << shift) + base
   const uint32_t base = (LAYOUT == kLane) ? hist_addr + lane * 4u - (magic_bits << 7) : hist_addr - (magic_bits << 2);
   constexpr int SHIFT = (LAYOUT == kLane) ? 7 : 2;
-
-  const long long C = p.total_chunks, G = gridDim.x;
-  const long long q0 = (long long)blockIdx.x * C / G, q1 = ((long long)blockIdx.x + 1) * C / G;
+  const unsigned long long C = (unsigned long long)p.total_chunks;
 
   __syncthreads();
-  if (q0 < q1) {
-    long long ib, jc;
-    chunk_coords(p, q0, ib, jc);
-    // first j-chunk
+  const unsigned int C32 = (unsigned int)C;
+  unsigned int q = s_ticket[0], qn = s_ticket[1];
+  if (q < C32) {
+    const int ni = (int)p.ni, nj = (int)p.nj;
+    int ib, jc;
+    chunk_coords(p, q, ib, jc);
     {
-      const long long j0 = jc * kJT;
-      const long long jn = min((long long)kJT, p.nj - j0);
+      const int j0 = jc * kJT;
+      const int jn = min(kJT, nj - j0);
       if (tid < jn) cp_async16(tiles_addr + tid * 16u, p.vj + j0 + tid);
-      cp_async_commit();
     }
+    cp_async_commit();
     float xi[K], yi[K], zi[K];
-    long long cur_ib = -1;
+    int cur_ib = -1;
     unsigned int since_flush = 0;
-    for (long long q = q0; q < q1; ++q) {
-      const int buf = (int)((q - q0) & 1);
-      // prefetch the next chunk into the other buffer
-      long long nib = ib, njc = jc + 1;
-      if (njc == p.chunks_per_row) {
-        nib = ib + 1;
-        njc = p.sym ? nib * p.row_step : 0;
-      }
-      if (q + 1 < q1) {
-        const long long j0 = njc * kJT;
-        const long long jn = min((long long)kJT, p.nj - j0);
-        if (tid < jn) cp_async16(tiles_addr + (uint32_t)((buf ^ 1) * kJT + tid) * 16u, p.vj + j0 + tid);
-      }
-      cp_async_commit();
-      // i-vectors of this row
-      const long long i0 = ib * BI;
+    int it = 0;  // iteration count: tile buffer it & 1, ticket mailbox slot it & 1
+    while (true) {
+      const int buf = it & 1;
+      const int i0 = ib * BI;
       if (ib != cur_ib) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          long long i = i0 + k * THREADS + tid;
-          i = i < p.ni ? i : p.ni - 1;
+          int i = i0 + k * THREADS + tid;
+          i = i < ni ? i : ni - 1;
           const float4 v = __ldg(p.vi + i);
           xi[k] = v.x;
           yi[k] = v.y;
           zi[k] = v.z;
-          ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 4, i, ib, v.x, v.y, v.z);
+          (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 4, i, ib, v.x, v.y, v.z);
         }
         cur_ib = ib;
       }
-      cp_async_wait<1>();
+      // One barrier per chunk: after it this chunk's tile is visible, every warp has finished the
+      // previous chunk (so the other buffer may be refilled) and the ticket that thread 0 posted
+      // in the previous iteration is readable.
+      cp_async_wait<0>();
       __syncthreads();
+      if (it > 0) qn = s_ticket[(it - 1) & 1];
+      int nib = 0, njc = 0;
+      if (qn < C32) {
+        chunk_coords(p, qn, nib, njc);
+        const int j0 = njc * kJT;
+        const int jn = min(kJT, nj - j0);
+        if (tid < jn) cp_async16(tiles_addr + (uint32_t)((buf ^ 1) * kJT + tid) * 16u, p.vj + j0 + tid);
+      }
+      cp_async_commit();
+      unsigned int t_after = 0;
+      if (tid == 0) t_after = atomicAdd(p.ticket, 1u);  // the chunk after qn; posted below
 
       const float4* tile = tiles + buf * kJT;
-      const long long j0 = jc * kJT;
-      const int jn = (int)min((long long)kJT, p.nj - j0);
-      const bool full = (jn == kJT) && (i0 + BI <= p.ni) && (!p.sym || j0 >= i0 + BI);
+      const int j0 = jc * kJT;
+      const int jn = min(kJT, nj - j0);
+      const bool full = (jn == kJT) && (i0 + BI <= ni) && (!p.sym || j0 >= i0 + BI);
 #ifdef ACF_DEBUG_BOUNDS
       for (int jj = 0; jj < jn; ++jj) {
         const float4 v = tile[jj];
-        ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 2, j0 + jj, q, v.x, v.y, v.z, (float)buf);
+        (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 2, j0 + jj, q, v.x, v.y, v.z, (float)buf);
       }
 #endif
       if (full) {
-#pragma unroll 2
+#pragma unroll kJJUnroll
         for (int jj = 0; jj < kJT; ++jj) {
           const float4 v = tile[jj];
 #pragma unroll
@@ -325,29 +380,42 @@ __global__ void __launch_bounds__(THREADS) pair_kernel(const PairParams p) {
           }
         }
       } else {
+        // pair (i, j) counts iff jj > thr[k]: thr = -1 for every j, a diagonal offset when only
+        // j > i counts (DD/RR), INT_MAX for an i beyond the catalog
+        int thr[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const int i = i0 + k * THREADS + tid;
+          const int t = p.sym ? i - j0 : -1;
+          thr[k] = (i >= ni) ? 0x7fffffff : max(-1, min(t, kJT));
+        }
         for (int jj = 0; jj < jn; ++jj) {
           const float4 v = tile[jj];
-          const long long j = j0 + jj;
 #pragma unroll
           for (int k = 0; k < K; ++k) {
-            const long long i = i0 + k * THREADS + tid;
-            const bool ok = (i < p.ni) && (!p.sym || j > i);
             const float code = pair_code<MAP, METHOD>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-            if (ok && ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
-                                (long long)(__float_as_uint(code) - magic_bits), i, code, xi[k], yi[k], zi[k], v.x,
-                                v.y, v.z, (float)jj))
+            if (jj > thr[k] &&
+                ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
+                          (long long)(__float_as_uint(code) - magic_bits), i0 + k * THREADS + tid, code, xi[k], yi[k],
+                          zi[k], v.x, v.y, v.z, (float)jj))
               red_shared_add((__float_as_uint(code) << SHIFT) + base, p.inc);
           }
         }
       }
-      __syncthreads();  // the buffer just read is refilled two chunks from now
+      // Slot it&1 is next written two iterations later, after a barrier every thread passes only
+      // once it has read this value, so one barrier per chunk is enough.
+      if (tid == 0) s_ticket[it & 1] = t_after;
       if (++since_flush == p.flush_every) {
+        __syncthreads();
         flush_hist<K, THREADS, LAYOUT, MAP, METHOD>(p, hist, true);
         __syncthreads();
         since_flush = 0;
       }
+      if (qn >= C32) break;
+      q = qn;
       ib = nib;
       jc = njc;
+      ++it;
     }
     cp_async_wait<0>();
   }
@@ -358,12 +426,27 @@ __global__ void __launch_bounds__(THREADS) pair_kernel(const PairParams p) {
 // ------------------------------------------------------------------ merge, omega, diagnostics
 
 // out[k] = sum over blocks of partial[b][k]; auto-correlations add the n self-pairs to bin 0.
-__global__ void merge_kernel(const unsigned long long* __restrict__ partial, int rows, int nbins,
-                             unsigned long long self_pairs, unsigned long long* __restrict__ out) {
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < nbins; k += gridDim.x * blockDim.x) {
-    unsigned long long s = (k == 0) ? self_pairs : 0ull;
-    for (int r = 0; r < rows; ++r) s += partial[(size_t)r * nbins + k];
-    out[k] = s;
+// A block owns 32 consecutive bins (one per lane, coalesced reads); its 8 warps split the rows
+// and combine their sums in shared memory.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const unsigned long long* __restrict__ partial,
+                                                                int rows, int nbins, unsigned long long self_pairs,
+                                                                unsigned long long* __restrict__ out) {
+  __shared__ unsigned long long acc[kMergeWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int k = blockIdx.x * 32 + lane;
+  unsigned long long s = 0ull;
+  if (k < nbins) {
+#pragma unroll 4
+    for (int r = warp; r < rows; r += kMergeWarps) s += partial[(size_t)r * nbins + k];
+  }
+  acc[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && k < nbins) {
+    unsigned long long t = (k == 0) ? self_pairs : 0ull;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) t += acc[w][lane];
+    out[k] = t;
   }
 }
 

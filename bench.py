@@ -1,0 +1,376 @@
+"""Benchmark of the GB300 angular-correlation path.
+
+One step = the whole hot path on the pages' workload shape: DD, DR and RR histograms of two
+100,000-galaxy catalogs (D clustered, R uniform; 720 bins of 0.25 degrees) plus omega, with the
+catalogs already resident in HBM. Reported value: logical pairs per second, (n_d^2 + n_d n_r +
+n_r^2) / step time, in G pairs/s ("CUDA Deep Dive: 10B Galaxy Pairs on an RTX 5080", section "The
+problem": N^2 pairs per family, three families).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 1]
+
+--impl reference times the fp64 CPU oracle (the reference arm) on a bounded row sample of the same
+workload. With N > 1 (launched by torch.distributed.run) every rank runs an independent replica
+of the job on its own GPU (weak scaling); the reference arm runs on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "G pairs/s (DD+DR+RR, N=100k each) and % of FP32 issue roofline"
+UNIT = "Gpairs/s"
+# Thread instructions per evaluated pair in the pair kernel's inner loop (chord, sign, polynomial,
+# sqrt, index, shared-memory add); see DESIGN.md "Roofline".
+INST_PER_PAIR = 23
+SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
+# The pages' kernel time for three 100k histograms on an RTX 5080 (another machine: context only)
+PAGE_KERNEL_MS = 22.747
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(values: list[float], world: int) -> list[float]:
+    """Element-wise max over ranks (host-side gloo all-reduce; no data-path collective)."""
+    if world <= 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def logical_pairs(n_d: int, n_r: int) -> int:
+    return n_d * n_d + n_d * n_r + n_r * n_r
+
+
+def evaluated_pairs(n_d: int, n_r: int) -> int:
+    """Pairs the kernels must evaluate: every DR pair, each unordered DD and RR pair once."""
+    return n_d * n_r + n_d * (n_d - 1) // 2 + n_r * (n_r - 1) // 2
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int, path: str | None):
+        self.device, self.path, self.proc = device, path, None
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w") if self.path else subprocess.DEVNULL
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.device), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            if self.path:
+                self.fh.write(out)
+                self.fh.close()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("all_pairs_angular_gb300/csrc/acf_kernels.cuh", "all_pairs_angular_gb300/csrc/acf.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str) -> float | None:
+    """dram read+write bytes per pair-kernel launch from the committed ncu summary, if it was
+    captured from the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "pair_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash() or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(cat, rows: int, seed: int, threads: int = 0) -> dict:
+    """Time the fp64 oracle on a row sample: `rows` rows of D against D, of D against R and of R
+    against R. Returns the oracle rate in logical G pairs/s."""
+    import oracle
+    idx_d = synth.sample_rows(cat.n_d, rows, seed)
+    idx_r = synth.sample_rows(cat.n_r, rows, seed + 1)
+    w, nb = cat.bin_width_deg, cat.nbins
+    t0 = time.perf_counter()
+    oracle.histogram(cat.ra_d[idx_d], cat.dec_d[idx_d], cat.ra_d, cat.dec_d, w, nb, threads=threads)
+    oracle.histogram(cat.ra_d[idx_d], cat.dec_d[idx_d], cat.ra_r, cat.dec_r, w, nb, threads=threads)
+    oracle.histogram(cat.ra_r[idx_r], cat.dec_r[idx_r], cat.ra_r, cat.dec_r, w, nb, threads=threads)
+    dt = time.perf_counter() - t0
+    pairs = rows * (2 * cat.n_d + cat.n_r)
+    cores = threads if threads > 0 else (os.cpu_count() or 1)
+    return {"value": pairs / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{rows} random rows each of DD, DR and RR against the full catalogs ({pairs:.3g} pairs)"}
+
+
+def run_reference(args, cat, workload, rank, world):
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    times = []
+    for s in range(args.warmup + args.steps):
+        r = cpu_baseline(cat, rows, seed=1000 + s)
+        if s >= args.warmup:
+            times.append(r["seconds"])
+    per_step_pairs = rows * (2 * cat.n_d + cat.n_r)
+    total = sum(times)
+    value = per_step_pairs * len(times) / total / 1e9
+    cb = {"value": value, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+          "sample": f"each step: {rows} random rows each of DD, DR and RR against the full catalogs"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "n_d": cat.n_d, "n_r": cat.n_r, "bin_width_deg": cat.bin_width_deg,
+                       "nbins": cat.nbins, "l2": "n/a (CPU)"},
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, cat, workload, rank, world, local):
+    import torch
+
+    import all_pairs_angular_gb300 as acf
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    ctx = acf.Context(local, stream)
+    ctx.set_option("kernel_timing", 1)
+    w, nb = cat.bin_width_deg, cat.nbins
+    with torch.cuda.stream(stream):
+        ra_d = torch.from_numpy(cat.ra_d).to(dev)
+        dec_d = torch.from_numpy(cat.dec_d).to(dev)
+        ra_r = torch.from_numpy(cat.ra_r).to(dev)
+        dec_r = torch.from_numpy(cat.dec_r).to(dev)
+        dd = torch.empty(nb, dtype=torch.int64, device=dev)
+        dr = torch.empty_like(dd)
+        rr = torch.empty_like(dd)
+        om = torch.empty(nb, dtype=torch.float64, device=dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    launches_per_step = 0
+
+    def step():
+        acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, None, None, 0, w, nb, dd)
+        acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, ra_r, dec_r, cat.n_r, w, nb, dr)
+        acf.acf_histogram(ctx.handle, ra_r, dec_r, cat.n_r, None, None, 0, w, nb, rr)
+        acf.acf_omega(ctx.handle, dd, dr, rr, nb, cat.n_d, cat.n_r, om)
+
+    # convert + pair + merge per histogram (two converts for DR) + omega
+    launches_per_step = 3 + 4 + 3 + 1
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        ctx.kernel_times()  # discard warm-up launches
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clock_log = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else None
+        with ClockSampler(local, clock_log) as clk:
+            for s in range(args.steps):
+                flush.zero_()                     # evict L2 outside the timed region
+                ev[s][0].record(stream)
+                step()
+                ev[s][1].record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kt = ctx.kernel_times()
+    total_ms = sum(step_ms)
+    total_ms_max, = reduce_max([total_ms], world)
+    pairs = logical_pairs(cat.n_d, cat.n_r)
+    value = world * pairs * args.steps / (total_ms_max / 1e3) / 1e9
+    # dominant kernel: the pair kernel (three launches per step: DD, DR, RR)
+    evals = evaluated_pairs(cat.n_d, cat.n_r)
+    pair_ms = sum(kt)
+    clocks = clk.summary()
+    peak = SMS * LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12  # T thread-instructions / s at the maximum clock
+    achieved = INST_PER_PAIR * evals * args.steps / (pair_ms / 1e3) / 1e12 if pair_ms > 0 else None
+    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
+            "frac": (achieved / peak) if achieved else None, "traffic": recorded_traffic(workload),
+            "inst_per_pair": INST_PER_PAIR, "pair_kernel_ms_per_launch": pair_ms / max(len(kt), 1),
+            "pair_kernel_launches": len(kt),
+            "peak_basis": f"{SMS} SMs x {LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz (maximum SM clock)"}
+    if clocks.get("sm_mhz"):
+        roof["frac_at_observed_clock"] = achieved / (SMS * LANES_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12)
+
+    # end to end through the C ABI with pinned host buffers: copies inside the timed region
+    h = {k: torch.from_numpy(getattr(cat, k)).pin_memory() for k in ("ra_d", "dec_d", "ra_r", "dec_r")}
+    hout = [torch.empty(nb, dtype=torch.int64).pin_memory() for _ in range(3)] + [
+        torch.empty(nb, dtype=torch.float64).pin_memory()]
+    ctx.set_option("kernel_timing", 0)
+
+    def e2e_step():
+        acf.acf_correlate_host(ctx.handle, h["ra_d"], h["dec_d"], cat.n_d, h["ra_r"], h["dec_r"], cat.n_r, w, nb,
+                               *hout)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e2e_step()  # synchronises before returning
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_total, = reduce_max([sum(e2e_times)], world)
+    e2e_value = world * pairs * args.steps / e2e_total / 1e9
+    h2d = 4 * (2 * cat.n_d + 2 * cat.n_r)
+    d2h = 8 * 4 * nb
+    assert np.array_equal(acf.as_uint64(hout[0]), acf.as_uint64(dd)), "e2e and device paths disagree"
+
+    if rank == 0:
+        cb = cpu_baseline(cat, args.cpu_rows, seed=77) if args.cpu_rows > 0 else None
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": value / (pairs / (PAGE_KERNEL_MS / 1e3) / 1e9),
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload, "n_d": cat.n_d, "n_r": cat.n_r, "bin_width_deg": w, "nbins": nb,
+                       "l2": "flushed between timed steps (256 MiB device write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "grid": ctx.info("grid"), "threads": ctx.info("threads"), "layout": ctx.info("layout")},
+            "evaluated_gpairs_per_s": world * evals * args.steps / (total_ms_max / 1e3) / 1e9,
+            "roofline": roof, "cpu_baseline": cb,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": 1e3 * e2e_total / args.steps},
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    return 0
+
+
+def run_profile(args, cat):
+    """One warm-up step and one step of DD, DR, RR and omega, nothing else: a short, fixed launch
+    list for Nsight Compute (pair kernel launches: 3 warm-up, then DD, DR, RR)."""
+    import torch
+
+    import all_pairs_angular_gb300 as acf
+
+    dev = torch.device("cuda", 0)
+    ctx = acf.Context(0)
+    w, nb = cat.bin_width_deg, cat.nbins
+    t = {k: torch.from_numpy(getattr(cat, k)).to(dev) for k in ("ra_d", "dec_d", "ra_r", "dec_r")}
+    out = [torch.empty(nb, dtype=torch.int64, device=dev) for _ in range(3)]
+    om = torch.empty(nb, dtype=torch.float64, device=dev)
+    for _ in range(2):
+        ctx.histogram(t["ra_d"], t["dec_d"], bin_width_deg=w, nbins=nb, out=out[0])
+        ctx.histogram(t["ra_d"], t["dec_d"], t["ra_r"], t["dec_r"], bin_width_deg=w, nbins=nb, out=out[1])
+        ctx.histogram(t["ra_r"], t["dec_r"], bin_width_deg=w, nbins=nb, out=out[2])
+        ctx.omega(out[0], out[1], out[2], cat.n_d, cat.n_r, out=om)
+    torch.cuda.synchronize()
+    sums = [int(acf.as_uint64(o).sum()) for o in out]
+    print(json.dumps({"profile": cat.name, "sums": sums, "grid": ctx.info("grid"), "threads": ctx.info("threads"),
+                      "kernel_source_hash": kernel_source_hash()}), flush=True)
+    ctx.close()
+    return 0 if sums == [cat.n_d ** 2, cat.n_d * cat.n_r, cat.n_r ** 2] else 1
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index (default 1: two 100k catalogs)")
+    ap.add_argument("--cpu-rows", type=int, default=2000, help="rows per family for the CPU baseline (0: skip)")
+    ap.add_argument("--ref-rows", type=int, default=200, help="rows per family per reference-arm step")
+    ap.add_argument("--profile", action="store_true", help="one warm-up step + one step only (for ncu)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        world = max(world, 1)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    cat = synth.config(args.config)
+    workload = (f"{cat.name}: D {cat.n_d} (half uniform, half in {synth.CONFIGS[args.config]['n_clumps']} clumps), "
+                f"R {cat.n_r} uniform, {cat.nbins} bins of {cat.bin_width_deg} deg, seed {cat.seed}")
+    if args.profile:
+        return run_profile(args, cat)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, cat, workload, rank, world)
+        return run_ours(args, cat, workload, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,52 @@
+"""Host-side logic of bench.py that needs no GPU: pair counts, clock parsing, and the max over
+ranks of the multi-replica run (two gloo ranks on the CPU)."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_pair_counts():
+    assert bench.logical_pairs(100_000, 100_000) == 3 * 10**10
+    assert bench.evaluated_pairs(100_000, 100_000) == 10**10 + 2 * (100_000 * 99_999 // 2)
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    cs = bench.ClockSampler(0, None)
+    cs.lines = ["0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active",
+                "0, 1965, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+                "0, 300, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    s = cs.summary()
+    assert s["sm_max_mhz"] == 2070 and s["sm_mhz"] == pytest.approx(2017.5) and s["reasons"] == ["sw_power_cap"]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    out = bench.reduce_max([1.0 + rank, 10.0 - rank], world)
+    bench.barrier(world)
+    q.put((rank, out))
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+    assert res[0] == res[1] == [2.0, 10.0]
