@@ -25,7 +25,7 @@ ACF_ERR_CUDA = -4
 
 EXPORTED = ["acf_version", "acf_create", "acf_destroy", "acf_last_error", "acf_set_stream", "acf_histogram",
             "acf_omega", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
-            "acf_kernel_times"]
+            "acf_kernel_times", "acf_histogram_noalloc"]
 
 _lib = None
 
@@ -61,6 +61,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "acf_last_error": (ctypes.c_char_p, [vp]),
         "acf_set_stream": (ci, [vp, vp]),
         "acf_histogram": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp]),
+        "acf_histogram_noalloc": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp]),
         "acf_omega": (ci, [vp, vp, vp, vp, i32, i64, i64, vp]),
         "acf_correlate_host": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp, vp, vp, vp]),
         "acf_pair_bins": (ci, [vp, vp, vp, vp, vp, i64, f64, i32, vp]),
@@ -121,6 +122,13 @@ def acf_set_stream(ctx: int, stream) -> None:
 def acf_histogram(ctx: int, ra, dec, n: int, ra2, dec2, n2: int, bin_width_deg: float, nbins: int, out) -> None:
     _check(ctx, load().acf_histogram(ctx, _ptr(ra), _ptr(dec), int(n), _ptr(ra2), _ptr(dec2), int(n2),
                                      float(bin_width_deg), int(nbins), _ptr(out)))
+
+
+def acf_histogram_noalloc(ctx: int, ra, dec, n: int, ra2, dec2, n2: int, bin_width_deg: float, nbins: int,
+                          out) -> None:
+    """acf_histogram with its scratch in the library's static 16 MiB device array (no allocation)."""
+    _check(ctx, load().acf_histogram_noalloc(ctx, _ptr(ra), _ptr(dec), int(n), _ptr(ra2), _ptr(dec2), int(n2),
+                                             float(bin_width_deg), int(nbins), _ptr(out)))
 
 
 def acf_omega(ctx: int, dd, dr, rr, nbins: int, n_d: int, n_r: int, omega) -> None:

@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -500,3 +501,87 @@ int acf_kernel_times(acf_ctx* c, float* ms, int32_t cap, int32_t* count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// acf_histogram_noalloc: the histogram with its scratch in a fixed, statically sized device
+// array instead of the context's workspace, for callers that cannot allocate device memory.
+//
+// The array below is what every GPU that loads this library reserves for it, until the process
+// exits. In host code its name is only a host-side stand-in for the device symbol; the device
+// address is looked up once per device with cudaGetSymbolAddress (with that device current) and
+// that address is what the kernels receive.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on `device` (which must be current); set up on first use.
+int noalloc_scratch(acf_ctx* c, int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return fail(c, ACF_ERR_UNSUPPORTED, "device %d out of range", device);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+    g_noalloc_ptr[device] = p;
+  }
+  *out = g_noalloc_ptr[device];
+  return ACF_OK;
+}
+
+}  // namespace
+
+extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2,
+                                     const float* dec2, int64_t n2, double w_deg, int32_t nbins, uint64_t* out) {
+  if (!c) return ACF_ERR_ARG;
+  if (n < 0) return fail(c, ACF_ERR_ARG, "n must be >= 0");
+  if (n > 2147483647ll || n2 > 2147483647ll) return fail(c, ACF_ERR_UNSUPPORTED, "catalogs are limited to 2^31-1 galaxies");
+  if (!out) return fail(c, ACF_ERR_ARG, "out is NULL");
+  const bool sym = (ra2 == nullptr && dec2 == nullptr) || (ra2 == ra && dec2 == dec && n2 == n);
+  if (!sym && n2 < 0) return fail(c, ACF_ERR_ARG, "n2 must be >= 0");
+  if (!sym && ((ra2 == nullptr) != (dec2 == nullptr))) return fail(c, ACF_ERR_ARG, "ra2 and dec2 must both be set");
+  const int64_t nj = sym ? n : n2;
+  Plan pl;
+  int rc = make_plan(c, w_deg, nbins, pl);
+  if (rc) return rc;
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  if (n == 0 || nj == 0) {
+    ACF_CUDA(c, cudaMemsetAsync(out, 0, sizeof(uint64_t) * (size_t)nbins, c->stream));
+    return ACF_OK;
+  }
+  if (!ra || !dec || (!sym && (!ra2 || !dec2))) return fail(c, ACF_ERR_ARG, "catalog pointer is NULL");
+  Launch L;
+  rc = plan_launch(c, pl, n, nj, sym, L);
+  if (rc) return rc;
+  const size_t b_vi = align256((size_t)n * sizeof(float4));
+  const size_t b_vj = sym ? 0 : align256((size_t)nj * sizeof(float4));
+  const size_t b_part = align256((size_t)L.grid * (size_t)nbins * sizeof(unsigned long long));
+  const size_t need = 256 + b_vi + b_vj + b_part;
+  if (need > kNoAllocScratchBytes)
+    return fail(c, ACF_ERR_UNSUPPORTED,
+                "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
+                "(16 bytes per galaxy of each catalog plus %lld blocks x nbins x 8 bytes); use acf_histogram",
+                need, kNoAllocScratchBytes, L.grid);
+  void* scratch = nullptr;
+  rc = noalloc_scratch(c, c->device, &scratch);
+  if (rc) return rc;
+  // Every byte the kernels read is rewritten first: the conversion kernel writes the vectors and
+  // zeroes the chunk ticket, and the pair kernel zeroes its partial rows before counting.
+  char* base = static_cast<char*>(scratch);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(base);
+  float4* vi = reinterpret_cast<float4*>(base + 256);
+  float4* vj = sym ? vi : reinterpret_cast<float4*>(base + 256 + b_vi);
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(base + 256 + b_vi + b_vj);
+  rc = launch_convert(c, ra, dec, n, vi, ticket);
+  if (rc) return rc;
+  if (!sym) {
+    rc = launch_convert(c, ra2, dec2, nj, vj, nullptr);
+    if (rc) return rc;
+  }
+  return histogram_vectors(c, vi, n, vj, nj, sym, pl, L, part, ticket, out);
+}

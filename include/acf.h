@@ -87,6 +87,28 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
                   int64_t n2, double bin_width_deg, int32_t nbins, uint64_t *out);
 
 /*
+ * acf_histogram without any device allocation. The page has no counterpart: this is a service of
+ * this library for callers that cannot call cudaMalloc, such as code whose process hands all
+ * device memory to another allocator (a framework's caching allocator) or latency-critical code
+ * that cannot afford the implicit device synchronisation and driver work of an allocation.
+ *
+ * Same arguments, semantics and results as acf_histogram, but its scratch (unit vectors, block
+ * rows, the chunk counter) lives in one file-scope device array of 16 MiB that the library
+ * reserves on every GPU that loads it, until the process exits. It calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *   - Limit: 256 + 16*n (+ 16*n2 for a cross-correlation) + (blocks * nbins * 8) bytes must fit in
+ *     16 MiB, blocks being the persistent grid (304 on a 152-SM GPU); larger requests return
+ *     ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need ~5 MB.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents; the
+ *     kernels re-initialise everything they read. Calls whose work overlaps on the GPU (other
+ *     streams, other host threads or contexts) race on it and must be serialised by the caller.
+ */
+int acf_histogram_noalloc(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, const float *ra2,
+                          const float *dec2, int64_t n2, double bin_width_deg, int32_t nbins, uint64_t *out);
+
+/*
  * Landy-Szalay estimator per bin (section "The problem"), computed in fp64 on the device:
  *     omega_k = (DD_k/N_dd - 2 DR_k/N_dr + RR_k/N_rr) / (RR_k/N_rr),
  * N_dd = n_d^2, N_dr = n_d n_r, N_rr = n_r^2 (with n_d == n_r this is (DD - 2DR + RR)/RR).
