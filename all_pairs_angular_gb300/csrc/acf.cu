@@ -21,12 +21,10 @@ using namespace acf;
 
 namespace {
 
-#ifndef ACF_K
-#define ACF_K 5
-#endif
-constexpr int kK = ACF_K;                      // i-galaxies per thread
+constexpr int kK = 4;                          // i-galaxies per thread (32 * kK == kJT)
 constexpr int kMaxEntries = 49152;             // histogram entries a block can hold (192 KB)
-constexpr size_t kTileBytes = 2 * kJT * sizeof(float4);
+constexpr size_t kWarpTileBytes = 2 * kJT * sizeof(float4);  // one warp's double-buffered j-tile
+constexpr size_t kMaxSmem = 232448;                             // opt-in dynamic shared memory per block
 constexpr int kMaxTimed = 4096;
 
 struct Plan {
@@ -54,6 +52,7 @@ struct acf_ctx {
   Workspace io;     // device staging for acf_correlate_host
   // options
   int opt_threads = 0, opt_ctas = 0, opt_method = kChordPoly, opt_layout = 0, opt_timing = 0;
+  long long opt_units_per_launch = 0;
   // info about the last histogram
   long long info_grid = 0, info_threads = 0, info_ctas = 0, info_chunks = 0, info_layout = 0, info_map = 0,
             info_entries = 0, info_smem = 0, info_pairs = 0, info_flush = 0;
@@ -138,17 +137,23 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     bp.magic = 8388608.0f;
     bp.clamp_c = (float)(entries - 1);
   }
-  // layout: 32 lane-private copies when they fit comfortably, else one block-shared copy
-  const size_t lane_bytes = kTileBytes + (size_t)bp.entries * 32 * 4;
+  // Shared memory = every warp's double-buffered j-tile (4 KB per warp) + the histogram: 32
+  // lane-private copies when they fit beside the tiles of at least 16 warps, else one block-shared
+  // copy. 1024 threads (32 warps, one block per SM) when everything fits, else 512.
+  const size_t lane_hist = (size_t)bp.entries * 32 * 4;
+  const size_t block_hist = (size_t)((bp.entries * 4 + 15) & ~15);
   int layout = c->opt_layout;
-  if (layout == 0) layout = (lane_bytes <= 200 * 1024) ? kLane : kBlock;
-  if (layout == kLane && lane_bytes > 227 * 1024)
-    return fail(c, ACF_ERR_UNSUPPORTED, "lane-private layout needs %zu bytes of shared memory", lane_bytes);
+  if (layout == 0) layout = (lane_hist + 16 * kWarpTileBytes <= kMaxSmem) ? kLane : kBlock;
+  const size_t hist_bytes = (layout == kLane) ? lane_hist : block_hist;
+  int threads = c->opt_threads;
+  if (threads == 0) threads = (hist_bytes + 32 * kWarpTileBytes <= kMaxSmem) ? 1024 : 512;
+  if (threads != 512 && threads != 1024) return fail(c, ACF_ERR_ARG, "threads must be 512 or 1024");
   pl.layout = layout;
-  pl.smem = (layout == kLane) ? lane_bytes : kTileBytes + (size_t)((bp.entries * 4 + 15) & ~15);
-  // 512 threads at <= 64 registers: two resident blocks give 32 warps per SM
-  pl.threads = c->opt_threads ? c->opt_threads : 512;
-  if (pl.threads != 256 && pl.threads != 512) return fail(c, ACF_ERR_ARG, "threads must be 256 or 512");
+  pl.threads = threads;
+  pl.smem = hist_bytes + (size_t)(threads / 32) * kWarpTileBytes;
+  if (pl.smem > kMaxSmem)
+    return fail(c, ACF_ERR_UNSUPPORTED, "%s histogram of %d entries with %d threads needs %zu bytes of shared memory",
+                layout == kLane ? "lane-private" : "block-shared", bp.entries, threads, pl.smem);
   return ACF_OK;
 }
 
@@ -157,27 +162,82 @@ typedef void (*PairKernelFn)(const PairParams);
 PairKernelFn pick_kernel(const Plan& pl) {
 #define ACF_PICK(T, L, M, X) \
   if (pl.threads == T && pl.layout == L && pl.map == M && pl.method == X) return pair_kernel<kK, T, L, M, X>;
-  ACF_PICK(256, kLane, kMirror, kChordPoly)
-  ACF_PICK(256, kLane, kClamp, kChordPoly)
-  ACF_PICK(256, kBlock, kMirror, kChordPoly)
-  ACF_PICK(256, kBlock, kClamp, kChordPoly)
+  ACF_PICK(1024, kLane, kMirror, kChordPoly)
+  ACF_PICK(1024, kLane, kClamp, kChordPoly)
+  ACF_PICK(1024, kBlock, kMirror, kChordPoly)
+  ACF_PICK(1024, kBlock, kClamp, kChordPoly)
   ACF_PICK(512, kLane, kMirror, kChordPoly)
   ACF_PICK(512, kLane, kClamp, kChordPoly)
   ACF_PICK(512, kBlock, kMirror, kChordPoly)
   ACF_PICK(512, kBlock, kClamp, kChordPoly)
-  ACF_PICK(256, kLane, kClamp, kDotAcos)
-  ACF_PICK(256, kBlock, kClamp, kDotAcos)
+  ACF_PICK(1024, kLane, kClamp, kDotAcos)
+  ACF_PICK(1024, kBlock, kClamp, kDotAcos)
   ACF_PICK(512, kLane, kClamp, kDotAcos)
   ACF_PICK(512, kBlock, kClamp, kDotAcos)
 #undef ACF_PICK
   return nullptr;
 }
 
-int launch_convert(acf_ctx* c, const float* ra, const float* dec, long long n, float4* v, unsigned int* ticket) {
-  if (n <= 0) return ACF_OK;
+// Device buffers of one histogram call, carved out of one scratch region.
+struct CatBufs {
+  float4* v_in = nullptr;    // unit vectors in input order
+  unsigned int* key = nullptr;
+  float4* v = nullptr;       // unit vectors in spatial order
+  int* perm = nullptr;       // input index of each sorted slot
+  float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
+  float4* cap128 = nullptr;  // caps of 128-galaxy chunks
+};
+struct Scratch {
+  unsigned int* ticket = nullptr;      // chunk dispenser (first word of a zeroed block)
+  unsigned int* cell_count = nullptr;  // kCells counters, zeroed with the ticket
+  unsigned int* cursor = nullptr;      // kCells
+  CatBufs a, b;                        // b only for cross-correlations
+  unsigned long long* partial = nullptr;
+};
+
+// Lay the buffers out from `base` (nullptr: only measure). Returns the bytes needed.
+size_t carve(char* base, long long n, long long nj, bool sym, long long grid, int nbins, Scratch* s) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  auto cat = [&](long long m, CatBufs& cb) {
+    const long long ch = (m + 127) / 128;
+    cb.v_in = reinterpret_cast<float4*>(take((size_t)m * 16));
+    cb.key = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
+    cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
+    cb.perm = reinterpret_cast<int*>(take((size_t)m * 4));
+    cb.cap32 = reinterpret_cast<float4*>(take((size_t)ch * 4 * 16));
+    cb.cap128 = reinterpret_cast<float4*>(take((size_t)ch * 16));
+  };
+  Scratch t;
+  Scratch& r = s ? *s : t;
+  char* head = take(256 + (size_t)kCells * 4);  // ticket, then the cell counters
+  r.ticket = reinterpret_cast<unsigned int*>(head);
+  r.cell_count = head ? reinterpret_cast<unsigned int*>(head + 256) : nullptr;
+  r.cursor = reinterpret_cast<unsigned int*>(take((size_t)kCells * 4));
+  cat(n, r.a);
+  if (!sym) cat(nj, r.b);
+  r.partial = reinterpret_cast<unsigned long long*>(take((size_t)grid * (size_t)nbins * 8));
+  return off;
+}
+
+// Unit vectors of one catalog in spatial order, with their caps. The cell counters start at zero
+// (cleared together with the chunk ticket by the caller) and are cleared again here after use.
+int prepare_catalog(acf_ctx* c, const float* ra, const float* dec, long long n, const Scratch& s, const CatBufs& cb) {
   const int threads = 256;
   const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 16);
-  convert_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, v, ticket);
+  ACF_CUDA(c, cudaMemsetAsync(s.cell_count, 0, (size_t)kCells * 4, c->stream));
+  prep_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, cb.v_in, cb.key, s.cell_count);
+  ACF_CUDA(c, cudaGetLastError());
+  scan_kernel<<<1, 1024, 0, c->stream>>>(s.cell_count, s.cursor);
+  ACF_CUDA(c, cudaGetLastError());
+  scatter_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(cb.v_in, cb.key, n, s.cursor, cb.v, cb.perm);
+  ACF_CUDA(c, cudaGetLastError());
+  const long long warps = (n + 127) / 128;
+  caps_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, c->stream>>>(cb.v, n, cb.cap32, cb.cap128);
   ACF_CUDA(c, cudaGetLastError());
   return ACF_OK;
 }
@@ -185,10 +245,10 @@ int launch_convert(acf_ctx* c, const float* ra, const float* dec, long long n, f
 struct Launch {
   PairKernelFn fn = nullptr;
   int ctas = 0;
-  long long grid = 0, chunks = 0, rows = 0, cj = 0, step = 0;
+  long long grid = 0, units = 0, rows = 0, cols = 0, per_launch = 0;
 };
 
-// Persistent grid: every SM gets as many blocks as can be resident, never more blocks than chunks.
+// Persistent grid: every SM gets as many blocks as can be resident (one, normally).
 int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym, Launch& L) {
   L.fn = pick_kernel(pl);
   if (!L.fn) return fail(c, ACF_ERR_UNSUPPORTED, "no kernel for this plan");
@@ -197,46 +257,53 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
   ACF_CUDA(c, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, L.fn, pl.threads, pl.smem));
   if (occ <= 0) return fail(c, ACF_ERR_UNSUPPORTED, "pair kernel cannot be resident (smem %zu)", pl.smem);
   L.ctas = c->opt_ctas > 0 ? std::min(c->opt_ctas, occ) : occ;
-  const long long bi = (long long)pl.threads * kK;
-  L.rows = (ni + bi - 1) / bi;
-  L.cj = (nj + kJT - 1) / kJT;
-  L.step = bi / kJT;
-  L.chunks = sym ? L.rows * L.cj - L.step * L.rows * (L.rows - 1) / 2 : L.rows * L.cj;
-  L.grid = std::min<long long>((long long)c->num_sms * L.ctas, std::max<long long>(L.chunks, 1));
-  // the kernel hands out chunks with a 32-bit ticket that may run past the end by 2 per block
-  if (L.chunks + 2 * L.grid + 2 >= 4294967295ll)
-    return fail(c, ACF_ERR_UNSUPPORTED, "%lld chunks exceed the 32-bit chunk dispenser", L.chunks);
+  L.rows = (ni + kJT - 1) / kJT;
+  L.cols = (nj + kJT - 1) / kJT;
+  L.units = sym ? L.rows * L.cols - L.rows * (L.rows - 1) / 2 : L.rows * L.cols;
+  L.grid = std::min<long long>((long long)c->num_sms * L.ctas, std::max<long long>(L.units, 1));
+  // One unit adds at most kK*kJT*inc to a lane-private 32-bit counter (32 times that to a
+  // block-shared one). Even if one block took every unit of a launch, no counter may wrap, so
+  // large problems are split into launches that add into the same block rows.
+  const double inc = sym ? 2.0 : 1.0;
+  const double per_unit = (pl.layout == kLane ? 1.0 : 32.0) * kK * kJT * inc;
+  L.per_launch = (long long)std::floor(4294967295.0 / per_unit);
+  if (c->opt_units_per_launch > 0) L.per_launch = std::min(L.per_launch, c->opt_units_per_launch);
   return ACF_OK;
 }
 
-// The pair kernel and merge for vectors already on the device. partial holds L.grid rows.
-int histogram_vectors(acf_ctx* c, const float4* vi, long long ni, const float4* vj, long long nj, bool sym,
+// The pair kernel (one or more launches) and the merge for prepared catalogs.
+int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs& cj, long long nj, bool sym,
                       const Plan& pl, const Launch& L, unsigned long long* partial, unsigned int* ticket,
                       uint64_t* out) {
   PairParams p;
-  p.vi = vi;
-  p.vj = vj;
+  p.vi = ci.v;
+  p.vj = cj.v;
+  p.icap32 = ci.cap32;
+  p.jcap32 = cj.cap32;
+  p.igroups = (ni + 31) / 32;
   p.ni = ni;
   p.nj = nj;
-  p.total_chunks = L.chunks;
-  p.chunks_per_row = L.cj;
   p.rows = L.rows;
+  p.cols = L.cols;
   p.sym = sym ? 1 : 0;
-  p.row_step = (int)L.step;
   p.inc = sym ? 2u : 1u;
-  // the largest number of increments one shared 32-bit word can take per chunk
-  const double per_chunk = (pl.layout == kLane ? (double)(pl.threads / 32) : (double)pl.threads) * kK * kJT * p.inc;
-  p.flush_every = (unsigned)std::max(1.0, std::floor(4294967295.0 / per_chunk));
   p.partial = partial;
   p.ticket = ticket;
   p.bp = pl.bp;
-  const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
-  if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
-  L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
-  ACF_CUDA(c, cudaGetLastError());
-  if (timed) {
-    ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
-    c->ev_used += 2;
+  int launches = 0;
+  for (long long ub = 0; ub < L.units; ub += L.per_launch, ++launches) {
+    p.unit_begin = ub;
+    p.unit_end = std::min(L.units, ub + L.per_launch);
+    p.accumulate = ub > 0 ? 1 : 0;
+    if (ub > 0) ACF_CUDA(c, cudaMemsetAsync(ticket, 0, 4, c->stream));
+    const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
+    if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
+    L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
+    ACF_CUDA(c, cudaGetLastError());
+    if (timed) {
+      ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
+      c->ev_used += 2;
+    }
   }
 #ifdef ACF_DEBUG_BOUNDS
   {
@@ -260,14 +327,27 @@ int histogram_vectors(acf_ctx* c, const float4* vi, long long ni, const float4* 
   c->info_grid = L.grid;
   c->info_threads = pl.threads;
   c->info_ctas = L.ctas;
-  c->info_chunks = L.chunks;
+  c->info_chunks = L.units;
   c->info_layout = pl.layout;
   c->info_map = pl.map;
   c->info_entries = pl.bp.entries;
   c->info_smem = (long long)pl.smem;
   c->info_pairs = sym ? ni * (ni - 1) / 2 : ni * nj;
-  c->info_flush = p.flush_every;
+  c->info_flush = launches;
   return ACF_OK;
+}
+
+// Everything after argument checks and workspace layout: prepare the catalogs, pair, merge.
+int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, const float* ra2, const float* dec2,
+                 long long nj, bool sym, const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
+  ACF_CUDA(c, cudaMemsetAsync(sc.ticket, 0, 4, c->stream));
+  int rc = prepare_catalog(c, ra, dec, n, sc, sc.a);
+  if (rc) return rc;
+  if (!sym) {
+    rc = prepare_catalog(c, ra2, dec2, nj, sc, sc.b);
+    if (rc) return rc;
+  }
+  return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc.partial, sc.ticket, out);
 }
 
 int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2, const float* dec2,
@@ -292,23 +372,11 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const size_t b_vi = align256((size_t)n * sizeof(float4));
-  const size_t b_vj = sym ? 0 : align256((size_t)nj * sizeof(float4));
-  const size_t b_part = align256((size_t)L.grid * (size_t)nbins * sizeof(unsigned long long));
-  rc = ensure(c, c->ws, 256 + b_vi + b_vj + b_part);
+  rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, nullptr));
   if (rc) return rc;
-  char* base = static_cast<char*>(c->ws.ptr);
-  unsigned int* ticket = reinterpret_cast<unsigned int*>(base);
-  float4* vi = reinterpret_cast<float4*>(base + 256);
-  float4* vj = sym ? vi : reinterpret_cast<float4*>(base + 256 + b_vi);
-  unsigned long long* part = reinterpret_cast<unsigned long long*>(base + 256 + b_vi + b_vj);
-  rc = launch_convert(c, ra, dec, n, vi, ticket);
-  if (rc) return rc;
-  if (!sym) {
-    rc = launch_convert(c, ra2, dec2, nj, vj, nullptr);
-    if (rc) return rc;
-  }
-  return histogram_vectors(c, vi, n, vj, nj, sym, pl, L, part, ticket, out);
+  Scratch sc;
+  carve(static_cast<char*>(c->ws.ptr), n, nj, sym, L.grid, nbins, &sc);
+  return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }
 
 }  // namespace
@@ -444,7 +512,7 @@ int acf_pair_bins(acf_ctx* c, const float* ra1, const float* dec1, const float* 
 int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   if (!c || !key) return ACF_ERR_ARG;
   if (!strcmp(key, "threads")) {
-    if (v != 0 && v != 256 && v != 512) return fail(c, ACF_ERR_ARG, "threads must be 0, 256 or 512");
+    if (v != 0 && v != 512 && v != 1024) return fail(c, ACF_ERR_ARG, "threads must be 0, 512 or 1024");
     c->opt_threads = (int)v;
   } else if (!strcmp(key, "ctas_per_sm")) {
     if (v < 0 || v > 8) return fail(c, ACF_ERR_ARG, "ctas_per_sm must be 0..8");
@@ -455,6 +523,9 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "layout")) {
     if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "layout must be 0, 1 or 2");
     c->opt_layout = (int)v;
+  } else if (!strcmp(key, "units_per_launch")) {
+    if (v < 0) return fail(c, ACF_ERR_ARG, "units_per_launch must be >= 0");
+    c->opt_units_per_launch = v;
   } else if (!strcmp(key, "kernel_timing")) {
     c->opt_timing = v ? 1 : 0;
     if (c->opt_timing && c->ev.empty()) {
@@ -475,9 +546,9 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
     const char* k;
     long long val;
   } t[] = {{"grid", c->info_grid},       {"threads", c->info_threads},   {"ctas_per_sm", c->info_ctas},
-           {"chunks", c->info_chunks},   {"layout", c->info_layout},     {"bin_map", c->info_map},
+           {"units", c->info_chunks},   {"layout", c->info_layout},     {"bin_map", c->info_map},
            {"hist_entries", c->info_entries}, {"smem_bytes", c->info_smem}, {"pairs_evaluated", c->info_pairs},
-           {"flush_every", c->info_flush}};
+           {"launches", c->info_flush}};
   for (auto& e : t)
     if (!strcmp(e.k, key)) {
       *v = e.val;
@@ -558,30 +629,18 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const size_t b_vi = align256((size_t)n * sizeof(float4));
-  const size_t b_vj = sym ? 0 : align256((size_t)nj * sizeof(float4));
-  const size_t b_part = align256((size_t)L.grid * (size_t)nbins * sizeof(unsigned long long));
-  const size_t need = 256 + b_vi + b_vj + b_part;
+  const size_t need = carve(nullptr, n, nj, sym, L.grid, nbins, nullptr);
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
-                "(16 bytes per galaxy of each catalog plus %lld blocks x nbins x 8 bytes); use acf_histogram",
+                "(about 41 bytes per galaxy of each catalog plus %lld blocks x nbins x 8 bytes); use acf_histogram",
                 need, kNoAllocScratchBytes, L.grid);
   void* scratch = nullptr;
   rc = noalloc_scratch(c, c->device, &scratch);
   if (rc) return rc;
-  // Every byte the kernels read is rewritten first: the conversion kernel writes the vectors and
-  // zeroes the chunk ticket, and the pair kernel zeroes its partial rows before counting.
-  char* base = static_cast<char*>(scratch);
-  unsigned int* ticket = reinterpret_cast<unsigned int*>(base);
-  float4* vi = reinterpret_cast<float4*>(base + 256);
-  float4* vj = sym ? vi : reinterpret_cast<float4*>(base + 256 + b_vi);
-  unsigned long long* part = reinterpret_cast<unsigned long long*>(base + 256 + b_vi + b_vj);
-  rc = launch_convert(c, ra, dec, n, vi, ticket);
-  if (rc) return rc;
-  if (!sym) {
-    rc = launch_convert(c, ra2, dec2, nj, vj, nullptr);
-    if (rc) return rc;
-  }
-  return histogram_vectors(c, vi, n, vj, nj, sym, pl, L, part, ticket, out);
+  // Every byte the kernels read is rewritten first: the ticket and cell counters are cleared,
+  // the preparation kernels write the vectors and caps, and the pair kernel zeroes its rows.
+  Scratch sc;
+  carve(static_cast<char*>(scratch), n, nj, sym, L.grid, nbins, &sc);
+  return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }

@@ -62,15 +62,18 @@ struct PairParams {
   const float4* __restrict__ vi;
   const float4* __restrict__ vj;
   long long ni, nj;
-  long long total_chunks;
-  long long chunks_per_row;    // CJ = ceil(nj / kJT)
-  long long rows;              // TI = ceil(ni / BI)
+  long long rows;              // i-sets of kJT galaxies: ceil(ni / kJT)
+  long long cols;              // j-chunks of kJT galaxies: ceil(nj / kJT)
+  long long unit_begin;        // this launch handles units [unit_begin, unit_end)
+  long long unit_end;
   int sym;                     // 1: pairs j > i of one catalog, counted twice
-  int row_step;                // BI / kJT (sym rows start at ib * row_step)
+  int accumulate;              // 0: zero the partial rows first; 1: add to them (later launches)
   unsigned int inc;            // 2 (sym) or 1 (cross)
-  unsigned int flush_every;    // chunks between flushes of the 32-bit shared counters
   unsigned long long* partial; // [gridDim.x][nbins]
-  unsigned int* ticket;        // chunk dispenser; zero before the launch
+  unsigned int* ticket;        // unit dispenser; zero before the launch
+  const float4* __restrict__ icap32;   // caps of 32-galaxy groups of the i catalog (sorted order)
+  const float4* __restrict__ jcap32;   // caps of 32-galaxy groups of the j catalog
+  long long igroups;                   // number of 32-galaxy groups of the i catalog
   BinParams bp;
 };
 
@@ -160,12 +163,156 @@ __device__ __forceinline__ float4 radec_to_unit(float ra_arcmin, float dec_arcmi
   return make_float4((float)(cd * ca), (float)(cd * sa), (float)sd, 0.0f);
 }
 
-// Also zeroes the pair kernel's chunk dispenser, which the next pair launch on the stream uses.
-__global__ void convert_kernel(const float* __restrict__ ra, const float* __restrict__ dec, long long n,
-                               float4* __restrict__ v, unsigned int* __restrict__ ticket) {
-  if (blockIdx.x == 0 && threadIdx.x == 0 && ticket) *ticket = 0u;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    v[i] = radec_to_unit(ra[i], dec[i]);
+// ------------------------------------------------------------------ spatial order and caps
+//
+// Catalogs are put in a spatial order before pairing: galaxies sorted by cell of a cube map
+// (6 faces x 64 x 64 cells, Morton order within a face). A warp's i-galaxies and a j-chunk then
+// each cover a small patch of sky, bounded by a "cap" (centre, angular radius). From two caps
+// the kernel knows when every pair of a (warp, chunk) is surely below or surely above 90
+// degrees, and drops the per-pair sign decision there. The order changes no result: every
+// pair's bin is computed by the same arithmetic whichever path evaluates it.
+
+constexpr int kFaceCells = 64;
+constexpr int kCells = 6 * kFaceCells * kFaceCells;
+
+__device__ __forceinline__ unsigned int spread_bits6(unsigned int x) {  // 6 bits -> even positions
+  x &= 63u;
+  x = (x | (x << 4)) & 0x30Fu;
+  x = (x | (x << 2)) & 0x333u;
+  x = (x | (x << 1)) & 0x555u;
+  return x;
+}
+
+__device__ __forceinline__ unsigned int cell_of(double x, double y, double z) {
+  const double ax = fabs(x), ay = fabs(y), az = fabs(z);
+  int face;
+  double u, v, m;
+  if (ax >= ay && ax >= az) { face = x >= 0 ? 0 : 1; m = ax; u = y; v = z; }
+  else if (ay >= az) { face = y >= 0 ? 2 : 3; m = ay; u = x; v = z; }
+  else { face = z >= 0 ? 4 : 5; m = az; u = x; v = y; }
+  int iu = (int)((u / m + 1.0) * 0.5 * kFaceCells);
+  int iv = (int)((v / m + 1.0) * 0.5 * kFaceCells);
+  iu = iu < 0 ? 0 : (iu >= kFaceCells ? kFaceCells - 1 : iu);
+  iv = iv < 0 ? 0 : (iv >= kFaceCells ? kFaceCells - 1 : iv);
+  return (unsigned int)face * (kFaceCells * kFaceCells) + (spread_bits6(iu) | (spread_bits6(iv) << 1));
+}
+
+// Unit vectors in input order plus each galaxy's cell, counted per cell.
+__global__ void prep_kernel(const float* __restrict__ ra, const float* __restrict__ dec, long long n,
+                            float4* __restrict__ v, unsigned int* __restrict__ key,
+                            unsigned int* __restrict__ cell_count) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const double k = 3.14159265358979323846 / 10800.0;
+    double a = (double)ra[i] * k, d = (double)dec[i] * k;
+    if (!isfinite(a) || !isfinite(d)) { a = 0.0; d = 0.0; }
+    double sa, ca, sd, cd;
+    sincos(a, &sa, &ca);
+    sincos(d, &sd, &cd);
+    const double x = cd * ca, y = cd * sa, z = sd;
+    v[i] = make_float4((float)x, (float)y, (float)z, 0.0f);
+    const unsigned int c = cell_of(x, y, z);
+    key[i] = c;
+    atomicAdd(cell_count + c, 1u);
+  }
+}
+
+// Exclusive prefix sum of the cell counts (one block of 1024 threads).
+__global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restrict__ cell_count,
+                                                     unsigned int* __restrict__ cursor) {
+  constexpr int PER = (kCells + 1023) / 1024;
+  __shared__ unsigned int part[1024];
+  const int t = threadIdx.x;
+  unsigned int loc[PER];
+  unsigned int s = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int c = t * PER + e;
+    loc[e] = c < kCells ? cell_count[c] : 0u;
+    s += loc[e];
+  }
+  part[t] = s;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan of the thread sums
+    const unsigned int add = t >= off ? part[t - off] : 0u;
+    __syncthreads();
+    part[t] += add;
+    __syncthreads();
+  }
+  unsigned int run = part[t] - s;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int c = t * PER + e;
+    if (c < kCells) cursor[c] = run;
+    run += loc[e];
+  }
+}
+
+// Counting-sort scatter: sorted vectors plus, per sorted slot, the input index.
+__global__ void scatter_kernel(const float4* __restrict__ v_in, const unsigned int* __restrict__ key, long long n,
+                               unsigned int* __restrict__ cursor, float4* __restrict__ v_out, int* __restrict__ perm) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const unsigned int pos = atomicAdd(cursor + key[i], 1u);
+    if (ACF_CHECK(pos < (unsigned long long)n, 5, i, pos)) {
+      v_out[pos] = v_in[i];
+      perm[pos] = (int)i;
+    }
+  }
+}
+
+// Angular radius, with a small safety margin, of the chord-distance sq = |c - v|^2.
+__device__ __forceinline__ float chord_to_angle(float sq) { return 2.0f * asinf(fminf(sqrtf(sq) * 0.5f, 1.0f)); }
+constexpr float kCapMargin = 2e-5f;
+
+// One warp per 128 sorted galaxies: the cap of each 32-galaxy group and of the whole chunk.
+// Empty groups get radius 4 (> pi), which no decision can use.
+__global__ void caps_kernel(const float4* __restrict__ v, long long n, float4* __restrict__ cap32,
+                            float4* __restrict__ cap128) {
+  const int lane = threadIdx.x & 31;
+  const long long chunk = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nchunks = (n + 127) / 128;
+  if (chunk >= nchunks) return;
+  float4 m[4];
+  bool ok[4];
+  float tx = 0.f, ty = 0.f, tz = 0.f;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const long long i = chunk * 128 + g * 32 + lane;
+    ok[g] = i < n;
+    m[g] = ok[g] ? v[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    tx += m[g].x; ty += m[g].y; tz += m[g].z;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tx += __shfl_xor_sync(0xffffffffu, tx, o);
+    ty += __shfl_xor_sync(0xffffffffu, ty, o);
+    tz += __shfl_xor_sync(0xffffffffu, tz, o);
+  }
+  const float tn = rsqrtf(fmaxf(tx * tx + ty * ty + tz * tz, 1e-30f));
+  tx *= tn; ty *= tn; tz *= tn;
+  float tmax = 0.f;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float gx = m[g].x, gy = m[g].y, gz = m[g].z;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gx += __shfl_xor_sync(0xffffffffu, gx, o);
+      gy += __shfl_xor_sync(0xffffffffu, gy, o);
+      gz += __shfl_xor_sync(0xffffffffu, gz, o);
+    }
+    const float gn = rsqrtf(fmaxf(gx * gx + gy * gy + gz * gz, 1e-30f));
+    gx *= gn; gy *= gn; gz *= gn;
+    float dx = gx - m[g].x, dy = gy - m[g].y, dz = gz - m[g].z;
+    float sq = ok[g] ? dx * dx + dy * dy + dz * dz : 0.f;
+    dx = tx - m[g].x; dy = ty - m[g].y; dz = tz - m[g].z;
+    tmax = fmaxf(tmax, ok[g] ? dx * dx + dy * dy + dz * dz : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq = fmaxf(sq, __shfl_xor_sync(0xffffffffu, sq, o));
+    const bool any = __any_sync(0xffffffffu, ok[g]);
+    if (lane == 0) cap32[chunk * 4 + g] = make_float4(gx, gy, gz, any ? chord_to_angle(sq) + kCapMargin : 4.0f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  if (lane == 0) cap128[chunk] = make_float4(tx, ty, tz, chord_to_angle(tmax) + kCapMargin);
 }
 
 // ------------------------------------------------------------------ bin index of one pair
@@ -228,27 +375,98 @@ __device__ __forceinline__ int entry_to_bin(int e, const BinParams& bp) {
   return k > bp.nbins - 1 ? bp.nbins - 1 : k;
 }
 
+// The same code as pair_code<MAP, kChordPoly> for a pair whose sign(u.v) is known in advance:
+// SIGN = +1 (separation below 90 degrees) or -1 (above). Bit for bit the general code takes these
+// steps for such a pair (u - v and u + v round the same way as fma(-1, v, u) and fma(1, v, u)),
+// minus the dot product and the two sign-bit operations.
+template <int MAP, int SIGN>
+__device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, float xj, float yj, float zj,
+                                                 const BinParams& bp) {
+  const float dx = SIGN > 0 ? xi - xj : xi + xj;
+  const float dy = SIGN > 0 ? yi - yj : yi + yj;
+  const float dz = SIGN > 0 ? zi - zj : zi + zj;
+  const float q = fmaf(dz, dz, fmaf(dy, dy, fmaf(dx, dx, 1e-30f)));
+  float p = fmaf(kP7, q, kP6);
+  p = fmaf(p, q, kP5);
+  p = fmaf(p, q, kP4);
+  p = fmaf(p, q, kP3);
+  p = fmaf(p, q, kP2);
+  p = fmaf(p, q, kP1);
+  p = fmaf(p, q, kP0);
+  const float th = sqrt_approx(p * q);
+  if (MAP == kMirror) {
+    return fma_rz(SIGN > 0 ? th : -th, bp.inv_w, bp.magic);
+  } else {
+    const float t = (SIGN > 0 ? th : 3.14159265358979323846f - th) * bp.inv_w;
+    return add_rz(fminf(t, bp.clamp_c), kMagic);
+  }
+}
+
+// Cap of K consecutive 32-galaxy groups: centre = normalised sum of the group centres, radius =
+// the largest (distance to a group centre + that group's radius). Empty groups are skipped.
+template <int K>
+__device__ __forceinline__ float4 union_caps(const float4* __restrict__ cap32, long long g0, long long ngroups) {
+  float cx = 0.f, cy = 0.f, cz = 0.f;
+  float4 c[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    c[k] = (g0 + k < ngroups) ? __ldg(cap32 + g0 + k) : make_float4(1.f, 0.f, 0.f, 4.0f);
+    if (c[k].w <= 3.2f) { cx += c[k].x; cy += c[k].y; cz += c[k].z; }
+  }
+  const float nn = rsqrtf(fmaxf(cx * cx + cy * cy + cz * cz, 1e-30f));
+  cx *= nn; cy *= nn; cz *= nn;
+  float r = 0.f;
+  bool any = false;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if (c[k].w <= 3.2f) {
+      const float dx = cx - c[k].x, dy = cy - c[k].y, dz = cz - c[k].z;
+      r = fmaxf(r, chord_to_angle(dx * dx + dy * dy + dz * dz) + c[k].w);
+      any = true;
+    }
+  }
+  return make_float4(cx, cy, cz, any ? r + kCapMargin : 4.0f);
+}
+
+enum Path { kGeneral = 0, kBelow90 = 1, kAbove90 = 2 };
+template <int P>
+struct PathTag {
+  static constexpr int value = P;
+};
+
+// Which loop a (warp, j-group) may use: every pair surely below 90 degrees, surely above, or
+// mixed. Two caps at centre angle tc and radii ra, rb hold only separations in
+// [tc - ra - rb, tc + ra + rb]; all are below 90 degrees iff cos tc > sin(ra + rb) and all above
+// iff cos tc < -sin(ra + rb). __sinf is accurate to ~1e-6 here and the margins cover it.
+__device__ __forceinline__ int choose_path(float4 a, float4 b) {
+  const float dot = a.x * b.x + a.y * b.y + a.z * b.z;
+  const float r = a.w + b.w + 1e-4f;
+  if (r >= 1.5f) return kGeneral;
+  const float sr = __sinf(r) + 1e-5f;
+  if (dot > sr) return kBelow90;
+  if (dot < -sr) return kAbove90;
+  return kGeneral;
+}
+
 // ------------------------------------------------------------------ pair kernel
 
-// Map chunk q to (row ib, chunk column jc). The host guarantees chunk counts below 2^32 and
-// catalogs below 2^31 galaxies, so 32-bit indices suffice.
-__device__ __forceinline__ void chunk_coords(const PairParams& p, unsigned int q, int& ib, int& jc) {
-  const long long cj = p.chunks_per_row;
+// Map unit u to (i-set row r, j-chunk column c). For DD/RR row r holds columns r .. cols-1 and
+// starts at S(r) = r*cols - r*(r-1)/2.
+__device__ __forceinline__ void unit_coords(const PairParams& p, long long u, int& r, int& c) {
+  const long long cj = p.cols;
   if (!p.sym) {
-    ib = (int)(q / (unsigned long long)cj);
-    jc = (int)(q - (unsigned long long)ib * cj);
+    r = (int)(u / cj);
+    c = (int)(u - (long long)r * cj);
     return;
   }
-  // row r starts at S(r) = r*CJ - R*r*(r-1)/2; largest r with S(r) <= q
   long long lo = 0, hi = p.rows - 1;
   while (lo < hi) {
     const long long mid = (lo + hi + 1) >> 1;
-    const long long s = mid * cj - (long long)p.row_step * mid * (mid - 1) / 2;
-    if (s <= (long long)q) lo = mid;
+    if (mid * cj - mid * (mid - 1) / 2 <= u) lo = mid;
     else hi = mid - 1;
   }
-  ib = (int)lo;
-  jc = (int)(lo * p.row_step + ((long long)q - (lo * cj - (long long)p.row_step * lo * (lo - 1) / 2)));
+  r = (int)lo;
+  c = (int)(lo + (u - (lo * cj - lo * (lo - 1) / 2)));
 }
 
 template <int K, int THREADS, int LAYOUT, int MAP, int METHOD>
@@ -274,110 +492,124 @@ __device__ __forceinline__ void flush_hist(const PairParams& p, uint32_t* hist, 
   }
 }
 
-// One chunk = the block's BI = THREADS*K i-galaxies (K per thread, in registers) against kJT
-// j-galaxies (in shared memory). Chunks are handed out by an atomic ticket so that uneven chunk
-// costs (ragged tails, diagonal chunks of DD/RR) spread over all blocks; the ticket two chunks
-// ahead is fetched while the current chunk is computed.
+// Work unit = one warp's i-set (kJT = 32*K spatially consecutive i-galaxies, K per lane, in
+// registers) against one j-chunk of kJT galaxies (in the warp's own shared-memory tile). Warps
+// take units from a global ticket independently and never wait for each other inside the loop:
+// each streams its own double-buffered j-tiles with cp.async and synchronises only with
+// __syncwarp. All warps of the block add into one shared histogram (lane-private copies).
 template <int K, int THREADS, int LAYOUT, int MAP, int METHOD>
-__global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) pair_kernel(const PairParams p) {
-  constexpr int BI = THREADS * K;
+__global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
+  static_assert(32 * K == kJT, "an i-set and a j-chunk have the same size");
+  constexpr int WARPS = THREADS / 32;
   extern __shared__ __align__(16) unsigned char smem[];
-  float4* tiles = reinterpret_cast<float4*>(smem);                    // [2][kJT]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + 2 * kJT * sizeof(float4));
-  __shared__ unsigned int s_ticket[2];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float4* my_tiles = reinterpret_cast<float4*>(smem) + warp * 2 * kJT;  // [2][kJT] per warp
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + WARPS * 2 * kJT * sizeof(float4));
 
-  // zero this block's histogram and its partial row
   const int words = (LAYOUT == kLane) ? p.bp.entries * 32 : p.bp.entries;
   for (int w = tid; w < words; w += THREADS) hist[w] = 0;
   unsigned long long* row = p.partial + (size_t)blockIdx.x * p.bp.nbins;
-  for (int k = tid; k < p.bp.nbins; k += THREADS) row[k] = 0ull;
-  if (tid == 0) {
-    s_ticket[0] = atomicAdd(p.ticket, 1u);
-    s_ticket[1] = atomicAdd(p.ticket, 1u);
-  }
+  if (!p.accumulate)
+    for (int k = tid; k < p.bp.nbins; k += THREADS) row[k] = 0ull;
+  __syncthreads();
 
   const uint32_t hist_addr = (uint32_t)__cvta_generic_to_shared(hist);
-  const uint32_t tiles_addr = (uint32_t)__cvta_generic_to_shared(tiles);
+  const uint32_t tiles_addr = (uint32_t)__cvta_generic_to_shared(my_tiles);
   // every code is the float 2^23 + entry (the mirror offset is already inside the code)
   const uint32_t magic_bits = __float_as_uint(kMagic);
   // address of entry e in this lane's copy = (code bits << shift) + base
   const uint32_t base = (LAYOUT == kLane) ? hist_addr + lane * 4u - (magic_bits << 7) : hist_addr - (magic_bits << 2);
   constexpr int SHIFT = (LAYOUT == kLane) ? 7 : 2;
-  const unsigned long long C = (unsigned long long)p.total_chunks;
+  const int ni = (int)p.ni, nj = (int)p.nj;
 
-  __syncthreads();
-  const unsigned int C32 = (unsigned int)C;
-  unsigned int q = s_ticket[0], qn = s_ticket[1];
-  if (q < C32) {
-    const int ni = (int)p.ni, nj = (int)p.nj;
-    int ib, jc;
-    chunk_coords(p, q, ib, jc);
-    {
-      const int j0 = jc * kJT;
-      const int jn = min(kJT, nj - j0);
-      if (tid < jn) cp_async16(tiles_addr + tid * 16u, p.vj + j0 + tid);
+  // tickets: the unit being computed (u), the one whose tile is in flight (un), and one fetched
+  // ahead by lane 0 while computing (its latency hides behind the unit)
+  unsigned int t = 0, tn = 0;
+  if (lane == 0) {
+    t = atomicAdd(p.ticket, 1u);
+    tn = atomicAdd(p.ticket, 1u);
+  }
+  long long u = p.unit_begin + __shfl_sync(0xffffffffu, t, 0);
+  long long un = p.unit_begin + __shfl_sync(0xffffffffu, tn, 0);
+  auto load_tile = [&](int c, int b) {
+    const int j0 = c * kJT;
+#pragma unroll
+    for (int m = 0; m < kJT / 32; ++m) {
+      const int jj = m * 32 + lane;
+      if (j0 + jj < nj) cp_async16(tiles_addr + (uint32_t)(b * kJT + jj) * 16u, p.vj + j0 + jj);
     }
     cp_async_commit();
+  };
+  if (u < p.unit_end) {
+    int r, c;
+    unit_coords(p, u, r, c);
+    load_tile(c, 0);
     float xi[K], yi[K], zi[K];
-    int cur_ib = -1;
-    unsigned int since_flush = 0;
-    int it = 0;  // iteration count: tile buffer it & 1, ticket mailbox slot it & 1
+    float4 icap = make_float4(1.f, 0.f, 0.f, 4.f);
+    int cur_r = -1, buf = 0;
     while (true) {
-      const int buf = it & 1;
-      const int i0 = ib * BI;
-      if (ib != cur_ib) {
+      int rn = 0, cn = 0;
+      if (un < p.unit_end) {
+        unit_coords(p, un, rn, cn);
+        load_tile(cn, buf ^ 1);
+      } else {
+        cp_async_commit();
+      }
+      unsigned int ta = 0;
+      if (lane == 0) ta = atomicAdd(p.ticket, 1u);
+      const int i0 = r * kJT;
+      if (r != cur_r) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          int i = i0 + k * THREADS + tid;
+          int i = i0 + k * 32 + lane;
           i = i < ni ? i : ni - 1;
           const float4 v = __ldg(p.vi + i);
           xi[k] = v.x;
           yi[k] = v.y;
           zi[k] = v.z;
-          (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 4, i, ib, v.x, v.y, v.z);
+          (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 4, i, r, v.x, v.y, v.z);
         }
-        cur_ib = ib;
+        if (METHOD == kChordPoly) icap = union_caps<K>(p.icap32, (long long)i0 / 32, p.igroups);
+        cur_r = r;
       }
-      // One barrier per chunk: after it this chunk's tile is visible, every warp has finished the
-      // previous chunk (so the other buffer may be refilled) and the ticket that thread 0 posted
-      // in the previous iteration is readable.
-      cp_async_wait<0>();
-      __syncthreads();
-      if (it > 0) qn = s_ticket[(it - 1) & 1];
-      int nib = 0, njc = 0;
-      if (qn < C32) {
-        chunk_coords(p, qn, nib, njc);
-        const int j0 = njc * kJT;
-        const int jn = min(kJT, nj - j0);
-        if (tid < jn) cp_async16(tiles_addr + (uint32_t)((buf ^ 1) * kJT + tid) * 16u, p.vj + j0 + tid);
-      }
-      cp_async_commit();
-      unsigned int t_after = 0;
-      if (tid == 0) t_after = atomicAdd(p.ticket, 1u);  // the chunk after qn; posted below
+      cp_async_wait<1>();
+      __syncwarp();  // this unit's tile, copied by all lanes, is visible to all lanes
 
-      const float4* tile = tiles + buf * kJT;
-      const int j0 = jc * kJT;
+      const float4* tile = my_tiles + buf * kJT;
+      const int j0 = c * kJT;
       const int jn = min(kJT, nj - j0);
-      const bool full = (jn == kJT) && (i0 + BI <= ni) && (!p.sym || j0 >= i0 + BI);
+      const bool full = (jn == kJT) && (i0 + kJT <= ni) && (!p.sym || c > r);
 #ifdef ACF_DEBUG_BOUNDS
       for (int jj = 0; jj < jn; ++jj) {
         const float4 v = tile[jj];
-        (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 2, j0 + jj, q, v.x, v.y, v.z, (float)buf);
+        (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 2, j0 + jj, u, v.x, v.y, v.z, (float)buf);
       }
 #endif
       if (full) {
+        // one loop per (32-galaxy j-group, path); the path is uniform across the warp
+        auto run = [&](auto tag, int jbeg) {
+          constexpr int P = decltype(tag)::value;
 #pragma unroll kJJUnroll
-        for (int jj = 0; jj < kJT; ++jj) {
-          const float4 v = tile[jj];
+          for (int jj = jbeg; jj < jbeg + 32; ++jj) {
+            const float4 v = tile[jj];
 #pragma unroll
-          for (int k = 0; k < K; ++k) {
-            const float code = pair_code<MAP, METHOD>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-            if (ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
-                          (long long)(__float_as_uint(code) - magic_bits), i0 + k * THREADS + tid, code, xi[k], yi[k],
-                          zi[k], v.x, v.y, v.z, (float)jj))
-              red_shared_add((__float_as_uint(code) << SHIFT) + base, p.inc);
+            for (int k = 0; k < K; ++k) {
+              const float code = (P == kBelow90)   ? pair_code_fixed<MAP, 1>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
+                                 : (P == kAbove90) ? pair_code_fixed<MAP, -1>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
+                                                   : pair_code<MAP, METHOD>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
+              if (ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
+                            (long long)(__float_as_uint(code) - magic_bits), i0 + k * 32 + lane, code, xi[k], yi[k],
+                            zi[k], v.x, v.y, v.z, (float)(P * 1000 + jj)))
+                red_shared_add((__float_as_uint(code) << SHIFT) + base, p.inc);
+            }
           }
+        };
+#pragma unroll 1
+        for (int g = 0; g < kJT / 32; ++g) {
+          const int path = (METHOD == kChordPoly) ? choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + g)) : kGeneral;
+          if (path == kBelow90) run(PathTag<kBelow90>(), g * 32);
+          else if (path == kAbove90) run(PathTag<kAbove90>(), g * 32);
+          else run(PathTag<kGeneral>(), g * 32);
         }
       } else {
         // pair (i, j) counts iff jj > thr[k]: thr = -1 for every j, a diagonal offset when only
@@ -385,9 +617,9 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) pair_kernel(c
         int thr[K];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          const int i = i0 + k * THREADS + tid;
-          const int t = p.sym ? i - j0 : -1;
-          thr[k] = (i >= ni) ? 0x7fffffff : max(-1, min(t, kJT));
+          const int i = i0 + k * 32 + lane;
+          const int tt = p.sym ? i - j0 : -1;
+          thr[k] = (i >= ni) ? 0x7fffffff : max(-1, min(tt, kJT));
         }
         for (int jj = 0; jj < jn; ++jj) {
           const float4 v = tile[jj];
@@ -396,26 +628,19 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) pair_kernel(c
             const float code = pair_code<MAP, METHOD>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
             if (jj > thr[k] &&
                 ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
-                          (long long)(__float_as_uint(code) - magic_bits), i0 + k * THREADS + tid, code, xi[k], yi[k],
+                          (long long)(__float_as_uint(code) - magic_bits), i0 + k * 32 + lane, code, xi[k], yi[k],
                           zi[k], v.x, v.y, v.z, (float)jj))
               red_shared_add((__float_as_uint(code) << SHIFT) + base, p.inc);
           }
         }
       }
-      // Slot it&1 is next written two iterations later, after a barrier every thread passes only
-      // once it has read this value, so one barrier per chunk is enough.
-      if (tid == 0) s_ticket[it & 1] = t_after;
-      if (++since_flush == p.flush_every) {
-        __syncthreads();
-        flush_hist<K, THREADS, LAYOUT, MAP, METHOD>(p, hist, true);
-        __syncthreads();
-        since_flush = 0;
-      }
-      if (qn >= C32) break;
-      q = qn;
-      ib = nib;
-      jc = njc;
-      ++it;
+      __syncwarp();  // every lane is done with this buffer before the next prefetch refills it
+      if (un >= p.unit_end) break;
+      u = un;
+      r = rn;
+      c = cn;
+      un = p.unit_begin + __shfl_sync(0xffffffffu, ta, 0);
+      buf ^= 1;
     }
     cp_async_wait<0>();
   }

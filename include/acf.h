@@ -96,9 +96,9 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  * rows, the chunk counter) lives in one file-scope device array of 16 MiB that the library
  * reserves on every GPU that loads it, until the process exits. It calls no cudaMalloc, cudaFree
  * or other allocating routine.
- *   - Limit: 256 + 16*n (+ 16*n2 for a cross-correlation) + (blocks * nbins * 8) bytes must fit in
- *     16 MiB, blocks being the persistent grid (304 on a 152-SM GPU); larger requests return
- *     ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need ~5 MB.
+ *   - Limit: about 197 KB + 41 bytes per galaxy of each catalog + (blocks * nbins * 8) bytes must
+ *     fit in 16 MiB, blocks being the persistent grid (304 on a 152-SM GPU); larger requests return
+ *     ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need ~10 MB.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
  *     make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's contents; the
@@ -142,20 +142,23 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
 
 /*
  * Tuning and measurement switches (all optional). Keys:
- *   "threads"        threads per block of the pair kernel: 256 or 512 (default: chosen)
+ *   "threads"        threads per block of the pair kernel: 512 or 1024 (default: 1024 when the
+ *                    shared-memory plan allows)
  *   "ctas_per_sm"    resident blocks per SM to launch (default: occupancy maximum)
  *   "bin_method"     0 = chord + arcsin^2 polynomial (default, meets the precision contract);
  *                    1 = dot product + acosf (the page's exact-acos form; measured alternative,
  *                        does NOT meet the precision contract at small or near-180 separations)
  *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram
+ *   "units_per_launch"  cap on work units (128 x 128 pairs) per pair-kernel launch; 0 = automatic
+ *                    (large problems are always split so that no 32-bit shared counter can wrap)
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
  */
 int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
 
 /*
  * Read back facts about the last acf_histogram call. Keys: "grid", "threads", "ctas_per_sm",
- * "chunks", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
- * "pairs_evaluated", "flush_every".
+ * "units", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
+ * "pairs_evaluated", "launches" (pair-kernel launches the call was split into).
  */
 int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
 

@@ -25,7 +25,7 @@ def main() -> int:
     cases = [
         (2000, 2000, 0.25, 720, 0, 0, 0), (1, 1, 0.25, 720, 0, 0, 0), (2049, 130, 0.25, 720, 0, 0, 0),
         (3000, 2500, 0.01, 18000, 0, 0, 0), (3000, 2500, 0.35, 515, 0, 0, 0), (3000, 2500, 0.25, 100, 0, 0, 0),
-        (3000, 2500, 0.25, 720, 2, 0, 0), (3000, 2500, 0.25, 720, 0, 512, 0), (3000, 2500, 0.25, 720, 0, 0, 1),
+        (3000, 2500, 0.25, 720, 2, 0, 0), (3000, 2500, 0.25, 720, 0, 512, 0), (3000, 2500, 0.25, 720, 0, 1024, 0), (3000, 2500, 0.25, 720, 0, 0, 1),
         (3000, 2500, 60.0, 3, 0, 0, 0),
     ]
     bad = 0

@@ -86,7 +86,7 @@ def test_binnings(acf, ctx, w, nb, layout):
         ctx.set_option("layout", 0)
 
 
-@pytest.mark.parametrize("threads", [256, 512])
+@pytest.mark.parametrize("threads", [512, 1024])
 def test_thread_counts(acf, ctx, threads):
     c = synth.catalogs(3000, 2500, 10, 30.0, seed=5)
     ctx.set_option("threads", threads)
@@ -144,7 +144,7 @@ def test_argument_errors_return_codes(acf, ctx):
     assert "exceeds" in acf.acf_last_error(h)
     assert lib.acf_omega(h, P(out), P(out), P(out), 0, 1, 1, P(out)) == acf.ACF_ERR_ARG
     assert lib.acf_set_option(h, b"no_such_option", 1) == acf.ACF_ERR_ARG
-    assert lib.acf_set_option(h, b"threads", 300) == acf.ACF_ERR_ARG
+    assert lib.acf_set_option(h, b"threads", 256) == acf.ACF_ERR_ARG
     # the context still works afterwards
     c = synth.catalogs(100, 100, 0, 0.0, seed=1)
     _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
@@ -246,3 +246,19 @@ def test_kernel_timing_records_launches(acf, ctx):
         assert len(t) == 2 and all(x > 0 for x in t)
     finally:
         ctx.set_option("kernel_timing", 0)
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_split_launches_accumulate(acf, ctx, layout):
+    # a few work units per launch: later launches add into the block rows of earlier ones
+    c = synth.catalogs(3000, 2600, 10, 30.0, seed=12)
+    ctx.set_option("units_per_launch", 7)
+    ctx.set_option("layout", layout)
+    try:
+        _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+        assert ctx.info("launches") == -(-ctx.info("units") // 7)
+        _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+        assert ctx.info("launches") > 1
+    finally:
+        ctx.set_option("units_per_launch", 0)
+        ctx.set_option("layout", 0)
