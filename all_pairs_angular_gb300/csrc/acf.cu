@@ -29,6 +29,9 @@ constexpr int kMaxTimed = 4096;
 
 struct Plan {
   BinParams bp;
+  double w_rad = 0.0;
+  int exact = 0;
+  float exact_lo = 0.f;
   int map = kMirror;
   int method = kChordPoly;
   int layout = kLane;
@@ -53,6 +56,10 @@ struct acf_ctx {
   // options
   int opt_threads = 0, opt_ctas = 0, opt_method = kChordPoly, opt_layout = 0, opt_timing = 0;
   long long opt_units_per_launch = 0;
+  int opt_exact = 1;              // 0 off, 1 near 0 and 180 degrees, 2 everywhere
+  double opt_exact_below_deg = 20.0;
+  unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
+  long long last_qcap = 0;
   // info about the last histogram
   long long info_grid = 0, info_threads = 0, info_ctas = 0, info_chunks = 0, info_layout = 0, info_map = 0,
             info_entries = 0, info_smem = 0, info_pairs = 0, info_flush = 0;
@@ -116,6 +123,7 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   bp.nbins = nbins;
   bp.inv_w = (float)(1.0 / w_rad);
   pl.method = c->opt_method;
+  pl.w_rad = w_rad;
   const double pr = std::rint(P);
   const bool integral = std::fabs(P - pr) <= 1e-9 * std::max(1.0, P) && pr >= 4.0;
   long long mirror_entries = integral ? 2 * (long long)std::ceil(pr / 2.0) + 4 : -1;
@@ -136,6 +144,43 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     bp.entries = (int)entries;
     bp.magic = 8388608.0f;
     bp.clamp_c = (float)(entries - 1);
+  }
+  // Exact mode: S fractional bits in the bin code make a window of 2^-S bins around every edge,
+  // wider than the fp32 path's error there (3.5e-7 rad near 0 and 180 degrees, 8e-7 rad anywhere).
+  pl.exact = (pl.method == kChordPoly) ? c->opt_exact : 0;
+  pl.exact_lo = (float)(c->opt_exact_below_deg * pi / 180.0);
+  if (pl.exact) {
+    // bound on the fp32 path's error: vectors 1.2e-7 plus terms that grow with the separation, up
+    // to 8e-7 rad near 90 degrees; mode 1 only re-decides separations within exact_lo of 0 or 180
+    const double zone = std::min(1.0, c->opt_exact_below_deg / 90.0);
+    const double err = (pl.exact == 2) ? 8e-7 : 1.5e-7 + 6.5e-7 * zone;
+    int S = (int)std::floor(std::log2(w_rad / err));
+    const int room = (int)std::floor(std::log2(8.0e6 / ((double)bp.entries + 2.0)));  // (entries+2) << S < 2^23
+    S = std::max(0, std::min(S, room));
+    bp.fine_shift = S;
+    bp.inv_w_f = (float)(std::ldexp(1.0, S) / w_rad);
+    bp.magic_f = (float)(8388608.0 + std::ldexp((double)bp.off, S));
+    bp.clamp_f = (float)std::ldexp((double)bp.clamp_c + 0.5, S);
+  }
+  bp.kmax = (int)std::min<double>((double)nbins - 1.0, std::floor(P + 1e-9));
+  // exact zone, as histogram entries: everything (mode 2), or separations within exact_lo of
+  // 0 or 180 degrees (mode 1): mirror entries off - L - 1 .. off + L, clamp entries <= L or >= floor(P) - L - 1
+  bp.zone0 = 0u; bp.span0 = 0xFFFFFFFFu; bp.zone1 = 0u; bp.span1 = 0u;
+  if (pl.exact == 1) {
+    // L + 2 bins stay within exact_lo, so every zone pair sits in a j-group the caps mark for
+    // re-decision whatever the grouping, and the set of re-decided pairs is order-independent
+    const long long L = std::max<long long>(0, (long long)std::floor(c->opt_exact_below_deg / w_deg) - 2);
+    if (pl.map == kMirror) {
+      bp.zone0 = (unsigned)std::max<long long>(0, bp.off - L - 1);
+      bp.span0 = (unsigned)(2 * L + 1);
+      bp.zone1 = 0xFFFFFFFFu;  // second range unused (e - zone1 wraps above span1 = 0 unless e == zone1)
+      bp.span1 = 0u;
+    } else {
+      bp.zone0 = 0u;
+      bp.span0 = (unsigned)L;
+      bp.zone1 = (unsigned)std::max<long long>(0, (long long)std::floor(P) - L - 1);
+      bp.span1 = 0xFFFFFFFFu - bp.zone1;
+    }
   }
   // Shared memory = every warp's double-buffered j-tile (4 KB per warp) + the histogram: 32
   // lane-private copies when they fit beside the tiles of at least 16 warps, else one block-shared
@@ -180,23 +225,30 @@ PairKernelFn pick_kernel(const Plan& pl) {
 
 // Device buffers of one histogram call, carved out of one scratch region.
 struct CatBufs {
-  float4* v_in = nullptr;    // unit vectors in input order
   unsigned int* key = nullptr;
-  float4* v = nullptr;       // unit vectors in spatial order
-  int* perm = nullptr;       // input index of each sorted slot
+  float4* v = nullptr;       // unit vectors in spatial order (fp32)
+  double4* v64 = nullptr;    // the same in fp64 (exact re-decision)
   float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
 };
 struct Scratch {
-  unsigned int* ticket = nullptr;      // chunk dispenser (first word of a zeroed block)
-  unsigned int* cell_count = nullptr;  // kCells counters, zeroed with the ticket
+  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue slots handed out, [2] moved pairs,
+                                       // [3] flagged pairs; bytes 64..103: pairs per path (u64)
+  unsigned int* cell_count = nullptr;  // kCells counters
   unsigned int* cursor = nullptr;      // kCells
   CatBufs a, b;                        // b only for cross-correlations
   unsigned long long* partial = nullptr;
+  double* T = nullptr;                 // exact mode: edge tables, nbins + 1 each
+  double* U = nullptr;
+  uint4* queue = nullptr;
+  long long qcap = 0;
 };
 
+constexpr long long kQueueCapMin = 1ll << 20;  // flagged pairs the workspace can hold: 16 MB ..
+constexpr long long kQueueCapMax = 1ll << 28;  // .. 4 GB
+
 // Lay the buffers out from `base` (nullptr: only measure). Returns the bytes needed.
-size_t carve(char* base, long long n, long long nj, bool sym, long long grid, int nbins, Scratch* s) {
+size_t carve(char* base, long long n, long long nj, bool sym, long long grid, int nbins, long long qcap, Scratch* s) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
     char* p = base ? base + off : nullptr;
@@ -205,36 +257,38 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   };
   auto cat = [&](long long m, CatBufs& cb) {
     const long long ch = (m + 127) / 128;
-    cb.v_in = reinterpret_cast<float4*>(take((size_t)m * 16));
     cb.key = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
     cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
-    cb.perm = reinterpret_cast<int*>(take((size_t)m * 4));
+    cb.v64 = reinterpret_cast<double4*>(take((size_t)m * 32));
     cb.cap32 = reinterpret_cast<float4*>(take((size_t)ch * 4 * 16));
     cb.cap128 = reinterpret_cast<float4*>(take((size_t)ch * 16));
   };
   Scratch t;
   Scratch& r = s ? *s : t;
-  char* head = take(256 + (size_t)kCells * 4);  // ticket, then the cell counters
-  r.ticket = reinterpret_cast<unsigned int*>(head);
+  char* head = take(256 + (size_t)kCells * 4);  // counters, then the cell counters
+  r.counters = reinterpret_cast<unsigned int*>(head);
   r.cell_count = head ? reinterpret_cast<unsigned int*>(head + 256) : nullptr;
   r.cursor = reinterpret_cast<unsigned int*>(take((size_t)kCells * 4));
   cat(n, r.a);
   if (!sym) cat(nj, r.b);
   r.partial = reinterpret_cast<unsigned long long*>(take((size_t)grid * (size_t)nbins * 8));
+  r.T = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
+  r.U = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
+  r.qcap = qcap;
+  r.queue = reinterpret_cast<uint4*>(take((size_t)qcap * 16));
   return off;
 }
 
-// Unit vectors of one catalog in spatial order, with their caps. The cell counters start at zero
-// (cleared together with the chunk ticket by the caller) and are cleared again here after use.
+// Unit vectors of one catalog in spatial order, with their caps.
 int prepare_catalog(acf_ctx* c, const float* ra, const float* dec, long long n, const Scratch& s, const CatBufs& cb) {
   const int threads = 256;
   const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 16);
   ACF_CUDA(c, cudaMemsetAsync(s.cell_count, 0, (size_t)kCells * 4, c->stream));
-  prep_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, cb.v_in, cb.key, s.cell_count);
+  prep_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, cb.key, s.cell_count);
   ACF_CUDA(c, cudaGetLastError());
   scan_kernel<<<1, 1024, 0, c->stream>>>(s.cell_count, s.cursor);
   ACF_CUDA(c, cudaGetLastError());
-  scatter_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(cb.v_in, cb.key, n, s.cursor, cb.v, cb.perm);
+  scatter_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, cb.key, n, s.cursor, cb.v, cb.v64);
   ACF_CUDA(c, cudaGetLastError());
   const long long warps = (n + 127) / 128;
   caps_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, c->stream>>>(cb.v, n, cb.cap32, cb.cap128);
@@ -273,9 +327,25 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
 
 // The pair kernel (one or more launches) and the merge for prepared catalogs.
 int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs& cj, long long nj, bool sym,
-                      const Plan& pl, const Launch& L, unsigned long long* partial, unsigned int* ticket,
-                      uint64_t* out) {
+                      const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
+  unsigned long long* partial = sc.partial;
+  unsigned int* ticket = sc.counters;
   PairParams p;
+  p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
+  p.exact_lo = pl.exact_lo;
+  p.queue = sc.queue;
+  p.qtotal = sc.counters + 1;
+  p.qflagged = sc.counters + 3;
+  p.qcap = (unsigned int)std::min<long long>(sc.qcap, 0xFFFFFFFFll);
+  // each block reserves a batch (half the queue spread over the blocks of every launch); blocks that
+  // flag more append past their batch through the global counter
+  {
+    const long long nlaunch = (L.units + L.per_launch - 1) / std::max<long long>(L.per_launch, 1);
+    p.qbatch = (unsigned int)std::max<long long>(
+        16, sc.qcap / (2 * std::max<long long>(L.grid, 1) * std::max<long long>(nlaunch, 1)));
+  }
+  p.path_pairs = reinterpret_cast<unsigned long long*>(sc.counters + 16);
+  if (p.qcap == 0) p.exact_mode = 0;
   p.vi = ci.v;
   p.vj = cj.v;
   p.icap32 = ci.cap32;
@@ -324,6 +394,21 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   merge_kernel<<<mblocks, 32 * kMergeWarps, 0, c->stream>>>(partial, (int)L.grid, pl.bp.nbins, self,
                                                              reinterpret_cast<unsigned long long*>(out));
   ACF_CUDA(c, cudaGetLastError());
+  if (p.exact_mode) {
+    // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
+    const int fblocks = c->num_sms * 8;
+    if (pl.map == kMirror)
+      fixup_kernel<kMirror><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
+                                                            sc.U, pl.bp, p.inc,
+                                                            reinterpret_cast<unsigned long long*>(out), sc.counters + 2);
+    else
+      fixup_kernel<kClamp><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
+                                                           sc.U, pl.bp, p.inc,
+                                                           reinterpret_cast<unsigned long long*>(out), sc.counters + 2);
+    ACF_CUDA(c, cudaGetLastError());
+  }
+  c->last_counters = sc.counters;
+  c->last_qcap = p.exact_mode ? p.qcap : 0;
   c->info_grid = L.grid;
   c->info_threads = pl.threads;
   c->info_ctas = L.ctas;
@@ -337,17 +422,22 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   return ACF_OK;
 }
 
-// Everything after argument checks and workspace layout: prepare the catalogs, pair, merge.
+// Everything after argument checks and workspace layout: prepare the catalogs, pair, merge,
+// and (exact mode) re-decide the flagged pairs.
 int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, const float* ra2, const float* dec2,
                  long long nj, bool sym, const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
-  ACF_CUDA(c, cudaMemsetAsync(sc.ticket, 0, 4, c->stream));
+  ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 128, c->stream));
   int rc = prepare_catalog(c, ra, dec, n, sc, sc.a);
   if (rc) return rc;
   if (!sym) {
     rc = prepare_catalog(c, ra2, dec2, nj, sc, sc.b);
     if (rc) return rc;
   }
-  return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc.partial, sc.ticket, out);
+  if (pl.exact && sc.qcap > 0) {
+    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U);
+    ACF_CUDA(c, cudaGetLastError());
+  }
+  return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc, out);
 }
 
 int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2, const float* dec2,
@@ -372,10 +462,16 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, nullptr));
+  // queue: every computed pair may be flagged with probability ~2^(1-S); twice that, within bounds
+  long long qcap = 0;
+  if (pl.exact) {
+    const double pairs = (double)L.units * kJT * kJT;
+    qcap = (long long)std::min<double>(kQueueCapMax, std::max<double>(kQueueCapMin, 4.0 * pairs * std::ldexp(1.0, -pl.bp.fine_shift)));
+  }
+  rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, qcap, nullptr));
   if (rc) return rc;
   Scratch sc;
-  carve(static_cast<char*>(c->ws.ptr), n, nj, sym, L.grid, nbins, &sc);
+  carve(static_cast<char*>(c->ws.ptr), n, nj, sym, L.grid, nbins, qcap, &sc);
   return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }
 
@@ -523,6 +619,12 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "layout")) {
     if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "layout must be 0, 1 or 2");
     c->opt_layout = (int)v;
+  } else if (!strcmp(key, "exact")) {
+    if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "exact must be 0, 1 or 2");
+    c->opt_exact = (int)v;
+  } else if (!strcmp(key, "exact_below_deg")) {
+    if (v < 0 || v > 180) return fail(c, ACF_ERR_ARG, "exact_below_deg must be 0..180");
+    c->opt_exact_below_deg = (double)v;
   } else if (!strcmp(key, "units_per_launch")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "units_per_launch must be >= 0");
     c->opt_units_per_launch = v;
@@ -554,6 +656,33 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
       *v = e.val;
       return ACF_OK;
     }
+  const char* path_keys[5] = {"pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact",
+                               "pairs_masked"};
+  for (int k = 0; k < 5; ++k)
+    if (!strcmp(key, path_keys[k])) {
+      // synchronises the stream; pairs the last histogram call evaluated on each pair-kernel path
+      unsigned long long h[5] = {0, 0, 0, 0, 0};
+      if (c->last_counters) {
+        if (cudaSetDevice(c->device) != cudaSuccess || cudaStreamSynchronize(c->stream) != cudaSuccess ||
+            cudaMemcpy(h, c->last_counters + 16, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+          return ACF_ERR_CUDA;
+      }
+      *v = (long long)h[k];
+      return ACF_OK;
+    }
+  if (!strcmp(key, "exact_flagged") || !strcmp(key, "exact_moved") || !strcmp(key, "exact_overflow")) {
+    // synchronises the stream; counts of the last histogram call
+    unsigned int h[4] = {0, 0, 0, 0};
+    if (c->last_counters && c->last_qcap > 0) {
+      if (cudaSetDevice(c->device) != cudaSuccess || cudaStreamSynchronize(c->stream) != cudaSuccess ||
+          cudaMemcpy(h, c->last_counters, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ACF_ERR_CUDA;
+    }
+    if (!strcmp(key, "exact_flagged")) *v = h[3];
+    else if (!strcmp(key, "exact_moved")) *v = h[2];
+    else *v = h[1] > c->last_qcap ? (long long)h[1] - c->last_qcap : 0;  // slots requested past the end
+    return ACF_OK;
+  }
   return ACF_ERR_ARG;
 }
 
@@ -629,7 +758,9 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const size_t need = carve(nullptr, n, nj, sym, L.grid, nbins, nullptr);
+  const size_t need = carve(nullptr, n, nj, sym, L.grid, nbins, 0, nullptr);
+  // the exact-mode queue takes whatever the static array has left
+  const long long qcap = pl.exact && need < kNoAllocScratchBytes ? (long long)((kNoAllocScratchBytes - need) / 16) - 16 : 0;
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
@@ -641,6 +772,6 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   // Every byte the kernels read is rewritten first: the ticket and cell counters are cleared,
   // the preparation kernels write the vectors and caps, and the pair kernel zeroes its rows.
   Scratch sc;
-  carve(static_cast<char*>(scratch), n, nj, sym, L.grid, nbins, &sc);
+  carve(static_cast<char*>(scratch), n, nj, sym, L.grid, nbins, std::max(qcap, 0ll), &sc);
   return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }

@@ -32,6 +32,10 @@ constexpr int kJT = 128;  // j-galaxies per shared-memory chunk
 #define ACF_JJ_UNROLL 4
 #endif
 constexpr int kJJUnroll = ACF_JJ_UNROLL;
+#ifndef ACF_JJ_UNROLL_FINE
+#define ACF_JJ_UNROLL_FINE 1
+#endif
+constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact-mode (fine code) loops
 #ifndef ACF_ASM_LOP3
 #define ACF_ASM_LOP3 1  // write the two sign-bit logic ops as explicit lop3 (2 ops, not 3)
 #endif  // j-loop unroll of the full-chunk path
@@ -50,6 +54,12 @@ __device__ constexpr float kP0 = 0.99999959294652097f, kP1 = 0.08334261162808559
 
 struct BinParams {
   float magic;     // 2^23 + off (mirror) or 2^23 (clamp)
+  float inv_w_f;   // exact mode: 2^S / w (fine code with S fractional bits)
+  float magic_f;   // exact mode: 2^23 + off * 2^S (mirror)
+  float clamp_f;   // exact mode: (clamp_c + 0.5) * 2^S (clamp map)
+  int fine_shift;  // exact mode: S
+  int kmax;        // exact mode: highest bin a separation <= 180 degrees can reach
+  unsigned int zone0, span0, zone1, span1;  // exact mode: entries e with e - zone <= span (unsigned) are re-decided
   float clamp_c;   // largest index (clamp map)
   float inv_w;     // 1 / w in radians (acos method)
   int off;         // mirror: index of theta' = 0 on the near side
@@ -74,6 +84,16 @@ struct PairParams {
   const float4* __restrict__ icap32;   // caps of 32-galaxy groups of the i catalog (sorted order)
   const float4* __restrict__ jcap32;   // caps of 32-galaxy groups of the j catalog
   long long igroups;                   // number of 32-galaxy groups of the i catalog
+  int exact_mode;                      // 0 off, 1 groups that may hold separations < theta_lo or > 180 - theta_lo, 2 all
+  float exact_lo;                      // theta_lo in radians
+  uint4* queue;                        // exact mode: flagged pairs (sorted i, sorted j, fine code bits, 0);
+                                       // i = 0xFFFFFFFF marks an unused slot
+  unsigned int* qtotal;                // slots handed out (reserved batches + single appends)
+  unsigned int* qflagged;              // pairs flagged (for reporting)
+  unsigned int qcap;                   // queue slots
+  unsigned int qbatch;                 // slots a block reserves at its start
+  unsigned long long* path_pairs;      // pairs evaluated per path: fixed, general, fixed+flag,
+                                       // general+flag, masked/ragged units (all pairs computed)
   BinParams bp;
 };
 
@@ -197,19 +217,25 @@ __device__ __forceinline__ unsigned int cell_of(double x, double y, double z) {
   return (unsigned int)face * (kFaceCells * kFaceCells) + (spread_bits6(iu) | (spread_bits6(iv) << 1));
 }
 
-// Unit vectors in input order plus each galaxy's cell, counted per cell.
+// (RA, Dec) arcminutes -> fp64 unit vector; non-finite inputs become (0, 0).
+__device__ __forceinline__ void unit64(float ra_arcmin, float dec_arcmin, double& x, double& y, double& z) {
+  const double k = 3.14159265358979323846 / 10800.0;
+  double a = (double)ra_arcmin * k, d = (double)dec_arcmin * k;
+  if (!isfinite(a) || !isfinite(d)) { a = 0.0; d = 0.0; }
+  double sa, ca, sd, cd;
+  sincos(a, &sa, &ca);
+  sincos(d, &sd, &cd);
+  x = cd * ca;
+  y = cd * sa;
+  z = sd;
+}
+
+// Each galaxy's cell, counted per cell.
 __global__ void prep_kernel(const float* __restrict__ ra, const float* __restrict__ dec, long long n,
-                            float4* __restrict__ v, unsigned int* __restrict__ key,
-                            unsigned int* __restrict__ cell_count) {
+                            unsigned int* __restrict__ key, unsigned int* __restrict__ cell_count) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const double k = 3.14159265358979323846 / 10800.0;
-    double a = (double)ra[i] * k, d = (double)dec[i] * k;
-    if (!isfinite(a) || !isfinite(d)) { a = 0.0; d = 0.0; }
-    double sa, ca, sd, cd;
-    sincos(a, &sa, &ca);
-    sincos(d, &sd, &cd);
-    const double x = cd * ca, y = cd * sa, z = sd;
-    v[i] = make_float4((float)x, (float)y, (float)z, 0.0f);
+    double x, y, z;
+    unit64(ra[i], dec[i], x, y, z);
     const unsigned int c = cell_of(x, y, z);
     key[i] = c;
     atomicAdd(cell_count + c, 1u);
@@ -247,14 +273,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restri
   }
 }
 
-// Counting-sort scatter: sorted vectors plus, per sorted slot, the input index.
-__global__ void scatter_kernel(const float4* __restrict__ v_in, const unsigned int* __restrict__ key, long long n,
-                               unsigned int* __restrict__ cursor, float4* __restrict__ v_out, int* __restrict__ perm) {
+// Counting-sort scatter: unit vectors in spatial order, as fp32 (pair kernel) and fp64 (exact
+// re-decision of flagged pairs).
+__global__ void scatter_kernel(const float* __restrict__ ra, const float* __restrict__ dec,
+                               const unsigned int* __restrict__ key, long long n, unsigned int* __restrict__ cursor,
+                               float4* __restrict__ v_out, double4* __restrict__ v64_out) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const unsigned int pos = atomicAdd(cursor + key[i], 1u);
     if (ACF_CHECK(pos < (unsigned long long)n, 5, i, pos)) {
-      v_out[pos] = v_in[i];
-      perm[pos] = (int)i;
+      double x, y, z;
+      unit64(ra[i], dec[i], x, y, z);
+      v_out[pos] = make_float4((float)x, (float)y, (float)z, 0.0f);
+      v64_out[pos] = make_double4(x, y, z, 0.0);
     }
   }
 }
@@ -319,7 +349,7 @@ __global__ void caps_kernel(const float4* __restrict__ v, long long n, float4* _
 
 // The float 2^23 + (histogram entry), whose bit pattern is bits(2^23) + entry. Symmetric in (u, v) bit for bit:
 // the products commute and u - s v = -(v - s u) rounds to the same magnitude.
-template <int MAP, int METHOD>
+template <int MAP, int METHOD, bool FINE = false>
 __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float xj, float yj, float zj,
                                            const BinParams& bp) {
   const float d = fmaf(zi, zj, fmaf(yi, yj, xi * xj));
@@ -354,14 +384,16 @@ __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float x
       // is exactly floor((pi - theta')/w) when P = pi/w is an integer.
       // theta' carrying the sign of d: th | (d & signmask), one logic op
 #if ACF_ASM_LOP3
-      return fma_rz(__uint_as_float(lop3<0xF8>(__float_as_uint(th), db, 0x80000000u)), bp.inv_w, bp.magic);
+      return fma_rz(__uint_as_float(lop3<0xF8>(__float_as_uint(th), db, 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w,
+                    FINE ? bp.magic_f : bp.magic);
 #else
-      return fma_rz(__uint_as_float(__float_as_uint(th) | (db & 0x80000000u)), bp.inv_w, bp.magic);
+      return fma_rz(__uint_as_float(__float_as_uint(th) | (db & 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w,
+                    FINE ? bp.magic_f : bp.magic);
 #endif
     } else {
       const float h = fmaf(ns, 1.57079632679489662f, 1.57079632679489662f);  // 0 or pi
-      const float t = fmaf(-ns, th, h) * bp.inv_w;                             // theta / w
-      return add_rz(fminf(t, bp.clamp_c), kMagic);
+      const float tr = fmaf(-ns, th, h);                                       // theta
+      return FINE ? add_rz(fminf(tr * bp.inv_w_f, bp.clamp_f), kMagic) : add_rz(fminf(tr * bp.inv_w, bp.clamp_c), kMagic);
     }
   }
 }
@@ -375,16 +407,18 @@ __device__ __forceinline__ int entry_to_bin(int e, const BinParams& bp) {
   return k > bp.nbins - 1 ? bp.nbins - 1 : k;
 }
 
-// The same code as pair_code<MAP, kChordPoly> for a pair whose sign(u.v) is known in advance:
-// SIGN = +1 (separation below 90 degrees) or -1 (above). Bit for bit the general code takes these
-// steps for such a pair (u - v and u + v round the same way as fma(-1, v, u) and fma(1, v, u)),
-// minus the dot product and the two sign-bit operations.
-template <int MAP, int SIGN>
-__device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, float xj, float yj, float zj,
-                                                 const BinParams& bp) {
-  const float dx = SIGN > 0 ? xi - xj : xi + xj;
-  const float dy = SIGN > 0 ? yi - yj : yi + yj;
-  const float dz = SIGN > 0 ? zi - zj : zi + zj;
+// The same code as pair_code<MAP, kChordPoly> for a pair whose sign(u.v) is known in advance
+// (the caps of its warp and j-group put every separation below 90 degrees, or every one above):
+// ns = -sign as +-1.0 and iws = sign / w (or sign * 2^S / w for the fine code) are registers
+// chosen per j-group. Bit for bit the general code takes these steps for such a pair:
+// fma(ns, v, u) is the same difference or sum, and the far-side code fma_rz(-theta', 1/w, m) is
+// fma_rz(theta', -1/w, m). Only the dot product and the two sign-bit operations are dropped.
+template <int MAP, bool FINE = false>
+__device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, float xj, float yj, float zj, float ns,
+                                                 float iws, float hs, const BinParams& bp) {
+  const float dx = fmaf(ns, xj, xi);
+  const float dy = fmaf(ns, yj, yi);
+  const float dz = fmaf(ns, zj, zi);
   const float q = fmaf(dz, dz, fmaf(dy, dy, fmaf(dx, dx, 1e-30f)));
   float p = fmaf(kP7, q, kP6);
   p = fmaf(p, q, kP5);
@@ -395,10 +429,11 @@ __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, f
   p = fmaf(p, q, kP0);
   const float th = sqrt_approx(p * q);
   if (MAP == kMirror) {
-    return fma_rz(SIGN > 0 ? th : -th, bp.inv_w, bp.magic);
+    return fma_rz(th, iws, FINE ? bp.magic_f : bp.magic);
   } else {
-    const float t = (SIGN > 0 ? th : 3.14159265358979323846f - th) * bp.inv_w;
-    return add_rz(fminf(t, bp.clamp_c), kMagic);
+    // theta / w = th * iws + hs with hs = 0 (near side) or pi / w (far side); iws = -1/w there
+    const float t = fmaf(th, iws, hs);
+    return add_rz(fminf(t, FINE ? bp.clamp_f : bp.clamp_c), kMagic);
   }
 }
 
@@ -437,15 +472,64 @@ struct PathTag {
 // Which loop a (warp, j-group) may use: every pair surely below 90 degrees, surely above, or
 // mixed. Two caps at centre angle tc and radii ra, rb hold only separations in
 // [tc - ra - rb, tc + ra + rb]; all are below 90 degrees iff cos tc > sin(ra + rb) and all above
-// iff cos tc < -sin(ra + rb). __sinf is accurate to ~1e-6 here and the margins cover it.
-__device__ __forceinline__ int choose_path(float4 a, float4 b) {
+// iff cos tc < -sin(ra + rb). __sinf/__cosf are accurate to ~1e-6 here and the margins cover it.
+// kExactBit is added when the exact mode must check this group: mode 2 always, mode 1 when some
+// separation may be below lo or above pi - lo (cos tc > cos(lo + r) or < -cos(lo + r)).
+constexpr int kExactBit = 4;
+__device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float lo) {
   const float dot = a.x * b.x + a.y * b.y + a.z * b.z;
   const float r = a.w + b.w + 1e-4f;
-  if (r >= 1.5f) return kGeneral;
-  const float sr = __sinf(r) + 1e-5f;
-  if (dot > sr) return kBelow90;
-  if (dot < -sr) return kAbove90;
-  return kGeneral;
+  int path = kGeneral;
+  if (r < 1.5f) {
+    const float sr = __sinf(r) + 1e-5f;
+    if (dot > sr) path = kBelow90;
+    else if (dot < -sr) path = kAbove90;
+  }
+  if (mode == 2) return path | kExactBit;
+  if (mode == 1) {
+    const float x = lo + r;
+    if (x >= 3.0f) return path | kExactBit;
+    const float cl = __cosf(x) - 1e-5f;
+    if (dot > cl || dot < -cl) return path | kExactBit;
+  }
+  return path;
+}
+
+template <bool F>
+struct FineTag {
+  static constexpr bool value = F;
+};
+
+// Add one pair to the shared histogram. With F (exact mode) the code carries fine_shift extra
+// fractional bits: the entry is the code's integer part, and a pair whose fraction lies within one
+// fine unit of an edge (fraction 0 or all ones) is queued for an fp64 re-decision.
+template <bool F>
+__device__ __forceinline__ void count_pair(const PairParams& p, float code, uint32_t base, uint32_t base_f, int shift,
+                                           uint32_t magic_bits, int i, int j, float xi, float yi, float zi,
+                                           float4 v, unsigned int* s_qcount) {
+  const uint32_t cb = __float_as_uint(code);
+  if (!F) {
+    if (ACF_CHECK(cb - magic_bits < (uint32_t)p.bp.entries, 1, (long long)(cb - magic_bits), i, code, xi, yi, zi, v.x,
+                  v.y, v.z, (float)j))
+      red_shared_add((cb << shift) + base, p.inc);
+  } else {
+    const int S = p.bp.fine_shift;
+    if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i, code,
+                  xi, yi, zi, v.x, v.y, v.z, (float)j))
+      red_shared_add(((cb >> S) << shift) + base_f, p.inc);
+    const uint32_t mask = (1u << S) - 1u;
+    if (((cb + 1u) & mask) <= 1u) {
+      // near an edge: re-decide it if its entry lies in the exact zone (a function of the pair's own
+      // code, so the set of re-decided pairs does not depend on grouping or order)
+      const uint32_t e = (cb - magic_bits) >> S;
+      if (e - p.bp.zone0 <= p.bp.span0 || e - p.bp.zone1 <= p.bp.span1) {
+        // a slot of this block's reserved batch (shared-memory counter), or past it a global one
+        const unsigned int local = atomicAdd(s_qcount, 1u);
+        const unsigned int slot = local < p.qbatch ? s_qcount[1] + local : atomicAdd(p.qtotal, 1u);
+        if (slot < p.qcap) p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ pair kernel
@@ -506,11 +590,16 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   float4* my_tiles = reinterpret_cast<float4*>(smem) + warp * 2 * kJT;  // [2][kJT] per warp
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + WARPS * 2 * kJT * sizeof(float4));
 
+  __shared__ unsigned int s_qcount[2];  // exact mode: [0] flags of this block, [1] first slot of its batch
   const int words = (LAYOUT == kLane) ? p.bp.entries * 32 : p.bp.entries;
   for (int w = tid; w < words; w += THREADS) hist[w] = 0;
   unsigned long long* row = p.partial + (size_t)blockIdx.x * p.bp.nbins;
   if (!p.accumulate)
     for (int k = tid; k < p.bp.nbins; k += THREADS) row[k] = 0ull;
+  if (tid == 0) {
+    s_qcount[0] = 0u;
+    s_qcount[1] = p.exact_mode ? atomicAdd(p.qtotal, p.qbatch) : 0u;
+  }
   __syncthreads();
 
   const uint32_t hist_addr = (uint32_t)__cvta_generic_to_shared(hist);
@@ -520,6 +609,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   // address of entry e in this lane's copy = (code bits << shift) + base
   const uint32_t base = (LAYOUT == kLane) ? hist_addr + lane * 4u - (magic_bits << 7) : hist_addr - (magic_bits << 2);
   constexpr int SHIFT = (LAYOUT == kLane) ? 7 : 2;
+  // exact mode: the fine code is 2^23 + (entry << S) + fraction; entry = (bits >> S) - (bits(2^23) >> S)
+  const uint32_t base_f = (LAYOUT == kLane) ? hist_addr + lane * 4u - ((magic_bits >> p.bp.fine_shift) << 7)
+                                            : hist_addr - ((magic_bits >> p.bp.fine_shift) << 2);
   const int ni = (int)p.ni, nj = (int)p.nj;
 
   // tickets: the unit being computed (u), the one whose tile is in flight (un), and one fetched
@@ -547,6 +639,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     float xi[K], yi[K], zi[K];
     float4 icap = make_float4(1.f, 0.f, 0.f, 4.f);
     int cur_r = -1, buf = 0;
+    // j-groups per path (x 32*kJT pairs): fixed, general, fixed+flag, general+flag
+    unsigned int g_fixed = 0, g_general = 0, g_fixed_f = 0, g_general_f = 0;
+    unsigned long long edge_pairs = 0ull;
     while (true) {
       int rn = 0, cn = 0;
       if (un < p.unit_end) {
@@ -586,30 +681,45 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       }
 #endif
       if (full) {
-        // one loop per (32-galaxy j-group, path); the path is uniform across the warp
-        auto run = [&](auto tag, int jbeg) {
-          constexpr int P = decltype(tag)::value;
-#pragma unroll kJJUnroll
+        // one loop per (32-galaxy j-group, path); the path is uniform across the warp. The fixed
+        // loops take the sign in registers (ns, iws, hs); the fine (exact) loops are rare and kept
+        // rolled so that all live loop bodies fit the instruction cache.
+        auto run = [&](auto fixed, auto fine, int jbeg, float ns, float iws, float hs) {
+          constexpr bool X = decltype(fixed)::value;
+          constexpr bool F = decltype(fine)::value;
+          constexpr int U = F ? kJJUnrollFine : kJJUnroll;
+#pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
             const float4 v = tile[jj];
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-              const float code = (P == kBelow90)   ? pair_code_fixed<MAP, 1>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
-                                 : (P == kAbove90) ? pair_code_fixed<MAP, -1>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
-                                                   : pair_code<MAP, METHOD>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-              if (ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
-                            (long long)(__float_as_uint(code) - magic_bits), i0 + k * 32 + lane, code, xi[k], yi[k],
-                            zi[k], v.x, v.y, v.z, (float)(P * 1000 + jj)))
-                red_shared_add((__float_as_uint(code) << SHIFT) + base, p.inc);
+              const float code = X ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, hs, p.bp)
+                                   : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
+              count_pair<F>(p, code, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
+                            zi[k], v, s_qcount);
             }
           }
         };
 #pragma unroll 1
         for (int g = 0; g < kJT / 32; ++g) {
-          const int path = (METHOD == kChordPoly) ? choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + g)) : kGeneral;
-          if (path == kBelow90) run(PathTag<kBelow90>(), g * 32);
-          else if (path == kAbove90) run(PathTag<kAbove90>(), g * 32);
-          else run(PathTag<kGeneral>(), g * 32);
+          const int pc = (METHOD == kChordPoly)
+                             ? choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + g), p.exact_mode, p.exact_lo)
+                             : kGeneral;
+          const int path = pc & 3;
+          const bool fine = (pc & kExactBit) != 0;
+          const float iw = fine ? p.bp.inv_w_f : p.bp.inv_w;
+          const float ns = (path == kBelow90) ? -1.0f : 1.0f;
+          const float iws = (path == kBelow90) ? iw : -iw;
+          const float hs = (path == kBelow90) ? 0.0f : 3.14159265358979323846f * iw;
+          if (path == kGeneral) (fine ? g_general_f : g_general) += 1;
+          else (fine ? g_fixed_f : g_fixed) += 1;
+          if (path == kGeneral) {
+            if (fine) run(FineTag<false>(), FineTag<true>(), g * 32, ns, iws, hs);
+            else run(FineTag<false>(), FineTag<false>(), g * 32, ns, iws, hs);
+          } else {
+            if (fine) run(FineTag<true>(), FineTag<true>(), g * 32, ns, iws, hs);
+            else run(FineTag<true>(), FineTag<false>(), g * 32, ns, iws, hs);
+          }
         }
       } else {
         // pair (i, j) counts iff jj > thr[k]: thr = -1 for every j, a diagonal offset when only
@@ -621,18 +731,23 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const int tt = p.sym ? i - j0 : -1;
           thr[k] = (i >= ni) ? 0x7fffffff : max(-1, min(tt, kJT));
         }
-        for (int jj = 0; jj < jn; ++jj) {
-          const float4 v = tile[jj];
+        auto edge = [&](auto fine) {
+          constexpr bool F = decltype(fine)::value;
+#pragma unroll 1
+          for (int jj = 0; jj < jn; ++jj) {
+            const float4 v = tile[jj];
 #pragma unroll
-          for (int k = 0; k < K; ++k) {
-            const float code = pair_code<MAP, METHOD>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-            if (jj > thr[k] &&
-                ACF_CHECK(__float_as_uint(code) - magic_bits < (uint32_t)p.bp.entries, 1,
-                          (long long)(__float_as_uint(code) - magic_bits), i0 + k * 32 + lane, code, xi[k], yi[k],
-                          zi[k], v.x, v.y, v.z, (float)jj))
-              red_shared_add((__float_as_uint(code) << SHIFT) + base, p.inc);
+            for (int k = 0; k < K; ++k) {
+              const float code = pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
+              if (jj > thr[k])
+                count_pair<F>(p, code, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
+                              zi[k], v, s_qcount);
+            }
           }
-        }
+        };
+        if (p.exact_mode && METHOD == kChordPoly) edge(FineTag<true>());
+        else edge(FineTag<false>());
+        edge_pairs += (unsigned long long)jn * kJT;
       }
       __syncwarp();  // every lane is done with this buffer before the next prefetch refills it
       if (un >= p.unit_end) break;
@@ -643,8 +758,24 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       buf ^= 1;
     }
     cp_async_wait<0>();
+    if (lane == 0) {
+      constexpr unsigned long long G = 32 * kJT;
+      if (g_fixed) atomicAdd(p.path_pairs + 0, g_fixed * G);
+      if (g_general) atomicAdd(p.path_pairs + 1, g_general * G);
+      if (g_fixed_f) atomicAdd(p.path_pairs + 2, g_fixed_f * G);
+      if (g_general_f) atomicAdd(p.path_pairs + 3, g_general_f * G);
+      if (edge_pairs) atomicAdd(p.path_pairs + 4, edge_pairs);
+    }
   }
   __syncthreads();
+  if (p.exact_mode) {
+    // mark the unused tail of this block's batch, and report its flags
+    for (unsigned int k = s_qcount[0] + tid; k < p.qbatch; k += THREADS) {
+      const unsigned int slot = s_qcount[1] + k;
+      if (slot < p.qcap) p.queue[slot] = make_uint4(0xFFFFFFFFu, 0u, 0u, 0u);
+    }
+    if (tid == 0) atomicAdd(p.qflagged, s_qcount[0]);
+  }
   flush_hist<K, THREADS, LAYOUT, MAP, METHOD>(p, hist, false);
 }
 
@@ -685,6 +816,56 @@ __global__ void omega_kernel(const unsigned long long* __restrict__ dd, const un
     } else {
       const double num = (double)dd[k] * f_dd - 2.0 * (double)dr[k] * f_dr + (double)r;
       omega[k] = num / (double)r;
+    }
+  }
+}
+
+// Edge thresholds of the exact re-decision, in fp64: bin k starts where the difference chord
+// reaches T[k] = 4 sin^2(k w / 2), or, for pairs past 90 degrees, where the sum chord falls to
+// U[k] = 4 cos^2(k w / 2).
+__global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ T, double* __restrict__ U) {
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k <= nbins; k += gridDim.x * blockDim.x) {
+    double sh, ch;
+    sincos(0.5 * w_rad * k, &sh, &ch);
+    T[k] = 4.0 * sh * sh;
+    U[k] = 4.0 * ch * ch;
+  }
+}
+
+// Re-decide every queued pair in fp64 from the fp64 unit vectors and move its count if the fast
+// code put it in a neighbouring bin. Runs after the merge, on the final histogram.
+template <int MAP>
+__global__ void fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qtotal,
+                             unsigned int qcap, const double4* __restrict__ vi, const double4* __restrict__ vj,
+                             const double* __restrict__ T, const double* __restrict__ U, BinParams bp,
+                             unsigned int inc, unsigned long long* __restrict__ out, unsigned int* __restrict__ moved) {
+  const unsigned int nq = min(*qtotal, qcap);
+  const uint32_t magic_bits = __float_as_uint(kMagic);
+  for (unsigned int s = blockIdx.x * blockDim.x + threadIdx.x; s < nq; s += gridDim.x * blockDim.x) {
+    const uint4 rec = queue[s];
+    if (rec.x == 0xFFFFFFFFu) continue;  // unused slot of a reserved batch
+    const double4 a = vi[rec.x], b = vj[rec.y];
+    int e = (int)((rec.z - magic_bits) >> bp.fine_shift);
+    e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
+    const int kf = entry_to_bin<MAP>(e, bp);
+    int k = kf;
+    const double dot = a.x * b.x + a.y * b.y + a.z * b.z;
+    k = k > bp.kmax ? bp.kmax : k;
+    if (dot >= 0.0) {
+      const double dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z;
+      const double q = dx * dx + dy * dy + dz * dz;
+      while (k > 0 && q < T[k]) --k;
+      while (k < bp.kmax && q >= T[k + 1]) ++k;
+    } else {
+      const double dx = a.x + b.x, dy = a.y + b.y, dz = a.z + b.z;
+      const double q = dx * dx + dy * dy + dz * dz;
+      while (k > 0 && q > U[k]) --k;
+      while (k < bp.kmax && q <= U[k + 1]) ++k;
+    }
+    if (k != kf) {
+      atomicAdd(out + kf, (unsigned long long)(-(long long)inc));
+      atomicAdd(out + k, (unsigned long long)inc);
+      atomicAdd(moved, 1u);
     }
   }
 }

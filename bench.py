@@ -32,9 +32,11 @@ import synth  # noqa: E402
 
 METRIC = "G pairs/s (DD+DR+RR, N=100k each) and % of FP32 issue roofline"
 UNIT = "Gpairs/s"
-# Thread instructions per evaluated pair in the pair kernel's inner loop (chord, sign, polynomial,
-# sqrt, index, shared-memory add); see DESIGN.md "Roofline".
-INST_PER_PAIR = 23
+# Thread instructions per pair of each pair-kernel path ("Roofline"): the general
+# chord + polynomial loop is 23; where the caps fix the sign of the dot product the dot and the two
+# sign operations drop out (18); the exact-mode flag adds 5 (fine-code address, edge test, branch).
+INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 23, "pairs_fixed_exact": 23, "pairs_general_exact": 28}
+INST_MASKED = 23  # diagonal / ragged units run the general loop on every computed pair
 SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
 # The pages' kernel time for three 100k histograms on an RTX 5080 (another machine: context only)
 PAGE_KERNEL_MS = 22.747
@@ -246,6 +248,22 @@ def run_ours(args, cat, workload, rank, world, local):
         barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kt = ctx.kernel_times()
+    # instructions the algorithm needs per step: one untimed step, reading each call's path counts
+    ctx.set_option("kernel_timing", 0)
+    alg_inst, alg_pairs = 0, 0
+    with torch.cuda.stream(stream):
+        for call in (lambda: acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, None, None, 0, w, nb, dd),
+                     lambda: acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, ra_r, dec_r, cat.n_r, w, nb, dr),
+                     lambda: acf.acf_histogram(ctx.handle, ra_r, dec_r, cat.n_r, None, None, 0, w, nb, rr)):
+            call()
+            for key, ipp in INST_PER_PATH.items():
+                n_pairs = ctx.info(key)
+                alg_inst += ipp * n_pairs
+                alg_pairs += n_pairs
+            masked = ctx.info("pairs_masked")
+            alg_inst += (INST_MASKED + (5 if ctx.info("pairs_fixed_exact") + ctx.info("pairs_general_exact") else 0)) * masked
+            alg_pairs += masked
+    path_mix = {k: ctx.info(k) for k in INST_PER_PATH}
     total_ms = sum(step_ms)
     total_ms_max, = reduce_max([total_ms], world)
     pairs = logical_pairs(cat.n_d, cat.n_r)
@@ -255,10 +273,11 @@ def run_ours(args, cat, workload, rank, world, local):
     pair_ms = sum(kt)
     clocks = clk.summary()
     peak = SMS * LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12  # T thread-instructions / s at the maximum clock
-    achieved = INST_PER_PAIR * evals * args.steps / (pair_ms / 1e3) / 1e12 if pair_ms > 0 else None
+    achieved = alg_inst * args.steps / (pair_ms / 1e3) / 1e12 if pair_ms > 0 else None
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
             "frac": (achieved / peak) if achieved else None, "traffic": recorded_traffic(workload),
-            "inst_per_pair": INST_PER_PAIR, "pair_kernel_ms_per_launch": pair_ms / max(len(kt), 1),
+            "inst_per_pair": alg_inst / max(alg_pairs, 1), "pairs_computed_per_step": alg_pairs,
+            "pair_kernel_ms_per_launch": pair_ms / max(len(kt), 1),
             "pair_kernel_launches": len(kt),
             "peak_basis": f"{SMS} SMs x {LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz (maximum SM clock)"}
     if clocks.get("sm_mhz"):
@@ -268,7 +287,6 @@ def run_ours(args, cat, workload, rank, world, local):
     h = {k: torch.from_numpy(getattr(cat, k)).pin_memory() for k in ("ra_d", "dec_d", "ra_r", "dec_r")}
     hout = [torch.empty(nb, dtype=torch.int64).pin_memory() for _ in range(3)] + [
         torch.empty(nb, dtype=torch.float64).pin_memory()]
-    ctx.set_option("kernel_timing", 0)
 
     def e2e_step():
         acf.acf_correlate_host(ctx.handle, h["ra_d"], h["dec_d"], cat.n_d, h["ra_r"], h["dec_r"], cat.n_r, w, nb,

@@ -11,6 +11,7 @@ os.environ["ACF_DEBUG_BOUNDS"] = "1"
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import all_pairs_angular_gb300 as acf  # noqa: E402
@@ -29,7 +30,13 @@ def main() -> int:
         (3000, 2500, 60.0, 3, 0, 0, 0),
     ]
     bad = 0
+    cases += [(3000, 2500, 0.25, 720, 0, 0, 10), (3000, 2500, 0.01, 18000, 0, 0, 10), (3000, 2500, 0.35, 515, 0, 0, 10),
+              (3000, 2500, 0.25, 720, 0, 0, 20)]
     for n1, n2, w, nb, layout, threads, method in cases:
+        # method 10 / 20: chord method with exact mode 2 / 0
+        exact = {10: 2, 20: 0}.get(method, 1)
+        method = 0 if method >= 10 else method
+        ctx.set_option("exact", exact)
         ctx.set_option("layout", layout)
         ctx.set_option("threads", threads)
         ctx.set_option("bin_method", method)
@@ -46,7 +53,10 @@ def main() -> int:
             o = oracle.histogram(*args, bin_width_deg=w, nbins=nb)
             rep = check.edge_flux(gh, o.hist, o.near_below, o.near_above)
             ok = rep.ok if method == 0 else int(gh.sum()) == int(o.hist.sum())
-            print("case", (n1, n2, w, nb, layout, threads, method), "ok" if ok else "MISMATCH " + str(rep), flush=True)
+            if exact == 2:
+                ok = ok and np.array_equal(gh, o.hist)
+            print("case", (n1, n2, w, nb, layout, threads, method, exact), "ok" if ok else "MISMATCH " + str(rep),
+                  flush=True)
             bad += 0 if ok else 1
     ctx.close()
     return 1 if bad else 0

@@ -69,6 +69,9 @@ def test_full_histograms_match_golden_oracle(acf, ctx, idx):
     dev = np.abs(om[big] - ref_om[big])
     print(f"config {idx}: net moved pairs {moved}; bins with RR>=1000: {int(big.sum())}, of which "
           f"{int((big & ~same).sum())} hold a moved pair; max |d omega| = {float(dev.max()):.3e}")
+    # the omega rule, literally: |d omega| <= 1e-5 on every bin with RR >= 1000 (the default exact
+    # mode re-decides near-edge pairs below 20 and above 160 degrees, where RR is small)
+    assert float(dev.max()) <= 1e-5
 
 
 def _row_sample_check(acf, ctx, c, rows, seed):
@@ -88,7 +91,9 @@ def _full_totals(acf, ctx, c):
     w, nb = c.bin_width_deg, c.nbins
     ra_d, dec_d, ra_r, dec_r = map(_dev, (c.ra_d, c.dec_d, c.ra_r, c.dec_r))
     dd = acf.as_uint64(ctx.histogram(ra_d, dec_d, bin_width_deg=w, nbins=nb))
+    assert ctx.info("exact_overflow") == 0
     dr = acf.as_uint64(ctx.histogram(ra_d, dec_d, ra_r, dec_r, bin_width_deg=w, nbins=nb))
+    assert ctx.info("exact_overflow") == 0
     rr = acf.as_uint64(ctx.histogram(ra_r, dec_r, bin_width_deg=w, nbins=nb))
     torch.cuda.synchronize()
     assert int(dd.sum()) == c.n_d ** 2 and int(dr.sum()) == c.n_d * c.n_r and int(rr.sum()) == c.n_r ** 2
@@ -111,3 +116,21 @@ def test_fine_binning_200k_rows_and_totals(acf, ctx):
     c = synth.config(4)
     _row_sample_check(acf, ctx, c, 2000, seed=5)
     _full_totals(acf, ctx, c)
+
+
+def test_exact_everywhere_is_bit_identical_at_full_size(acf, ctx):
+    # exact mode 2 re-decides every pair within one fine unit of an edge in fp64
+    with open(os.path.join(GOLDEN, "config1_oracle.json")) as f:
+        g = json.load(f)
+    c = synth.config(1)
+    assert c.digest() == g["digest"]
+    ctx.set_option("exact", 2)
+    try:
+        ra_d, dec_d, ra_r, dec_r = map(_dev, (c.ra_d, c.dec_d, c.ra_r, c.dec_r))
+        for fam, args in (("DD", (ra_d, dec_d)), ("DR", (ra_d, dec_d, ra_r, dec_r)), ("RR", (ra_r, dec_r))):
+            h = acf.as_uint64(ctx.histogram(*args, bin_width_deg=c.bin_width_deg, nbins=c.nbins))
+            torch.cuda.synchronize()
+            assert np.array_equal(h, np.array(g[fam]["hist"], np.uint64)), fam
+            assert ctx.info("exact_overflow") == 0
+    finally:
+        ctx.set_option("exact", 1)

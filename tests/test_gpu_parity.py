@@ -262,3 +262,37 @@ def test_split_launches_accumulate(acf, ctx, layout):
     finally:
         ctx.set_option("units_per_launch", 0)
         ctx.set_option("layout", 0)
+
+
+@pytest.mark.parametrize("w,nb", [(0.25, 720), (0.35, 515), (0.01, 18000), (0.25, 1440)])
+def test_exact_mode_2_equals_oracle_bin_for_bin(acf, ctx, w, nb):
+    c = synth.catalogs(4000, 3100, 12, 30.0, seed=14)
+    ctx.set_option("exact", 2)
+    try:
+        for args in ((c.ra_d, c.dec_d, None, None), (c.ra_d, c.dec_d, c.ra_r, c.dec_r)):
+            g, o, rep = _compare(acf, ctx, *args, w, nb)
+            assert np.array_equal(g, o.hist), rep
+    finally:
+        ctx.set_option("exact", 1)
+
+
+def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
+    c = synth.catalogs(4000, 3100, 12, 30.0, seed=15)
+    ctx.set_option("exact", 0)
+    try:
+        _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+        _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+        assert ctx.info("exact_flagged") == 0
+    finally:
+        ctx.set_option("exact", 1)
+
+
+def test_path_counters_cover_every_computed_pair(acf, ctx):
+    c = synth.catalogs(5000, 4100, 12, 30.0, seed=16)
+    ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+    keys = ("pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact", "pairs_masked")
+    got = {k: ctx.info(k) for k in keys}
+    rows = -(-5000 // 128)
+    # every unit computes its whole 128-wide i-set against the j-chunk's real length
+    assert sum(got.values()) == rows * 128 * 4100, got
+    assert got["pairs_fixed"] > 0 and got["pairs_masked"] > 0
