@@ -186,21 +186,34 @@ __device__ __forceinline__ float4 radec_to_unit(float ra_arcmin, float dec_arcmi
 // ------------------------------------------------------------------ spatial order and caps
 //
 // Catalogs are put in a spatial order before pairing: galaxies sorted by cell of a cube map
-// (6 faces x 64 x 64 cells, Morton order within a face). A warp's i-galaxies and a j-chunk then
+// (6 faces x 128 x 128 cells, Hilbert order within a face). A warp's i-galaxies and a j-chunk then
 // each cover a small patch of sky, bounded by a "cap" (centre, angular radius). From two caps
 // the kernel knows when every pair of a (warp, chunk) is surely below or surely above 90
 // degrees, and drops the per-pair sign decision there. The order changes no result: every
 // pair's bin is computed by the same arithmetic whichever path evaluates it.
 
-constexpr int kFaceCells = 64;
+constexpr int kFaceBits = 7;
+constexpr int kFaceCells = 1 << kFaceBits;
 constexpr int kCells = 6 * kFaceCells * kFaceCells;
 
-__device__ __forceinline__ unsigned int spread_bits6(unsigned int x) {  // 6 bits -> even positions
-  x &= 63u;
-  x = (x | (x << 4)) & 0x30Fu;
-  x = (x | (x << 2)) & 0x333u;
-  x = (x | (x << 1)) & 0x555u;
-  return x;
+// Position of cell (x, y) along the Hilbert curve through a 2^kFaceBits square: consecutive
+// positions are adjacent cells, so runs of sorted galaxies stay compact (no Morton jumps).
+__device__ __forceinline__ unsigned int hilbert_index(unsigned int x, unsigned int y) {
+  unsigned int d = 0;
+  for (unsigned int s = kFaceCells / 2; s > 0; s >>= 1) {
+    const unsigned int rx = (x & s) ? 1u : 0u, ry = (y & s) ? 1u : 0u;
+    d += s * s * ((3u * rx) ^ ry);
+    if (ry == 0) {
+      if (rx == 1) {
+        x = s - 1 - (x & (s - 1)) + (x & ~(s - 1));
+        y = s - 1 - (y & (s - 1)) + (y & ~(s - 1));
+      }
+      const unsigned int t = x;
+      x = y;
+      y = t;
+    }
+  }
+  return d;
 }
 
 __device__ __forceinline__ unsigned int cell_of(double x, double y, double z) {
@@ -214,7 +227,7 @@ __device__ __forceinline__ unsigned int cell_of(double x, double y, double z) {
   int iv = (int)((v / m + 1.0) * 0.5 * kFaceCells);
   iu = iu < 0 ? 0 : (iu >= kFaceCells ? kFaceCells - 1 : iu);
   iv = iv < 0 ? 0 : (iv >= kFaceCells ? kFaceCells - 1 : iv);
-  return (unsigned int)face * (kFaceCells * kFaceCells) + (spread_bits6(iu) | (spread_bits6(iv) << 1));
+  return (unsigned int)face * (kFaceCells * kFaceCells) + hilbert_index((unsigned)iu, (unsigned)iv);
 }
 
 // (RA, Dec) arcminutes -> fp64 unit vector; non-finite inputs become (0, 0).
@@ -242,19 +255,17 @@ __global__ void prep_kernel(const float* __restrict__ ra, const float* __restric
   }
 }
 
-// Exclusive prefix sum of the cell counts (one block of 1024 threads).
+// Exclusive prefix sum of the cell counts (one block of 1024 threads, each owning PER consecutive
+// cells: sum them, scan the sums across the block, then walk the cells again writing offsets).
 __global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restrict__ cell_count,
                                                      unsigned int* __restrict__ cursor) {
   constexpr int PER = (kCells + 1023) / 1024;
   __shared__ unsigned int part[1024];
   const int t = threadIdx.x;
-  unsigned int loc[PER];
   unsigned int s = 0;
-#pragma unroll
   for (int e = 0; e < PER; ++e) {
     const int c = t * PER + e;
-    loc[e] = c < kCells ? cell_count[c] : 0u;
-    s += loc[e];
+    s += c < kCells ? cell_count[c] : 0u;
   }
   part[t] = s;
   __syncthreads();
@@ -265,11 +276,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restri
     __syncthreads();
   }
   unsigned int run = part[t] - s;
-#pragma unroll
   for (int e = 0; e < PER; ++e) {
     const int c = t * PER + e;
-    if (c < kCells) cursor[c] = run;
-    run += loc[e];
+    if (c < kCells) {
+      cursor[c] = run;
+      run += cell_count[c];
+    }
   }
 }
 
@@ -501,34 +513,35 @@ struct FineTag {
 };
 
 // Add one pair to the shared histogram. With F (exact mode) the code carries fine_shift extra
-// fractional bits: the entry is the code's integer part, and a pair whose fraction lies within one
-// fine unit of an edge (fraction 0 or all ones) is queued for an fp64 re-decision.
+// fractional bits: the entry is the code's integer part. Returns whether the pair lies within one
+// fine unit of an edge (fraction 0 or all ones); such pairs go to push_flagged.
 template <bool F>
-__device__ __forceinline__ void count_pair(const PairParams& p, float code, uint32_t base, uint32_t base_f, int shift,
-                                           uint32_t magic_bits, int i, int j, float xi, float yi, float zi,
-                                           float4 v, unsigned int* s_qcount) {
-  const uint32_t cb = __float_as_uint(code);
+__device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint32_t base, uint32_t base_f, int shift,
+                                         uint32_t magic_bits, int i, int j, float xi, float yi, float zi, float4 v) {
   if (!F) {
-    if (ACF_CHECK(cb - magic_bits < (uint32_t)p.bp.entries, 1, (long long)(cb - magic_bits), i, code, xi, yi, zi, v.x,
-                  v.y, v.z, (float)j))
+    if (ACF_CHECK(cb - magic_bits < (uint32_t)p.bp.entries, 1, (long long)(cb - magic_bits), i,
+                  __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
       red_shared_add((cb << shift) + base, p.inc);
+    return false;
   } else {
     const int S = p.bp.fine_shift;
-    if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i, code,
-                  xi, yi, zi, v.x, v.y, v.z, (float)j))
+    if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i,
+                  __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
       red_shared_add(((cb >> S) << shift) + base_f, p.inc);
-    const uint32_t mask = (1u << S) - 1u;
-    if (((cb + 1u) & mask) <= 1u) {
-      // near an edge: re-decide it if its entry lies in the exact zone (a function of the pair's own
-      // code, so the set of re-decided pairs does not depend on grouping or order)
-      const uint32_t e = (cb - magic_bits) >> S;
-      if (e - p.bp.zone0 <= p.bp.span0 || e - p.bp.zone1 <= p.bp.span1) {
-        // a slot of this block's reserved batch (shared-memory counter), or past it a global one
-        const unsigned int local = atomicAdd(s_qcount, 1u);
-        const unsigned int slot = local < p.qbatch ? s_qcount[1] + local : atomicAdd(p.qtotal, 1u);
-        if (slot < p.qcap) p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
-      }
-    }
+    return ((cb + 1u) & ((1u << S) - 1u)) <= 1u;
+  }
+}
+
+// Queue a near-edge pair for the fp64 re-decision if its entry lies in the exact zone (a function
+// of the pair's own code, so the set of re-decided pairs does not depend on grouping or order).
+__device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, uint32_t magic_bits, int i, int j,
+                                             unsigned int* s_qcount) {
+  const uint32_t e = (cb - magic_bits) >> p.bp.fine_shift;
+  if (e - p.bp.zone0 <= p.bp.span0 || e - p.bp.zone1 <= p.bp.span1) {
+    // a slot of this block's reserved batch (shared-memory counter), or past it a global one
+    const unsigned int local = atomicAdd(s_qcount, 1u);
+    const unsigned int slot = local < p.qbatch ? s_qcount[1] + local : atomicAdd(p.qtotal, 1u);
+    if (slot < p.qcap) p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
   }
 }
 
@@ -691,12 +704,22 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
             const float4 v = tile[jj];
+            uint32_t cbs[K];
+            unsigned int near = 0u;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               const float code = X ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, hs, p.bp)
                                    : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-              count_pair<F>(p, code, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
-                            zi[k], v, s_qcount);
+              cbs[k] = __float_as_uint(code);
+              if (add_pair<F>(p, cbs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
+                              yi[k], zi[k], v))
+                near |= 1u << k;
+            }
+            // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
+            if (F && __any_sync(0xffffffffu, near != 0u)) {
+#pragma unroll
+              for (int k = 0; k < K; ++k)
+                if (near & (1u << k)) push_flagged(p, cbs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
             }
           }
         };
@@ -738,10 +761,10 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             const float4 v = tile[jj];
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-              const float code = pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-              if (jj > thr[k])
-                count_pair<F>(p, code, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
-                              zi[k], v, s_qcount);
+              const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
+              if (jj > thr[k] &&
+                  add_pair<F>(p, cb, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k], v))
+                push_flagged(p, cb, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
             }
           }
         };
