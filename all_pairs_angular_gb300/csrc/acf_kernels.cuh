@@ -186,13 +186,13 @@ __device__ __forceinline__ float4 radec_to_unit(float ra_arcmin, float dec_arcmi
 // ------------------------------------------------------------------ spatial order and caps
 //
 // Catalogs are put in a spatial order before pairing: galaxies sorted by cell of a cube map
-// (6 faces x 128 x 128 cells, Hilbert order within a face). A warp's i-galaxies and a j-chunk then
+// (6 faces x 64 x 64 cells, Hilbert order within a face). A warp's i-galaxies and a j-chunk then
 // each cover a small patch of sky, bounded by a "cap" (centre, angular radius). From two caps
 // the kernel knows when every pair of a (warp, chunk) is surely below or surely above 90
 // degrees, and drops the per-pair sign decision there. The order changes no result: every
 // pair's bin is computed by the same arithmetic whichever path evaluates it.
 
-constexpr int kFaceBits = 7;
+constexpr int kFaceBits = 6;
 constexpr int kFaceCells = 1 << kFaceBits;
 constexpr int kCells = 6 * kFaceCells * kFaceCells;
 
@@ -255,33 +255,41 @@ __global__ void prep_kernel(const float* __restrict__ ra, const float* __restric
   }
 }
 
-// Exclusive prefix sum of the cell counts (one block of 1024 threads, each owning PER consecutive
-// cells: sum them, scan the sums across the block, then walk the cells again writing offsets).
+// Exclusive prefix sum of the cell counts, one block of 1024 threads: rounds of 1024 consecutive
+// cells (coalesced loads), each scanned with warp shuffles and the 32 warp totals, plus the carry.
 __global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restrict__ cell_count,
                                                      unsigned int* __restrict__ cursor) {
-  constexpr int PER = (kCells + 1023) / 1024;
-  __shared__ unsigned int part[1024];
-  const int t = threadIdx.x;
-  unsigned int s = 0;
-  for (int e = 0; e < PER; ++e) {
-    const int c = t * PER + e;
-    s += c < kCells ? cell_count[c] : 0u;
-  }
-  part[t] = s;
+  __shared__ unsigned int warp_sum[32];
+  __shared__ unsigned int carry;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) carry = 0u;
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan of the thread sums
-    const unsigned int add = t >= off ? part[t - off] : 0u;
-    __syncthreads();
-    part[t] += add;
-    __syncthreads();
-  }
-  unsigned int run = part[t] - s;
-  for (int e = 0; e < PER; ++e) {
-    const int c = t * PER + e;
-    if (c < kCells) {
-      cursor[c] = run;
-      run += cell_count[c];
+  for (int base = 0; base < kCells; base += 1024) {
+    const int c = base + t;
+    const unsigned int x = c < kCells ? cell_count[c] : 0u;
+    unsigned int v = x;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
     }
+    if (lane == 31) warp_sum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {  // scan the warp totals
+      unsigned int w = warp_sum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    const unsigned int before = carry + (warp > 0 ? warp_sum[warp - 1] : 0u) + v - x;
+    if (c < kCells) cursor[c] = before;
+    __syncthreads();
+    if (t == 1023) carry = before + x;
+    __syncthreads();
   }
 }
 
