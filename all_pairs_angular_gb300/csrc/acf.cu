@@ -63,6 +63,7 @@ struct acf_ctx {
   // info about the last histogram
   long long info_grid = 0, info_threads = 0, info_ctas = 0, info_chunks = 0, info_layout = 0, info_map = 0,
             info_entries = 0, info_smem = 0, info_pairs = 0, info_flush = 0;
+  long long kernel_launches = 0;  // kernels this context has launched, over its lifetime
   // kernel timing
   std::vector<cudaEvent_t> ev;  // pairs (start, stop)
   int ev_used = 0;
@@ -88,6 +89,13 @@ int cuda_fail(acf_ctx* c, cudaError_t e, const char* what) {
   do {                                                     \
     cudaError_t e_ = (call);                               \
     if (e_ != cudaSuccess) return cuda_fail((c), e_, #call); \
+  } while (0)
+
+// Check a kernel launch just made on context c and count it.
+#define ACF_LAUNCHED(c)                   \
+  do {                                    \
+    ACF_CUDA((c), cudaGetLastError());    \
+    ++(c)->kernel_launches;               \
   } while (0)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -285,14 +293,14 @@ int prepare_catalog(acf_ctx* c, const float* ra, const float* dec, long long n, 
   const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 16);
   ACF_CUDA(c, cudaMemsetAsync(s.cell_count, 0, (size_t)kCells * 4, c->stream));
   prep_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, cb.key, s.cell_count);
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   scan_kernel<<<1, 1024, 0, c->stream>>>(s.cell_count, s.cursor);
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   scatter_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, cb.key, n, s.cursor, cb.v, cb.v64);
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   const long long warps = (n + 127) / 128;
   caps_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, c->stream>>>(cb.v, n, cb.cap32, cb.cap128);
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   return ACF_OK;
 }
 
@@ -369,7 +377,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
     if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
     L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
-    ACF_CUDA(c, cudaGetLastError());
+    ACF_LAUNCHED(c);
     if (timed) {
       ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
       c->ev_used += 2;
@@ -393,7 +401,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   const int mblocks = (pl.bp.nbins + 31) / 32;
   merge_kernel<<<mblocks, 32 * kMergeWarps, 0, c->stream>>>(partial, (int)L.grid, pl.bp.nbins, self,
                                                              reinterpret_cast<unsigned long long*>(out));
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   if (p.exact_mode) {
     // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
     const int fblocks = c->num_sms * 8;
@@ -405,7 +413,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
       fixup_kernel<kClamp><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
                                                            sc.U, pl.bp, p.inc,
                                                            reinterpret_cast<unsigned long long*>(out), sc.counters + 2);
-    ACF_CUDA(c, cudaGetLastError());
+    ACF_LAUNCHED(c);
   }
   c->last_counters = sc.counters;
   c->last_qcap = p.exact_mode ? p.qcap : 0;
@@ -435,7 +443,7 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
   }
   if (pl.exact && sc.qcap > 0) {
     edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U);
-    ACF_CUDA(c, cudaGetLastError());
+    ACF_LAUNCHED(c);
   }
   return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc, out);
 }
@@ -541,7 +549,7 @@ int acf_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t
                                                    reinterpret_cast<const unsigned long long*>(dr),
                                                    reinterpret_cast<const unsigned long long*>(rr), nbins, f_dd, f_dr,
                                                    omega);
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   return ACF_OK;
 }
 
@@ -601,7 +609,7 @@ int acf_pair_bins(acf_ctx* c, const float* ra1, const float* dec1, const float* 
     pair_bins_kernel<kMirror, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
   else
     pair_bins_kernel<kClamp, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
-  ACF_CUDA(c, cudaGetLastError());
+  ACF_LAUNCHED(c);
   return ACF_OK;
 }
 
@@ -650,7 +658,7 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
   } t[] = {{"grid", c->info_grid},       {"threads", c->info_threads},   {"ctas_per_sm", c->info_ctas},
            {"units", c->info_chunks},   {"layout", c->info_layout},     {"bin_map", c->info_map},
            {"hist_entries", c->info_entries}, {"smem_bytes", c->info_smem}, {"pairs_evaluated", c->info_pairs},
-           {"launches", c->info_flush}};
+           {"launches", c->info_flush},  {"kernel_launches", c->kernel_launches}};
   for (auto& e : t)
     if (!strcmp(e.k, key)) {
       *v = e.val;
@@ -764,7 +772,7 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
-                "(about 41 bytes per galaxy of each catalog plus %lld blocks x nbins x 8 bytes); use acf_histogram",
+                "(about 53 bytes per galaxy of each catalog plus %lld blocks x nbins x 8 bytes); use acf_histogram",
                 need, kNoAllocScratchBytes, L.grid);
   void* scratch = nullptr;
   rc = noalloc_scratch(c, c->device, &scratch);

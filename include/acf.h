@@ -16,6 +16,9 @@
  * Precision contract: the kernels work in fp32 on unit vectors built in fp64. The computed
  * separation of every pair is within 1e-6 rad of the fp64 value of the formula above, so a pair
  * can land in a neighbouring bin only if its fp64 theta lies within 1e-6 rad of that bin edge.
+ * In "exact" mode (option below; on by default for separations within 20 degrees of 0 and 180)
+ * pairs whose fp32 separation falls that close to an edge are re-decided in fp64 from the same
+ * unit vectors, so there the bin is the one the fp64 formula gives (up to ~1e-15 relative).
  *
  * Conventions for every entry point:
  *   - Array arguments marked "device" are caller-owned CUDA device pointers on the context's
@@ -96,9 +99,12 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  * rows, the chunk counter) lives in one file-scope device array of 16 MiB that the library
  * reserves on every GPU that loads it, until the process exits. It calls no cudaMalloc, cudaFree
  * or other allocating routine.
- *   - Limit: about 197 KB + 41 bytes per galaxy of each catalog + (blocks * nbins * 8) bytes must
- *     fit in 16 MiB, blocks being the persistent grid (304 on a 152-SM GPU); larger requests return
- *     ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need ~10 MB.
+ *   - Limit: about 197 KB + 53 bytes per galaxy of each catalog + (blocks * nbins * 8) bytes must
+ *     fit in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
+ *     return ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need
+ *     ~11 MB. In exact mode the rest of the array holds the queue of pairs to re-decide; pairs that
+ *     do not fit keep their fp32 bin (still within the precision contract) and are counted by the
+ *     "exact_overflow" info key.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
  *     make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's contents; the
@@ -149,16 +155,31 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    1 = dot product + acosf (the page's exact-acos form; measured alternative,
  *                        does NOT meet the precision contract at small or near-180 separations)
  *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram
+ *   "exact"          0 = fp32 bins only (precision contract above);
+ *                    1 = re-decide in fp64 the pairs within ~1e-6 rad of an edge whose separation is
+ *                        below "exact_below_deg" or above 180 minus it (default);
+ *                    2 = re-decide such pairs at every separation: the histograms then equal those
+ *                        of the fp64 formula
+ *   "exact_below_deg"  the window of mode 1, whole degrees 0..180 (default 20)
  *   "units_per_launch"  cap on work units (128 x 128 pairs) per pair-kernel launch; 0 = automatic
  *                    (large problems are always split so that no 32-bit shared counter can wrap)
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
+ * Unknown keys and out-of-range values return ACF_ERR_ARG and leave the option unchanged.
  */
 int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
 
 /*
  * Read back facts about the last acf_histogram call. Keys: "grid", "threads", "ctas_per_sm",
  * "units", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
- * "pairs_evaluated", "launches" (pair-kernel launches the call was split into).
+ * "pairs_evaluated", "launches" (pair-kernel launches the call was split into),
+ * "kernel_launches" (kernels this context has launched since acf_create, all entry points).
+ * These keys synchronise the context's stream and read device counters of the last call:
+ *   "pairs_fixed", "pairs_general"  pairs evaluated on the fixed-sign and general loops
+ *   "pairs_fixed_exact", "pairs_general_exact"  the same loops with edge flagging (exact mode)
+ *   "pairs_masked"                  pairs of diagonal or ragged units (one compare per pair more)
+ *   "exact_flagged"  pairs flagged for re-decision;  "exact_moved"  of those, pairs moved a bin;
+ *   "exact_overflow"  flagged pairs that did not fit in the queue (kept their fp32 bin)
+ * Unknown keys return ACF_ERR_ARG.
  */
 int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
 

@@ -296,3 +296,23 @@ def test_path_counters_cover_every_computed_pair(acf, ctx):
     # every unit computes its whole 128-wide i-set against the j-chunk's real length
     assert sum(got.values()) == rows * 128 * 4100, got
     assert got["pairs_fixed"] > 0 and got["pairs_masked"] > 0
+
+
+def test_kernel_launch_counter(acf, ctx):
+    """kernel_launches counts every kernel of a call: four catalog-preparation kernels per catalog,
+    the pair kernel and the merge, plus the edge tables and the fix-up in exact mode."""
+    c = synth.catalogs(3000, 2500, 12, 30.0, seed=17)
+
+    def launched(fn):
+        before = ctx.info("kernel_launches")
+        fn()
+        return ctx.info("kernel_launches") - before
+
+    assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 4 + 2 + 2
+    assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25,
+                                          nbins=720)) == 8 + 2 + 2
+    ctx.set_option("exact", 0)
+    try:
+        assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 4 + 2
+    finally:
+        ctx.set_option("exact", 1)
