@@ -32,7 +32,7 @@ struct Plan {
   double w_rad = 0.0;
   int exact = 0;
   float exact_lo = 0.f;
-  int map = kMirror;
+  int map = kDirect;
   int method = kChordPoly;
   int layout = kLane;
   int threads = 256;
@@ -58,6 +58,8 @@ struct acf_ctx {
   long long opt_units_per_launch = 0;
   int opt_exact = 1;              // 0 off, 1 near 0 and 180 degrees, 2 everywhere
   double opt_exact_below_deg = 20.0;
+  int opt_mid = 1;                // 1: the dot form between 45 and 135 degrees
+  int opt_pair_bins_form = 0;     // acf_pair_bins: 0 chord form, 1 dot form where |u.v| < cos 45 deg
   unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
   long long last_qcap = 0;
   // info about the last histogram
@@ -134,14 +136,18 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   pl.w_rad = w_rad;
   const double pr = std::rint(P);
   const bool integral = std::fabs(P - pr) <= 1e-9 * std::max(1.0, P) && pr >= 4.0;
-  long long mirror_entries = integral ? 2 * (long long)std::ceil(pr / 2.0) + 4 : -1;
-  if (pl.method == kChordPoly && integral && mirror_entries <= kMaxEntries) {
-    pl.map = kMirror;
-    bp.off = (int)std::ceil(pr / 2.0) + 2;
-    bp.p_int = (int)pr;
-    bp.entries = (int)mirror_entries;
-    bp.magic = (float)(8388608.0 + bp.off);
+  // direct map: every code is floor(theta / w) exactly, in [0, P - 1] (near-side chords reach at
+  // most P/2 + 1); two spare entries
+  const long long direct_entries = integral ? (long long)pr + 2 : -1;
+  if (pl.method == kChordPoly && integral && direct_entries <= kMaxEntries) {
+    pl.map = kDirect;
+    bp.entries = (int)direct_entries;
+    bp.magic_far = (float)(8388608.0 + pr);
     bp.clamp_c = (float)(bp.entries - 1);
+    // the dot form needs 2^23 + P/2 to be an integer
+    bp.mid = (c->opt_mid && std::fmod(pr, 2.0) == 0.0) ? 1 : 0;
+    bp.magic_mid = (float)(8388608.0 + pr / 2.0);
+    for (int k = 0; k < 8; ++k) bp.rc[k] = (float)(kR[k] / w_rad);
   } else {
     pl.map = kClamp;
     const double fp = std::floor(P * (1.0 + 1e-6)) + 1.0;  // indices the clamp-free range can reach
@@ -150,7 +156,6 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
       return fail(c, ACF_ERR_UNSUPPORTED, "histogram of %lld entries exceeds the %d-entry shared-memory plan",
                   entries, kMaxEntries);
     bp.entries = (int)entries;
-    bp.magic = 8388608.0f;
     bp.clamp_c = (float)(entries - 1);
   }
   // Exact mode: S fractional bits in the bin code make a window of 2^-S bins around every edge,
@@ -167,28 +172,26 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     S = std::max(0, std::min(S, room));
     bp.fine_shift = S;
     bp.inv_w_f = (float)(std::ldexp(1.0, S) / w_rad);
-    bp.magic_f = (float)(8388608.0 + std::ldexp((double)bp.off, S));
+    if (pl.map == kDirect) {
+      bp.magic_far_f = (float)(8388608.0 + std::ldexp(pr, S));
+      bp.magic_mid_f = (float)(8388608.0 + std::ldexp(pr / 2.0, S));
+      for (int k = 0; k < 8; ++k) bp.rc_f[k] = (float)(std::ldexp(kR[k], S) / w_rad);
+    }
     bp.clamp_f = (float)std::ldexp((double)bp.clamp_c + 0.5, S);
   }
   bp.kmax = (int)std::min<double>((double)nbins - 1.0, std::floor(P + 1e-9));
   // exact zone, as histogram entries: everything (mode 2), or separations within exact_lo of
-  // 0 or 180 degrees (mode 1): mirror entries off - L - 1 .. off + L, clamp entries <= L or >= floor(P) - L - 1
+  // 0 or 180 degrees (mode 1): entries <= L or >= floor(P) - L - 1 (both maps index entries by bin)
   bp.zone0 = 0u; bp.span0 = 0xFFFFFFFFu; bp.zone1 = 0u; bp.span1 = 0u;
   if (pl.exact == 1) {
     // L + 2 bins stay within exact_lo, so every zone pair sits in a j-group the caps mark for
-    // re-decision whatever the grouping, and the set of re-decided pairs is order-independent
+    // re-decision (and bin by the chord form) whatever the grouping, and the set of re-decided
+    // pairs is order-independent
     const long long L = std::max<long long>(0, (long long)std::floor(c->opt_exact_below_deg / w_deg) - 2);
-    if (pl.map == kMirror) {
-      bp.zone0 = (unsigned)std::max<long long>(0, bp.off - L - 1);
-      bp.span0 = (unsigned)(2 * L + 1);
-      bp.zone1 = 0xFFFFFFFFu;  // second range unused (e - zone1 wraps above span1 = 0 unless e == zone1)
-      bp.span1 = 0u;
-    } else {
-      bp.zone0 = 0u;
-      bp.span0 = (unsigned)L;
-      bp.zone1 = (unsigned)std::max<long long>(0, (long long)std::floor(P) - L - 1);
-      bp.span1 = 0xFFFFFFFFu - bp.zone1;
-    }
+    bp.zone0 = 0u;
+    bp.span0 = (unsigned)L;
+    bp.zone1 = (unsigned)std::max<long long>(0, (long long)std::floor(P + 1e-9) - L - 1);
+    bp.span1 = 0xFFFFFFFFu - bp.zone1;
   }
   // Shared memory = every warp's double-buffered j-tile (4 KB per warp) + the histogram: 32
   // lane-private copies when they fit beside the tiles of at least 16 warps, else one block-shared
@@ -215,13 +218,13 @@ typedef void (*PairKernelFn)(const PairParams);
 PairKernelFn pick_kernel(const Plan& pl) {
 #define ACF_PICK(T, L, M, X) \
   if (pl.threads == T && pl.layout == L && pl.map == M && pl.method == X) return pair_kernel<kK, T, L, M, X>;
-  ACF_PICK(1024, kLane, kMirror, kChordPoly)
+  ACF_PICK(1024, kLane, kDirect, kChordPoly)
   ACF_PICK(1024, kLane, kClamp, kChordPoly)
-  ACF_PICK(1024, kBlock, kMirror, kChordPoly)
+  ACF_PICK(1024, kBlock, kDirect, kChordPoly)
   ACF_PICK(1024, kBlock, kClamp, kChordPoly)
-  ACF_PICK(512, kLane, kMirror, kChordPoly)
+  ACF_PICK(512, kLane, kDirect, kChordPoly)
   ACF_PICK(512, kLane, kClamp, kChordPoly)
-  ACF_PICK(512, kBlock, kMirror, kChordPoly)
+  ACF_PICK(512, kBlock, kDirect, kChordPoly)
   ACF_PICK(512, kBlock, kClamp, kChordPoly)
   ACF_PICK(1024, kLane, kClamp, kDotAcos)
   ACF_PICK(1024, kBlock, kClamp, kDotAcos)
@@ -233,7 +236,6 @@ PairKernelFn pick_kernel(const Plan& pl) {
 
 // Device buffers of one histogram call, carved out of one scratch region.
 struct CatBufs {
-  unsigned int* key = nullptr;
   float4* v = nullptr;       // unit vectors in spatial order (fp32)
   double4* v64 = nullptr;    // the same in fp64 (exact re-decision)
   float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
@@ -241,9 +243,11 @@ struct CatBufs {
 };
 struct Scratch {
   unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue slots handed out, [2] moved pairs,
-                                       // [3] flagged pairs; bytes 64..103: pairs per path (u64)
-  unsigned int* cell_count = nullptr;  // kCells counters
-  unsigned int* cursor = nullptr;      // kCells
+                                       // [3] flagged pairs; bytes 64..119: pairs per path (u64)
+  unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
+  unsigned int* key1 = nullptr;        // sort: keys after the first pass
+  unsigned int* idx1 = nullptr;        // sort: input indices after the first pass
+  unsigned int* counts = nullptr;      // sort: digit counts per tile, then their offsets
   CatBufs a, b;                        // b only for cross-correlations
   unsigned long long* partial = nullptr;
   double* T = nullptr;                 // exact mode: edge tables, nbins + 1 each
@@ -265,7 +269,6 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   };
   auto cat = [&](long long m, CatBufs& cb) {
     const long long ch = (m + 127) / 128;
-    cb.key = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
     cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
     cb.v64 = reinterpret_cast<double4*>(take((size_t)m * 32));
     cb.cap32 = reinterpret_cast<float4*>(take((size_t)ch * 4 * 16));
@@ -273,10 +276,13 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   };
   Scratch t;
   Scratch& r = s ? *s : t;
-  char* head = take(256 + (size_t)kCells * 4);  // counters, then the cell counters
-  r.counters = reinterpret_cast<unsigned int*>(head);
-  r.cell_count = head ? reinterpret_cast<unsigned int*>(head + 256) : nullptr;
-  r.cursor = reinterpret_cast<unsigned int*>(take((size_t)kCells * 4));
+  r.counters = reinterpret_cast<unsigned int*>(take(256));
+  const long long msort = std::max(n, sym ? n : nj);
+  const long long tiles = (msort + kSortTile - 1) / kSortTile;
+  r.key0 = reinterpret_cast<unsigned int*>(take((size_t)msort * 4));
+  r.key1 = reinterpret_cast<unsigned int*>(take((size_t)msort * 4));
+  r.idx1 = reinterpret_cast<unsigned int*>(take((size_t)msort * 4));
+  r.counts = reinterpret_cast<unsigned int*>(take((size_t)tiles * kSortDigits * 4));
   cat(n, r.a);
   if (!sym) cat(nj, r.b);
   r.partial = reinterpret_cast<unsigned long long*>(take((size_t)grid * (size_t)nbins * 8));
@@ -287,16 +293,29 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   return off;
 }
 
-// Unit vectors of one catalog in spatial order, with their caps.
+// Unit vectors of one catalog in spatial order (a stable radix sort on the cell key: low 8 bits,
+// then high 7; then the fp64 vectors in that order), with their caps.
 int prepare_catalog(acf_ctx* c, const float* ra, const float* dec, long long n, const Scratch& s, const CatBufs& cb) {
-  const int threads = 256;
-  const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 16);
-  ACF_CUDA(c, cudaMemsetAsync(s.cell_count, 0, (size_t)kCells * 4, c->stream));
-  prep_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, n, cb.key, s.cell_count);
+  const long long tiles = (n + kSortTile - 1) / kSortTile;
+  const unsigned grid = (unsigned)tiles;
+  const long long m = tiles * kSortDigits;
+  sort_count_kernel<<<grid, kSortThreads, 0, c->stream>>>(ra, dec, nullptr, s.key0, n, 0, (int)tiles, s.counts);
   ACF_LAUNCHED(c);
-  scan_kernel<<<1, 1024, 0, c->stream>>>(s.cell_count, s.cursor);
+  scan_kernel<<<1, 1024, 0, c->stream>>>(s.counts, m);
   ACF_LAUNCHED(c);
-  scatter_kernel<<<(unsigned)blocks, threads, 0, c->stream>>>(ra, dec, cb.key, n, s.cursor, cb.v, cb.v64);
+  sort_scatter_kernel<false><<<grid, kSortThreads, 0, c->stream>>>(s.key0, nullptr, n, 0, (int)tiles, s.counts, s.key1,
+                                                                  s.idx1);
+  ACF_LAUNCHED(c);
+  sort_count_kernel<<<grid, kSortThreads, 0, c->stream>>>(ra, dec, s.key1, nullptr, n, 8, (int)tiles, s.counts);
+  ACF_LAUNCHED(c);
+  scan_kernel<<<1, 1024, 0, c->stream>>>(s.counts, m);
+  ACF_LAUNCHED(c);
+  // the final order (sorted position -> input index) reuses key0, which pass 2 no longer reads
+  sort_scatter_kernel<true><<<grid, kSortThreads, 0, c->stream>>>(s.key1, s.idx1, n, 8, (int)tiles, s.counts, nullptr,
+                                                                 s.key0);
+  ACF_LAUNCHED(c);
+  const long long vblocks = std::min<long long>((n + 255) / 256, (long long)c->num_sms * 8);
+  vectors_kernel<<<(unsigned)vblocks, 256, 0, c->stream>>>(ra, dec, s.key0, n, cb.v, cb.v64);
   ACF_LAUNCHED(c);
   const long long warps = (n + 127) / 128;
   caps_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, c->stream>>>(cb.v, n, cb.cap32, cb.cap128);
@@ -405,8 +424,8 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   if (p.exact_mode) {
     // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
     const int fblocks = c->num_sms * 8;
-    if (pl.map == kMirror)
-      fixup_kernel<kMirror><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
+    if (pl.map == kDirect)
+      fixup_kernel<kDirect><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
                                                             sc.U, pl.bp, p.inc,
                                                             reinterpret_cast<unsigned long long*>(out), sc.counters + 2);
     else
@@ -604,11 +623,14 @@ int acf_pair_bins(acf_ctx* c, const float* ra1, const float* dec1, const float* 
   const int threads = 256;
   const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 32);
   if (pl.method == kDotAcos)
-    pair_bins_kernel<kClamp, kDotAcos><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
-  else if (pl.map == kMirror)
-    pair_bins_kernel<kMirror, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
+    pair_bins_kernel<kClamp, kDotAcos><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp,
+                                                                                  c->opt_pair_bins_form, bins);
+  else if (pl.map == kDirect)
+    pair_bins_kernel<kDirect, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp,
+                                                                                  c->opt_pair_bins_form, bins);
   else
-    pair_bins_kernel<kClamp, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp, bins);
+    pair_bins_kernel<kClamp, kChordPoly><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp,
+                                                                                  c->opt_pair_bins_form, bins);
   ACF_LAUNCHED(c);
   return ACF_OK;
 }
@@ -633,6 +655,12 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "exact_below_deg")) {
     if (v < 0 || v > 180) return fail(c, ACF_ERR_ARG, "exact_below_deg must be 0..180");
     c->opt_exact_below_deg = (double)v;
+  } else if (!strcmp(key, "mid")) {
+    if (v != 0 && v != 1) return fail(c, ACF_ERR_ARG, "mid must be 0 or 1");
+    c->opt_mid = (int)v;
+  } else if (!strcmp(key, "pair_bins_form")) {
+    if (v != 0 && v != 1) return fail(c, ACF_ERR_ARG, "pair_bins_form must be 0 or 1");
+    c->opt_pair_bins_form = (int)v;
   } else if (!strcmp(key, "units_per_launch")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "units_per_launch must be >= 0");
     c->opt_units_per_launch = v;
@@ -664,12 +692,12 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
       *v = e.val;
       return ACF_OK;
     }
-  const char* path_keys[5] = {"pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact",
-                               "pairs_masked"};
-  for (int k = 0; k < 5; ++k)
+  const char* path_keys[7] = {"pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact",
+                               "pairs_masked", "pairs_mid", "pairs_mid_exact"};
+  for (int k = 0; k < 7; ++k)
     if (!strcmp(key, path_keys[k])) {
       // synchronises the stream; pairs the last histogram call evaluated on each pair-kernel path
-      unsigned long long h[5] = {0, 0, 0, 0, 0};
+      unsigned long long h[7] = {0, 0, 0, 0, 0, 0, 0};
       if (c->last_counters) {
         if (cudaSetDevice(c->device) != cudaSuccess || cudaStreamSynchronize(c->stream) != cudaSuccess ||
             cudaMemcpy(h, c->last_counters + 16, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -772,7 +800,7 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
-                "(about 53 bytes per galaxy of each catalog plus %lld blocks x nbins x 8 bytes); use acf_histogram",
+                "(about 61 bytes per galaxy of each catalog plus (%lld blocks + 2) x nbins x 8 bytes); use acf_histogram",
                 need, kNoAllocScratchBytes, L.grid);
   void* scratch = nullptr;
   rc = noalloc_scratch(c, c->device, &scratch);

@@ -7,19 +7,27 @@
 // What differs from the page, and why:
 //   * each galaxy becomes an fp32 unit vector once (built in fp64), so a pair costs a dot product
 //     instead of a cosine of the RA difference;
-//   * the separation is taken from the CHORD, not from arccos of the dot product: with
-//     s = sign(u.v), q = |u - s v|^2 = 4 sin^2(theta'/2), theta' = theta (s = +1) or
-//     pi - theta (s = -1), theta' <= 90 deg. q keeps full relative precision at small and near-
-//     antipodal separations, where arccos of an fp32 dot product loses up to ~3e-4 rad;
-//   * theta'^2 / w^2 = q * P(q) with a degree-7 polynomial P (absolute theta' error <= 2.5e-8 rad),
-//     one sqrt.approx gives t' = theta'/w, and the bin index comes from t' by exact float
-//     rounding tricks instead of acos, multiply and float-to-int conversion;
+//   * catalogs are sorted along a Hilbert curve over cube-map cells, and each run of 32 sorted
+//     galaxies gets a cap (centre, radius); from two caps the kernel knows the range of separations
+//     of a (warp, j-group) block of pairs and picks the cheapest exact-enough form for it;
+//   * below 45 and above 135 degrees the separation is taken from the CHORD, not from arccos of the
+//     dot product: with s = sign(u.v), q = |u - s v|^2 = 4 sin^2(theta'/2), theta' = theta
+//     (s = +1) or pi - theta (s = -1), theta' <= 90 deg; q keeps full relative precision at small
+//     and near-antipodal separations, where arccos of an fp32 dot product loses up to ~3e-4 rad.
+//     theta'^2 = q * P(q) with a degree-7 polynomial P, then one sqrt.approx;
+//   * between 45 and 135 degrees the dot product itself is precise enough: theta = pi/2 - d R(d^2)
+//     with a degree-7 polynomial R and no square root (14 instead of 18 instructions per pair);
+//   * the bin index comes from exact float rounding (one fma rounded toward zero onto 2^23 + c)
+//     instead of acos, multiply and float-to-int conversion;
 //   * each histogram lives in shared memory as 32 lane-private copies (word = bin*32 + lane), so a
 //     warp's 32 increments always hit 32 different banks and the shared-memory atomic unit
 //     retires one warp instruction per clock; very fine binnings fall back to one block-shared
 //     copy;
-//   * persistent blocks walk a precomputed chunk list (only the upper triangle for DD/RR), and
-//     per-block counts go to per-block uint64 rows that a final kernel reduces.
+//   * persistent blocks whose warps take 128 x 128-pair work units from a global ticket (only the
+//     upper triangle for DD/RR); per-block counts go to per-block uint64 rows that a final kernel
+//     reduces;
+//   * optionally (exact mode), pairs whose fast code lies within a fine unit of a bin edge are
+//     queued and re-decided in fp64 after the merge.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -42,7 +50,7 @@ constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact
 constexpr float kMagic = 8388608.0f;  // 2^23: adding it with round-toward-zero floors into the mantissa
 
 enum Layout { kLane = 1, kBlock = 2 };
-enum BinMap { kMirror = 0, kClamp = 1 };
+enum BinMap { kDirect = 0, kClamp = 1 };
 enum Method { kChordPoly = 0, kDotAcos = 1 };
 
 // theta'^2 = q * P(q) for a chord q = |u - v|^2 on [0, 2] (theta' <= 90 degrees), P of degree 7
@@ -52,20 +60,32 @@ __device__ constexpr float kP0 = 0.99999959294652097f, kP1 = 0.08334261162808559
                            kP5 = 0.00029099553526503564f, kP6 = -9.1427792701640403e-05f,
                            kP7 = 2.3068911858269848e-05f;
 
+// Between 45 and 135 degrees the dot product d = u.v loses nothing: theta = pi/2 - asin(d) with
+// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(43 deg), degree 7: absolute
+// theta error <= 1.4e-8 rad (2.8e-8 after fp32 rounding). Scaled by 1/w on the host.
+constexpr double kR[8] = {0.9999996836724383,  0.16669323778385681, 0.074351930865433416, 0.051668908380561249,
+                          -0.0092763923538493106, 0.14513595031397153, -0.18466868067833839, 0.16096802275189068};
+constexpr float kMidRad = 0.78539816339744831f;  // groups whose separations all lie in (45, 135) degrees use the dot form
+
+// Every code is the float 2^23 + (histogram entry), entry = floor(theta / w) (direct map, where
+// P = pi / w is an integer) or the clamped index (clamp map); the merge clamps entries to nbins - 1.
 struct BinParams {
-  float magic;     // 2^23 + off (mirror) or 2^23 (clamp)
-  float inv_w_f;   // exact mode: 2^S / w (fine code with S fractional bits)
-  float magic_f;   // exact mode: 2^23 + off * 2^S (mirror)
-  float clamp_f;   // exact mode: (clamp_c + 0.5) * 2^S (clamp map)
-  int fine_shift;  // exact mode: S
-  int kmax;        // exact mode: highest bin a separation <= 180 degrees can reach
+  float magic_far;    // direct: 2^23 + P, the far-side (theta > 90 deg) constant of the chord form
+  float magic_mid;    // direct, P even: 2^23 + P/2, the constant of the dot form
+  float inv_w_f;      // exact mode: 2^S / w (fine code with S fractional bits)
+  float magic_far_f;  // exact mode: 2^23 + P 2^S
+  float magic_mid_f;  // exact mode: 2^23 + (P/2) 2^S
+  float clamp_f;      // exact mode: (clamp_c + 0.5) * 2^S (clamp map)
+  float rc[8];        // dot form: kR[k] / w
+  float rc_f[8];      // exact mode: kR[k] 2^S / w
+  int mid;            // 1: groups between 45 and 135 degrees use the dot form
+  int fine_shift;     // exact mode: S
+  int kmax;           // exact mode: highest bin a separation <= 180 degrees can reach
   unsigned int zone0, span0, zone1, span1;  // exact mode: entries e with e - zone <= span (unsigned) are re-decided
-  float clamp_c;   // largest index (clamp map)
-  float inv_w;     // 1 / w in radians (acos method)
-  int off;         // mirror: index of theta' = 0 on the near side
-  int p_int;       // mirror: P as an integer
+  float clamp_c;      // largest index (clamp map)
+  float inv_w;        // 1 / w in radians
   int nbins;
-  int entries;     // histogram entries in shared memory
+  int entries;        // histogram entries in shared memory
 };
 
 struct PairParams {
@@ -92,8 +112,9 @@ struct PairParams {
   unsigned int* qflagged;              // pairs flagged (for reporting)
   unsigned int qcap;                   // queue slots
   unsigned int qbatch;                 // slots a block reserves at its start
-  unsigned long long* path_pairs;      // pairs evaluated per path: fixed, general, fixed+flag,
-                                       // general+flag, masked/ragged units (all pairs computed)
+  unsigned long long* path_pairs;      // pairs evaluated per path: chord fixed, chord general,
+                                       // chord fixed+flag, chord general+flag, masked/ragged units,
+                                       // dot form, dot form+flag (all pairs computed)
   BinParams bp;
 };
 
@@ -189,8 +210,10 @@ __device__ __forceinline__ float4 radec_to_unit(float ra_arcmin, float dec_arcmi
 // (6 faces x 64 x 64 cells, Hilbert order within a face). A warp's i-galaxies and a j-chunk then
 // each cover a small patch of sky, bounded by a "cap" (centre, angular radius). From two caps
 // the kernel knows when every pair of a (warp, chunk) is surely below or surely above 90
-// degrees, and drops the per-pair sign decision there. The order changes no result: every
-// pair's bin is computed by the same arithmetic whichever path evaluates it.
+// degrees, and drops the per-pair sign decision there, and when every pair lies between 45 and
+// 135 degrees, where it uses the dot form. The chord loops compute every pair's code with the same
+// arithmetic whichever of them evaluates it; the dot form computes a different (equally valid)
+// approximation, so a mid-range pair within ~4e-7 rad of an edge may bin by its grouping.
 
 constexpr int kFaceBits = 6;
 constexpr int kFaceCells = 1 << kFaceBits;
@@ -230,6 +253,18 @@ __device__ __forceinline__ unsigned int cell_of(double x, double y, double z) {
   return (unsigned int)face * (kFaceCells * kFaceCells) + hilbert_index((unsigned)iu, (unsigned)iv);
 }
 
+// Sort key of a galaxy: its cell, from fp32 arithmetic (the key only has to be a deterministic
+// function of the input; vectors near a cell border may fall on either side).
+__device__ __forceinline__ unsigned int cell_key(float ra_arcmin, float dec_arcmin) {
+  const float k = 3.14159265358979323846f / 10800.0f;
+  float a = ra_arcmin * k, d = dec_arcmin * k;
+  if (!isfinite(a) || !isfinite(d)) { a = 0.0f; d = 0.0f; }
+  float sa, ca, sd, cd;
+  sincosf(a, &sa, &ca);
+  sincosf(d, &sd, &cd);
+  return cell_of((double)(cd * ca), (double)(cd * sa), (double)sd);
+}
+
 // (RA, Dec) arcminutes -> fp64 unit vector; non-finite inputs become (0, 0).
 __device__ __forceinline__ void unit64(float ra_arcmin, float dec_arcmin, double& x, double& y, double& z) {
   const double k = 3.14159265358979323846 / 10800.0;
@@ -243,37 +278,61 @@ __device__ __forceinline__ void unit64(float ra_arcmin, float dec_arcmin, double
   z = sd;
 }
 
-// Each galaxy's cell, counted per cell.
-__global__ void prep_kernel(const float* __restrict__ ra, const float* __restrict__ dec, long long n,
-                            unsigned int* __restrict__ key, unsigned int* __restrict__ cell_count) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    double x, y, z;
-    unit64(ra[i], dec[i], x, y, z);
-    const unsigned int c = cell_of(x, y, z);
-    key[i] = c;
-    atomicAdd(cell_count + c, 1u);
+// The sort is a stable two-pass LSD radix sort on the cell key (15 bits: 8, then 7), so galaxies
+// of one cell keep their input order and the spatial order, the groups and their caps depend on
+// the input alone. Each pass: per-tile digit counts, one exclusive scan over (digit, tile), and a
+// stable scatter in which every tile ranks its elements round by round (warp match + warp totals).
+constexpr int kSortThreads = 256;
+constexpr int kSortRounds = 8;
+constexpr int kSortTile = kSortThreads * kSortRounds;  // elements per tile (one block)
+constexpr int kSortDigits = 256;
+
+// Digit counts of one tile. Pass 1 (keys_in == nullptr) also computes every galaxy's cell key.
+__global__ void __launch_bounds__(kSortThreads) sort_count_kernel(const float* __restrict__ ra,
+                                                                  const float* __restrict__ dec,
+                                                                  const unsigned int* __restrict__ keys_in,
+                                                                  unsigned int* __restrict__ keys_out, long long n,
+                                                                  int shift, int ntiles, unsigned int* __restrict__ counts) {
+  __shared__ unsigned int h[kSortDigits];
+  for (int d = threadIdx.x; d < kSortDigits; d += kSortThreads) h[d] = 0u;
+  __syncthreads();
+  const long long base = (long long)blockIdx.x * kSortTile;
+  for (int r = 0; r < kSortRounds; ++r) {
+    const long long i = base + r * kSortThreads + threadIdx.x;
+    if (i < n) {
+      unsigned int k;
+      if (keys_in) {
+        k = keys_in[i];
+      } else {
+        k = cell_key(ra[i], dec[i]);
+        keys_out[i] = k;
+      }
+      atomicAdd(&h[(k >> shift) & (kSortDigits - 1)], 1u);
+    }
   }
+  __syncthreads();
+  for (int d = threadIdx.x; d < kSortDigits; d += kSortThreads) counts[(size_t)d * ntiles + blockIdx.x] = h[d];
 }
 
-// Exclusive prefix sum of the cell counts, one block of 1024 threads: rounds of 1024 consecutive
-// cells (coalesced loads), each scanned with warp shuffles and the 32 warp totals, plus the carry.
-__global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restrict__ cell_count,
-                                                     unsigned int* __restrict__ cursor) {
+// In-place exclusive prefix sum of m counts, one block of 1024 threads: rounds of 1024
+// consecutive values (coalesced loads), each scanned with warp shuffles and the 32 warp totals,
+// plus the carry.
+__global__ void __launch_bounds__(1024) scan_kernel(unsigned int* __restrict__ v, long long m) {
   __shared__ unsigned int warp_sum[32];
   __shared__ unsigned int carry;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   if (t == 0) carry = 0u;
   __syncthreads();
-  for (int base = 0; base < kCells; base += 1024) {
-    const int c = base + t;
-    const unsigned int x = c < kCells ? cell_count[c] : 0u;
-    unsigned int v = x;  // inclusive scan within the warp
+  for (long long base = 0; base < m; base += 1024) {
+    const long long c = base + t;
+    const unsigned int x = c < m ? v[c] : 0u;
+    unsigned int s = x;  // inclusive scan within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const unsigned int y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
+      const unsigned int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
     }
-    if (lane == 31) warp_sum[warp] = v;
+    if (lane == 31) warp_sum[warp] = s;
     __syncthreads();
     if (warp == 0) {  // scan the warp totals
       unsigned int w = warp_sum[lane];
@@ -285,26 +344,72 @@ __global__ void __launch_bounds__(1024) scan_kernel(const unsigned int* __restri
       warp_sum[lane] = w;  // inclusive
     }
     __syncthreads();
-    const unsigned int before = carry + (warp > 0 ? warp_sum[warp - 1] : 0u) + v - x;
-    if (c < kCells) cursor[c] = before;
+    const unsigned int before = carry + (warp > 0 ? warp_sum[warp - 1] : 0u) + s - x;
+    if (c < m) v[c] = before;
     __syncthreads();
     if (t == 1023) carry = before + x;
     __syncthreads();
   }
 }
 
-// Counting-sort scatter: unit vectors in spatial order, as fp32 (pair kernel) and fp64 (exact
-// re-decision of flagged pairs).
-__global__ void scatter_kernel(const float* __restrict__ ra, const float* __restrict__ dec,
-                               const unsigned int* __restrict__ key, long long n, unsigned int* __restrict__ cursor,
-                               float4* __restrict__ v_out, double4* __restrict__ v64_out) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const unsigned int pos = atomicAdd(cursor + key[i], 1u);
-    if (ACF_CHECK(pos < (unsigned long long)n, 5, i, pos)) {
+// Stable scatter of one tile. Element i of the tile goes to offset(digit, tile) + the number of
+// earlier elements of the tile with the same digit: rounds of 256 in input order; within a round a
+// warp ranks its lanes with __match_any_sync, and the warps' per-digit totals rank the warps.
+// Pass 1 (FINAL = false) moves (key, input index); pass 2 only the input index.
+template <bool FINAL>
+__global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(
+    const unsigned int* __restrict__ keys_in, const unsigned int* __restrict__ idx_in, long long n, int shift,
+    int ntiles, const unsigned int* __restrict__ offsets, unsigned int* __restrict__ keys_out,
+    unsigned int* __restrict__ idx_out) {
+  constexpr int W = kSortThreads / 32;
+  __shared__ unsigned int running[kSortDigits];      // elements of each digit placed by earlier rounds
+  __shared__ unsigned int wcount[W][kSortDigits];    // this round: elements of each digit per warp
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int d = t; d < kSortDigits; d += kSortThreads) running[d] = offsets[(size_t)d * ntiles + blockIdx.x];
+  const long long base = (long long)blockIdx.x * kSortTile;
+  const unsigned int lt = (1u << lane) - 1u;
+  for (int r = 0; r < kSortRounds; ++r) {
+    for (int k = t; k < W * kSortDigits; k += kSortThreads) (&wcount[0][0])[k] = 0u;
+    __syncthreads();
+    const long long i = base + r * kSortThreads + t;
+    const bool ok = i < n;
+    const unsigned int key = ok ? keys_in[i] : 0u;
+    const unsigned int dig = ok ? (key >> shift) & (kSortDigits - 1) : kSortDigits;  // kSortDigits: no element
+    const unsigned int peers = __match_any_sync(0xffffffffu, dig);
+    const unsigned int rank = __popc(peers & lt);
+    if (ok && rank == 0) wcount[warp][dig] = __popc(peers);
+    __syncthreads();
+    if (ok) {
+      unsigned int pos = running[dig] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcount[w][dig];
+      if (ACF_CHECK(pos < (unsigned long long)n, 5, i, pos)) {
+        idx_out[pos] = FINAL ? idx_in[i] : (unsigned int)i;
+        if (!FINAL) keys_out[pos] = key;
+      }
+    }
+    __syncthreads();
+    for (int d = t; d < kSortDigits; d += kSortThreads) {
+      unsigned int tot = 0u;
+#pragma unroll
+      for (int w = 0; w < W; ++w) tot += wcount[w][d];
+      running[d] += tot;
+    }
+    __syncthreads();
+  }
+}
+
+// Unit vectors in sorted order, as fp32 (pair kernel) and fp64 (exact re-decision of flagged
+// pairs): position p holds input galaxy order[p].
+__global__ void vectors_kernel(const float* __restrict__ ra, const float* __restrict__ dec,
+                               const unsigned int* __restrict__ order, long long n, float4* __restrict__ v_out,
+                               double4* __restrict__ v64_out) {
+  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n; p += (long long)gridDim.x * blockDim.x) {
+    const unsigned int src = order[p];
+    if (ACF_CHECK(src < (unsigned long long)n, 5, p, src)) {
       double x, y, z;
-      unit64(ra[i], dec[i], x, y, z);
-      v_out[pos] = make_float4((float)x, (float)y, (float)z, 0.0f);
-      v64_out[pos] = make_double4(x, y, z, 0.0);
+      unit64(ra[src], dec[src], x, y, z);
+      v_out[p] = make_float4((float)x, (float)y, (float)z, 0.0f);
+      v64_out[p] = make_double4(x, y, z, 0.0);
     }
   }
 }
@@ -398,17 +503,16 @@ __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float x
     p = fmaf(p, q, kP1);
     p = fmaf(p, q, kP0);
     const float th = sqrt_approx(p * q);  // theta' in radians
-    if (MAP == kMirror) {
-      // near side (s = +1): floor(theta'/w) exactly, by one fma rounded toward zero onto 2^23 + off;
-      // far side: the same fma of -theta' gives off - ceil(theta'/w), and bin P - ceil(theta'/w)
-      // is exactly floor((pi - theta')/w) when P = pi/w is an integer.
+    if (MAP == kDirect) {
+      // near side (s = +1): floor(theta'/w) exactly, by one fma rounded toward zero onto 2^23;
+      // far side: the same fma of -theta' onto 2^23 + P gives P - ceil(theta'/w), which is exactly
+      // floor((pi - theta')/w) = floor(theta/w) when P = pi/w is an integer.
       // theta' carrying the sign of d: th | (d & signmask), one logic op
+      const float m = (int)db < 0 ? (FINE ? bp.magic_far_f : bp.magic_far) : kMagic;
 #if ACF_ASM_LOP3
-      return fma_rz(__uint_as_float(lop3<0xF8>(__float_as_uint(th), db, 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w,
-                    FINE ? bp.magic_f : bp.magic);
+      return fma_rz(__uint_as_float(lop3<0xF8>(__float_as_uint(th), db, 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w, m);
 #else
-      return fma_rz(__uint_as_float(__float_as_uint(th) | (db & 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w,
-                    FINE ? bp.magic_f : bp.magic);
+      return fma_rz(__uint_as_float(__float_as_uint(th) | (db & 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w, m);
 #endif
     } else {
       const float h = fmaf(ns, 1.57079632679489662f, 1.57079632679489662f);  // 0 or pi
@@ -418,24 +522,23 @@ __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float x
   }
 }
 
-// histogram entry -> bin
+// histogram entry -> bin (both maps index entries by bin; entries past the last bin clamp to it)
 template <int MAP>
 __device__ __forceinline__ int entry_to_bin(int e, const BinParams& bp) {
-  int k = e;
-  if (MAP == kMirror) k = (e >= bp.off) ? e - bp.off : e + bp.p_int - bp.off;
-  k = k < 0 ? 0 : k;
+  const int k = e < 0 ? 0 : e;
   return k > bp.nbins - 1 ? bp.nbins - 1 : k;
 }
 
 // The same code as pair_code<MAP, kChordPoly> for a pair whose sign(u.v) is known in advance
 // (the caps of its warp and j-group put every separation below 90 degrees, or every one above):
-// ns = -sign as +-1.0 and iws = sign / w (or sign * 2^S / w for the fine code) are registers
-// chosen per j-group. Bit for bit the general code takes these steps for such a pair:
-// fma(ns, v, u) is the same difference or sum, and the far-side code fma_rz(-theta', 1/w, m) is
-// fma_rz(theta', -1/w, m). Only the dot product and the two sign-bit operations are dropped.
+// ns = -sign as +-1.0, iws = sign / w (or sign * 2^S / w for the fine code) and h (direct map:
+// 2^23 or the far-side constant; clamp map: 0 or pi / w) are registers chosen per j-group. Bit for
+// bit the general code takes these steps for such a pair: fma(ns, v, u) is the same difference or
+// sum, and the far-side code fma_rz(-theta', 1/w, m) is fma_rz(theta', -1/w, m). Only the dot
+// product, the sign-bit operation and the choice of constant are dropped.
 template <int MAP, bool FINE = false>
 __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, float xj, float yj, float zj, float ns,
-                                                 float iws, float hs, const BinParams& bp) {
+                                                 float iws, float h, const BinParams& bp) {
   const float dx = fmaf(ns, xj, xi);
   const float dy = fmaf(ns, yj, yi);
   const float dz = fmaf(ns, zj, zi);
@@ -448,13 +551,35 @@ __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, f
   p = fmaf(p, q, kP1);
   p = fmaf(p, q, kP0);
   const float th = sqrt_approx(p * q);
-  if (MAP == kMirror) {
-    return fma_rz(th, iws, FINE ? bp.magic_f : bp.magic);
+  if (MAP == kDirect) {
+    return fma_rz(th, iws, h);
   } else {
-    // theta / w = th * iws + hs with hs = 0 (near side) or pi / w (far side); iws = -1/w there
-    const float t = fmaf(th, iws, hs);
+    // theta / w = th * iws + h with h = 0 (near side) or pi / w (far side); iws = -1/w there
+    const float t = fmaf(th, iws, h);
     return add_rz(fminf(t, FINE ? bp.clamp_f : bp.clamp_c), kMagic);
   }
+}
+
+// The dot form, for pairs whose caps put theta in (45, 135) degrees (direct map, P even):
+// theta / w = P/2 - d R(d^2) / w, floored exactly by one fma rounded toward zero onto 2^23 + P/2
+// (the product of the two fp32 operands enters unrounded). Worst-case theta error: d carries
+// <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 3.1e-7 rad where sin theta >=
+// sin 43 deg, plus <= 1e-7 from the polynomial and its rounding.
+template <bool FINE = false>
+__device__ __forceinline__ float pair_code_mid(float xi, float yi, float zi, float xj, float yj, float zj,
+                                               const BinParams& bp) {
+#define ACF_RC(k) (FINE ? bp.rc_f[k] : bp.rc[k])
+  const float d = fmaf(zi, zj, fmaf(yi, yj, xi * xj));
+  const float t = d * d;
+  float p = fmaf(ACF_RC(7), t, ACF_RC(6));
+  p = fmaf(p, t, ACF_RC(5));
+  p = fmaf(p, t, ACF_RC(4));
+  p = fmaf(p, t, ACF_RC(3));
+  p = fmaf(p, t, ACF_RC(2));
+  p = fmaf(p, t, ACF_RC(1));
+  p = fmaf(p, t, ACF_RC(0));
+#undef ACF_RC
+  return fma_rz(-d, p, FINE ? bp.magic_mid_f : bp.magic_mid);
 }
 
 // Cap of K consecutive 32-galaxy groups: centre = normalised sum of the group centres, radius =
@@ -495,8 +620,12 @@ struct PathTag {
 // iff cos tc < -sin(ra + rb). __sinf/__cosf are accurate to ~1e-6 here and the margins cover it.
 // kExactBit is added when the exact mode must check this group: mode 2 always, mode 1 when some
 // separation may be below lo or above pi - lo (cos tc > cos(lo + r) or < -cos(lo + r)).
+// kMidBit is added when every separation lies in (45, 135) degrees (|cos tc| < cos(45 deg + r))
+// and the dot form is on; in mode 1 never for a group the exact mode checks, so every pair the
+// exact mode may re-decide is binned by the chord form whatever its grouping.
 constexpr int kExactBit = 4;
-__device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float lo) {
+constexpr int kMidBit = 8;
+__device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float lo, int mid) {
   const float dot = a.x * b.x + a.y * b.y + a.z * b.z;
   const float r = a.w + b.w + 1e-4f;
   int path = kGeneral;
@@ -505,12 +634,16 @@ __device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float l
     if (dot > sr) path = kBelow90;
     else if (dot < -sr) path = kAbove90;
   }
+  if (mid && r < 0.75f) {
+    const float cm = __cosf(kMidRad + r) - 1e-5f;
+    if (fabsf(dot) < cm) path |= kMidBit;
+  }
   if (mode == 2) return path | kExactBit;
   if (mode == 1) {
     const float x = lo + r;
-    if (x >= 3.0f) return path | kExactBit;
+    if (x >= 3.0f) return (path & 3) | kExactBit;
     const float cl = __cosf(x) - 1e-5f;
-    if (dot > cl || dot < -cl) return path | kExactBit;
+    if (dot > cl || dot < -cl) return (path & 3) | kExactBit;
   }
   return path;
 }
@@ -518,6 +651,10 @@ __device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float l
 template <bool F>
 struct FineTag {
   static constexpr bool value = F;
+};
+template <int X>
+struct FormTag {
+  static constexpr int value = X;
 };
 
 // Add one pair to the shared histogram. With F (exact mode) the code carries fine_shift extra
@@ -660,8 +797,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     float xi[K], yi[K], zi[K];
     float4 icap = make_float4(1.f, 0.f, 0.f, 4.f);
     int cur_r = -1, buf = 0;
-    // j-groups per path (x 32*kJT pairs): fixed, general, fixed+flag, general+flag
-    unsigned int g_fixed = 0, g_general = 0, g_fixed_f = 0, g_general_f = 0;
+    // j-groups per path (x 32*kJT pairs): chord fixed, chord general, the same with flags, dot form,
+    // dot form with flags
+    unsigned int g_fixed = 0, g_general = 0, g_fixed_f = 0, g_general_f = 0, g_mid = 0, g_mid_f = 0;
     unsigned long long edge_pairs = 0ull;
     while (true) {
       int rn = 0, cn = 0;
@@ -703,12 +841,14 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #endif
       if (full) {
         // one loop per (32-galaxy j-group, path); the path is uniform across the warp. The fixed
-        // loops take the sign in registers (ns, iws, hs); the fine (exact) loops are rare and kept
-        // rolled so that all live loop bodies fit the instruction cache.
-        auto run = [&](auto fixed, auto fine, int jbeg, float ns, float iws, float hs) {
-          constexpr bool X = decltype(fixed)::value;
+        // chord loops take the sign in registers (ns, iws, h); the dot-form loop needs no sign; the
+        // fine (exact) loops are rare and kept rolled so that all live loop bodies fit the
+        // instruction cache.
+        auto run = [&](auto form, auto fine, int jbeg, float ns, float iws, float h) {
+          constexpr int X = decltype(form)::value;  // 0 chord general, 1 chord fixed sign, 2 dot form
           constexpr bool F = decltype(fine)::value;
-          constexpr int U = F ? kJJUnrollFine : kJJUnroll;
+          // the general chord loop is rare once the caps pick the dot form across 90 degrees: rolled
+          constexpr int U = (F || X == 0) ? kJJUnrollFine : kJJUnroll;
 #pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
             const float4 v = tile[jj];
@@ -716,8 +856,10 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             unsigned int near = 0u;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-              const float code = X ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, hs, p.bp)
-                                   : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
+              const float code =
+                  X == 2 ? pair_code_mid<F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
+                  : X == 1 ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h, p.bp)
+                           : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
               cbs[k] = __float_as_uint(code);
               if (add_pair<F>(p, cbs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
                               yi[k], zi[k], v))
@@ -733,23 +875,31 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         };
 #pragma unroll 1
         for (int g = 0; g < kJT / 32; ++g) {
-          const int pc = (METHOD == kChordPoly)
-                             ? choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + g), p.exact_mode, p.exact_lo)
-                             : kGeneral;
+          const int pc = (METHOD == kChordPoly) ? choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + g), p.exact_mode,
+                                                              p.exact_lo, MAP == kDirect ? p.bp.mid : 0)
+                                                : kGeneral;
           const int path = pc & 3;
           const bool fine = (pc & kExactBit) != 0;
+          if (pc & kMidBit) {
+            (fine ? g_mid_f : g_mid) += 1;
+            if (fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f);
+            else run(FormTag<2>(), FineTag<false>(), g * 32, 0.f, 0.f, 0.f);
+            continue;
+          }
           const float iw = fine ? p.bp.inv_w_f : p.bp.inv_w;
           const float ns = (path == kBelow90) ? -1.0f : 1.0f;
           const float iws = (path == kBelow90) ? iw : -iw;
-          const float hs = (path == kBelow90) ? 0.0f : 3.14159265358979323846f * iw;
+          float h;
+          if (MAP == kDirect) h = (path == kBelow90) ? kMagic : (fine ? p.bp.magic_far_f : p.bp.magic_far);
+          else h = (path == kBelow90) ? 0.0f : 3.14159265358979323846f * iw;
           if (path == kGeneral) (fine ? g_general_f : g_general) += 1;
           else (fine ? g_fixed_f : g_fixed) += 1;
           if (path == kGeneral) {
-            if (fine) run(FineTag<false>(), FineTag<true>(), g * 32, ns, iws, hs);
-            else run(FineTag<false>(), FineTag<false>(), g * 32, ns, iws, hs);
+            if (fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h);
+            else run(FormTag<0>(), FineTag<false>(), g * 32, ns, iws, h);
           } else {
-            if (fine) run(FineTag<true>(), FineTag<true>(), g * 32, ns, iws, hs);
-            else run(FineTag<true>(), FineTag<false>(), g * 32, ns, iws, hs);
+            if (fine) run(FormTag<1>(), FineTag<true>(), g * 32, ns, iws, h);
+            else run(FormTag<1>(), FineTag<false>(), g * 32, ns, iws, h);
           }
         }
       } else {
@@ -796,6 +946,8 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       if (g_fixed_f) atomicAdd(p.path_pairs + 2, g_fixed_f * G);
       if (g_general_f) atomicAdd(p.path_pairs + 3, g_general_f * G);
       if (edge_pairs) atomicAdd(p.path_pairs + 4, edge_pairs);
+      if (g_mid) atomicAdd(p.path_pairs + 5, g_mid * G);
+      if (g_mid_f) atomicAdd(p.path_pairs + 6, g_mid_f * G);
     }
   }
   __syncthreads();
@@ -901,15 +1053,20 @@ __global__ void fixup_kernel(const uint4* __restrict__ queue, const unsigned int
   }
 }
 
+// form 1: pairs with |u.v| < cos(45 deg) take the dot form (as in a group the caps put between
+// 45 and 135 degrees), the others the chord form; form 0: the chord form for every pair.
 template <int MAP, int METHOD>
 __global__ void pair_bins_kernel(const float* __restrict__ ra1, const float* __restrict__ dec1,
                                  const float* __restrict__ ra2, const float* __restrict__ dec2, long long n,
-                                 BinParams bp, int* __restrict__ bins) {
+                                 BinParams bp, int form, int* __restrict__ bins) {
   const uint32_t magic_bits = __float_as_uint(kMagic);  // code = 2^23 + entry
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const float4 u = radec_to_unit(ra1[i], dec1[i]);
     const float4 v = radec_to_unit(ra2[i], dec2[i]);
-    const float code = pair_code<MAP, METHOD>(u.x, u.y, u.z, v.x, v.y, v.z, bp);
+    const float d = fmaf(u.z, v.z, fmaf(u.y, v.y, u.x * v.x));
+    const bool mid = form == 1 && MAP == kDirect && METHOD == kChordPoly && bp.mid && fabsf(d) < 0.70710678f;
+    const float code = mid ? pair_code_mid<false>(u.x, u.y, u.z, v.x, v.y, v.z, bp)
+                           : pair_code<MAP, METHOD>(u.x, u.y, u.z, v.x, v.y, v.z, bp);
     int e = (int)(__float_as_uint(code) - magic_bits);
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     bins[i] = entry_to_bin<MAP>(e, bp);

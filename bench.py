@@ -32,11 +32,15 @@ import synth  # noqa: E402
 
 METRIC = "G pairs/s (DD+DR+RR, N=100k each) and % of FP32 issue roofline"
 UNIT = "Gpairs/s"
-# Thread instructions per pair of each pair-kernel path ("Roofline"): the general
-# chord + polynomial loop is 23; where the caps fix the sign of the dot product the dot and the two
-# sign operations drop out (18); the exact-mode flag adds 5 (fine-code address, edge test, branch).
-INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 23, "pairs_fixed_exact": 23, "pairs_general_exact": 28}
-INST_MASKED = 23  # diagonal / ragged units run the general loop on every computed pair
+# Thread instructions per pair of each pair-kernel path: the general chord + polynomial loop is 25
+# (dot product, sign, chord, polynomial, sqrt, sign-dependent constant, rounding fma, address,
+# shared atomic); where the caps fix the sign of the dot product the dot, the sign operation and the
+# constant choice drop out (18); the dot form for groups between 45 and 135 degrees is 14 (dot,
+# square, 7-term polynomial, rounding fma, address, atomic); the exact-mode flag adds 5 (fine-code
+# address, edge test, branch).
+INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 23, "pairs_general_exact": 30,
+                 "pairs_mid": 14, "pairs_mid_exact": 19}
+INST_MASKED = 25  # diagonal / ragged units run the general loop on every computed pair
 SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
 # The pages' kernel time for three 100k histograms on an RTX 5080 (another machine: context only)
 PAGE_KERNEL_MS = 22.747

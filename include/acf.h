@@ -99,8 +99,8 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  * rows, the chunk counter) lives in one file-scope device array of 16 MiB that the library
  * reserves on every GPU that loads it, until the process exits. It calls no cudaMalloc, cudaFree
  * or other allocating routine.
- *   - Limit: about 197 KB + 53 bytes per galaxy of each catalog + (blocks * nbins * 8) bytes must
- *     fit in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
+ *   - Limit: about 61 bytes per galaxy of each catalog + ((blocks + 2) * nbins * 8) bytes must fit
+ *     in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
  *     return ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need
  *     ~11 MB. In exact mode the rest of the array holds the queue of pairs to re-decide; pairs that
  *     do not fit keep their fp32 bin (still within the precision contract) and are counted by the

@@ -62,18 +62,18 @@ def test_ragged_cross_and_auto(acf, ctx, n1, n2):
 
 
 @pytest.mark.parametrize("w,nb,layout", [
-    (0.25, 720, 0),     # mirror map, lane-private copies
-    (0.25, 720, 2),     # mirror map, forced block-shared histogram
+    (0.25, 720, 0),     # direct map, lane-private copies
+    (0.25, 720, 2),     # direct map, forced block-shared histogram
     (0.25, 1440, 0),    # the page's 1440 bins: bins beyond 180 degrees stay empty
     (0.25, 100, 0),     # bins stop at 25 degrees: the rest is clamped into bin 99
     (0.35, 515, 0),     # 180/w not an integer: clamp map
     (0.35, 40, 0),      # clamp map with heavy clamping
     (1.0, 180, 0),
     (10.0, 18, 0),
-    (45.0, 4, 0),       # tiny P: still the mirror map
+    (45.0, 4, 0),       # tiny P: still the direct map (P odd: no dot form)
     (60.0, 3, 0),       # P = 3 < 4: clamp map
     (0.01, 18000, 0),   # fine binning: block-shared layout
-    (0.03, 2000, 0),    # 6000 half-turn bins, 2000 used: mirror map, block layout
+    (0.03, 2000, 0),    # 6000 half-turn bins, 2000 used: direct map, block layout
     (7.0, 1, 0),        # one bin
 ])
 def test_binnings(acf, ctx, w, nb, layout):
@@ -166,8 +166,9 @@ def test_correlate_host_matches_device_path(acf, ctx):
 
 
 def _pair_sets(n, seed):
-    """Random pairs over the whole sphere, tight pairs (< 1 deg), near-antipodal pairs and pairs
-    near 90 degrees, where the kernel switches between the difference and the sum chord."""
+    """Random pairs over the whole sphere, tight pairs (< 1 deg), near-antipodal pairs, pairs near
+    90 degrees, where the kernel switches between the difference and the sum chord, and pairs near
+    45 and 135 degrees, the edges of the dot form's range."""
     rng = np.random.default_rng(seed)
     ra1, dec1 = synth.uniform_sphere(n, seed)
     ra2, dec2 = synth.uniform_sphere(n, seed + 1)
@@ -184,39 +185,60 @@ def _pair_sets(n, seed):
                  rng.uniform(-30, 30, n).astype(np.float32)))
     sets.append((ra1, np.zeros(n, np.float32), ((ra1 + 5400 + rng.uniform(-30, 30, n)) % 21600).astype(np.float32),
                  rng.uniform(-30, 30, n).astype(np.float32)))
+    # near 45 and 135 degrees, where groups switch between the chord form and the dot form
+    for lo in (43.0, 133.0):
+        dra = rng.uniform(lo * 60, (lo + 4) * 60, n)
+        sets.append((ra1, rng.uniform(-30, 30, n).astype(np.float32), ((ra1 + dra) % 21600).astype(np.float32),
+                     rng.uniform(-30, 30, n).astype(np.float32)))
     return sets
 
 
+@pytest.mark.parametrize("form", [0, 1])
 @pytest.mark.parametrize("w,nb", [(0.25, 720), (0.01, 18000), (0.35, 515)])
-def test_per_pair_bins_only_move_within_tolerance_of_an_edge(acf, ctx, w, nb):
+def test_per_pair_bins_only_move_within_tolerance_of_an_edge(acf, ctx, w, nb, form):
+    # form 0: the chord form for every pair; form 1: the dot form wherever |u.v| < cos 45 deg (what
+    # a group between 45 and 135 degrees computes), the chord form elsewhere
     w_rad = math.radians(w)
     worst = 0.0
-    for s in _pair_sets(400_000, seed=123):
-        ra1, dec1, ra2, dec2 = (np.ascontiguousarray(a, dtype=np.float32) for a in s)
-        gb = ctx.pair_bins(ra1, dec1, ra2, dec2, w, nb).cpu().numpy()
-        ob = oracle.pair_bin(ra1, dec1, ra2, dec2, w, nb)
-        th = oracle.pair_theta(ra1, dec1, ra2, dec2)
-        bad = np.nonzero(gb != ob)[0]
-        if len(bad):
-            assert np.all(np.abs(gb[bad] - ob[bad]) == 1)
-            edge = np.maximum(gb[bad], ob[bad]) * w_rad
-            dist = np.abs(th[bad] - edge)
-            worst = max(worst, float(dist.max()))
-            assert np.all(dist < TOL), f"moved pair {float(dist.max()):.3e} rad from its edge"
-    print(f"w={w}: largest distance from the edge of a moved pair {worst:.3e} rad")
+    ctx.set_option("pair_bins_form", form)
+    try:
+        for s in _pair_sets(400_000, seed=123):
+            ra1, dec1, ra2, dec2 = (np.ascontiguousarray(a, dtype=np.float32) for a in s)
+            gb = ctx.pair_bins(ra1, dec1, ra2, dec2, w, nb).cpu().numpy()
+            ob = oracle.pair_bin(ra1, dec1, ra2, dec2, w, nb)
+            th = oracle.pair_theta(ra1, dec1, ra2, dec2)
+            bad = np.nonzero(gb != ob)[0]
+            if len(bad):
+                assert np.all(np.abs(gb[bad] - ob[bad]) == 1)
+                edge = np.maximum(gb[bad], ob[bad]) * w_rad
+                dist = np.abs(th[bad] - edge)
+                worst = max(worst, float(dist.max()))
+                assert np.all(dist < TOL), f"moved pair {float(dist.max()):.3e} rad from its edge"
+    finally:
+        ctx.set_option("pair_bins_form", 0)
+    print(f"w={w} form={form}: largest distance from the edge of a moved pair {worst:.3e} rad")
 
 
-def test_auto_correlation_decomposes_into_parts(acf, ctx):
-    # DD(A u B) = DD(A) + DD(B) + 2 X(A, B) exactly: the symmetric path and the cross path bin
-    # every pair identically
+@pytest.mark.parametrize("mid,exact", [(0, 1), (0, 0), (1, 2)])
+def test_auto_correlation_decomposes_into_parts(acf, ctx, mid, exact):
+    # DD(A u B) = DD(A) + DD(B) + 2 X(A, B) exactly. With the chord form alone (mid 0) the
+    # symmetric and the cross path bin every pair identically whatever its grouping; with the dot
+    # form a mid-range pair near an edge may bin differently in another grouping, unless exact
+    # mode 2 re-decides every near-edge pair in fp64.
     c = synth.catalogs(9000, 0, 20, 30.0, seed=8)
     a, b = slice(0, 4100), slice(4100, 9000)
-    full = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)).astype(object)
-    da = acf.as_uint64(ctx.histogram(c.ra_d[a], c.dec_d[a], bin_width_deg=0.25, nbins=720)).astype(object)
-    db = acf.as_uint64(ctx.histogram(c.ra_d[b], c.dec_d[b], bin_width_deg=0.25, nbins=720)).astype(object)
-    x = acf.as_uint64(ctx.histogram(c.ra_d[a], c.dec_d[a], c.ra_d[b], c.dec_d[b], bin_width_deg=0.25,
-                                    nbins=720)).astype(object)
-    torch.cuda.synchronize()
+    ctx.set_option("mid", mid)
+    ctx.set_option("exact", exact)
+    try:
+        full = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)).astype(object)
+        da = acf.as_uint64(ctx.histogram(c.ra_d[a], c.dec_d[a], bin_width_deg=0.25, nbins=720)).astype(object)
+        db = acf.as_uint64(ctx.histogram(c.ra_d[b], c.dec_d[b], bin_width_deg=0.25, nbins=720)).astype(object)
+        x = acf.as_uint64(ctx.histogram(c.ra_d[a], c.dec_d[a], c.ra_d[b], c.dec_d[b], bin_width_deg=0.25,
+                                        nbins=720)).astype(object)
+        torch.cuda.synchronize()
+    finally:
+        ctx.set_option("mid", 1)
+        ctx.set_option("exact", 1)
     assert list(full) == list(da + db + 2 * x)
 
 
@@ -287,20 +309,48 @@ def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
         ctx.set_option("exact", 1)
 
 
+PATH_KEYS = ("pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact", "pairs_masked",
+             "pairs_mid", "pairs_mid_exact")
+
+
 def test_path_counters_cover_every_computed_pair(acf, ctx):
     c = synth.catalogs(5000, 4100, 12, 30.0, seed=16)
     ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
-    keys = ("pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact", "pairs_masked")
-    got = {k: ctx.info(k) for k in keys}
+    got = {k: ctx.info(k) for k in PATH_KEYS}
     rows = -(-5000 // 128)
     # every unit computes its whole 128-wide i-set against the j-chunk's real length
     assert sum(got.values()) == rows * 128 * 4100, got
-    assert got["pairs_fixed"] > 0 and got["pairs_masked"] > 0
+    assert got["pairs_fixed"] > 0 and got["pairs_masked"] > 0 and got["pairs_mid"] > 0
+    assert got["pairs_mid_exact"] == 0  # exact mode 1 never sends a group to the dot form
+
+
+@pytest.mark.parametrize("w,nb,mid_expected", [(0.25, 720, True), (4.0, 45, False), (0.35, 515, False)])
+def test_dot_form_on_off_and_where_it_applies(acf, ctx, w, nb, mid_expected):
+    # the dot form needs the direct map with P = 180 / w even (0.25 deg: P = 720; 4 deg: P = 45 is
+    # odd; 0.35 deg: P is not an integer, clamp map). With it on or off the edge rule holds.
+    c = synth.catalogs(6000, 5000, 12, 30.0, seed=18)
+    for mid in (1, 0):
+        ctx.set_option("mid", mid)
+        try:
+            _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
+            got = {k: ctx.info(k) for k in PATH_KEYS}
+        finally:
+            ctx.set_option("mid", 1)
+        assert (got["pairs_mid"] > 0) == (mid == 1 and mid_expected), got
+    ctx.set_option("exact", 2)
+    try:
+        g, o, _ = _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
+        assert np.array_equal(g, o.hist)
+        if mid_expected:
+            assert ctx.info("pairs_mid_exact") > 0 and ctx.info("pairs_mid") == 0
+    finally:
+        ctx.set_option("exact", 1)
 
 
 def test_kernel_launch_counter(acf, ctx):
-    """kernel_launches counts every kernel of a call: four catalog-preparation kernels per catalog,
-    the pair kernel and the merge, plus the edge tables and the fix-up in exact mode."""
+    """kernel_launches counts every kernel of a call: eight catalog-preparation kernels per catalog
+    (two radix-sort passes of count, scan and scatter, the vectors, the caps), the pair kernel and
+    the merge, plus the edge tables and the fix-up in exact mode."""
     c = synth.catalogs(3000, 2500, 12, 30.0, seed=17)
 
     def launched(fn):
@@ -308,11 +358,11 @@ def test_kernel_launch_counter(acf, ctx):
         fn()
         return ctx.info("kernel_launches") - before
 
-    assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 4 + 2 + 2
+    assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2 + 2
     assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25,
-                                          nbins=720)) == 8 + 2 + 2
+                                          nbins=720)) == 16 + 2 + 2
     ctx.set_option("exact", 0)
     try:
-        assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 4 + 2
+        assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2
     finally:
         ctx.set_option("exact", 1)

@@ -43,8 +43,8 @@ def test_no_alloc_matches_allocating_entry_point_twice(acf):
                              w, nb)
         assert check.edge_flux(g, o.hist, o.near_below, o.near_above).ok
         assert int(g.sum()) == n1 * (n2 if ra2 is not None else n1)
-    # too large for the static array (20k galaxies fill the 304-block grid; 304 x 18000 bins x
-    # 8 bytes of block rows = 43.8 MB): refused, and the context keeps working
+    # too large for the static array (20k galaxies fill the 152-block grid; 152 x 18000 bins x
+    # 8 bytes of block rows = 21.9 MB): refused, and the context keeps working
     big = synth.catalogs(20000, 0, 0, 0.0, seed=5)
     ra_b, dec_b = _dev(big.ra_d), _dev(big.dec_d)
     out = torch.empty(18000, dtype=torch.int64, device="cuda")
