@@ -24,7 +24,7 @@ ACF_ERR_NOMEM = -3
 ACF_ERR_CUDA = -4
 
 EXPORTED = ["acf_version", "acf_create", "acf_destroy", "acf_last_error", "acf_set_stream", "acf_histogram",
-            "acf_omega", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
+            "acf_omega", "acf_correlate", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
             "acf_kernel_times", "acf_histogram_noalloc"]
 
 _lib = None
@@ -63,6 +63,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "acf_histogram": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp]),
         "acf_histogram_noalloc": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp]),
         "acf_omega": (ci, [vp, vp, vp, vp, i32, i64, i64, vp]),
+        "acf_correlate": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp, vp, vp, vp]),
         "acf_correlate_host": (ci, [vp, vp, vp, i64, vp, vp, i64, f64, i32, vp, vp, vp, vp]),
         "acf_pair_bins": (ci, [vp, vp, vp, vp, vp, i64, f64, i32, vp]),
         "acf_set_option": (ci, [vp, ctypes.c_char_p, i64]),
@@ -133,6 +134,13 @@ def acf_histogram_noalloc(ctx: int, ra, dec, n: int, ra2, dec2, n2: int, bin_wid
 
 def acf_omega(ctx: int, dd, dr, rr, nbins: int, n_d: int, n_r: int, omega) -> None:
     _check(ctx, load().acf_omega(ctx, _ptr(dd), _ptr(dr), _ptr(rr), int(nbins), int(n_d), int(n_r), _ptr(omega)))
+
+
+def acf_correlate(ctx: int, ra_d, dec_d, n_d: int, ra_r, dec_r, n_r: int, bin_width_deg: float, nbins: int,
+                  dd, dr, rr, omega) -> None:
+    """DD, DR, RR and omega from device catalogs into device outputs (asynchronous)."""
+    _check(ctx, load().acf_correlate(ctx, _ptr(ra_d), _ptr(dec_d), int(n_d), _ptr(ra_r), _ptr(dec_r), int(n_r),
+                                     float(bin_width_deg), int(nbins), _ptr(dd), _ptr(dr), _ptr(rr), _ptr(omega)))
 
 
 def acf_correlate_host(ctx: int, ra_d, dec_d, n_d: int, ra_r, dec_r, n_r: int, bin_width_deg: float, nbins: int,
@@ -220,6 +228,18 @@ class Context:
             out = self.torch.empty(dd.numel(), dtype=self.torch.float64, device=self.device)
         acf_omega(self.handle, dd, dr, rr, dd.numel(), n_d, n_r, out)
         return out
+
+    def correlate(self, ra_d, dec_d, ra_r, dec_r, bin_width_deg: float = 0.25, nbins: int = 720, out=None):
+        """Whole job on the device; returns device tensors (dd, dr, rr as int64 holding uint64, omega)."""
+        ra_d, dec_d, ra_r, dec_r = (self._f32(a) for a in (ra_d, dec_d, ra_r, dec_r))
+        if out is None:
+            t = self.torch
+            out = tuple(t.empty(nbins, dtype=t.int64, device=self.device) for _ in range(3)) + (
+                t.empty(nbins, dtype=t.float64, device=self.device),)
+        dd, dr, rr, om = out
+        acf_correlate(self.handle, ra_d, dec_d, ra_d.numel(), ra_r, dec_r, ra_r.numel(), bin_width_deg, nbins,
+                      dd, dr, rr, om)
+        return dd, dr, rr, om
 
     def correlate_host(self, ra_d, dec_d, ra_r, dec_r, bin_width_deg: float = 0.25, nbins: int = 720, out=None):
         """Whole job from host arrays; returns host (dd, dr, rr, omega)."""

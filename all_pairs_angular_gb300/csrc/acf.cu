@@ -357,6 +357,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
                       const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
   unsigned long long* partial = sc.partial;
   unsigned int* ticket = sc.counters;
+  ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 128, c->stream));  // ticket, queue, path counters
   PairParams p;
   p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
   p.exact_lo = pl.exact_lo;
@@ -453,7 +454,6 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
 // and (exact mode) re-decide the flagged pairs.
 int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, const float* ra2, const float* dec2,
                  long long nj, bool sym, const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
-  ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 128, c->stream));
   int rc = prepare_catalog(c, ra, dec, n, sc, sc.a);
   if (rc) return rc;
   if (!sym) {
@@ -465,6 +465,65 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
     ACF_LAUNCHED(c);
   }
   return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc, out);
+}
+
+// Exact-mode queue slots for a histogram of `units` work units: every computed pair may be flagged
+// with probability ~2^(1-S); twice that, within bounds.
+long long queue_slots(const Plan& pl, long long units) {
+  if (!pl.exact) return 0;
+  const double pairs = (double)units * kJT * kJT;
+  return (long long)std::min<double>(kQueueCapMax,
+                                     std::max<double>(kQueueCapMin, 4.0 * pairs * std::ldexp(1.0, -pl.bp.fine_shift)));
+}
+
+int launch_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t* rr, int32_t nbins, int64_t n_d,
+                 int64_t n_r, double* omega) {
+  const double nd = (double)n_d, nr = (double)n_r;
+  const double f_dd = (nr * nr) / (nd * nd), f_dr = (nr * nr) / (nd * nr);
+  const int threads = 256;
+  const int blocks = std::min((nbins + threads - 1) / threads, 4096);
+  omega_kernel<<<blocks, threads, 0, c->stream>>>(reinterpret_cast<const unsigned long long*>(dd),
+                                                   reinterpret_cast<const unsigned long long*>(dr),
+                                                   reinterpret_cast<const unsigned long long*>(rr), nbins, f_dd, f_dr,
+                                                   omega);
+  ACF_LAUNCHED(c);
+  return ACF_OK;
+}
+
+// DD, DR, RR and omega from device catalogs: each catalog is sorted and converted once, the
+// edge tables built once, then the three histograms run back to back on the same workspace.
+int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_d, const float* ra_r,
+                   const float* dec_r, int64_t n_r, double w_deg, int32_t nbins, uint64_t* dd, uint64_t* dr,
+                   uint64_t* rr, double* omega) {
+  if (!ra_d || !dec_d || !ra_r || !dec_r || !dd || !dr || !rr || !omega)
+    return fail(c, ACF_ERR_ARG, "correlate: NULL pointer");
+  if (n_d <= 0 || n_r <= 0) return fail(c, ACF_ERR_ARG, "correlate: n_d and n_r must be > 0");
+  if (n_d > 2147483647ll || n_r > 2147483647ll) return fail(c, ACF_ERR_UNSUPPORTED, "catalogs are limited to 2^31-1 galaxies");
+  Plan pl;
+  int rc = make_plan(c, w_deg, nbins, pl);
+  if (rc) return rc;
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  Launch Ldd, Ldr, Lrr;
+  if ((rc = plan_launch(c, pl, n_d, n_d, true, Ldd)) || (rc = plan_launch(c, pl, n_d, n_r, false, Ldr)) ||
+      (rc = plan_launch(c, pl, n_r, n_r, true, Lrr)))
+    return rc;
+  const long long grid = std::max(Ldd.grid, std::max(Ldr.grid, Lrr.grid));
+  const long long qcap = queue_slots(pl, std::max(Ldd.units, std::max(Ldr.units, Lrr.units)));
+  rc = ensure(c, c->ws, carve(nullptr, n_d, n_r, false, grid, nbins, qcap, nullptr));
+  if (rc) return rc;
+  Scratch sc;
+  carve(static_cast<char*>(c->ws.ptr), n_d, n_r, false, grid, nbins, qcap, &sc);
+  if ((rc = prepare_catalog(c, ra_d, dec_d, n_d, sc, sc.a)) || (rc = prepare_catalog(c, ra_r, dec_r, n_r, sc, sc.b)))
+    return rc;
+  if (pl.exact && sc.qcap > 0) {
+    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U);
+    ACF_LAUNCHED(c);
+  }
+  if ((rc = histogram_vectors(c, sc.a, n_d, sc.a, n_d, true, pl, Ldd, sc, dd)) ||
+      (rc = histogram_vectors(c, sc.a, n_d, sc.b, n_r, false, pl, Ldr, sc, dr)) ||
+      (rc = histogram_vectors(c, sc.b, n_r, sc.b, n_r, true, pl, Lrr, sc, rr)))
+    return rc;
+  return launch_omega(c, dd, dr, rr, nbins, n_d, n_r, omega);
 }
 
 int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2, const float* dec2,
@@ -489,12 +548,7 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  // queue: every computed pair may be flagged with probability ~2^(1-S); twice that, within bounds
-  long long qcap = 0;
-  if (pl.exact) {
-    const double pairs = (double)L.units * kJT * kJT;
-    qcap = (long long)std::min<double>(kQueueCapMax, std::max<double>(kQueueCapMin, 4.0 * pairs * std::ldexp(1.0, -pl.bp.fine_shift)));
-  }
+  const long long qcap = queue_slots(pl, L.units);
   rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, qcap, nullptr));
   if (rc) return rc;
   Scratch sc;
@@ -560,16 +614,14 @@ int acf_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t
   if (!dd || !dr || !rr || !omega) return fail(c, ACF_ERR_ARG, "omega: NULL pointer");
   if (nbins <= 0 || n_d <= 0 || n_r <= 0) return fail(c, ACF_ERR_ARG, "omega: nbins, n_d, n_r must be > 0");
   ACF_CUDA(c, cudaSetDevice(c->device));
-  const double nd = (double)n_d, nr = (double)n_r;
-  const double f_dd = (nr * nr) / (nd * nd), f_dr = (nr * nr) / (nd * nr);
-  const int threads = 256;
-  const int blocks = std::min((nbins + threads - 1) / threads, 4096);
-  omega_kernel<<<blocks, threads, 0, c->stream>>>(reinterpret_cast<const unsigned long long*>(dd),
-                                                   reinterpret_cast<const unsigned long long*>(dr),
-                                                   reinterpret_cast<const unsigned long long*>(rr), nbins, f_dd, f_dr,
-                                                   omega);
-  ACF_LAUNCHED(c);
-  return ACF_OK;
+  return launch_omega(c, dd, dr, rr, nbins, n_d, n_r, omega);
+}
+
+int acf_correlate(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_d, const float* ra_r,
+                  const float* dec_r, int64_t n_r, double w_deg, int32_t nbins, uint64_t* dd, uint64_t* dr, uint64_t* rr,
+                  double* omega) {
+  if (!c) return ACF_ERR_ARG;
+  return correlate_impl(c, ra_d, dec_d, n_d, ra_r, dec_r, n_r, w_deg, nbins, dd, dr, rr, omega);
 }
 
 int acf_correlate_host(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_d, const float* ra_r,
@@ -598,10 +650,8 @@ int acf_correlate_host(acf_ctx* c, const float* ra_d, const float* dec_d, int64_
   ACF_CUDA(c, cudaMemcpyAsync(d_dec_d, dec_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
   ACF_CUDA(c, cudaMemcpyAsync(d_ra_r, ra_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
   ACF_CUDA(c, cudaMemcpyAsync(d_dec_r, dec_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
-  if ((rc = histogram_impl(c, d_ra_d, d_dec_d, n_d, nullptr, nullptr, 0, w_deg, nbins, d_dd))) return rc;
-  if ((rc = histogram_impl(c, d_ra_d, d_dec_d, n_d, d_ra_r, d_dec_r, n_r, w_deg, nbins, d_dr))) return rc;
-  if ((rc = histogram_impl(c, d_ra_r, d_dec_r, n_r, nullptr, nullptr, 0, w_deg, nbins, d_rr))) return rc;
-  if ((rc = acf_omega(c, d_dd, d_dr, d_rr, nbins, n_d, n_r, d_om))) return rc;
+  if ((rc = correlate_impl(c, d_ra_d, d_dec_d, n_d, d_ra_r, d_dec_r, n_r, w_deg, nbins, d_dd, d_dr, d_rr, d_om)))
+    return rc;
   ACF_CUDA(c, cudaMemcpyAsync(dd, d_dd, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
   ACF_CUDA(c, cudaMemcpyAsync(dr, d_dr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
   ACF_CUDA(c, cudaMemcpyAsync(rr, d_rr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));

@@ -223,10 +223,8 @@ def run_ours(args, cat, workload, rank, world, local):
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
 
     def step():
-        acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, None, None, 0, w, nb, dd)
-        acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, ra_r, dec_r, cat.n_r, w, nb, dr)
-        acf.acf_histogram(ctx.handle, ra_r, dec_r, cat.n_r, None, None, 0, w, nb, rr)
-        acf.acf_omega(ctx.handle, dd, dr, rr, nb, cat.n_d, cat.n_r, om)
+        # the whole hot path: both catalogs sorted and converted, DD, DR, RR and omega
+        acf.acf_correlate(ctx.handle, ra_d, dec_d, cat.n_d, ra_r, dec_r, cat.n_r, w, nb, dd, dr, rr, om)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -347,10 +345,7 @@ def run_profile(args, cat):
     out = [torch.empty(nb, dtype=torch.int64, device=dev) for _ in range(3)]
     om = torch.empty(nb, dtype=torch.float64, device=dev)
     for _ in range(2):
-        ctx.histogram(t["ra_d"], t["dec_d"], bin_width_deg=w, nbins=nb, out=out[0])
-        ctx.histogram(t["ra_d"], t["dec_d"], t["ra_r"], t["dec_r"], bin_width_deg=w, nbins=nb, out=out[1])
-        ctx.histogram(t["ra_r"], t["dec_r"], bin_width_deg=w, nbins=nb, out=out[2])
-        ctx.omega(out[0], out[1], out[2], cat.n_d, cat.n_r, out=om)
+        ctx.correlate(t["ra_d"], t["dec_d"], t["ra_r"], t["dec_r"], w, nb, out=(*out, om))
     torch.cuda.synchronize()
     sums = [int(acf.as_uint64(o).sum()) for o in out]
     print(json.dumps({"profile": cat.name, "sums": sums, "grid": ctx.info("grid"), "threads": ctx.info("threads"),

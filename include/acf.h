@@ -127,8 +127,21 @@ int acf_omega(acf_ctx *ctx, const uint64_t *dd, const uint64_t *dr, const uint64
               int64_t n_r, double *omega);
 
 /*
- * The whole job from HOST memory: copies the two catalogs to the device, computes DD, DR, RR and
- * omega, copies the four results back and synchronises the stream before returning.
+ * The whole job on the device (section "The problem"): DD of the data catalog, DR, RR of the
+ * random catalog, and omega. Each catalog is sorted and converted once for the three histograms,
+ * so this costs less than three acf_histogram calls plus acf_omega, with the same results.
+ *   ra_d, dec_d  device float[n_d];  ra_r, dec_r  device float[n_r]  (arcminutes)
+ *   dd, dr, rr   device uint64[nbins], overwritten;  omega  device double[nbins], overwritten
+ * Same binning rules as acf_histogram; n_d and n_r must be > 0. Asynchronous on the context's
+ * stream. Afterwards the acf_get_info counters describe the last histogram of the three (RR).
+ */
+int acf_correlate(acf_ctx *ctx, const float *ra_d, const float *dec_d, int64_t n_d, const float *ra_r,
+                  const float *dec_r, int64_t n_r, double bin_width_deg, int32_t nbins, uint64_t *dd, uint64_t *dr,
+                  uint64_t *rr, double *omega);
+
+/*
+ * The whole job from HOST memory: copies the two catalogs to the device, runs acf_correlate,
+ * copies the four results back and synchronises the stream before returning.
  *   ra_d, dec_d  host float[n_d];  ra_r, dec_r  host float[n_r]  (arcminutes; pinned memory
  *                gives asynchronous copies, pageable memory works too)
  *   dd, dr, rr   host uint64[nbins], overwritten;  omega  host double[nbins], overwritten

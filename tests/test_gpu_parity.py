@@ -165,6 +165,23 @@ def test_correlate_host_matches_device_path(acf, ctx):
     assert check.omega_close(om, oracle.omega(dd, dr, rr, c.n_d, c.n_r), rel=1e-12)
 
 
+def test_correlate_equals_separate_histograms(acf, ctx):
+    # one call, each catalog prepared once: the same counts as three histogram calls, and the
+    # same omega as acf_omega on them
+    c = synth.catalogs(5000, 6100, 12, 30.0, seed=19)
+    dd, dr, rr, om = ctx.correlate(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+    tdd = ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)
+    tdr = ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+    trr = ctx.histogram(c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+    tom = ctx.omega(tdd, tdr, trr, c.n_d, c.n_r)
+    torch.cuda.synchronize()
+    for a, b in ((dd, tdd), (dr, tdr), (rr, trr)):
+        assert torch.equal(a, b)
+    assert check.omega_close(om.cpu().numpy(), tom.cpu().numpy(), rel=0.0)
+    o = oracle.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)
+    assert check.edge_flux(acf.as_uint64(dr), o.hist, o.near_below, o.near_above).ok
+
+
 def _pair_sets(n, seed):
     """Random pairs over the whole sphere, tight pairs (< 1 deg), near-antipodal pairs, pairs near
     90 degrees, where the kernel switches between the difference and the sum chord, and pairs near
@@ -361,6 +378,8 @@ def test_kernel_launch_counter(acf, ctx):
     assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2 + 2
     assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25,
                                           nbins=720)) == 16 + 2 + 2
+    # the whole job: two catalogs prepared once, one edge table, three histograms, omega
+    assert launched(lambda: ctx.correlate(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)) == 16 + 1 + 3 * 3 + 1
     ctx.set_option("exact", 0)
     try:
         assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2
