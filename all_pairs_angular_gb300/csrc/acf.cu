@@ -58,7 +58,7 @@ struct acf_ctx {
   long long opt_units_per_launch = 0;
   int opt_exact = 1;              // 0 off, 1 near 0 and 180 degrees, 2 everywhere
   double opt_exact_below_deg = 20.0;
-  int opt_mid = 1;                // 1: the dot form between 45 and 135 degrees
+  int opt_range_forms = 1;        // 1: cheaper forms where the caps bound the separations
   int opt_pair_bins_form = 0;     // acf_pair_bins: 0 chord form, 1 dot form where |u.v| < cos 45 deg
   unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
   long long last_qcap = 0;
@@ -145,7 +145,7 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     bp.magic_far = (float)(8388608.0 + pr);
     bp.clamp_c = (float)(bp.entries - 1);
     // the dot form needs 2^23 + P/2 to be an integer
-    bp.mid = (c->opt_mid && std::fmod(pr, 2.0) == 0.0) ? 1 : 0;
+    bp.mid = (c->opt_range_forms && std::fmod(pr, 2.0) == 0.0) ? 1 : 0;
     bp.magic_mid = (float)(8388608.0 + pr / 2.0);
     for (int k = 0; k < 8; ++k) bp.rc[k] = (float)(kR[k] / w_rad);
   } else {
@@ -158,6 +158,7 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     bp.entries = (int)entries;
     bp.clamp_c = (float)(entries - 1);
   }
+  bp.small = c->opt_range_forms ? 1 : 0;
   // Exact mode: S fractional bits in the bin code make a window of 2^-S bins around every edge,
   // wider than the fp32 path's error there (3.5e-7 rad near 0 and 180 degrees, 8e-7 rad anywhere).
   pl.exact = (pl.method == kChordPoly) ? c->opt_exact : 0;
@@ -243,7 +244,7 @@ struct CatBufs {
 };
 struct Scratch {
   unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue slots handed out, [2] moved pairs,
-                                       // [3] flagged pairs; bytes 64..119: pairs per path (u64)
+                                       // [3] flagged pairs; bytes 64..135: pairs per path (u64)
   unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
   unsigned int* key1 = nullptr;        // sort: keys after the first pass
   unsigned int* idx1 = nullptr;        // sort: input indices after the first pass
@@ -357,7 +358,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
                       const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
   unsigned long long* partial = sc.partial;
   unsigned int* ticket = sc.counters;
-  ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 128, c->stream));  // ticket, queue, path counters
+  ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 256, c->stream));  // ticket, queue, path counters
   PairParams p;
   p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
   p.exact_lo = pl.exact_lo;
@@ -705,9 +706,9 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "exact_below_deg")) {
     if (v < 0 || v > 180) return fail(c, ACF_ERR_ARG, "exact_below_deg must be 0..180");
     c->opt_exact_below_deg = (double)v;
-  } else if (!strcmp(key, "mid")) {
-    if (v != 0 && v != 1) return fail(c, ACF_ERR_ARG, "mid must be 0 or 1");
-    c->opt_mid = (int)v;
+  } else if (!strcmp(key, "range_forms")) {
+    if (v != 0 && v != 1) return fail(c, ACF_ERR_ARG, "range_forms must be 0 or 1");
+    c->opt_range_forms = (int)v;
   } else if (!strcmp(key, "pair_bins_form")) {
     if (v != 0 && v != 1) return fail(c, ACF_ERR_ARG, "pair_bins_form must be 0 or 1");
     c->opt_pair_bins_form = (int)v;
@@ -742,12 +743,13 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
       *v = e.val;
       return ACF_OK;
     }
-  const char* path_keys[7] = {"pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact",
-                               "pairs_masked", "pairs_mid", "pairs_mid_exact"};
-  for (int k = 0; k < 7; ++k)
+  const char* path_keys[9] = {"pairs_fixed",  "pairs_general",   "pairs_fixed_exact", "pairs_general_exact",
+                               "pairs_masked", "pairs_mid",       "pairs_mid_exact",   "pairs_small",
+                               "pairs_small_exact"};
+  for (int k = 0; k < 9; ++k)
     if (!strcmp(key, path_keys[k])) {
       // synchronises the stream; pairs the last histogram call evaluated on each pair-kernel path
-      unsigned long long h[7] = {0, 0, 0, 0, 0, 0, 0};
+      unsigned long long h[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
       if (c->last_counters) {
         if (cudaSetDevice(c->device) != cudaSuccess || cudaStreamSynchronize(c->stream) != cudaSuccess ||
             cudaMemcpy(h, c->last_counters + 16, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)

@@ -44,6 +44,12 @@ constexpr int kJJUnroll = ACF_JJ_UNROLL;
 #define ACF_JJ_UNROLL_FINE 1
 #endif
 constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact-mode (fine code) loops
+#ifndef ACF_JJ_BATCH
+#define ACF_JJ_BATCH 2
+#endif
+// j-galaxies per step of the hot loops: their tile loads first, then every code, then every atomic
+// (the atomics' memory clobber would otherwise keep the next tile load behind them)
+constexpr int kJJBatch = ACF_JJ_BATCH;
 #ifndef ACF_ASM_LOP3
 #define ACF_ASM_LOP3 1  // write the two sign-bit logic ops as explicit lop3 (2 ops, not 3)
 #endif  // j-loop unroll of the full-chunk path
@@ -59,6 +65,13 @@ __device__ constexpr float kP0 = 0.99999959294652097f, kP1 = 0.08334261162808559
                            kP3 = 0.0019657095570993176f, kP4 = 4.2347086002697957e-05f,
                            kP5 = 0.00029099553526503564f, kP6 = -9.1427792701640403e-05f,
                            kP7 = 2.3068911858269848e-05f;
+
+// The same on theta' <= 66.4 degrees (q <= 1.2) with degree 5, for groups whose caps keep every
+// theta' below 66 degrees: absolute theta' error <= 1.3e-8 rad (1.7e-8 after fp32 rounding).
+__device__ constexpr float kS0 = 0.99999969522972076f, kS1 = 0.083340197828446816f, kS2 = 0.011067258098628368f,
+                           kS3 = 0.0019039784386728404f, kS4 = 0.00016731237856202599f,
+                           kS5 = 0.000144248943642142f;
+constexpr float kSmallRad = 1.1519173063162575f;  // 66 degrees
 
 // Between 45 and 135 degrees the dot product d = u.v loses nothing: theta = pi/2 - asin(d) with
 // asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(43 deg), degree 7: absolute
@@ -79,6 +92,7 @@ struct BinParams {
   float rc[8];        // dot form: kR[k] / w
   float rc_f[8];      // exact mode: kR[k] 2^S / w
   int mid;            // 1: groups between 45 and 135 degrees use the dot form
+  int small;          // 1: groups whose theta' stays below 66 degrees use the degree-5 chord polynomial
   int fine_shift;     // exact mode: S
   int kmax;           // exact mode: highest bin a separation <= 180 degrees can reach
   unsigned int zone0, span0, zone1, span1;  // exact mode: entries e with e - zone <= span (unsigned) are re-decided
@@ -114,7 +128,8 @@ struct PairParams {
   unsigned int qbatch;                 // slots a block reserves at its start
   unsigned long long* path_pairs;      // pairs evaluated per path: chord fixed, chord general,
                                        // chord fixed+flag, chord general+flag, masked/ragged units,
-                                       // dot form, dot form+flag (all pairs computed)
+                                       // dot form, dot form+flag, short chord, short chord+flag
+                                       // (all pairs computed)
   BinParams bp;
 };
 
@@ -536,20 +551,30 @@ __device__ __forceinline__ int entry_to_bin(int e, const BinParams& bp) {
 // bit the general code takes these steps for such a pair: fma(ns, v, u) is the same difference or
 // sum, and the far-side code fma_rz(-theta', 1/w, m) is fma_rz(theta', -1/w, m). Only the dot
 // product, the sign-bit operation and the choice of constant are dropped.
-template <int MAP, bool FINE = false>
+// SMALL: the degree-5 polynomial, for groups whose caps keep every theta' below 66 degrees.
+template <int MAP, bool FINE = false, bool SMALL = false>
 __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, float xj, float yj, float zj, float ns,
                                                  float iws, float h, const BinParams& bp) {
   const float dx = fmaf(ns, xj, xi);
   const float dy = fmaf(ns, yj, yi);
   const float dz = fmaf(ns, zj, zi);
   const float q = fmaf(dz, dz, fmaf(dy, dy, fmaf(dx, dx, 1e-30f)));
-  float p = fmaf(kP7, q, kP6);
-  p = fmaf(p, q, kP5);
-  p = fmaf(p, q, kP4);
-  p = fmaf(p, q, kP3);
-  p = fmaf(p, q, kP2);
-  p = fmaf(p, q, kP1);
-  p = fmaf(p, q, kP0);
+  float p;
+  if (SMALL) {
+    p = fmaf(kS5, q, kS4);
+    p = fmaf(p, q, kS3);
+    p = fmaf(p, q, kS2);
+    p = fmaf(p, q, kS1);
+    p = fmaf(p, q, kS0);
+  } else {
+    p = fmaf(kP7, q, kP6);
+    p = fmaf(p, q, kP5);
+    p = fmaf(p, q, kP4);
+    p = fmaf(p, q, kP3);
+    p = fmaf(p, q, kP2);
+    p = fmaf(p, q, kP1);
+    p = fmaf(p, q, kP0);
+  }
   const float th = sqrt_approx(p * q);
   if (MAP == kDirect) {
     return fma_rz(th, iws, h);
@@ -622,10 +647,12 @@ struct PathTag {
 // separation may be below lo or above pi - lo (cos tc > cos(lo + r) or < -cos(lo + r)).
 // kMidBit is added when every separation lies in (45, 135) degrees (|cos tc| < cos(45 deg + r))
 // and the dot form is on; in mode 1 never for a group the exact mode checks, so every pair the
-// exact mode may re-decide is binned by the chord form whatever its grouping.
+// exact mode may re-decide is binned by a chord form. Otherwise kSmallBit is added when every
+// theta' lies below 66 degrees on one side of 90 (|cos tc| > cos(66 deg - r)).
 constexpr int kExactBit = 4;
 constexpr int kMidBit = 8;
-__device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float lo, int mid) {
+constexpr int kSmallBit = 16;
+__device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float lo, int mid, int small) {
   const float dot = a.x * b.x + a.y * b.y + a.z * b.z;
   const float r = a.w + b.w + 1e-4f;
   int path = kGeneral;
@@ -638,12 +665,16 @@ __device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float l
     const float cm = __cosf(kMidRad + r) - 1e-5f;
     if (fabsf(dot) < cm) path |= kMidBit;
   }
+  if (small && !(path & kMidBit) && r < kSmallRad) {
+    const float cs = __cosf(kSmallRad - r) + 1e-5f;
+    if (fabsf(dot) > cs) path |= kSmallBit;  // implies a fixed sign
+  }
   if (mode == 2) return path | kExactBit;
   if (mode == 1) {
     const float x = lo + r;
-    if (x >= 3.0f) return (path & 3) | kExactBit;
+    if (x >= 3.0f) return (path & ~kMidBit) | kExactBit;
     const float cl = __cosf(x) - 1e-5f;
-    if (dot > cl || dot < -cl) return (path & 3) | kExactBit;
+    if (dot > cl || dot < -cl) return (path & ~kMidBit) | kExactBit;
   }
   return path;
 }
@@ -799,7 +830,8 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     int cur_r = -1, buf = 0;
     // j-groups per path (x 32*kJT pairs): chord fixed, chord general, the same with flags, dot form,
     // dot form with flags
-    unsigned int g_fixed = 0, g_general = 0, g_fixed_f = 0, g_general_f = 0, g_mid = 0, g_mid_f = 0;
+    unsigned int g_fixed = 0, g_general = 0, g_fixed_f = 0, g_general_f = 0, g_mid = 0, g_mid_f = 0, g_small = 0,
+                 g_small_f = 0;
     unsigned long long edge_pairs = 0ull;
     while (true) {
       int rn = 0, cn = 0;
@@ -845,10 +877,40 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         // fine (exact) loops are rare and kept rolled so that all live loop bodies fit the
         // instruction cache.
         auto run = [&](auto form, auto fine, int jbeg, float ns, float iws, float h) {
-          constexpr int X = decltype(form)::value;  // 0 chord general, 1 chord fixed sign, 2 dot form
+          constexpr int X = decltype(form)::value;  // 0 chord general, 1 chord fixed sign, 2 dot form,
+                                                    // 3 short chord (fixed sign)
           constexpr bool F = decltype(fine)::value;
-          // the general chord loop is rare once the caps pick the dot form across 90 degrees: rolled
-          constexpr int U = (F || X == 0) ? kJJUnrollFine : kJJUnroll;
+          // the general and the full-range fixed chord loops are rare once the caps pick the dot form
+          // across 90 degrees and the short chord below 66: rolled
+          constexpr int U = (F || X == 0 || X == 1) ? kJJUnrollFine : kJJUnroll;
+          auto code_of = [&](int k, float4 v) -> uint32_t {
+            return __float_as_uint(
+                X == 2   ? pair_code_mid<F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
+                : X == 3 ? pair_code_fixed<MAP, F, true>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h, p.bp)
+                : X == 1 ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h, p.bp)
+                         : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
+          };
+          if constexpr (!F && U > 1 && kJJBatch > 1) {
+            constexpr int B = kJJBatch;
+#pragma unroll 1
+            for (int jj = jbeg; jj < jbeg + 32; jj += B) {
+              float4 vv[B];
+#pragma unroll
+              for (int u = 0; u < B; ++u) vv[u] = tile[jj + u];
+              uint32_t cb[B][K];
+#pragma unroll
+              for (int u = 0; u < B; ++u)
+#pragma unroll
+                for (int k = 0; k < K; ++k) cb[u][k] = code_of(k, vv[u]);
+#pragma unroll
+              for (int u = 0; u < B; ++u)
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+                  add_pair<false>(p, cb[u][k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj + u, xi[k],
+                                  yi[k], zi[k], vv[u]);
+            }
+            return;
+          }
 #pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
             const float4 v = tile[jj];
@@ -856,11 +918,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             unsigned int near = 0u;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-              const float code =
-                  X == 2 ? pair_code_mid<F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
-                  : X == 1 ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h, p.bp)
-                           : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp);
-              cbs[k] = __float_as_uint(code);
+              cbs[k] = code_of(k, v);
               if (add_pair<F>(p, cbs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
                               yi[k], zi[k], v))
                 near |= 1u << k;
@@ -873,11 +931,14 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             }
           }
         };
+        // the four j-groups' paths, one per lane of lanes 0..3 (one pass of the decision per unit)
+        int pc_lane = kGeneral;
+        if (METHOD == kChordPoly && lane < kJT / 32)
+          pc_lane = choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + lane), p.exact_mode, p.exact_lo,
+                                MAP == kDirect ? p.bp.mid : 0, p.bp.small);
 #pragma unroll 1
         for (int g = 0; g < kJT / 32; ++g) {
-          const int pc = (METHOD == kChordPoly) ? choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + g), p.exact_mode,
-                                                              p.exact_lo, MAP == kDirect ? p.bp.mid : 0)
-                                                : kGeneral;
+          const int pc = __shfl_sync(0xffffffffu, pc_lane, g);
           const int path = pc & 3;
           const bool fine = (pc & kExactBit) != 0;
           if (pc & kMidBit) {
@@ -892,6 +953,12 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           float h;
           if (MAP == kDirect) h = (path == kBelow90) ? kMagic : (fine ? p.bp.magic_far_f : p.bp.magic_far);
           else h = (path == kBelow90) ? 0.0f : 3.14159265358979323846f * iw;
+          if (pc & kSmallBit) {
+            (fine ? g_small_f : g_small) += 1;
+            if (fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h);
+            else run(FormTag<3>(), FineTag<false>(), g * 32, ns, iws, h);
+            continue;
+          }
           if (path == kGeneral) (fine ? g_general_f : g_general) += 1;
           else (fine ? g_fixed_f : g_fixed) += 1;
           if (path == kGeneral) {
@@ -948,6 +1015,8 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       if (edge_pairs) atomicAdd(p.path_pairs + 4, edge_pairs);
       if (g_mid) atomicAdd(p.path_pairs + 5, g_mid * G);
       if (g_mid_f) atomicAdd(p.path_pairs + 6, g_mid_f * G);
+      if (g_small) atomicAdd(p.path_pairs + 7, g_small * G);
+      if (g_small_f) atomicAdd(p.path_pairs + 8, g_small_f * G);
     }
   }
   __syncthreads();
@@ -1053,8 +1122,9 @@ __global__ void fixup_kernel(const uint4* __restrict__ queue, const unsigned int
   }
 }
 
-// form 1: pairs with |u.v| < cos(45 deg) take the dot form (as in a group the caps put between
-// 45 and 135 degrees), the others the chord form; form 0: the chord form for every pair.
+// form 1: what a group the caps bound tightly computes: pairs with |u.v| < cos(45 deg) take the
+// dot form, pairs with |u.v| > cos(66 deg) the short chord, the others the full-range chord form;
+// form 0: the full-range chord form for every pair.
 template <int MAP, int METHOD>
 __global__ void pair_bins_kernel(const float* __restrict__ ra1, const float* __restrict__ dec1,
                                  const float* __restrict__ ra2, const float* __restrict__ dec2, long long n,
@@ -1065,8 +1135,18 @@ __global__ void pair_bins_kernel(const float* __restrict__ ra1, const float* __r
     const float4 v = radec_to_unit(ra2[i], dec2[i]);
     const float d = fmaf(u.z, v.z, fmaf(u.y, v.y, u.x * v.x));
     const bool mid = form == 1 && MAP == kDirect && METHOD == kChordPoly && bp.mid && fabsf(d) < 0.70710678f;
-    const float code = mid ? pair_code_mid<false>(u.x, u.y, u.z, v.x, v.y, v.z, bp)
-                           : pair_code<MAP, METHOD>(u.x, u.y, u.z, v.x, v.y, v.z, bp);
+    const bool small = form == 1 && METHOD == kChordPoly && bp.small && fabsf(d) > 0.40673664f;  // cos 66 deg
+    float code;
+    if (mid) {
+      code = pair_code_mid<false>(u.x, u.y, u.z, v.x, v.y, v.z, bp);
+    } else if (small) {
+      const bool near = !(__float_as_uint(d) >> 31);
+      const float h = MAP == kDirect ? (near ? kMagic : bp.magic_far) : (near ? 0.0f : 3.14159265358979323846f * bp.inv_w);
+      code = pair_code_fixed<MAP, false, true>(u.x, u.y, u.z, v.x, v.y, v.z, near ? -1.0f : 1.0f,
+                                               near ? bp.inv_w : -bp.inv_w, h, bp);
+    } else {
+      code = pair_code<MAP, METHOD>(u.x, u.y, u.z, v.x, v.y, v.z, bp);
+    }
     int e = (int)(__float_as_uint(code) - magic_bits);
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     bins[i] = entry_to_bin<MAP>(e, bp);

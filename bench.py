@@ -35,11 +35,12 @@ UNIT = "Gpairs/s"
 # Thread instructions per pair of each pair-kernel path: the general chord + polynomial loop is 25
 # (dot product, sign, chord, polynomial, sqrt, sign-dependent constant, rounding fma, address,
 # shared atomic); where the caps fix the sign of the dot product the dot, the sign operation and the
-# constant choice drop out (18); the dot form for groups between 45 and 135 degrees is 14 (dot,
-# square, 7-term polynomial, rounding fma, address, atomic); the exact-mode flag adds 5 (fine-code
-# address, edge test, branch).
+# constant choice drop out (18); where every theta' stays below 66 degrees the polynomial is of
+# degree 5 instead of 7 (16); the dot form for groups between 45 and 135 degrees is 14 (dot, square,
+# 7-term polynomial, rounding fma, address, atomic); the exact-mode flag adds 5 (fine-code address,
+# edge test, branch).
 INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 23, "pairs_general_exact": 30,
-                 "pairs_mid": 14, "pairs_mid_exact": 19}
+                 "pairs_mid": 14, "pairs_mid_exact": 19, "pairs_small": 16, "pairs_small_exact": 21}
 INST_MASKED = 25  # diagonal / ragged units run the general loop on every computed pair
 SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
 # The pages' kernel time for three 100k histograms on an RTX 5080 (another machine: context only)
@@ -262,7 +263,9 @@ def run_ours(args, cat, workload, rank, world, local):
                 alg_inst += ipp * n_pairs
                 alg_pairs += n_pairs
             masked = ctx.info("pairs_masked")
-            alg_inst += (INST_MASKED + (5 if ctx.info("pairs_fixed_exact") + ctx.info("pairs_general_exact") else 0)) * masked
+            exact_on = sum(ctx.info(k) for k in ("pairs_fixed_exact", "pairs_general_exact", "pairs_small_exact",
+                                                 "pairs_mid_exact")) > 0
+            alg_inst += (INST_MASKED + (5 if exact_on else 0)) * masked
             alg_pairs += masked
     path_mix = {k: ctx.info(k) for k in INST_PER_PATH}
     total_ms = sum(step_ms)

@@ -174,6 +174,14 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    2 = re-decide such pairs at every separation: the histograms then equal those
  *                        of the fp64 formula
  *   "exact_below_deg"  the window of mode 1, whole degrees 0..180 (default 20)
+ *   "range_forms"    1 = where the caps of a block of pairs bound its separations, use a cheaper
+ *                        form that meets the same precision contract: the dot product with an
+ *                        asin polynomial between 45 and 135 degrees (needs 180/w an even integer),
+ *                        a degree-5 chord polynomial where theta' stays below 66 degrees (default);
+ *                    0 = the full-range chord form for every pair (every pair then gets the same
+ *                        code whichever block computes it, so DD of a union splits exactly)
+ *   "pair_bins_form" acf_pair_bins: 0 = full-range chord form (default); 1 = the form a tightly
+ *                    bounded block would use for that pair's own dot product
  *   "units_per_launch"  cap on work units (128 x 128 pairs) per pair-kernel launch; 0 = automatic
  *                    (large problems are always split so that no 32-bit shared counter can wrap)
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
@@ -190,6 +198,8 @@ int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
  *   "pairs_fixed", "pairs_general"  pairs evaluated on the fixed-sign and general loops
  *   "pairs_fixed_exact", "pairs_general_exact"  the same loops with edge flagging (exact mode)
  *   "pairs_masked"                  pairs of diagonal or ragged units (one compare per pair more)
+ *   "pairs_mid", "pairs_mid_exact"  the dot form (45..135 degrees), without and with flagging
+ *   "pairs_small", "pairs_small_exact"  the degree-5 chord form, without and with flagging
  *   "exact_flagged"  pairs flagged for re-decision;  "exact_moved"  of those, pairs moved a bin;
  *   "exact_overflow"  flagged pairs that did not fit in the queue (kept their fp32 bin)
  * Unknown keys return ACF_ERR_ARG.

@@ -98,10 +98,10 @@ def _full_totals(acf, ctx, c):
     torch.cuda.synchronize()
     assert int(dd.sum()) == c.n_d ** 2 and int(dr.sum()) == c.n_d * c.n_r and int(rr.sum()) == c.n_r ** 2
     # split identity on the full catalog: DD(A u B) = DD(A) + DD(B) + 2 X(A, B), exactly, with the
-    # chord form alone (the dot form's bin of a mid-range pair within ~4e-7 rad of an edge may
-    # depend on its grouping)
+    # full-range chord form alone (with the range forms, the bin of a pair within ~4e-7 rad of an
+    # edge may depend on the form its grouping picks)
     h = c.n_d // 3
-    ctx.set_option("mid", 0)
+    ctx.set_option("range_forms", 0)
     try:
         full = acf.as_uint64(ctx.histogram(ra_d, dec_d, bin_width_deg=w, nbins=nb)).astype(object)
         a = acf.as_uint64(ctx.histogram(ra_d[:h], dec_d[:h], bin_width_deg=w, nbins=nb)).astype(object)
@@ -110,7 +110,7 @@ def _full_totals(acf, ctx, c):
                                         nbins=nb)).astype(object)
         torch.cuda.synchronize()
     finally:
-        ctx.set_option("mid", 1)
+        ctx.set_option("range_forms", 1)
     assert list(full) == list(a + b + 2 * x)
 
 

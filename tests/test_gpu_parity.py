@@ -184,8 +184,8 @@ def test_correlate_equals_separate_histograms(acf, ctx):
 
 def _pair_sets(n, seed):
     """Random pairs over the whole sphere, tight pairs (< 1 deg), near-antipodal pairs, pairs near
-    90 degrees, where the kernel switches between the difference and the sum chord, and pairs near
-    45 and 135 degrees, the edges of the dot form's range."""
+    90 degrees, where the kernel switches between the difference and the sum chord, pairs near 45
+    and 135 degrees, the edges of the dot form's range, and near 66 and 114, the short chord's."""
     rng = np.random.default_rng(seed)
     ra1, dec1 = synth.uniform_sphere(n, seed)
     ra2, dec2 = synth.uniform_sphere(n, seed + 1)
@@ -203,7 +203,7 @@ def _pair_sets(n, seed):
     sets.append((ra1, np.zeros(n, np.float32), ((ra1 + 5400 + rng.uniform(-30, 30, n)) % 21600).astype(np.float32),
                  rng.uniform(-30, 30, n).astype(np.float32)))
     # near 45 and 135 degrees, where groups switch between the chord form and the dot form
-    for lo in (43.0, 133.0):
+    for lo in (43.0, 133.0, 64.0, 112.0):
         dra = rng.uniform(lo * 60, (lo + 4) * 60, n)
         sets.append((ra1, rng.uniform(-30, 30, n).astype(np.float32), ((ra1 + dra) % 21600).astype(np.float32),
                      rng.uniform(-30, 30, n).astype(np.float32)))
@@ -213,8 +213,8 @@ def _pair_sets(n, seed):
 @pytest.mark.parametrize("form", [0, 1])
 @pytest.mark.parametrize("w,nb", [(0.25, 720), (0.01, 18000), (0.35, 515)])
 def test_per_pair_bins_only_move_within_tolerance_of_an_edge(acf, ctx, w, nb, form):
-    # form 0: the chord form for every pair; form 1: the dot form wherever |u.v| < cos 45 deg (what
-    # a group between 45 and 135 degrees computes), the chord form elsewhere
+    # form 0: the full-range chord form for every pair; form 1: the form a tightly bounded group
+    # computes: the dot form wherever |u.v| < cos 45 deg, the short chord where |u.v| > cos 66 deg
     w_rad = math.radians(w)
     worst = 0.0
     ctx.set_option("pair_bins_form", form)
@@ -236,15 +236,15 @@ def test_per_pair_bins_only_move_within_tolerance_of_an_edge(acf, ctx, w, nb, fo
     print(f"w={w} form={form}: largest distance from the edge of a moved pair {worst:.3e} rad")
 
 
-@pytest.mark.parametrize("mid,exact", [(0, 1), (0, 0), (1, 2)])
-def test_auto_correlation_decomposes_into_parts(acf, ctx, mid, exact):
-    # DD(A u B) = DD(A) + DD(B) + 2 X(A, B) exactly. With the chord form alone (mid 0) the
-    # symmetric and the cross path bin every pair identically whatever its grouping; with the dot
-    # form a mid-range pair near an edge may bin differently in another grouping, unless exact
-    # mode 2 re-decides every near-edge pair in fp64.
+@pytest.mark.parametrize("forms,exact", [(0, 1), (0, 0), (1, 2)])
+def test_auto_correlation_decomposes_into_parts(acf, ctx, forms, exact):
+    # DD(A u B) = DD(A) + DD(B) + 2 X(A, B) exactly. With the full-range chord form alone
+    # (range_forms 0) the symmetric and the cross path bin every pair identically whatever its
+    # grouping; with the range forms a pair near an edge may bin differently in another grouping,
+    # unless exact mode 2 re-decides every near-edge pair in fp64.
     c = synth.catalogs(9000, 0, 20, 30.0, seed=8)
     a, b = slice(0, 4100), slice(4100, 9000)
-    ctx.set_option("mid", mid)
+    ctx.set_option("range_forms", forms)
     ctx.set_option("exact", exact)
     try:
         full = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)).astype(object)
@@ -254,7 +254,7 @@ def test_auto_correlation_decomposes_into_parts(acf, ctx, mid, exact):
                                         nbins=720)).astype(object)
         torch.cuda.synchronize()
     finally:
-        ctx.set_option("mid", 1)
+        ctx.set_option("range_forms", 1)
         ctx.set_option("exact", 1)
     assert list(full) == list(da + db + 2 * x)
 
@@ -327,7 +327,7 @@ def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
 
 
 PATH_KEYS = ("pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact", "pairs_masked",
-             "pairs_mid", "pairs_mid_exact")
+             "pairs_mid", "pairs_mid_exact", "pairs_small", "pairs_small_exact")
 
 
 def test_path_counters_cover_every_computed_pair(acf, ctx):
@@ -337,29 +337,33 @@ def test_path_counters_cover_every_computed_pair(acf, ctx):
     rows = -(-5000 // 128)
     # every unit computes its whole 128-wide i-set against the j-chunk's real length
     assert sum(got.values()) == rows * 128 * 4100, got
-    assert got["pairs_fixed"] > 0 and got["pairs_masked"] > 0 and got["pairs_mid"] > 0
+    assert got["pairs_masked"] > 0 and got["pairs_mid"] > 0 and got["pairs_small"] > 0
+    assert got["pairs_small_exact"] > 0  # groups near 0 and 180 degrees: short chord with flags
     assert got["pairs_mid_exact"] == 0  # exact mode 1 never sends a group to the dot form
 
 
 @pytest.mark.parametrize("w,nb,mid_expected", [(0.25, 720, True), (4.0, 45, False), (0.35, 515, False)])
-def test_dot_form_on_off_and_where_it_applies(acf, ctx, w, nb, mid_expected):
+def test_range_forms_on_off_and_where_they_apply(acf, ctx, w, nb, mid_expected):
     # the dot form needs the direct map with P = 180 / w even (0.25 deg: P = 720; 4 deg: P = 45 is
-    # odd; 0.35 deg: P is not an integer, clamp map). With it on or off the edge rule holds.
+    # odd; 0.35 deg: P is not an integer, clamp map); the short chord applies to every binning.
+    # With the range forms on or off the edge rule holds.
     c = synth.catalogs(6000, 5000, 12, 30.0, seed=18)
-    for mid in (1, 0):
-        ctx.set_option("mid", mid)
+    for forms in (1, 0):
+        ctx.set_option("range_forms", forms)
         try:
             _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
             got = {k: ctx.info(k) for k in PATH_KEYS}
         finally:
-            ctx.set_option("mid", 1)
-        assert (got["pairs_mid"] > 0) == (mid == 1 and mid_expected), got
+            ctx.set_option("range_forms", 1)
+        assert (got["pairs_mid"] > 0) == (forms == 1 and mid_expected), got
+        assert (got["pairs_small"] + got["pairs_small_exact"] > 0) == (forms == 1), got
     ctx.set_option("exact", 2)
     try:
         g, o, _ = _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
         assert np.array_equal(g, o.hist)
         if mid_expected:
             assert ctx.info("pairs_mid_exact") > 0 and ctx.info("pairs_mid") == 0
+        assert ctx.info("pairs_small_exact") > 0 and ctx.info("pairs_small") == 0
     finally:
         ctx.set_option("exact", 1)
 
