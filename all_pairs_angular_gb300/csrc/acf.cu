@@ -24,7 +24,7 @@ namespace {
 constexpr int kK = 4;                          // i-galaxies per thread (32 * kK == kJT)
 constexpr int kMaxEntries = 49152;             // histogram entries a block can hold (192 KB)
 constexpr size_t kWarpTileBytes = 2 * kJT * sizeof(float4);  // one warp's double-buffered j-tile
-constexpr size_t kMaxSmem = 232448;                             // opt-in dynamic shared memory per block
+constexpr size_t kMaxSmem = 232448 - 2048;  // dynamic shared memory per block: 227 KB less the pair kernel's static arrays
 constexpr int kMaxTimed = 4096;
 
 struct Plan {
@@ -56,10 +56,10 @@ struct acf_ctx {
   // options
   int opt_threads = 0, opt_ctas = 0, opt_method = kChordPoly, opt_layout = 0, opt_timing = 0;
   long long opt_units_per_launch = 0;
-  int opt_exact = 1;              // 0 off, 1 near 0 and 180 degrees, 2 everywhere
+  int opt_exact = 2;              // 0 off, 1 near 0 and 180 degrees, 2 everywhere
   double opt_exact_below_deg = 20.0;
   int opt_range_forms = 1;        // 1: cheaper forms where the caps bound the separations
-  int opt_pair_bins_form = 0;     // acf_pair_bins: 0 chord form, 1 dot form where |u.v| < cos 45 deg
+  int opt_pair_bins_form = 0;     // acf_pair_bins: 0 full-range chord form, 1 the range forms by own u.v
   unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
   long long last_qcap = 0;
   // info about the last histogram
@@ -147,7 +147,7 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     // the dot form needs 2^23 + P/2 to be an integer
     bp.mid = (c->opt_range_forms && std::fmod(pr, 2.0) == 0.0) ? 1 : 0;
     bp.magic_mid = (float)(8388608.0 + pr / 2.0);
-    for (int k = 0; k < 8; ++k) bp.rc[k] = (float)(kR[k] / w_rad);
+    for (int k = 0; k < kRTerms; ++k) bp.rc[k] = (float)(kR[k] / w_rad);
   } else {
     pl.map = kClamp;
     const double fp = std::floor(P * (1.0 + 1e-6)) + 1.0;  // indices the clamp-free range can reach
@@ -173,10 +173,12 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
     S = std::max(0, std::min(S, room));
     bp.fine_shift = S;
     bp.inv_w_f = (float)(std::ldexp(1.0, S) / w_rad);
+    // fine codes carry a bias of one fine unit (see BinParams)
+    bp.magic_f = 8388609.0f;
     if (pl.map == kDirect) {
-      bp.magic_far_f = (float)(8388608.0 + std::ldexp(pr, S));
-      bp.magic_mid_f = (float)(8388608.0 + std::ldexp(pr / 2.0, S));
-      for (int k = 0; k < 8; ++k) bp.rc_f[k] = (float)(std::ldexp(kR[k], S) / w_rad);
+      bp.magic_far_f = (float)(8388609.0 + std::ldexp(pr, S));
+      bp.magic_mid_f = (float)(8388609.0 + std::ldexp(pr / 2.0, S));
+      for (int k = 0; k < kRTerms; ++k) bp.rc_f[k] = (float)(std::ldexp(kR[k], S) / w_rad);
     }
     bp.clamp_f = (float)std::ldexp((double)bp.clamp_c + 0.5, S);
   }
@@ -243,14 +245,16 @@ struct CatBufs {
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
 };
 struct Scratch {
-  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue slots handed out, [2] moved pairs,
-                                       // [3] flagged pairs; bytes 64..135: pairs per path (u64)
+  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue slots handed out (this launch),
+                                       // [2] moved pairs, [3] flagged pairs, [4] queue overflow;
+                                       // bytes 64..135: pairs per path (u64)
   unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
   unsigned int* key1 = nullptr;        // sort: keys after the first pass
   unsigned int* idx1 = nullptr;        // sort: input indices after the first pass
   unsigned int* counts = nullptr;      // sort: digit counts per tile, then their offsets
   CatBufs a, b;                        // b only for cross-correlations
   unsigned long long* partial = nullptr;
+  unsigned long long* delta = nullptr; // exact mode: count moves of the fp64 re-decision, per bin
   double* T = nullptr;                 // exact mode: edge tables, nbins + 1 each
   double* U = nullptr;
   uint4* queue = nullptr;
@@ -287,6 +291,7 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   cat(n, r.a);
   if (!sym) cat(nj, r.b);
   r.partial = reinterpret_cast<unsigned long long*>(take((size_t)grid * (size_t)nbins * 8));
+  r.delta = reinterpret_cast<unsigned long long*>(take((size_t)nbins * 8));
   r.T = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
   r.U = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
   r.qcap = qcap;
@@ -359,6 +364,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   unsigned long long* partial = sc.partial;
   unsigned int* ticket = sc.counters;
   ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 256, c->stream));  // ticket, queue, path counters
+  if (pl.exact && sc.qcap > 0) ACF_CUDA(c, cudaMemsetAsync(sc.delta, 0, (size_t)pl.bp.nbins * 8, c->stream));
   PairParams p;
   p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
   p.exact_lo = pl.exact_lo;
@@ -366,13 +372,10 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   p.qtotal = sc.counters + 1;
   p.qflagged = sc.counters + 3;
   p.qcap = (unsigned int)std::min<long long>(sc.qcap, 0xFFFFFFFFll);
-  // each block reserves a batch (half the queue spread over the blocks of every launch); blocks that
-  // flag more append past their batch through the global counter
-  {
-    const long long nlaunch = (L.units + L.per_launch - 1) / std::max<long long>(L.per_launch, 1);
-    p.qbatch = (unsigned int)std::max<long long>(
-        16, sc.qcap / (2 * std::max<long long>(L.grid, 1) * std::max<long long>(nlaunch, 1)));
-  }
+  // each block reserves a batch (half the queue spread over the blocks of a launch; the queue is
+  // drained after every launch); blocks that flag more append past their batch through the
+  // global counter
+  p.qbatch = (unsigned int)std::max<long long>(16, sc.qcap / (2 * std::max<long long>(L.grid, 1)));
   p.path_pairs = reinterpret_cast<unsigned long long*>(sc.counters + 16);
   if (p.qcap == 0) p.exact_mode = 0;
   p.vi = ci.v;
@@ -394,7 +397,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     p.unit_begin = ub;
     p.unit_end = std::min(L.units, ub + L.per_launch);
     p.accumulate = ub > 0 ? 1 : 0;
-    if (ub > 0) ACF_CUDA(c, cudaMemsetAsync(ticket, 0, 4, c->stream));
+    if (ub > 0) ACF_CUDA(c, cudaMemsetAsync(ticket, 0, 8, c->stream));  // ticket and queue slots
     const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
     if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
     L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
@@ -402,6 +405,19 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     if (timed) {
       ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
       c->ev_used += 2;
+    }
+    if (p.exact_mode) {
+      // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
+      const int fblocks = c->num_sms * 8;
+      if (pl.map == kDirect)
+        fixup_kernel<kDirect><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
+                                                              sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,
+                                                              sc.counters + 4);
+      else
+        fixup_kernel<kClamp><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
+                                                             sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,
+                                                             sc.counters + 4);
+      ACF_LAUNCHED(c);
     }
   }
 #ifdef ACF_DEBUG_BOUNDS
@@ -421,21 +437,9 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   const unsigned long long self = sym ? (unsigned long long)ni : 0ull;
   const int mblocks = (pl.bp.nbins + 31) / 32;
   merge_kernel<<<mblocks, 32 * kMergeWarps, 0, c->stream>>>(partial, (int)L.grid, pl.bp.nbins, self,
+                                                             p.exact_mode ? sc.delta : nullptr,
                                                              reinterpret_cast<unsigned long long*>(out));
   ACF_LAUNCHED(c);
-  if (p.exact_mode) {
-    // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
-    const int fblocks = c->num_sms * 8;
-    if (pl.map == kDirect)
-      fixup_kernel<kDirect><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
-                                                            sc.U, pl.bp, p.inc,
-                                                            reinterpret_cast<unsigned long long*>(out), sc.counters + 2);
-    else
-      fixup_kernel<kClamp><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
-                                                           sc.U, pl.bp, p.inc,
-                                                           reinterpret_cast<unsigned long long*>(out), sc.counters + 2);
-    ACF_LAUNCHED(c);
-  }
   c->last_counters = sc.counters;
   c->last_qcap = p.exact_mode ? p.qcap : 0;
   c->info_grid = L.grid;
@@ -471,6 +475,7 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
 // Exact-mode queue slots for a histogram of `units` work units: every computed pair may be flagged
 // with probability ~2^(1-S); twice that, within bounds.
 long long queue_slots(const Plan& pl, long long units) {
+  // the queue is drained after every launch: it holds one launch's flagged pairs
   if (!pl.exact) return 0;
   const double pairs = (double)units * kJT * kJT;
   return (long long)std::min<double>(kQueueCapMax,
@@ -509,7 +514,9 @@ int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_
       (rc = plan_launch(c, pl, n_r, n_r, true, Lrr)))
     return rc;
   const long long grid = std::max(Ldd.grid, std::max(Ldr.grid, Lrr.grid));
-  const long long qcap = queue_slots(pl, std::max(Ldd.units, std::max(Ldr.units, Lrr.units)));
+  const long long qcap = queue_slots(pl, std::max(std::min(Ldd.units, Ldd.per_launch),
+                                                  std::max(std::min(Ldr.units, Ldr.per_launch),
+                                                           std::min(Lrr.units, Lrr.per_launch))));
   rc = ensure(c, c->ws, carve(nullptr, n_d, n_r, false, grid, nbins, qcap, nullptr));
   if (rc) return rc;
   Scratch sc;
@@ -549,7 +556,7 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const long long qcap = queue_slots(pl, L.units);
+  const long long qcap = queue_slots(pl, std::min(L.units, L.per_launch));
   rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, qcap, nullptr));
   if (rc) return rc;
   Scratch sc;
@@ -760,7 +767,7 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
     }
   if (!strcmp(key, "exact_flagged") || !strcmp(key, "exact_moved") || !strcmp(key, "exact_overflow")) {
     // synchronises the stream; counts of the last histogram call
-    unsigned int h[4] = {0, 0, 0, 0};
+    unsigned int h[5] = {0, 0, 0, 0, 0};
     if (c->last_counters && c->last_qcap > 0) {
       if (cudaSetDevice(c->device) != cudaSuccess || cudaStreamSynchronize(c->stream) != cudaSuccess ||
           cudaMemcpy(h, c->last_counters, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -768,7 +775,7 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
     }
     if (!strcmp(key, "exact_flagged")) *v = h[3];
     else if (!strcmp(key, "exact_moved")) *v = h[2];
-    else *v = h[1] > c->last_qcap ? (long long)h[1] - c->last_qcap : 0;  // slots requested past the end
+    else *v = h[4];  // slots requested past the end, over all launches
     return ACF_OK;
   }
   return ACF_ERR_ARG;

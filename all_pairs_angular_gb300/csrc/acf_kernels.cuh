@@ -10,12 +10,13 @@
 //   * catalogs are sorted along a Hilbert curve over cube-map cells, and each run of 32 sorted
 //     galaxies gets a cap (centre, radius); from two caps the kernel knows the range of separations
 //     of a (warp, j-group) block of pairs and picks the cheapest exact-enough form for it;
-//   * below 45 and above 135 degrees the separation is taken from the CHORD, not from arccos of the
+//   * below 55 and above 125 degrees the separation is taken from the CHORD, not from arccos of the
 //     dot product: with s = sign(u.v), q = |u - s v|^2 = 4 sin^2(theta'/2), theta' = theta
 //     (s = +1) or pi - theta (s = -1), theta' <= 90 deg; q keeps full relative precision at small
 //     and near-antipodal separations, where arccos of an fp32 dot product loses up to ~3e-4 rad.
-//     theta'^2 = q * P(q) with a degree-7 polynomial P, then one sqrt.approx;
-//   * between 45 and 135 degrees the dot product itself is precise enough: theta = pi/2 - d R(d^2)
+//     theta'^2 = q * P(q) with a polynomial P (degree 5 where theta' < 72 deg, else 7), then one
+//     sqrt.approx;
+//   * between 55 and 125 degrees the dot product itself is precise enough: theta = pi/2 - d R(d^2)
 //     with a degree-7 polynomial R and no square root (14 instead of 18 instructions per pair);
 //   * the bin index comes from exact float rounding (one fma rounded toward zero onto 2^23 + c)
 //     instead of acos, multiply and float-to-int conversion;
@@ -50,6 +51,10 @@ constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact
 // j-galaxies per step of the hot loops: their tile loads first, then every code, then every atomic
 // (the atomics' memory clobber would otherwise keep the next tile load behind them)
 constexpr int kJJBatch = ACF_JJ_BATCH;
+#ifndef ACF_JJ_BATCH_FINE
+#define ACF_JJ_BATCH_FINE 1
+#endif
+constexpr int kJJBatchFine = ACF_JJ_BATCH_FINE;  // the same for the exact-mode (flagging) loops
 #ifndef ACF_ASM_LOP3
 #define ACF_ASM_LOP3 1  // write the two sign-bit logic ops as explicit lop3 (2 ops, not 3)
 #endif  // j-loop unroll of the full-chunk path
@@ -66,19 +71,20 @@ __device__ constexpr float kP0 = 0.99999959294652097f, kP1 = 0.08334261162808559
                            kP5 = 0.00029099553526503564f, kP6 = -9.1427792701640403e-05f,
                            kP7 = 2.3068911858269848e-05f;
 
-// The same on theta' <= 66.4 degrees (q <= 1.2) with degree 5, for groups whose caps keep every
-// theta' below 66 degrees: absolute theta' error <= 1.3e-8 rad (1.7e-8 after fp32 rounding).
-__device__ constexpr float kS0 = 0.99999969522972076f, kS1 = 0.083340197828446816f, kS2 = 0.011067258098628368f,
-                           kS3 = 0.0019039784386728404f, kS4 = 0.00016731237856202599f,
-                           kS5 = 0.000144248943642142f;
-constexpr float kSmallRad = 1.1519173063162575f;  // 66 degrees
+// The same on theta' <= 72.4 degrees with degree 5, for groups whose caps keep every theta' below
+// 72 degrees: absolute theta' error <= 4.3e-8 rad (5.5e-8 after fp32 rounding).
+__device__ constexpr float kS0 = 0.99999908438480867f, kS1 = 0.083350941003199425f, kS2 = 0.011015189062680493f,
+                           kS3 = 0.0020057633993448608f, kS4 = 8.1054448294636845e-05f,
+                           kS5 = 0.00017064219833417058f;
+constexpr float kSmallRad = 1.2566370614359172f;  // 72 degrees
 
-// Between 45 and 135 degrees the dot product d = u.v loses nothing: theta = pi/2 - asin(d) with
-// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(43 deg), degree 7: absolute
-// theta error <= 1.4e-8 rad (2.8e-8 after fp32 rounding). Scaled by 1/w on the host.
-constexpr double kR[8] = {0.9999996836724383,  0.16669323778385681, 0.074351930865433416, 0.051668908380561249,
-                          -0.0092763923538493106, 0.14513595031397153, -0.18466868067833839, 0.16096802275189068};
-constexpr float kMidRad = 0.78539816339744831f;  // groups whose separations all lie in (45, 135) degrees use the dot form
+// Between 55 and 125 degrees the dot product d = u.v loses little: theta = pi/2 - asin(d) with
+// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(53 deg), degree 5: absolute
+// theta error <= 2.1e-8 rad (3.3e-8 after fp32 rounding). Scaled by 1/w on the host.
+constexpr int kRTerms = 6;
+constexpr double kR[kRTerms] = {0.99999956256812916,  0.16669876877905515,   0.07433148849621074,
+                                0.050509827344902551, 0.0062717738364129879, 0.065395572657082512};
+constexpr float kMidRad = 0.95993108859688125f;  // groups whose separations all lie in (55, 125) degrees use the dot form
 
 // Every code is the float 2^23 + (histogram entry), entry = floor(theta / w) (direct map, where
 // P = pi / w is an integer) or the clamped index (clamp map); the merge clamps entries to nbins - 1.
@@ -86,13 +92,16 @@ struct BinParams {
   float magic_far;    // direct: 2^23 + P, the far-side (theta > 90 deg) constant of the chord form
   float magic_mid;    // direct, P even: 2^23 + P/2, the constant of the dot form
   float inv_w_f;      // exact mode: 2^S / w (fine code with S fractional bits)
-  float magic_far_f;  // exact mode: 2^23 + P 2^S
-  float magic_mid_f;  // exact mode: 2^23 + (P/2) 2^S
+  // The fine code is biased by one fine unit (every fine constant carries + 1), so a pair lies
+  // within one fine unit of an edge exactly when its low S bits are 0 or 1.
+  float magic_f;      // exact mode: 2^23 + 1
+  float magic_far_f;  // exact mode: 2^23 + P 2^S + 1
+  float magic_mid_f;  // exact mode: 2^23 + (P/2) 2^S + 1
   float clamp_f;      // exact mode: (clamp_c + 0.5) * 2^S (clamp map)
-  float rc[8];        // dot form: kR[k] / w
-  float rc_f[8];      // exact mode: kR[k] 2^S / w
-  int mid;            // 1: groups between 45 and 135 degrees use the dot form
-  int small;          // 1: groups whose theta' stays below 66 degrees use the degree-5 chord polynomial
+  float rc[kRTerms];   // dot form: kR[k] / w
+  float rc_f[kRTerms]; // exact mode: kR[k] 2^S / w
+  int mid;            // 1: groups between 55 and 125 degrees use the dot form
+  int small;          // 1: groups whose theta' stays below 72 degrees use the degree-5 chord polynomial
   int fine_shift;     // exact mode: S
   int kmax;           // exact mode: highest bin a separation <= 180 degrees can reach
   unsigned int zone0, span0, zone1, span1;  // exact mode: entries e with e - zone <= span (unsigned) are re-decided
@@ -225,8 +234,8 @@ __device__ __forceinline__ float4 radec_to_unit(float ra_arcmin, float dec_arcmi
 // (6 faces x 64 x 64 cells, Hilbert order within a face). A warp's i-galaxies and a j-chunk then
 // each cover a small patch of sky, bounded by a "cap" (centre, angular radius). From two caps
 // the kernel knows when every pair of a (warp, chunk) is surely below or surely above 90
-// degrees, and drops the per-pair sign decision there, and when every pair lies between 45 and
-// 135 degrees, where it uses the dot form. The chord loops compute every pair's code with the same
+// degrees, and drops the per-pair sign decision there, and when every pair lies between 55 and
+// 125 degrees, where it uses the dot form. The chord loops compute every pair's code with the same
 // arithmetic whichever of them evaluates it; the dot form computes a different (equally valid)
 // approximation, so a mid-range pair within ~4e-7 rad of an edge may bin by its grouping.
 
@@ -523,7 +532,7 @@ __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float x
       // far side: the same fma of -theta' onto 2^23 + P gives P - ceil(theta'/w), which is exactly
       // floor((pi - theta')/w) = floor(theta/w) when P = pi/w is an integer.
       // theta' carrying the sign of d: th | (d & signmask), one logic op
-      const float m = (int)db < 0 ? (FINE ? bp.magic_far_f : bp.magic_far) : kMagic;
+      const float m = (int)db < 0 ? (FINE ? bp.magic_far_f : bp.magic_far) : (FINE ? bp.magic_f : kMagic);
 #if ACF_ASM_LOP3
       return fma_rz(__uint_as_float(lop3<0xF8>(__float_as_uint(th), db, 0x80000000u)), FINE ? bp.inv_w_f : bp.inv_w, m);
 #else
@@ -532,7 +541,7 @@ __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float x
     } else {
       const float h = fmaf(ns, 1.57079632679489662f, 1.57079632679489662f);  // 0 or pi
       const float tr = fmaf(-ns, th, h);                                       // theta
-      return FINE ? add_rz(fminf(tr * bp.inv_w_f, bp.clamp_f), kMagic) : add_rz(fminf(tr * bp.inv_w, bp.clamp_c), kMagic);
+      return FINE ? add_rz(fminf(tr * bp.inv_w_f, bp.clamp_f), bp.magic_f) : add_rz(fminf(tr * bp.inv_w, bp.clamp_c), kMagic);
     }
   }
 }
@@ -551,7 +560,7 @@ __device__ __forceinline__ int entry_to_bin(int e, const BinParams& bp) {
 // bit the general code takes these steps for such a pair: fma(ns, v, u) is the same difference or
 // sum, and the far-side code fma_rz(-theta', 1/w, m) is fma_rz(theta', -1/w, m). Only the dot
 // product, the sign-bit operation and the choice of constant are dropped.
-// SMALL: the degree-5 polynomial, for groups whose caps keep every theta' below 66 degrees.
+// SMALL: the degree-5 polynomial, for groups whose caps keep every theta' below 72 degrees.
 template <int MAP, bool FINE = false, bool SMALL = false>
 __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, float xj, float yj, float zj, float ns,
                                                  float iws, float h, const BinParams& bp) {
@@ -581,24 +590,22 @@ __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, f
   } else {
     // theta / w = th * iws + h with h = 0 (near side) or pi / w (far side); iws = -1/w there
     const float t = fmaf(th, iws, h);
-    return add_rz(fminf(t, FINE ? bp.clamp_f : bp.clamp_c), kMagic);
+    return add_rz(fminf(t, FINE ? bp.clamp_f : bp.clamp_c), FINE ? bp.magic_f : kMagic);
   }
 }
 
-// The dot form, for pairs whose caps put theta in (45, 135) degrees (direct map, P even):
+// The dot form, for pairs whose caps put theta in (55, 125) degrees (direct map, P even):
 // theta / w = P/2 - d R(d^2) / w, floored exactly by one fma rounded toward zero onto 2^23 + P/2
 // (the product of the two fp32 operands enters unrounded). Worst-case theta error: d carries
-// <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 3.1e-7 rad where sin theta >=
-// sin 43 deg, plus <= 1e-7 from the polynomial and its rounding.
+// <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 2.7e-7 rad where sin theta >=
+// sin 53 deg, plus <= 1e-7 from the polynomial and its rounding.
 template <bool FINE = false>
 __device__ __forceinline__ float pair_code_mid(float xi, float yi, float zi, float xj, float yj, float zj,
                                                const BinParams& bp) {
 #define ACF_RC(k) (FINE ? bp.rc_f[k] : bp.rc[k])
   const float d = fmaf(zi, zj, fmaf(yi, yj, xi * xj));
   const float t = d * d;
-  float p = fmaf(ACF_RC(7), t, ACF_RC(6));
-  p = fmaf(p, t, ACF_RC(5));
-  p = fmaf(p, t, ACF_RC(4));
+  float p = fmaf(ACF_RC(5), t, ACF_RC(4));
   p = fmaf(p, t, ACF_RC(3));
   p = fmaf(p, t, ACF_RC(2));
   p = fmaf(p, t, ACF_RC(1));
@@ -645,10 +652,10 @@ struct PathTag {
 // iff cos tc < -sin(ra + rb). __sinf/__cosf are accurate to ~1e-6 here and the margins cover it.
 // kExactBit is added when the exact mode must check this group: mode 2 always, mode 1 when some
 // separation may be below lo or above pi - lo (cos tc > cos(lo + r) or < -cos(lo + r)).
-// kMidBit is added when every separation lies in (45, 135) degrees (|cos tc| < cos(45 deg + r))
+// kMidBit is added when every separation lies in (55, 125) degrees (|cos tc| < cos(55 deg + r))
 // and the dot form is on; in mode 1 never for a group the exact mode checks, so every pair the
 // exact mode may re-decide is binned by a chord form. Otherwise kSmallBit is added when every
-// theta' lies below 66 degrees on one side of 90 (|cos tc| > cos(66 deg - r)).
+// theta' lies below 72 degrees on one side of 90 (|cos tc| > cos(72 deg - r)).
 constexpr int kExactBit = 4;
 constexpr int kMidBit = 8;
 constexpr int kSmallBit = 16;
@@ -689,8 +696,9 @@ struct FormTag {
 };
 
 // Add one pair to the shared histogram. With F (exact mode) the code carries fine_shift extra
-// fractional bits: the entry is the code's integer part. Returns whether the pair lies within one
-// fine unit of an edge (fraction 0 or all ones); such pairs go to push_flagged.
+// fractional bits, biased by one unit: the entry is the code's integer part. Returns whether the
+// pair lies within one fine unit of an edge (biased fraction 0 or 1); such pairs go to push_flagged.
+// A pair at one fine unit below an edge is counted one entry up; the fp64 re-decision moves it.
 template <bool F>
 __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint32_t base, uint32_t base_f, int shift,
                                          uint32_t magic_bits, int i, int j, float xi, float yi, float zi, float4 v) {
@@ -704,20 +712,32 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
     if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i,
                   __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
       red_shared_add(((cb >> S) << shift) + base_f, p.inc);
-    return ((cb + 1u) & ((1u << S) - 1u)) <= 1u;
+    return (cb & ((1u << S) - 1u)) <= 1u;
   }
 }
 
 // Queue a near-edge pair for the fp64 re-decision if its entry lies in the exact zone (a function
 // of the pair's own code, so the set of re-decided pairs does not depend on grouping or order).
+// A pair that is not queued (outside the zone, or the queue is full) keeps its fp32 bin: if the
+// one-unit bias carried it into the next entry (biased fraction 0), its count moves back.
 __device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, uint32_t magic_bits, int i, int j,
-                                             unsigned int* s_qcount) {
-  const uint32_t e = (cb - magic_bits) >> p.bp.fine_shift;
+                                             unsigned int* s_qcount, uint32_t base_f, int shift) {
+  const int S = p.bp.fine_shift;
+  const uint32_t e = (cb - magic_bits) >> S;
+  bool queued = false;
   if (e - p.bp.zone0 <= p.bp.span0 || e - p.bp.zone1 <= p.bp.span1) {
     // a slot of this block's reserved batch (shared-memory counter), or past it a global one
     const unsigned int local = atomicAdd(s_qcount, 1u);
     const unsigned int slot = local < p.qbatch ? s_qcount[1] + local : atomicAdd(p.qtotal, 1u);
-    if (slot < p.qcap) p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
+    if (slot < p.qcap) {
+      p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
+      queued = true;
+    }
+  }
+  if (!queued && (cb & ((1u << S) - 1u)) == 0u) {
+    const uint32_t a = ((cb >> S) << shift) + base_f;
+    red_shared_add(a, 0u - p.inc);
+    red_shared_add(a - (1u << shift), p.inc);
   }
 }
 
@@ -780,6 +800,10 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + WARPS * 2 * kJT * sizeof(float4));
 
   __shared__ unsigned int s_qcount[2];  // exact mode: [0] flags of this block, [1] first slot of its batch
+  // per warp: j-groups run on each path (see path_pairs), and the cap of the warp's current i-set
+  // (kept here, not in registers, to leave the hot loops all the registers)
+  __shared__ unsigned int s_paths[WARPS][9];
+  __shared__ float4 s_icap[WARPS];
   const int words = (LAYOUT == kLane) ? p.bp.entries * 32 : p.bp.entries;
   for (int w = tid; w < words; w += THREADS) hist[w] = 0;
   unsigned long long* row = p.partial + (size_t)blockIdx.x * p.bp.nbins;
@@ -826,13 +850,15 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     unit_coords(p, u, r, c);
     load_tile(c, 0);
     float xi[K], yi[K], zi[K];
-    float4 icap = make_float4(1.f, 0.f, 0.f, 4.f);
+    if (lane < 9) s_paths[warp][lane] = 0u;
     int cur_r = -1, buf = 0;
     // j-groups per path (x 32*kJT pairs): chord fixed, chord general, the same with flags, dot form,
     // dot form with flags
-    unsigned int g_fixed = 0, g_general = 0, g_fixed_f = 0, g_general_f = 0, g_mid = 0, g_mid_f = 0, g_small = 0,
-                 g_small_f = 0;
-    unsigned long long edge_pairs = 0ull;
+    // path slots: 0 chord fixed, 1 chord general, 2 and 3 the same with flags, 4 masked units (in
+    // units of kJT pairs), 5 dot form, 6 dot form with flags, 7 short chord, 8 short chord with flags
+    auto count_path = [&](int slot, unsigned int n) {
+      if (lane == 0) s_paths[warp][slot] += n;
+    };
     while (true) {
       int rn = 0, cn = 0;
       if (un < p.unit_end) {
@@ -855,7 +881,11 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           zi[k] = v.z;
           (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 4, i, r, v.x, v.y, v.z);
         }
-        if (METHOD == kChordPoly) icap = union_caps<K>(p.icap32, (long long)i0 / 32, p.igroups);
+        if (METHOD == kChordPoly) {
+          const float4 icap = union_caps<K>(p.icap32, (long long)i0 / 32, p.igroups);
+          if (lane == 0) s_icap[warp] = icap;
+          __syncwarp();
+        }
         cur_r = r;
       }
       cp_async_wait<1>();
@@ -881,7 +911,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                                                     // 3 short chord (fixed sign)
           constexpr bool F = decltype(fine)::value;
           // the general and the full-range fixed chord loops are rare once the caps pick the dot form
-          // across 90 degrees and the short chord below 66: rolled
+          // across 90 degrees and the short chord below 72: rolled
           constexpr int U = (F || X == 0 || X == 1) ? kJJUnrollFine : kJJUnroll;
           auto code_of = [&](int k, float4 v) -> uint32_t {
             return __float_as_uint(
@@ -890,51 +920,69 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                 : X == 1 ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h, p.bp)
                          : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
           };
-          if constexpr (!F && U > 1 && kJJBatch > 1) {
-            constexpr int B = kJJBatch;
+          constexpr int B = F ? kJJBatchFine : kJJBatch;
+          if constexpr ((F || U > 1) && B > 1) {
+            const uint32_t fmask = (1u << p.bp.fine_shift) - 1u;
 #pragma unroll 1
             for (int jj = jbeg; jj < jbeg + 32; jj += B) {
               float4 vv[B];
 #pragma unroll
               for (int u = 0; u < B; ++u) vv[u] = tile[jj + u];
-              uint32_t cb[B][K];
+              uint32_t cb[B * K];
 #pragma unroll
               for (int u = 0; u < B; ++u)
 #pragma unroll
-                for (int k = 0; k < K; ++k) cb[u][k] = code_of(k, vv[u]);
+                for (int k = 0; k < K; ++k) cb[u * K + k] = code_of(k, vv[u]);
+              uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of the batch
 #pragma unroll
               for (int u = 0; u < B; ++u)
 #pragma unroll
-                for (int k = 0; k < K; ++k)
-                  add_pair<false>(p, cb[u][k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj + u, xi[k],
-                                  yi[k], zi[k], vv[u]);
+                for (int k = 0; k < K; ++k) {
+                  add_pair<F>(p, cb[u * K + k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
+                              xi[k], yi[k], zi[k], vv[u]);
+                  if (F) low = min(low, cb[u * K + k] & fmask);
+                }
+              // near-edge pairs are rare: one warp vote per batch; the lanes that hold one walk
+              // their batch once (the code picked by a select chain keeps the array in registers)
+              if (F && __any_sync(0xffffffffu, low <= 1u)) {
+#pragma unroll 1
+                for (int t = 0; t < B * K; ++t) {
+                  uint32_t c = cb[0];
+#pragma unroll
+                  for (int q = 1; q < B * K; ++q) c = (t == q) ? cb[q] : c;
+                  if ((c & fmask) <= 1u) push_flagged(p, c, magic_bits, i0 + (t % K) * 32 + lane, j0 + jj + t / K, s_qcount,
+                                                        base_f, SHIFT);
+                }
+              }
             }
             return;
           }
+          const uint32_t fmask = (1u << p.bp.fine_shift) - 1u;
 #pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
             const float4 v = tile[jj];
             uint32_t cbs[K];
-            unsigned int near = 0u;
+            uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               cbs[k] = code_of(k, v);
-              if (add_pair<F>(p, cbs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
-                              yi[k], zi[k], v))
-                near |= 1u << k;
+              add_pair<F>(p, cbs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
+                          v);
+              if (F) low = min(low, cbs[k] & fmask);
             }
             // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
-            if (F && __any_sync(0xffffffffu, near != 0u)) {
+            if (F && __any_sync(0xffffffffu, low <= 1u)) {
 #pragma unroll
               for (int k = 0; k < K; ++k)
-                if (near & (1u << k)) push_flagged(p, cbs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
+                if ((cbs[k] & fmask) <= 1u)
+                  push_flagged(p, cbs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
             }
           }
         };
         // the four j-groups' paths, one per lane of lanes 0..3 (one pass of the decision per unit)
         int pc_lane = kGeneral;
         if (METHOD == kChordPoly && lane < kJT / 32)
-          pc_lane = choose_path(icap, __ldg(p.jcap32 + c * (kJT / 32) + lane), p.exact_mode, p.exact_lo,
+          pc_lane = choose_path(s_icap[warp], __ldg(p.jcap32 + c * (kJT / 32) + lane), p.exact_mode, p.exact_lo,
                                 MAP == kDirect ? p.bp.mid : 0, p.bp.small);
 #pragma unroll 1
         for (int g = 0; g < kJT / 32; ++g) {
@@ -942,7 +990,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const int path = pc & 3;
           const bool fine = (pc & kExactBit) != 0;
           if (pc & kMidBit) {
-            (fine ? g_mid_f : g_mid) += 1;
+            count_path(fine ? 6 : 5, 1u);
             if (fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f);
             else run(FormTag<2>(), FineTag<false>(), g * 32, 0.f, 0.f, 0.f);
             continue;
@@ -951,16 +999,16 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const float ns = (path == kBelow90) ? -1.0f : 1.0f;
           const float iws = (path == kBelow90) ? iw : -iw;
           float h;
-          if (MAP == kDirect) h = (path == kBelow90) ? kMagic : (fine ? p.bp.magic_far_f : p.bp.magic_far);
+          if (MAP == kDirect)
+            h = (path == kBelow90) ? (fine ? p.bp.magic_f : kMagic) : (fine ? p.bp.magic_far_f : p.bp.magic_far);
           else h = (path == kBelow90) ? 0.0f : 3.14159265358979323846f * iw;
           if (pc & kSmallBit) {
-            (fine ? g_small_f : g_small) += 1;
+            count_path(fine ? 8 : 7, 1u);
             if (fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h);
             else run(FormTag<3>(), FineTag<false>(), g * 32, ns, iws, h);
             continue;
           }
-          if (path == kGeneral) (fine ? g_general_f : g_general) += 1;
-          else (fine ? g_fixed_f : g_fixed) += 1;
+          count_path(path == kGeneral ? (fine ? 3 : 1) : (fine ? 2 : 0), 1u);
           if (path == kGeneral) {
             if (fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h);
             else run(FormTag<0>(), FineTag<false>(), g * 32, ns, iws, h);
@@ -989,13 +1037,13 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
               if (jj > thr[k] &&
                   add_pair<F>(p, cb, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k], v))
-                push_flagged(p, cb, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
+                push_flagged(p, cb, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
             }
           }
         };
         if (p.exact_mode && METHOD == kChordPoly) edge(FineTag<true>());
         else edge(FineTag<false>());
-        edge_pairs += (unsigned long long)jn * kJT;
+        count_path(4, (unsigned int)jn);
       }
       __syncwarp();  // every lane is done with this buffer before the next prefetch refills it
       if (un >= p.unit_end) break;
@@ -1008,15 +1056,11 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     cp_async_wait<0>();
     if (lane == 0) {
       constexpr unsigned long long G = 32 * kJT;
-      if (g_fixed) atomicAdd(p.path_pairs + 0, g_fixed * G);
-      if (g_general) atomicAdd(p.path_pairs + 1, g_general * G);
-      if (g_fixed_f) atomicAdd(p.path_pairs + 2, g_fixed_f * G);
-      if (g_general_f) atomicAdd(p.path_pairs + 3, g_general_f * G);
-      if (edge_pairs) atomicAdd(p.path_pairs + 4, edge_pairs);
-      if (g_mid) atomicAdd(p.path_pairs + 5, g_mid * G);
-      if (g_mid_f) atomicAdd(p.path_pairs + 6, g_mid_f * G);
-      if (g_small) atomicAdd(p.path_pairs + 7, g_small * G);
-      if (g_small_f) atomicAdd(p.path_pairs + 8, g_small_f * G);
+#pragma unroll 1
+      for (int k = 0; k < 9; ++k) {
+        const unsigned long long n = (unsigned long long)s_paths[warp][k] * (k == 4 ? (unsigned long long)kJT : G);
+        if (n) atomicAdd(p.path_pairs + k, n);
+      }
     }
   }
   __syncthreads();
@@ -1039,6 +1083,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const unsigned long long* __restrict__ partial,
                                                                 int rows, int nbins, unsigned long long self_pairs,
+                                                                const unsigned long long* __restrict__ delta,
                                                                 unsigned long long* __restrict__ out) {
   __shared__ unsigned long long acc[kMergeWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1052,6 +1097,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const unsigned 
   __syncthreads();
   if (warp == 0 && k < nbins) {
     unsigned long long t = (k == 0) ? self_pairs : 0ull;
+    if (delta) t += delta[k];  // exact mode: counts moved by the fp64 re-decision (two's complement)
 #pragma unroll
     for (int w = 0; w < kMergeWarps; ++w) t += acc[w][lane];
     out[k] = t;
@@ -1084,14 +1130,18 @@ __global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ 
   }
 }
 
-// Re-decide every queued pair in fp64 from the fp64 unit vectors and move its count if the fast
-// code put it in a neighbouring bin. Runs after the merge, on the final histogram.
+// Re-decide every queued pair in fp64 from the fp64 unit vectors and record the move of its count
+// in delta[] if the fast code put it in a neighbouring bin. Runs after every pair-kernel launch
+// (the queue then starts empty again); the merge adds delta to the counts. Slots requested past
+// the queue's end are added to *overflow (those pairs kept their fp32 bin).
 template <int MAP>
 __global__ void fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qtotal,
                              unsigned int qcap, const double4* __restrict__ vi, const double4* __restrict__ vj,
                              const double* __restrict__ T, const double* __restrict__ U, BinParams bp,
-                             unsigned int inc, unsigned long long* __restrict__ out, unsigned int* __restrict__ moved) {
+                             unsigned int inc, unsigned long long* __restrict__ delta, unsigned int* __restrict__ moved,
+                             unsigned int* __restrict__ overflow) {
   const unsigned int nq = min(*qtotal, qcap);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && *qtotal > qcap) atomicAdd(overflow, *qtotal - qcap);
   const uint32_t magic_bits = __float_as_uint(kMagic);
   for (unsigned int s = blockIdx.x * blockDim.x + threadIdx.x; s < nq; s += gridDim.x * blockDim.x) {
     const uint4 rec = queue[s];
@@ -1115,15 +1165,15 @@ __global__ void fixup_kernel(const uint4* __restrict__ queue, const unsigned int
       while (k < bp.kmax && q <= U[k + 1]) ++k;
     }
     if (k != kf) {
-      atomicAdd(out + kf, (unsigned long long)(-(long long)inc));
-      atomicAdd(out + k, (unsigned long long)inc);
+      atomicAdd(delta + kf, (unsigned long long)(-(long long)inc));
+      atomicAdd(delta + k, (unsigned long long)inc);
       atomicAdd(moved, 1u);
     }
   }
 }
 
-// form 1: what a group the caps bound tightly computes: pairs with |u.v| < cos(45 deg) take the
-// dot form, pairs with |u.v| > cos(66 deg) the short chord, the others the full-range chord form;
+// form 1: what a group the caps bound tightly computes: pairs with |u.v| < cos(55 deg) take the
+// dot form, pairs with |u.v| > cos(72 deg) the short chord, the others the full-range chord form;
 // form 0: the full-range chord form for every pair.
 template <int MAP, int METHOD>
 __global__ void pair_bins_kernel(const float* __restrict__ ra1, const float* __restrict__ dec1,
@@ -1134,8 +1184,8 @@ __global__ void pair_bins_kernel(const float* __restrict__ ra1, const float* __r
     const float4 u = radec_to_unit(ra1[i], dec1[i]);
     const float4 v = radec_to_unit(ra2[i], dec2[i]);
     const float d = fmaf(u.z, v.z, fmaf(u.y, v.y, u.x * v.x));
-    const bool mid = form == 1 && MAP == kDirect && METHOD == kChordPoly && bp.mid && fabsf(d) < 0.70710678f;
-    const bool small = form == 1 && METHOD == kChordPoly && bp.small && fabsf(d) > 0.40673664f;  // cos 66 deg
+    const bool mid = form == 1 && MAP == kDirect && METHOD == kChordPoly && bp.mid && fabsf(d) < 0.57357644f;
+    const bool small = form == 1 && METHOD == kChordPoly && bp.small && fabsf(d) > 0.30901699f;  // cos 72 deg
     float code;
     if (mid) {
       code = pair_code_mid<false>(u.x, u.y, u.z, v.x, v.y, v.z, bp);

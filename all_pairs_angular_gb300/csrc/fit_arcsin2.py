@@ -8,7 +8,7 @@ f evaluated in 40-digit arithmetic. Prints the coefficients (highest degree last
 theta' error before and after rounding them to fp32.
 
 The kernel uses two fits: degree 7 on theta' <= 90 degrees (any chord), and degree 5 on
-theta' <= 66.4 degrees (q <= 1.2, for groups whose caps keep every theta' below 66 degrees).
+theta' <= 72.4 degrees (for groups whose caps keep every theta' below 72 degrees).
 
 Run: python fit_arcsin2.py [degree [theta_max_deg]]   (defaults: 7 90)
 """

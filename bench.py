@@ -35,13 +35,14 @@ UNIT = "Gpairs/s"
 # Thread instructions per pair of each pair-kernel path: the general chord + polynomial loop is 25
 # (dot product, sign, chord, polynomial, sqrt, sign-dependent constant, rounding fma, address,
 # shared atomic); where the caps fix the sign of the dot product the dot, the sign operation and the
-# constant choice drop out (18); where every theta' stays below 66 degrees the polynomial is of
-# degree 5 instead of 7 (16); the dot form for groups between 45 and 135 degrees is 14 (dot, square,
-# 7-term polynomial, rounding fma, address, atomic); the exact-mode flag adds 5 (fine-code address,
-# edge test, branch).
-INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 23, "pairs_general_exact": 30,
-                 "pairs_mid": 14, "pairs_mid_exact": 19, "pairs_small": 16, "pairs_small_exact": 21}
+# constant choice drop out (18); where every theta' stays below 72 degrees the polynomial is of
+# degree 5 instead of 7 (16); the dot form for groups between 55 and 125 degrees is 12 (dot, square,
+# 5-term polynomial, rounding fma, address, atomic); the exact-mode flag adds 3 (fine-code shift,
+# fraction mask, running minimum of the batch).
+INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 21, "pairs_general_exact": 28,
+                 "pairs_mid": 12, "pairs_mid_exact": 15, "pairs_small": 16, "pairs_small_exact": 19}
 INST_MASKED = 25  # diagonal / ragged units run the general loop on every computed pair
+INST_MASKED_EXACT = 4  # and with flags: fine-code shift, fraction mask, test, branch per pair
 SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
 # The pages' kernel time for three 100k histograms on an RTX 5080 (another machine: context only)
 PAGE_KERNEL_MS = 22.747
@@ -265,7 +266,7 @@ def run_ours(args, cat, workload, rank, world, local):
             masked = ctx.info("pairs_masked")
             exact_on = sum(ctx.info(k) for k in ("pairs_fixed_exact", "pairs_general_exact", "pairs_small_exact",
                                                  "pairs_mid_exact")) > 0
-            alg_inst += (INST_MASKED + (5 if exact_on else 0)) * masked
+            alg_inst += (INST_MASKED + (INST_MASKED_EXACT if exact_on else 0)) * masked
             alg_pairs += masked
     path_mix = {k: ctx.info(k) for k in INST_PER_PATH}
     total_ms = sum(step_ms)

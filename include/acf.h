@@ -16,9 +16,9 @@
  * Precision contract: the kernels work in fp32 on unit vectors built in fp64. The computed
  * separation of every pair is within 1e-6 rad of the fp64 value of the formula above, so a pair
  * can land in a neighbouring bin only if its fp64 theta lies within 1e-6 rad of that bin edge.
- * In "exact" mode (option below; on by default for separations within 20 degrees of 0 and 180)
- * pairs whose fp32 separation falls that close to an edge are re-decided in fp64 from the same
- * unit vectors, so there the bin is the one the fp64 formula gives (up to ~1e-15 relative).
+ * In "exact" mode (option below; on by default, mode 2) pairs whose fp32 separation falls that
+ * close to an edge are re-decided in fp64 from the same unit vectors, so every bin is the one the
+ * fp64 formula gives (up to ~1e-15 relative): the histograms equal those of the fp64 definition.
  *
  * Conventions for every entry point:
  *   - Array arguments marked "device" are caller-owned CUDA device pointers on the context's
@@ -170,14 +170,14 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram
  *   "exact"          0 = fp32 bins only (precision contract above);
  *                    1 = re-decide in fp64 the pairs within ~1e-6 rad of an edge whose separation is
- *                        below "exact_below_deg" or above 180 minus it (default);
+ *                        below "exact_below_deg" or above 180 minus it;
  *                    2 = re-decide such pairs at every separation: the histograms then equal those
- *                        of the fp64 formula
+ *                        of the fp64 formula (default)
  *   "exact_below_deg"  the window of mode 1, whole degrees 0..180 (default 20)
  *   "range_forms"    1 = where the caps of a block of pairs bound its separations, use a cheaper
  *                        form that meets the same precision contract: the dot product with an
- *                        asin polynomial between 45 and 135 degrees (needs 180/w an even integer),
- *                        a degree-5 chord polynomial where theta' stays below 66 degrees (default);
+ *                        asin polynomial between 55 and 125 degrees (needs 180/w an even integer),
+ *                        a degree-5 chord polynomial where theta' stays below 72 degrees (default);
  *                    0 = the full-range chord form for every pair (every pair then gets the same
  *                        code whichever block computes it, so DD of a union splits exactly)
  *   "pair_bins_form" acf_pair_bins: 0 = full-range chord form (default); 1 = the form a tightly
@@ -198,7 +198,7 @@ int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
  *   "pairs_fixed", "pairs_general"  pairs evaluated on the fixed-sign and general loops
  *   "pairs_fixed_exact", "pairs_general_exact"  the same loops with edge flagging (exact mode)
  *   "pairs_masked"                  pairs of diagonal or ragged units (one compare per pair more)
- *   "pairs_mid", "pairs_mid_exact"  the dot form (45..135 degrees), without and with flagging
+ *   "pairs_mid", "pairs_mid_exact"  the dot form (55..125 degrees), without and with flagging
  *   "pairs_small", "pairs_small_exact"  the degree-5 chord form, without and with flagging
  *   "exact_flagged"  pairs flagged for re-decision;  "exact_moved"  of those, pairs moved a bin;
  *   "exact_overflow"  flagged pairs that did not fit in the queue (kept their fp32 bin)

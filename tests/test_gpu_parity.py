@@ -19,6 +19,7 @@ from oracle import check
 pytestmark = pytest.mark.gpu
 
 TOL = oracle.EDGE_TOL_RAD
+DEFAULT_EXACT = 2
 
 
 @pytest.fixture(scope="module")
@@ -184,8 +185,8 @@ def test_correlate_equals_separate_histograms(acf, ctx):
 
 def _pair_sets(n, seed):
     """Random pairs over the whole sphere, tight pairs (< 1 deg), near-antipodal pairs, pairs near
-    90 degrees, where the kernel switches between the difference and the sum chord, pairs near 45
-    and 135 degrees, the edges of the dot form's range, and near 66 and 114, the short chord's."""
+    90 degrees, where the kernel switches between the difference and the sum chord, pairs near 55
+    and 125 degrees, the edges of the dot form's range, and near 72 and 108, the short chord's."""
     rng = np.random.default_rng(seed)
     ra1, dec1 = synth.uniform_sphere(n, seed)
     ra2, dec2 = synth.uniform_sphere(n, seed + 1)
@@ -202,8 +203,8 @@ def _pair_sets(n, seed):
                  rng.uniform(-30, 30, n).astype(np.float32)))
     sets.append((ra1, np.zeros(n, np.float32), ((ra1 + 5400 + rng.uniform(-30, 30, n)) % 21600).astype(np.float32),
                  rng.uniform(-30, 30, n).astype(np.float32)))
-    # near 45 and 135 degrees, where groups switch between the chord form and the dot form
-    for lo in (43.0, 133.0, 64.0, 112.0):
+    # near the edges of the dot form (55, 125 degrees) and of the short chord (72, 108 degrees)
+    for lo in (53.0, 123.0, 70.0, 106.0):
         dra = rng.uniform(lo * 60, (lo + 4) * 60, n)
         sets.append((ra1, rng.uniform(-30, 30, n).astype(np.float32), ((ra1 + dra) % 21600).astype(np.float32),
                      rng.uniform(-30, 30, n).astype(np.float32)))
@@ -214,7 +215,7 @@ def _pair_sets(n, seed):
 @pytest.mark.parametrize("w,nb", [(0.25, 720), (0.01, 18000), (0.35, 515)])
 def test_per_pair_bins_only_move_within_tolerance_of_an_edge(acf, ctx, w, nb, form):
     # form 0: the full-range chord form for every pair; form 1: the form a tightly bounded group
-    # computes: the dot form wherever |u.v| < cos 45 deg, the short chord where |u.v| > cos 66 deg
+    # computes: the dot form wherever |u.v| < cos 55 deg, the short chord where |u.v| > cos 72 deg
     w_rad = math.radians(w)
     worst = 0.0
     ctx.set_option("pair_bins_form", form)
@@ -255,7 +256,7 @@ def test_auto_correlation_decomposes_into_parts(acf, ctx, forms, exact):
         torch.cuda.synchronize()
     finally:
         ctx.set_option("range_forms", 1)
-        ctx.set_option("exact", 1)
+        ctx.set_option("exact", DEFAULT_EXACT)
     assert list(full) == list(da + db + 2 * x)
 
 
@@ -312,7 +313,7 @@ def test_exact_mode_2_equals_oracle_bin_for_bin(acf, ctx, w, nb):
             g, o, rep = _compare(acf, ctx, *args, w, nb)
             assert np.array_equal(g, o.hist), rep
     finally:
-        ctx.set_option("exact", 1)
+        ctx.set_option("exact", DEFAULT_EXACT)
 
 
 def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
@@ -323,23 +324,34 @@ def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
         _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
         assert ctx.info("exact_flagged") == 0
     finally:
-        ctx.set_option("exact", 1)
+        ctx.set_option("exact", DEFAULT_EXACT)
 
 
 PATH_KEYS = ("pairs_fixed", "pairs_general", "pairs_fixed_exact", "pairs_general_exact", "pairs_masked",
              "pairs_mid", "pairs_mid_exact", "pairs_small", "pairs_small_exact")
 
 
-def test_path_counters_cover_every_computed_pair(acf, ctx):
+@pytest.mark.parametrize("exact", [1, 2])
+def test_path_counters_cover_every_computed_pair(acf, ctx, exact):
     c = synth.catalogs(5000, 4100, 12, 30.0, seed=16)
-    ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
-    got = {k: ctx.info(k) for k in PATH_KEYS}
+    ctx.set_option("exact", exact)
+    try:
+        ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+        got = {k: ctx.info(k) for k in PATH_KEYS}
+    finally:
+        ctx.set_option("exact", DEFAULT_EXACT)
     rows = -(-5000 // 128)
     # every unit computes its whole 128-wide i-set against the j-chunk's real length
     assert sum(got.values()) == rows * 128 * 4100, got
-    assert got["pairs_masked"] > 0 and got["pairs_mid"] > 0 and got["pairs_small"] > 0
-    assert got["pairs_small_exact"] > 0  # groups near 0 and 180 degrees: short chord with flags
-    assert got["pairs_mid_exact"] == 0  # exact mode 1 never sends a group to the dot form
+    assert got["pairs_masked"] > 0
+    if exact == 1:
+        assert got["pairs_mid"] > 0 and got["pairs_small"] > 0
+        assert got["pairs_small_exact"] > 0  # groups near 0 and 180 degrees: short chord with flags
+        assert got["pairs_mid_exact"] == 0  # exact mode 1 never sends a group to the dot form
+    else:
+        # exact mode 2: every group flags near-edge pairs
+        assert got["pairs_mid"] == got["pairs_small"] == got["pairs_fixed"] == got["pairs_general"] == 0
+        assert got["pairs_mid_exact"] > 0 and got["pairs_small_exact"] > 0
 
 
 @pytest.mark.parametrize("w,nb,mid_expected", [(0.25, 720, True), (4.0, 45, False), (0.35, 515, False)])
@@ -350,11 +362,13 @@ def test_range_forms_on_off_and_where_they_apply(acf, ctx, w, nb, mid_expected):
     c = synth.catalogs(6000, 5000, 12, 30.0, seed=18)
     for forms in (1, 0):
         ctx.set_option("range_forms", forms)
+        ctx.set_option("exact", 1)
         try:
             _compare(acf, ctx, c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
             got = {k: ctx.info(k) for k in PATH_KEYS}
         finally:
             ctx.set_option("range_forms", 1)
+            ctx.set_option("exact", DEFAULT_EXACT)
         assert (got["pairs_mid"] > 0) == (forms == 1 and mid_expected), got
         assert (got["pairs_small"] + got["pairs_small_exact"] > 0) == (forms == 1), got
     ctx.set_option("exact", 2)
@@ -365,7 +379,7 @@ def test_range_forms_on_off_and_where_they_apply(acf, ctx, w, nb, mid_expected):
             assert ctx.info("pairs_mid_exact") > 0 and ctx.info("pairs_mid") == 0
         assert ctx.info("pairs_small_exact") > 0 and ctx.info("pairs_small") == 0
     finally:
-        ctx.set_option("exact", 1)
+        ctx.set_option("exact", DEFAULT_EXACT)
 
 
 def test_kernel_launch_counter(acf, ctx):
@@ -388,4 +402,4 @@ def test_kernel_launch_counter(acf, ctx):
     try:
         assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2
     finally:
-        ctx.set_option("exact", 1)
+        ctx.set_option("exact", DEFAULT_EXACT)
