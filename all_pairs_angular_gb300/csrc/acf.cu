@@ -245,7 +245,7 @@ struct CatBufs {
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
 };
 struct Scratch {
-  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue slots handed out (this launch),
+  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue spill slots handed out (this launch),
                                        // [2] moved pairs, [3] flagged pairs, [4] queue overflow;
                                        // bytes 64..135: pairs per path (u64)
   unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
@@ -258,6 +258,7 @@ struct Scratch {
   double* T = nullptr;                 // exact mode: edge tables, nbins + 1 each
   double* U = nullptr;
   uint4* queue = nullptr;
+  unsigned int* qused = nullptr;       // per pair-kernel block: slots of its queue region in use
   long long qcap = 0;
 };
 
@@ -295,6 +296,7 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   r.T = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
   r.U = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
   r.qcap = qcap;
+  r.qused = reinterpret_cast<unsigned int*>(take((size_t)grid * 4));
   r.queue = reinterpret_cast<uint4*>(take((size_t)qcap * 16));
   return off;
 }
@@ -369,13 +371,17 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
   p.exact_lo = pl.exact_lo;
   p.queue = sc.queue;
-  p.qtotal = sc.counters + 1;
+  p.qspill = sc.counters + 1;
+  p.qused = sc.qused;
   p.qflagged = sc.counters + 3;
   p.qcap = (unsigned int)std::min<long long>(sc.qcap, 0xFFFFFFFFll);
-  // each block reserves a batch (half the queue spread over the blocks of a launch; the queue is
-  // drained after every launch); blocks that flag more append past their batch through the
-  // global counter
-  p.qbatch = (unsigned int)std::max<long long>(16, sc.qcap / (2 * std::max<long long>(L.grid, 1)));
+  // each block owns a region of the queue (half the queue spread over the blocks of a launch, a
+  // power of two each; the queue is drained after every launch); blocks that flag more append to
+  // the spill region through the global counter
+  int qbatch_log2 = -1;
+  for (long long qb = sc.qcap / (2 * std::max<long long>(L.grid, 1)); qb > 0; qb >>= 1) ++qbatch_log2;
+  if (qbatch_log2 < 0) p.qcap = 0;  // too small to use
+  p.qbatch = qbatch_log2 >= 0 ? (1u << qbatch_log2) : 0u;
   p.path_pairs = reinterpret_cast<unsigned long long*>(sc.counters + 16);
   if (p.qcap == 0) p.exact_mode = 0;
   p.vi = ci.v;
@@ -409,14 +415,21 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     if (p.exact_mode) {
       // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
       const int fblocks = c->num_sms * 8;
-      if (pl.map == kDirect)
-        fixup_kernel<kDirect><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
-                                                              sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,
-                                                              sc.counters + 4);
-      else
-        fixup_kernel<kClamp><<<fblocks, 256, 0, c->stream>>>(sc.queue, sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T,
-                                                             sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,
-                                                             sc.counters + 4);
+      const size_t fsmem = (size_t)(3 * pl.bp.nbins + 2) * 8 + (size_t)L.grid * 4;
+      const bool fs = fsmem <= 48 * 1024;
+#define ACF_FIXUP(M, SM)                                                                                           \
+  fixup_kernel<M, SM><<<fblocks, 256, SM ? fsmem : 0, c->stream>>>(sc.queue, sc.qused, (int)L.grid, qbatch_log2,    \
+                                                                    sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T, \
+                                                                    sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,  \
+                                                                    sc.counters + 4)
+      if (pl.map == kDirect) {
+        if (fs) ACF_FIXUP(kDirect, true);
+        else ACF_FIXUP(kDirect, false);
+      } else {
+        if (fs) ACF_FIXUP(kClamp, true);
+        else ACF_FIXUP(kClamp, false);
+      }
+#undef ACF_FIXUP
       ACF_LAUNCHED(c);
     }
   }

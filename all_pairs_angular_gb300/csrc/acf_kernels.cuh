@@ -129,12 +129,14 @@ struct PairParams {
   long long igroups;                   // number of 32-galaxy groups of the i catalog
   int exact_mode;                      // 0 off, 1 groups that may hold separations < theta_lo or > 180 - theta_lo, 2 all
   float exact_lo;                      // theta_lo in radians
-  uint4* queue;                        // exact mode: flagged pairs (sorted i, sorted j, fine code bits, 0);
-                                       // i = 0xFFFFFFFF marks an unused slot
-  unsigned int* qtotal;                // slots handed out (reserved batches + single appends)
+  uint4* queue;                        // exact mode: flagged pairs (sorted i, sorted j, fine code bits, 0):
+                                       // block b owns slots [b qbatch, (b + 1) qbatch), then a shared
+                                       // spill region from gridDim.x qbatch on
+  unsigned int* qspill;                // spill slots handed out
+  unsigned int* qused;                 // per block: slots of its own region in use
   unsigned int* qflagged;              // pairs flagged (for reporting)
   unsigned int qcap;                   // queue slots
-  unsigned int qbatch;                 // slots a block reserves at its start
+  unsigned int qbatch;                 // slots a block owns (a power of two)
   unsigned long long* path_pairs;      // pairs evaluated per path: chord fixed, chord general,
                                        // chord fixed+flag, chord general+flag, masked/ragged units,
                                        // dot form, dot form+flag, short chord, short chord+flag
@@ -728,7 +730,8 @@ __device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, u
   if (e - p.bp.zone0 <= p.bp.span0 || e - p.bp.zone1 <= p.bp.span1) {
     // a slot of this block's reserved batch (shared-memory counter), or past it a global one
     const unsigned int local = atomicAdd(s_qcount, 1u);
-    const unsigned int slot = local < p.qbatch ? s_qcount[1] + local : atomicAdd(p.qtotal, 1u);
+    const unsigned int slot =
+        local < p.qbatch ? blockIdx.x * p.qbatch + local : gridDim.x * p.qbatch + atomicAdd(p.qspill, 1u);
     if (slot < p.qcap) {
       p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
       queued = true;
@@ -799,7 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   float4* my_tiles = reinterpret_cast<float4*>(smem) + warp * 2 * kJT;  // [2][kJT] per warp
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + WARPS * 2 * kJT * sizeof(float4));
 
-  __shared__ unsigned int s_qcount[2];  // exact mode: [0] flags of this block, [1] first slot of its batch
+  __shared__ unsigned int s_qcount[1];  // exact mode: pairs this block flagged
   // per warp: j-groups run on each path (see path_pairs), and the cap of the warp's current i-set
   // (kept here, not in registers, to leave the hot loops all the registers)
   __shared__ unsigned int s_paths[WARPS][9];
@@ -811,7 +814,6 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     for (int k = tid; k < p.bp.nbins; k += THREADS) row[k] = 0ull;
   if (tid == 0) {
     s_qcount[0] = 0u;
-    s_qcount[1] = p.exact_mode ? atomicAdd(p.qtotal, p.qbatch) : 0u;
   }
   __syncthreads();
 
@@ -1064,13 +1066,10 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     }
   }
   __syncthreads();
-  if (p.exact_mode) {
-    // mark the unused tail of this block's batch, and report its flags
-    for (unsigned int k = s_qcount[0] + tid; k < p.qbatch; k += THREADS) {
-      const unsigned int slot = s_qcount[1] + k;
-      if (slot < p.qcap) p.queue[slot] = make_uint4(0xFFFFFFFFu, 0u, 0u, 0u);
-    }
-    if (tid == 0) atomicAdd(p.qflagged, s_qcount[0]);
+  if (p.exact_mode && tid == 0) {
+    // the slots of this block's own region in use, and its flags for reporting
+    p.qused[blockIdx.x] = min(s_qcount[0], p.qbatch);
+    atomicAdd(p.qflagged, s_qcount[0]);
   }
   flush_hist<K, THREADS, LAYOUT, MAP, METHOD>(p, hist, false);
 }
@@ -1131,44 +1130,87 @@ __global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ 
 }
 
 // Re-decide every queued pair in fp64 from the fp64 unit vectors and record the move of its count
-// in delta[] if the fast code put it in a neighbouring bin. Runs after every pair-kernel launch
-// (the queue then starts empty again); the merge adds delta to the counts. Slots requested past
-// the queue's end are added to *overflow (those pairs kept their fp32 bin).
-template <int MAP>
-__global__ void fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qtotal,
-                             unsigned int qcap, const double4* __restrict__ vi, const double4* __restrict__ vj,
-                             const double* __restrict__ T, const double* __restrict__ U, BinParams bp,
-                             unsigned int inc, unsigned long long* __restrict__ delta, unsigned int* __restrict__ moved,
-                             unsigned int* __restrict__ overflow) {
-  const unsigned int nq = min(*qtotal, qcap);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && *qtotal > qcap) atomicAdd(overflow, *qtotal - qcap);
+// if the fast code put it in a neighbouring bin. Runs after every pair-kernel launch (the queue then
+// starts empty again); the merge adds delta[] to the counts. Slots requested past the queue's end
+// are added to *overflow (those pairs kept their fp32 bin).
+// The queue holds pair_grid regions of qbatch slots (region b: qused[b] in use), then spill slots.
+// With SMEM the edge tables, the per-bin moves and the region use sit in shared memory (nbins up to
+// a few thousand); the moves reach delta[] once per block.
+template <int MAP, bool SMEM>
+__global__ void __launch_bounds__(256) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
+                                                    int pair_grid, int qbatch_log2,
+                                                    const unsigned int* __restrict__ qspill, unsigned int qcap,
+                                                    const double4* __restrict__ vi, const double4* __restrict__ vj,
+                                                    const double* __restrict__ T, const double* __restrict__ U,
+                                                    BinParams bp, unsigned int inc, unsigned long long* __restrict__ delta,
+                                                    unsigned int* __restrict__ moved, unsigned int* __restrict__ overflow) {
+  extern __shared__ __align__(16) unsigned char fsm[];
+  __shared__ unsigned int s_moved;
+  const int nb = bp.nbins;
+  const double* tT = T;
+  const double* tU = U;
+  unsigned long long* dl = delta;
+  const unsigned int* used = qused;
+  if (SMEM) {
+    double* sT = reinterpret_cast<double*>(fsm);
+    double* sU = sT + (nb + 1);
+    unsigned long long* sd = reinterpret_cast<unsigned long long*>(sU + (nb + 1));
+    unsigned int* su = reinterpret_cast<unsigned int*>(sd + nb);
+    for (int k = threadIdx.x; k <= nb; k += blockDim.x) {
+      sT[k] = T[k];
+      sU[k] = U[k];
+      if (k < nb) sd[k] = 0ull;
+    }
+    for (int b = threadIdx.x; b < pair_grid; b += blockDim.x) su[b] = qused[b];
+    tT = sT;
+    tU = sU;
+    dl = sd;
+    used = su;
+  }
+  if (threadIdx.x == 0) s_moved = 0u;
+  __syncthreads();
+  const unsigned int qbatch = 1u << qbatch_log2;
+  const unsigned int nbatch = (unsigned int)pair_grid << qbatch_log2;
+  const unsigned int spill = *qspill;
+  const unsigned int room = qcap - nbatch;
+  const unsigned int nspill = min(spill, room);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && spill > room) atomicAdd(overflow, spill - room);
   const uint32_t magic_bits = __float_as_uint(kMagic);
-  for (unsigned int s = blockIdx.x * blockDim.x + threadIdx.x; s < nq; s += gridDim.x * blockDim.x) {
+  unsigned int my_moved = 0u;
+  for (unsigned int s = blockIdx.x * blockDim.x + threadIdx.x; s < nbatch + nspill; s += gridDim.x * blockDim.x) {
+    if (s < nbatch && (s & (qbatch - 1u)) >= used[s >> qbatch_log2]) continue;  // unused slot of a region
     const uint4 rec = queue[s];
-    if (rec.x == 0xFFFFFFFFu) continue;  // unused slot of a reserved batch
     const double4 a = vi[rec.x], b = vj[rec.y];
     int e = (int)((rec.z - magic_bits) >> bp.fine_shift);
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     const int kf = entry_to_bin<MAP>(e, bp);
-    int k = kf;
-    const double dot = a.x * b.x + a.y * b.y + a.z * b.z;
-    k = k > bp.kmax ? bp.kmax : k;
-    if (dot >= 0.0) {
+    int k = kf > bp.kmax ? bp.kmax : kf;
+    // bins up to 90 degrees compare the difference chord with T, the others the sum chord with U
+    // (both exact enough near 90 degrees, each where the other loses relative precision)
+    if (tT[k] <= 2.0) {
       const double dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z;
       const double q = dx * dx + dy * dy + dz * dz;
-      while (k > 0 && q < T[k]) --k;
-      while (k < bp.kmax && q >= T[k + 1]) ++k;
+      while (k > 0 && q < tT[k]) --k;
+      while (k < bp.kmax && q >= tT[k + 1]) ++k;
     } else {
       const double dx = a.x + b.x, dy = a.y + b.y, dz = a.z + b.z;
       const double q = dx * dx + dy * dy + dz * dz;
-      while (k > 0 && q > U[k]) --k;
-      while (k < bp.kmax && q <= U[k + 1]) ++k;
+      while (k > 0 && q > tU[k]) --k;
+      while (k < bp.kmax && q <= tU[k + 1]) ++k;
     }
     if (k != kf) {
-      atomicAdd(delta + kf, (unsigned long long)(-(long long)inc));
-      atomicAdd(delta + k, (unsigned long long)inc);
-      atomicAdd(moved, 1u);
+      atomicAdd(dl + kf, (unsigned long long)(-(long long)inc));
+      atomicAdd(dl + k, (unsigned long long)inc);
+      ++my_moved;
     }
+  }
+  for (int o = 16; o > 0; o >>= 1) my_moved += __shfl_xor_sync(0xffffffffu, my_moved, o);
+  if ((threadIdx.x & 31) == 0 && my_moved) atomicAdd(&s_moved, my_moved);
+  __syncthreads();
+  if (threadIdx.x == 0 && s_moved) atomicAdd(moved, s_moved);
+  if (SMEM) {
+    for (int k = threadIdx.x; k < nb; k += blockDim.x)
+      if (dl[k]) atomicAdd(delta + k, dl[k]);
   }
 }
 
