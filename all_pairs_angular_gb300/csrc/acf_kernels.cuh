@@ -596,6 +596,45 @@ __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, f
   }
 }
 
+// Exact mode, fixed sign: the fine code (returned) and the plain code of the same pair (coarse),
+// from one theta'. The fine constants are the plain ones times 2^S exactly (plus the bias), so
+// both floor the same real number: their entries agree unless the fine code flags the pair.
+template <int MAP, bool SMALL>
+__device__ __forceinline__ float pair_code_fixed2(float xi, float yi, float zi, float xj, float yj, float zj,
+                                                  float ns, float iws_f, float h_f, float iws, float h,
+                                                  const BinParams& bp, uint32_t& coarse) {
+  const float dx = fmaf(ns, xj, xi);
+  const float dy = fmaf(ns, yj, yi);
+  const float dz = fmaf(ns, zj, zi);
+  const float q = fmaf(dz, dz, fmaf(dy, dy, fmaf(dx, dx, 1e-30f)));
+  float p;
+  if (SMALL) {
+    p = fmaf(kS5, q, kS4);
+    p = fmaf(p, q, kS3);
+    p = fmaf(p, q, kS2);
+    p = fmaf(p, q, kS1);
+    p = fmaf(p, q, kS0);
+  } else {
+    p = fmaf(kP7, q, kP6);
+    p = fmaf(p, q, kP5);
+    p = fmaf(p, q, kP4);
+    p = fmaf(p, q, kP3);
+    p = fmaf(p, q, kP2);
+    p = fmaf(p, q, kP1);
+    p = fmaf(p, q, kP0);
+  }
+  const float th = sqrt_approx(p * q);
+  if (MAP == kDirect) {
+    coarse = __float_as_uint(fma_rz(th, iws, h));
+    return fma_rz(th, iws_f, h_f);
+  } else {
+    const float t = fmaf(th, iws, h);
+    const float tf = fmaf(th, iws_f, h_f);
+    coarse = __float_as_uint(add_rz(fminf(t, bp.clamp_c), kMagic));
+    return add_rz(fminf(tf, bp.clamp_f), bp.magic_f);
+  }
+}
+
 // The dot form, for pairs whose caps put theta in (55, 125) degrees (direct map, P even):
 // theta / w = P/2 - d R(d^2) / w, floored exactly by one fma rounded toward zero onto 2^23 + P/2
 // (the product of the two fp32 operands enters unrounded). Worst-case theta error: d carries
@@ -722,26 +761,57 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
 // of the pair's own code, so the set of re-decided pairs does not depend on grouping or order).
 // A pair that is not queued (outside the zone, or the queue is full) keeps its fp32 bin: if the
 // one-unit bias carried it into the next entry (biased fraction 0), its count moves back.
-__device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, uint32_t magic_bits, int i, int j,
-                                             unsigned int* s_qcount, uint32_t base_f, int shift) {
-  const int S = p.bp.fine_shift;
-  const uint32_t e = (cb - magic_bits) >> S;
+struct QueueArgs {
+  uint4* queue;
+  unsigned int* qspill;
+  unsigned int qcap, qbatch, zone0, span0, zone1, span1, inc;
+  int fine_shift;
+};
+// cb is the pair's fine code; e_cnt the entry its count went to: the fine code's integer part
+// (single-code loops, where the bias may have carried) or the plain code's (two-code loops, may_carry
+// false). The queue record keeps both, so the re-decision moves the count from where it is.
+__device__ __forceinline__ void push_flagged_body(const QueueArgs& q, uint32_t cb, uint32_t e_cnt, bool may_carry, int i,
+                                                  int j, unsigned int* s_qcount, uint32_t base_f, int shift) {
+  const int S = q.fine_shift;
+  const uint32_t e = e_cnt;
   bool queued = false;
-  if (e - p.bp.zone0 <= p.bp.span0 || e - p.bp.zone1 <= p.bp.span1) {
-    // a slot of this block's reserved batch (shared-memory counter), or past it a global one
+  if (e - q.zone0 <= q.span0 || e - q.zone1 <= q.span1) {
+    // a slot of this block's own region (shared-memory counter), or past it a spill slot
     const unsigned int local = atomicAdd(s_qcount, 1u);
-    const unsigned int slot =
-        local < p.qbatch ? blockIdx.x * p.qbatch + local : gridDim.x * p.qbatch + atomicAdd(p.qspill, 1u);
-    if (slot < p.qcap) {
-      p.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, 0u);
+    const unsigned int slot = local < q.qbatch ? blockIdx.x * q.qbatch + local : gridDim.x * q.qbatch + atomicAdd(q.qspill, 1u);
+    if (slot < q.qcap) {
+      q.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, e_cnt);
       queued = true;
     }
   }
-  if (!queued && (cb & ((1u << S) - 1u)) == 0u) {
+  if (!queued && may_carry && (cb & ((1u << S) - 1u)) == 0u) {
     const uint32_t a = ((cb >> S) << shift) + base_f;
-    red_shared_add(a, 0u - p.inc);
-    red_shared_add(a - (1u << shift), p.inc);
+    red_shared_add(a, 0u - q.inc);
+    red_shared_add(a - (1u << shift), q.inc);
   }
+}
+// Out of line: the flagged path is rare, and one call per site keeps the hot loop bodies small.
+__device__ __noinline__ void push_flagged_call(QueueArgs q, uint32_t cb, uint32_t e_cnt, bool may_carry, int i, int j,
+                                               unsigned int* s_qcount, uint32_t base_f, int shift) {
+  push_flagged_body(q, cb, e_cnt, may_carry, i, j, s_qcount, base_f, shift);
+}
+#ifndef ACF_PUSH_NOINLINE
+#define ACF_PUSH_NOINLINE 0
+#endif
+__device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, uint32_t magic_bits, int i, int j,
+                                             unsigned int* s_qcount, uint32_t base_f, int shift) {
+  const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc,
+                    p.bp.fine_shift};
+  const uint32_t e_cnt = (cb - magic_bits) >> p.bp.fine_shift;
+  if (ACF_PUSH_NOINLINE) push_flagged_call(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
+  else push_flagged_body(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
+}
+// The same for a two-code loop: the count went to the plain code's entry.
+__device__ __forceinline__ void push_flagged2(const PairParams& p, uint32_t cb, uint32_t coarse, uint32_t magic_bits,
+                                              int i, int j, unsigned int* s_qcount) {
+  const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc,
+                    p.bp.fine_shift};
+  push_flagged_body(q, cb, coarse - magic_bits, false, i, j, s_qcount, 0u, 0);
 }
 
 // ------------------------------------------------------------------ pair kernel
@@ -908,7 +978,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         // chord loops take the sign in registers (ns, iws, h); the dot-form loop needs no sign; the
         // fine (exact) loops are rare and kept rolled so that all live loop bodies fit the
         // instruction cache.
-        auto run = [&](auto form, auto fine, int jbeg, float ns, float iws, float h) {
+        // (ns, iws, h): sign, scale and constant of a fixed-sign chord loop (fine ones when F);
+        // (iws_c, h_c): the plain scale and constant, for the two-code fine loops
+        auto run = [&](auto form, auto fine, int jbeg, float ns, float iws, float h, float iws_c, float h_c) {
           constexpr int X = decltype(form)::value;  // 0 chord general, 1 chord fixed sign, 2 dot form,
                                                     // 3 short chord (fixed sign)
           constexpr bool F = decltype(fine)::value;
@@ -960,6 +1032,30 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             return;
           }
           const uint32_t fmask = (1u << p.bp.fine_shift) - 1u;
+          if constexpr (F && (X == 1 || X == 3)) {
+            // fixed-sign chord with flags: the plain code addresses the histogram (as without flags),
+            // the fine code, from the same theta', only decides the flag
+#pragma unroll 1
+            for (int jj = jbeg; jj < jbeg + 32; ++jj) {
+              const float4 v = tile[jj];
+              uint32_t cfs[K], ccs[K];
+              uint32_t low = 0xFFFFFFFFu;
+#pragma unroll
+              for (int k = 0; k < K; ++k) {
+                cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
+                                                                        iws_c, h_c, p.bp, ccs[k]));
+                add_pair<false>(p, ccs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
+                                zi[k], v);
+                low = min(low, cfs[k] & fmask);
+              }
+              if (__any_sync(0xffffffffu, low <= 1u)) {
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+                  if ((cfs[k] & fmask) <= 1u) push_flagged2(p, cfs[k], ccs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
+              }
+            }
+            return;
+          }
 #pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
             const float4 v = tile[jj];
@@ -993,30 +1089,35 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const bool fine = (pc & kExactBit) != 0;
           if (pc & kMidBit) {
             count_path(fine ? 6 : 5, 1u);
-            if (fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f);
-            else run(FormTag<2>(), FineTag<false>(), g * 32, 0.f, 0.f, 0.f);
+            if (fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
+            else run(FormTag<2>(), FineTag<false>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
             continue;
           }
-          const float iw = fine ? p.bp.inv_w_f : p.bp.inv_w;
-          const float ns = (path == kBelow90) ? -1.0f : 1.0f;
-          const float iws = (path == kBelow90) ? iw : -iw;
-          float h;
-          if (MAP == kDirect)
-            h = (path == kBelow90) ? (fine ? p.bp.magic_f : kMagic) : (fine ? p.bp.magic_far_f : p.bp.magic_far);
-          else h = (path == kBelow90) ? 0.0f : 3.14159265358979323846f * iw;
+          const bool below = path == kBelow90;
+          const float ns = below ? -1.0f : 1.0f;
+          const float iws_c = below ? p.bp.inv_w : -p.bp.inv_w;
+          float h_c;
+          if (MAP == kDirect) h_c = below ? kMagic : p.bp.magic_far;
+          else h_c = below ? 0.0f : 3.14159265358979323846f * p.bp.inv_w;
+          float iws = iws_c, h = h_c;
+          if (fine) {
+            iws = below ? p.bp.inv_w_f : -p.bp.inv_w_f;
+            if (MAP == kDirect) h = below ? p.bp.magic_f : p.bp.magic_far_f;
+            else h = below ? 0.0f : 3.14159265358979323846f * p.bp.inv_w_f;
+          }
           if (pc & kSmallBit) {
             count_path(fine ? 8 : 7, 1u);
-            if (fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h);
-            else run(FormTag<3>(), FineTag<false>(), g * 32, ns, iws, h);
+            if (fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
+            else run(FormTag<3>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
             continue;
           }
           count_path(path == kGeneral ? (fine ? 3 : 1) : (fine ? 2 : 0), 1u);
           if (path == kGeneral) {
-            if (fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h);
-            else run(FormTag<0>(), FineTag<false>(), g * 32, ns, iws, h);
+            if (fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
+            else run(FormTag<0>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
           } else {
-            if (fine) run(FormTag<1>(), FineTag<true>(), g * 32, ns, iws, h);
-            else run(FormTag<1>(), FineTag<false>(), g * 32, ns, iws, h);
+            if (fine) run(FormTag<1>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
+            else run(FormTag<1>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
           }
         }
       } else {
@@ -1181,7 +1282,7 @@ __global__ void __launch_bounds__(256) fixup_kernel(const uint4* __restrict__ qu
     if (s < nbatch && (s & (qbatch - 1u)) >= used[s >> qbatch_log2]) continue;  // unused slot of a region
     const uint4 rec = queue[s];
     const double4 a = vi[rec.x], b = vj[rec.y];
-    int e = (int)((rec.z - magic_bits) >> bp.fine_shift);
+    int e = (int)rec.w;  // the entry the pair's count went to
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     const int kf = entry_to_bin<MAP>(e, bp);
     int k = kf > bp.kmax ? bp.kmax : kf;
