@@ -25,7 +25,7 @@ ACF_ERR_CUDA = -4
 
 EXPORTED = ["acf_version", "acf_create", "acf_destroy", "acf_last_error", "acf_set_stream", "acf_histogram",
             "acf_omega", "acf_correlate", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
-            "acf_kernel_times", "acf_histogram_noalloc"]
+            "acf_kernel_times", "acf_histogram_noalloc", "acf_fp32_peak"]
 
 _lib = None
 
@@ -69,6 +69,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "acf_set_option": (ci, [vp, ctypes.c_char_p, i64]),
         "acf_get_info": (ci, [vp, ctypes.c_char_p, ctypes.POINTER(i64)]),
         "acf_kernel_times": (ci, [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]),
+        "acf_fp32_peak": (ci, [vp, i64, ctypes.POINTER(f64), ctypes.POINTER(ctypes.c_float)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -170,6 +171,15 @@ def acf_kernel_times(ctx: int, cap: int = 4096) -> list[float]:
     cnt = ctypes.c_int32()
     _check(ctx, load().acf_kernel_times(ctx, buf, int(cap), ctypes.byref(cnt)))
     return [buf[k] for k in range(cnt.value)]
+
+
+def acf_fp32_peak(ctx: int, iters: int = 1 << 16) -> tuple[float, float]:
+    """FMA thread-instructions per second of this GPU (the FP32 issue ceiling), and thread 0's
+    chain sum for a host replay."""
+    rate = ctypes.c_double()
+    t0 = ctypes.c_float()
+    _check(ctx, load().acf_fp32_peak(ctx, int(iters), ctypes.byref(rate), ctypes.byref(t0)))
+    return rate.value, t0.value
 
 
 # ------------------------------------------------------------- convenience layer

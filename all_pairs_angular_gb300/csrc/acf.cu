@@ -794,6 +794,34 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
   return ACF_ERR_ARG;
 }
 
+int acf_fp32_peak(acf_ctx* c, int64_t iters, double* ffma_per_s, float* thread0) {
+  if (!c || !ffma_per_s || iters <= 0) return ACF_ERR_ARG;
+  ACF_CUDA(c, cudaSetDevice(c->device));
+  const int blocks = c->num_sms * 2, threads = 1024;
+  float* out = nullptr;
+  ACF_CUDA(c, cudaMallocAsync(reinterpret_cast<void**>(&out), (size_t)blocks * threads * sizeof(float), c->stream));
+  cudaEvent_t e0, e1;
+  ACF_CUDA(c, cudaEventCreate(&e0));
+  ACF_CUDA(c, cudaEventCreate(&e1));
+  const float a = 0.9999999f, b = 1e-7f;
+  fma_peak_kernel<<<blocks, threads, 0, c->stream>>>(a, b, iters / 8 + 1, out);  // warm-up
+  ACF_LAUNCHED(c);
+  ACF_CUDA(c, cudaEventRecord(e0, c->stream));
+  fma_peak_kernel<<<blocks, threads, 0, c->stream>>>(a, b, iters, out);
+  ACF_LAUNCHED(c);
+  ACF_CUDA(c, cudaEventRecord(e1, c->stream));
+  ACF_CUDA(c, cudaEventSynchronize(e1));
+  float ms = 0.f;
+  ACF_CUDA(c, cudaEventElapsedTime(&ms, e0, e1));
+  if (thread0) ACF_CUDA(c, cudaMemcpyAsync(thread0, out, sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+  ACF_CUDA(c, cudaFreeAsync(out, c->stream));
+  ACF_CUDA(c, cudaStreamSynchronize(c->stream));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  *ffma_per_s = (double)blocks * threads * (double)iters * kFmaChains / (ms * 1e-3);
+  return ACF_OK;
+}
+
 int acf_kernel_times(acf_ctx* c, float* ms, int32_t cap, int32_t* count) {
   if (!c || !count || (cap > 0 && !ms)) return ACF_ERR_ARG;
   *count = 0;

@@ -181,11 +181,9 @@ __device__ __forceinline__ float sqrt_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ float add_rz(float a, float b) {
-  float y;
-  asm("add.rz.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
-  return y;
-}
+// round-toward-zero add and fma as compiler intrinsics (not inline asm), so that a constant operand
+// can come straight from the constant bank instead of a register
+__device__ __forceinline__ float add_rz(float a, float b) { return __fadd_rz(a, b); }
 
 // three-input logic op; lut is the truth table over (a=0xF0, b=0xCC, c=0xAA)
 template <int LUT>
@@ -196,11 +194,7 @@ __device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
 }
 
 // a * b + c with one rounding, toward zero
-__device__ __forceinline__ float fma_rz(float a, float b, float c) {
-  float y;
-  asm("fma.rz.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
-  return y;
-}
+__device__ __forceinline__ float fma_rz(float a, float b, float c) { return __fmaf_rz(a, b, c); }
 
 __device__ __forceinline__ void red_shared_add(uint32_t addr, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -1344,6 +1338,28 @@ __global__ void pair_bins_kernel(const float* __restrict__ ra1, const float* __r
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     bins[i] = entry_to_bin<MAP>(e, bp);
   }
+}
+
+// ------------------------------------------------------------------ FP32 issue ceiling
+
+// Independent FMA chains (kFmaChains per thread) for a runtime iteration count: the FP32 issue rate
+// the hardware sustains, measured the way a roofline ceiling is (one instruction class, enough
+// independent work to cover its latency). Every thread writes the sum of its chains so nothing is
+// dead code; the host replays thread 0 to check the kernel really ran.
+constexpr int kFmaChains = 8;
+__global__ void __launch_bounds__(1024) fma_peak_kernel(float a, float b, long long iters, float* __restrict__ out) {
+  float x[kFmaChains];
+#pragma unroll
+  for (int c = 0; c < kFmaChains; ++c) x[c] = (float)threadIdx.x * 1e-3f + (float)c;
+#pragma unroll 16
+  for (long long it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int c = 0; c < kFmaChains; ++c) x[c] = fmaf(x[c], a, b);
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kFmaChains; ++c) s += x[c];
+  out[blockIdx.x * (long long)blockDim.x + threadIdx.x] = s;
 }
 
 }  // namespace acf

@@ -37,10 +37,11 @@ UNIT = "Gpairs/s"
 # shared atomic); where the caps fix the sign of the dot product the dot, the sign operation and the
 # constant choice drop out (18); where every theta' stays below 72 degrees the polynomial is of
 # degree 5 instead of 7 (16); the dot form for groups between 55 and 125 degrees is 12 (dot, square,
-# 5-term polynomial, rounding fma, address, atomic); the exact-mode flag adds 3 (fine-code shift,
-# fraction mask, running minimum of the batch).
-INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 21, "pairs_general_exact": 28,
-                 "pairs_mid": 12, "pairs_mid_exact": 15, "pairs_small": 16, "pairs_small_exact": 19}
+# 5-term polynomial, rounding fma, address, atomic). Exact-mode flagging adds 3.25: the fine code
+# (a second rounding fma, or a shift of the one code), the fraction mask, a 3-input running minimum
+# shared by 2 pairs, and one warp vote with its compare and branch per j (4 pairs per lane).
+INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 21.25, "pairs_general_exact": 28.25,
+                 "pairs_mid": 12, "pairs_mid_exact": 15.25, "pairs_small": 16, "pairs_small_exact": 19.25}
 INST_MASKED = 25  # diagonal / ragged units run the general loop on every computed pair
 INST_MASKED_EXACT = 4  # and with flags: fine-code shift, fraction mask, test, branch per pair
 SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
@@ -287,6 +288,10 @@ def run_ours(args, cat, workload, rank, world, local):
             "peak_basis": f"{SMS} SMs x {LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz (maximum SM clock)"}
     if clocks.get("sm_mhz"):
         roof["frac_at_observed_clock"] = achieved / (SMS * LANES_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12)
+    # the FP32 issue ceiling measured on this GPU in this run (independent FMA chains)
+    fma_rate, _ = acf.acf_fp32_peak(ctx.handle, 1 << 16)
+    roof["fma_chain_ceiling"] = fma_rate / 1e12
+    roof["frac_of_fma_chain_ceiling"] = achieved / (fma_rate / 1e12) if achieved else None
 
     # end to end through the C ABI with pinned host buffers: copies inside the timed region
     h = {k: torch.from_numpy(getattr(cat, k)).pin_memory() for k in ("ra_d", "dec_d", "ra_r", "dec_r")}

@@ -213,6 +213,17 @@ int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
  */
 int acf_kernel_times(acf_ctx *ctx, float *ms, int32_t cap, int32_t *count);
 
+/*
+ * Measure the FP32 issue ceiling of this GPU, the denominator of the pair kernel's roofline
+ * (independent FMA chains, the method of the "roofline.cu" page's compute ceiling): one timed
+ * launch of 2 blocks of 1024 threads per SM, each thread running 8 independent fmaf chains
+ * x = x * 0.9999999f + 1e-7f for `iters` iterations from x = tid * 1e-3f + c (c = chain index).
+ * Synchronous. *ffma_per_s receives FMA thread-instructions per second; thread0 (nullable, host)
+ * receives thread 0's sum of its chains (c = 0..7 in order) so a caller can replay it on the host.
+ * Allocates a small device buffer (stream-ordered) for the results.
+ */
+int acf_fp32_peak(acf_ctx *ctx, int64_t iters, double *ffma_per_s, float *thread0);
+
 #ifdef __cplusplus
 }
 #endif

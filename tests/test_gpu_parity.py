@@ -403,3 +403,20 @@ def test_kernel_launch_counter(acf, ctx):
         assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2
     finally:
         ctx.set_option("exact", DEFAULT_EXACT)
+
+
+def test_fp32_ceiling_probe_runs_the_arithmetic(acf, ctx):
+    # the roofline's measured FP32 ceiling: a sane rate, and thread 0's chains replayed on the host
+    # (fp32 fma emulated exactly in fp64: the product of two fp32 values and the sum with b = 1e-7
+    # fit in 53 bits here, so one rounding to fp32 gives fmaf's result)
+    iters = 1 << 14
+    rate, t0 = acf.acf_fp32_peak(ctx.handle, iters)
+    assert 5e12 < rate < 2e14, rate
+    a, b = np.float64(np.float32(0.9999999)), np.float64(np.float32(1e-7))
+    x = np.arange(8, dtype=np.float32)
+    for _ in range(iters):
+        x = (x.astype(np.float64) * a + b).astype(np.float32)
+    s = np.float32(0.0)
+    for c in range(8):
+        s = np.float32(s + x[c])
+    assert np.float32(t0) == s
