@@ -25,7 +25,8 @@ ACF_ERR_CUDA = -4
 
 EXPORTED = ["acf_version", "acf_create", "acf_destroy", "acf_last_error", "acf_set_stream", "acf_histogram",
             "acf_omega", "acf_correlate", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
-            "acf_kernel_times", "acf_histogram_noalloc", "acf_fp32_peak"]
+            "acf_kernel_times", "acf_histogram_noalloc", "acf_fp32_peak", "acf_read_catalog", "acf_free_catalog",
+            "acf_write_omega"]
 
 _lib = None
 
@@ -70,6 +71,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "acf_get_info": (ci, [vp, ctypes.c_char_p, ctypes.POINTER(i64)]),
         "acf_kernel_times": (ci, [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]),
         "acf_fp32_peak": (ci, [vp, i64, ctypes.POINTER(f64), ctypes.POINTER(ctypes.c_float)]),
+        "acf_read_catalog": (ci, [ctypes.c_char_p, ctypes.POINTER(ctypes.POINTER(ctypes.c_float)),
+                                  ctypes.POINTER(ctypes.POINTER(ctypes.c_float)), ctypes.POINTER(i64),
+                                  ctypes.c_char_p, i32]),
+        "acf_free_catalog": (None, [vp, vp]),
+        "acf_write_omega": (ci, [ctypes.c_char_p, vp, vp, vp, vp, i32, f64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -180,6 +186,39 @@ def acf_fp32_peak(ctx: int, iters: int = 1 << 16) -> tuple[float, float]:
     t0 = ctypes.c_float()
     _check(ctx, load().acf_fp32_peak(ctx, int(iters), ctypes.byref(rate), ctypes.byref(t0)))
     return rate.value, t0.value
+
+
+def acf_read_catalog(path: str) -> tuple[np.ndarray, np.ndarray]:
+    """Read a catalog file (count line, then "ra dec" rows in arcminutes): float32 (ra, dec)."""
+    lib = load()
+    ra = ctypes.POINTER(ctypes.c_float)()
+    dec = ctypes.POINTER(ctypes.c_float)()
+    n = ctypes.c_int64()
+    err = ctypes.create_string_buffer(512)
+    rc = lib.acf_read_catalog(os.fsencode(path), ctypes.byref(ra), ctypes.byref(dec), ctypes.byref(n), err, 512)
+    if rc != ACF_OK:
+        raise AcfError(rc, err.value.decode())
+    try:
+        out = (np.ctypeslib.as_array(ra, shape=(n.value,)).copy() if n.value else np.empty(0, np.float32),
+               np.ctypeslib.as_array(dec, shape=(n.value,)).copy() if n.value else np.empty(0, np.float32))
+    finally:
+        lib.acf_free_catalog(ctypes.cast(ra, ctypes.c_void_p), ctypes.cast(dec, ctypes.c_void_p))
+    return out
+
+
+def acf_write_omega(path: str, dd, dr, rr, omega, bin_width_deg: float) -> None:
+    """Write the result table (one row per bin with RR > 0) from host arrays."""
+    dd, dr, rr = (np.ascontiguousarray(a, dtype=np.uint64) for a in (dd, dr, rr))
+    omega = np.ascontiguousarray(omega, dtype=np.float64)
+    rc = load().acf_write_omega(os.fsencode(path), dd.ctypes.data, dr.ctypes.data, rr.ctypes.data, omega.ctypes.data,
+                                len(dd), float(bin_width_deg))
+    if rc != ACF_OK:
+        raise AcfError(rc, "cannot write " + str(path))
+
+
+def cli_path() -> str:
+    """The acf_cli program (catalog files in, omega table out), built next to the library."""
+    return _build.build_cli()
 
 
 # ------------------------------------------------------------- convenience layer

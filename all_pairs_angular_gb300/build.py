@@ -1,4 +1,4 @@
-"""Build libacf.so in-tree for sm_103a with nvcc (one translation unit, no cmake)."""
+"""Build libacf.so in-tree for sm_103a with nvcc (no cmake), and the acf_cli program on top of it."""
 from __future__ import annotations
 
 import os
@@ -10,8 +10,11 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libacf.so")
 DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libacf_debug.so")  # -DACF_DEBUG_BOUNDS
-SOURCES = [os.path.join(HERE, "csrc", "acf.cu")]
+SOURCES = [os.path.join(HERE, "csrc", "acf.cu"), os.path.join(HERE, "csrc", "acf_io.cpp")]
+CLI_SOURCE = os.path.join(HERE, "csrc", "acf_cli.cpp")
+CLI_PATH = os.path.join(BUILD_DIR, "acf_cli")
 DEPENDS = SOURCES + [os.path.join(HERE, "csrc", "acf_kernels.cuh"), os.path.join(ROOT, "include", "acf.h")]
+# (acf_cli.cpp includes the header by path: build_cli passes -I include)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,6 +47,25 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
         print(res.stdout + res.stderr)
     os.replace(tmp, path)
     return path
+
+
+def build_cli(force: bool = False) -> str:
+    """Compile acf_cli (host C++, linked against libacf.so in the same folder) and return its path."""
+    lib = build()
+    if not force and os.path.exists(CLI_PATH) and os.path.getmtime(CLI_PATH) >= max(
+            os.path.getmtime(lib), os.path.getmtime(CLI_SOURCE)):
+        return CLI_PATH
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if not cxx:
+        raise RuntimeError("no C++ compiler for acf_cli")
+    tmp = CLI_PATH + ".tmp%d" % os.getpid()
+    cmd = [cxx, "-O2", "-std=c++17", "-I", os.path.join(ROOT, "include"), CLI_SOURCE, "-o", tmp, "-L", BUILD_DIR,
+           "-lacf", "-Wl,-rpath,$ORIGIN"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("acf_cli failed to build:\n" + res.stdout + res.stderr)
+    os.replace(tmp, CLI_PATH)
+    return CLI_PATH
 
 
 if __name__ == "__main__":

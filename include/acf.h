@@ -214,6 +214,28 @@ int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
 int acf_kernel_times(acf_ctx *ctx, float *ms, int32_t cap, int32_t *count);
 
 /*
+ * Catalog files and the result table, in the formats of the page's program (sections "mmap +
+ * hand-rolled parser vs. fscanf" and its output step). Host code; no context, no GPU needed.
+ *
+ * acf_read_catalog: read an ASCII catalog (the galaxy count, then that many "ra dec" pairs in
+ * arcminutes, separated by any whitespace). On success *ra and *dec receive malloc'ed host arrays
+ * of *n floats (free them with acf_free_catalog). Numbers are parsed with correct rounding to
+ * float. A missing file, a bad count or fewer pairs than the count give ACF_ERR_ARG with a message
+ * (line number) in err[err_len] (nullable); nothing is allocated then.
+ */
+int acf_read_catalog(const char *path, float **ra, float **dec, int64_t *n, char *err, int32_t err_len);
+void acf_free_catalog(float *ra, float *dec);
+
+/*
+ * acf_write_omega: write the result table: a header line, then for every bin k with rr[k] > 0 one
+ * tab-separated row "bin start (degrees, k * bin_width_deg, %6.3f)  omega (%15f)  DD  DR  RR".
+ * Host arrays of nbins values. ACF_ERR_ARG if an argument is invalid or the file cannot be
+ * written.
+ */
+int acf_write_omega(const char *path, const uint64_t *dd, const uint64_t *dr, const uint64_t *rr,
+                    const double *omega, int32_t nbins, double bin_width_deg);
+
+/*
  * Measure the FP32 issue ceiling of this GPU, the denominator of the pair kernel's roofline
  * (independent FMA chains, the method of the "roofline.cu" page's compute ceiling): one timed
  * launch of 2 blocks of 1024 threads per SM, each thread running 8 independent fmaf chains
