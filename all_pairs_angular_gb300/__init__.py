@@ -26,7 +26,7 @@ ACF_ERR_CUDA = -4
 EXPORTED = ["acf_version", "acf_create", "acf_destroy", "acf_last_error", "acf_set_stream", "acf_histogram",
             "acf_omega", "acf_correlate", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
             "acf_kernel_times", "acf_histogram_noalloc", "acf_fp32_peak", "acf_read_catalog", "acf_free_catalog",
-            "acf_write_omega"]
+            "acf_write_omega", "acf_ladder"]
 
 _lib = None
 
@@ -76,6 +76,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                   ctypes.c_char_p, i32]),
         "acf_free_catalog": (None, [vp, vp]),
         "acf_write_omega": (ci, [ctypes.c_char_p, vp, vp, vp, vp, i32, f64]),
+        "acf_ladder": (ci, [ci, vp, vp, vp, vp, i64, f64, i32, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,6 +215,18 @@ def acf_write_omega(path: str, dd, dr, rr, omega, bin_width_deg: float) -> None:
                                 len(dd), float(bin_width_deg))
     if rc != ACF_OK:
         raise AcfError(rc, "cannot write " + str(path))
+
+
+def acf_ladder(level: int, ra_d, dec_d, ra_r, dec_r, bin_width_deg: float, nbins: int, dd, dr, rr,
+               stream=None) -> float:
+    """One level of the page's optimisation ladder on device catalogs; returns the kernel's ms."""
+    ms = ctypes.c_float()
+    rc = load().acf_ladder(int(level), _ptr(ra_d), _ptr(dec_d), _ptr(ra_r), _ptr(dec_r), ra_d.numel(),
+                           float(bin_width_deg), int(nbins), _ptr(dd), _ptr(dr), _ptr(rr),
+                           getattr(stream, "cuda_stream", stream), ctypes.byref(ms))
+    if rc != ACF_OK:
+        raise AcfError(rc, "acf_ladder level %d failed" % level)
+    return ms.value
 
 
 def cli_path() -> str:

@@ -10,7 +10,8 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libacf.so")
 DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libacf_debug.so")  # -DACF_DEBUG_BOUNDS
-SOURCES = [os.path.join(HERE, "csrc", "acf.cu"), os.path.join(HERE, "csrc", "acf_io.cpp")]
+SOURCES = [os.path.join(HERE, "csrc", "acf.cu"), os.path.join(HERE, "csrc", "acf_io.cpp"),
+           os.path.join(HERE, "csrc", "ladder.cu")]
 CLI_SOURCE = os.path.join(HERE, "csrc", "acf_cli.cpp")
 CLI_PATH = os.path.join(BUILD_DIR, "acf_cli")
 DEPENDS = SOURCES + [os.path.join(HERE, "csrc", "acf_kernels.cuh"), os.path.join(ROOT, "include", "acf.h")]

@@ -233,6 +233,10 @@ PairKernelFn pick_kernel(const Plan& pl) {
   ACF_PICK(1024, kBlock, kClamp, kDotAcos)
   ACF_PICK(512, kLane, kClamp, kDotAcos)
   ACF_PICK(512, kBlock, kClamp, kDotAcos)
+  ACF_PICK(1024, kLane, kClamp, kDotFastAcos)
+  ACF_PICK(1024, kBlock, kClamp, kDotFastAcos)
+  ACF_PICK(512, kLane, kClamp, kDotFastAcos)
+  ACF_PICK(512, kBlock, kClamp, kDotFastAcos)
 #undef ACF_PICK
   return nullptr;
 }
@@ -693,7 +697,10 @@ int acf_pair_bins(acf_ctx* c, const float* ra1, const float* dec1, const float* 
   ACF_CUDA(c, cudaSetDevice(c->device));
   const int threads = 256;
   const long long blocks = std::min<long long>((n + threads - 1) / threads, (long long)c->num_sms * 32);
-  if (pl.method == kDotAcos)
+  if (pl.method == kDotFastAcos)
+    pair_bins_kernel<kClamp, kDotFastAcos><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp,
+                                                                                      c->opt_pair_bins_form, bins);
+  else if (pl.method == kDotAcos)
     pair_bins_kernel<kClamp, kDotAcos><<<(unsigned)blocks, threads, 0, c->stream>>>(ra1, dec1, ra2, dec2, n, pl.bp,
                                                                                   c->opt_pair_bins_form, bins);
   else if (pl.map == kDirect)
@@ -715,7 +722,7 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
     if (v < 0 || v > 8) return fail(c, ACF_ERR_ARG, "ctas_per_sm must be 0..8");
     c->opt_ctas = (int)v;
   } else if (!strcmp(key, "bin_method")) {
-    if (v != kChordPoly && v != kDotAcos) return fail(c, ACF_ERR_ARG, "bin_method must be 0 or 1");
+    if (v != kChordPoly && v != kDotAcos && v != kDotFastAcos) return fail(c, ACF_ERR_ARG, "bin_method must be 0, 1 or 2");
     c->opt_method = (int)v;
   } else if (!strcmp(key, "layout")) {
     if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "layout must be 0, 1 or 2");

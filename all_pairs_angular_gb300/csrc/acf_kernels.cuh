@@ -62,7 +62,19 @@ constexpr float kMagic = 8388608.0f;  // 2^23: adding it with round-toward-zero 
 
 enum Layout { kLane = 1, kBlock = 2 };
 enum BinMap { kDirect = 0, kClamp = 1 };
-enum Method { kChordPoly = 0, kDotAcos = 1 };
+enum Method { kChordPoly = 0, kDotAcos = 1, kDotFastAcos = 2 };
+
+// arccos(x) for x in [0, 1] as sqrt(1 - x) (a0 + a1 x + a2 x^2 + a3 x^3): Abramowitz and Stegun,
+// Handbook of Mathematical Functions, formula 4.4.45 (|error| <= 6.7e-5 rad), extended to
+// [-1, 0) by arccos(-x) = pi - arccos(x). The approximate mode: fast, not held to the 1e-6 rule.
+__device__ __forceinline__ float acos_as4445(float x) {
+  const float ax = fabsf(x);
+  float r = fmaf(-0.0187293f, ax, 0.0742610f);
+  r = fmaf(r, ax, -0.2121144f);
+  r = fmaf(r, ax, 1.5707288f);
+  r *= sqrtf(1.0f - ax);
+  return x < 0.0f ? 3.14159265358979f - r : r;
+}
 
 // theta'^2 = q * P(q) for a chord q = |u - v|^2 on [0, 2] (theta' <= 90 degrees), P of degree 7
 // fitted by fit_arcsin2.py: absolute theta' error <= 1.8e-8 rad (2.5e-8 after fp32 rounding).
@@ -498,9 +510,11 @@ template <int MAP, int METHOD, bool FINE = false>
 __device__ __forceinline__ float pair_code(float xi, float yi, float zi, float xj, float yj, float zj,
                                            const BinParams& bp) {
   const float d = fmaf(zi, zj, fmaf(yi, yj, xi * xj));
-  if (METHOD == kDotAcos) {
-    // the page's route: arccos of the (clamped) cosine, scaled by 1/w and truncated
-    const float t = acosf(fminf(fmaxf(d, -1.0f), 1.0f)) * bp.inv_w;
+  if (METHOD == kDotAcos || METHOD == kDotFastAcos) {
+    // the page's route: arccos of the (clamped) cosine, scaled by 1/w and truncated; acosf, or the
+    // polynomial of the approximate mode
+    const float c = fminf(fmaxf(d, -1.0f), 1.0f);
+    const float t = (METHOD == kDotAcos ? acosf(c) : acos_as4445(c)) * bp.inv_w;
     return add_rz(fminf(t, bp.clamp_c), kMagic);
   } else {
     const uint32_t db = __float_as_uint(d);

@@ -363,6 +363,95 @@ def run_profile(args, cat):
     return 0 if sums == [cat.n_d ** 2, cat.n_d * cat.n_r, cat.n_r ** 2] else 1
 
 
+# The page's kernel times per ladder level on its RTX 5080 (section "The ladder"): context only.
+PAGE_LADDER_MS = {0: 188.653, 1: 169.209, 2: 163.435, 3: 34.027, 4: 24.528, 5: 22.747}
+ABLATION_VARIANTS = [
+    ("default (exact 2, range forms)", {}),
+    ("exact mode 1 (re-decide within 20 deg of 0 and 180)", {"exact": 1}),
+    ("exact mode 0 (fp32 bins only)", {"exact": 0}),
+    ("range forms off (full-range chord for every pair), exact 2", {"range_forms": 0}),
+    ("range forms off, exact 0", {"range_forms": 0, "exact": 0}),
+    ("dot product + acosf (the page's form)", {"bin_method": 1}),
+    ("dot product + A&S 4.4.45 arccos (approximate mode)", {"bin_method": 2}),
+    ("one block-shared histogram instead of 32 lane copies", {"layout": 2}),
+    ("512 threads per block", {"threads": 512}),
+]
+
+
+def run_ablation(args, cat) -> int:
+    """The page's optimisation ladder rebuilt on this GPU, then one change at a time from this
+    library's default, all on one workload: pair-kernel time and what each does to the counts
+    against the oracle's (tests/golden, for the workloads that have a golden file)."""
+    import statistics
+
+    import torch
+
+    import all_pairs_angular_gb300 as acf
+
+    dev = torch.device("cuda", 0)
+    w, nb = cat.bin_width_deg, cat.nbins
+    t = {k: torch.from_numpy(getattr(cat, k)).to(dev) for k in ("ra_d", "dec_d", "ra_r", "dec_r")}
+    gold = None
+    gpath = os.path.join(ROOT, "tests", "golden", f"config{args.config}_oracle.json")
+    if os.path.exists(gpath):
+        with open(gpath) as f:
+            g = json.load(f)
+        if g.get("digest") == cat.digest():
+            gold = g
+
+    def compare(hs):
+        if gold is None:
+            return {}
+        moved = {}
+        for fam, h in zip(("DD", "DR", "RR"), hs):
+            ref = np.array(gold[fam]["hist"], np.int64)
+            moved[fam] = int(np.abs(np.cumsum(h.astype(np.int64) - ref)).sum())
+        rr = np.array(gold["RR"]["hist"], np.float64)
+        nd2, ndr, nr2 = float(cat.n_d) ** 2, float(cat.n_d) * cat.n_r, float(cat.n_r) ** 2
+        with np.errstate(invalid="ignore", divide="ignore"):
+            om = (hs[0] / nd2 - 2.0 * hs[1] / ndr + hs[2] / nr2) / (hs[2] / nr2)
+        ref_om = np.array([np.nan if x is None else x for x in gold["omega"]])
+        big = rr >= 1000
+        return {"moved_pairs": moved, "max_abs_domega_rr_ge_1000": float(np.nanmax(np.abs(om[big] - ref_om[big])))}
+
+    rows = []
+    evaluated = cat.n_d * cat.n_r + cat.n_d * (cat.n_d + 1) // 2 + cat.n_r * (cat.n_r + 1) // 2
+    if cat.n_d == cat.n_r:
+        for level in range(6):
+            hs = [torch.empty(nb, dtype=torch.int64, device=dev) for _ in range(3)]
+            times = [acf.acf_ladder(level, t["ra_d"], t["dec_d"], t["ra_r"], t["dec_r"], w, nb, *hs)
+                     for _ in range(3 if level < 3 else 5)]
+            ms = statistics.median(times[1:])
+            pairs = 3 * cat.n_d * cat.n_d if level == 0 else evaluated
+            rows.append({"row": f"page ladder L{level}", "kernel_ms": ms, "evaluated_gpairs_per_s": pairs / ms / 1e6,
+                         "page_rtx5080_ms": PAGE_LADDER_MS[level], **compare([acf.as_uint64(h) for h in hs])})
+            print(json.dumps(rows[-1]), flush=True)
+    for name, opts in ABLATION_VARIANTS:
+        ctx = acf.Context(0)
+        for k, v in opts.items():
+            ctx.set_option(k, v)
+        ctx.set_option("kernel_timing", 1)
+        out = None
+        step_ms = []
+        for rep in range(4):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            out = ctx.correlate(t["ra_d"], t["dec_d"], t["ra_r"], t["dec_r"], w, nb)
+            e1.record()
+            torch.cuda.synchronize()
+            if rep:
+                step_ms.append(e0.elapsed_time(e1))
+        kt = ctx.kernel_times()
+        pair_ms = sum(kt[len(kt) // 4:]) / 3.0  # the last three of four steps
+        hs = [acf.as_uint64(h) for h in out[:3]]
+        rows.append({"row": name, "options": opts, "step_ms": statistics.median(step_ms), "pair_kernels_ms": pair_ms,
+                     "logical_gpairs_per_s": logical_pairs(cat.n_d, cat.n_r) / statistics.median(step_ms) / 1e6,
+                     **compare(hs)})
+        print(json.dumps(rows[-1]), flush=True)
+        ctx.close()
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -373,6 +462,8 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-rows", type=int, default=2000, help="rows per family for the CPU baseline (0: skip)")
     ap.add_argument("--ref-rows", type=int, default=200, help="rows per family per reference-arm step")
     ap.add_argument("--profile", action="store_true", help="one warm-up step + one step only (for ncu)")
+    ap.add_argument("--ablation", action="store_true",
+                    help="the page's ladder and one-change variants of the library, timed and checked")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -387,6 +478,8 @@ def main(argv=None) -> int:
                 f"R {cat.n_r} uniform, {cat.nbins} bins of {cat.bin_width_deg} deg, seed {cat.seed}")
     if args.profile:
         return run_profile(args, cat)
+    if args.ablation:
+        return run_ablation(args, cat)
     try:
         if args.impl == "reference":
             return run_reference(args, cat, workload, rank, world)

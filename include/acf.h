@@ -166,7 +166,10 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *   "ctas_per_sm"    resident blocks per SM to launch (default: occupancy maximum)
  *   "bin_method"     0 = chord + arcsin^2 polynomial (default, meets the precision contract);
  *                    1 = dot product + acosf (the page's exact-acos form; measured alternative,
- *                        does NOT meet the precision contract at small or near-180 separations)
+ *                        does NOT meet the precision contract at small or near-180 separations);
+ *                    2 = dot product + the arccos polynomial of Abramowitz and Stegun 4.4.45 (the
+ *                        approximate mode: error up to 6.7e-5 rad, so many pairs near edges move;
+ *                        sums stay exact). Methods 1 and 2 take no exact mode and no range forms.
  *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram
  *   "exact"          0 = fp32 bins only (precision contract above);
  *                    1 = re-decide in fp64 the pairs within ~1e-6 rad of an edge whose separation is
@@ -234,6 +237,23 @@ void acf_free_catalog(float *ra, float *dec);
  */
 int acf_write_omega(const char *path, const uint64_t *dd, const uint64_t *dr, const uint64_t *rr,
                     const double *omega, int32_t nbins, double bin_width_deg);
+
+/*
+ * The optimisation ladder of the page (section "The ladder", levels 0 to 5: one thread per pair;
+ * + DD/RR symmetry; + per-galaxy sin/cos; + shared-memory j-tiles; + arccos polynomial; + unroll,
+ * launch bounds and whole-block diagonal skip), rebuilt for this GPU as a measurement of each step.
+ * Not the library's path: fp32 acos misbins near-edge pairs, level 4 and 5 by design; totals stay
+ * exact. Levels 1 to 3 give identical histograms, as do 4 and 5.
+ *   level        0..5
+ *   ra_d, dec_d, ra_r, dec_r  device float[n] (arcminutes), both catalogs of the same size n
+ *   dd, dr, rr   device uint64[nbins], overwritten;  nbins <= 4000
+ *   stream       cudaStream_t (NULL: legacy default stream)
+ *   kernel_ms    (nullable) host: the histogram kernel's time from CUDA events
+ * Synchronous (waits for its stream). Allocates a small scratch buffer (stream-ordered).
+ */
+int acf_ladder(int level, const float *ra_d, const float *dec_d, const float *ra_r, const float *dec_r, int64_t n,
+               double bin_width_deg, int32_t nbins, uint64_t *dd, uint64_t *dr, uint64_t *rr, void *stream,
+               float *kernel_ms);
 
 /*
  * Measure the FP32 issue ceiling of this GPU, the denominator of the pair kernel's roofline

@@ -420,3 +420,26 @@ def test_fp32_ceiling_probe_runs_the_arithmetic(acf, ctx):
     for c in range(8):
         s = np.float32(s + x[c])
     assert np.float32(t0) == s
+
+
+def test_approximate_mode_keeps_totals_and_stays_near_the_edges(acf, ctx):
+    # bin_method 2: dot product + the Abramowitz-Stegun 4.4.45 arccos polynomial (error <= 6.7e-5
+    # rad plus fp32 dot-product error): totals exact, and every moved pair lies within 5e-4 rad of
+    # an edge it crossed
+    c = synth.catalogs(3000, 2500, 10, 30.0, seed=43)
+    ctx.set_option("bin_method", 2)
+    try:
+        g = acf.as_uint64(ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720))
+        ra1, dec1 = synth.uniform_sphere(200_000, 77)
+        ra2, dec2 = synth.uniform_sphere(200_000, 78)
+        gb = ctx.pair_bins(ra1, dec1, ra2, dec2, 0.25, 720).cpu().numpy()
+        torch.cuda.synchronize()
+    finally:
+        ctx.set_option("bin_method", 0)
+    assert int(g.sum()) == 3000 * 2500
+    ob = oracle.pair_bin(ra1, dec1, ra2, dec2, 0.25, 720)
+    th = oracle.pair_theta(ra1, dec1, ra2, dec2)
+    bad = np.nonzero(gb != ob)[0]
+    assert len(bad) > 0 and np.all(np.abs(gb[bad] - ob[bad]) == 1)
+    edge = np.maximum(gb[bad], ob[bad]) * math.radians(0.25)
+    assert float(np.abs(th[bad] - edge).max()) < 5e-4
