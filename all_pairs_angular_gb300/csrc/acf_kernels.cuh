@@ -91,11 +91,13 @@ __device__ constexpr float kS0 = 0.99999908438480867f, kS1 = 0.08335094100319942
 constexpr float kSmallRad = 1.2566370614359172f;  // 72 degrees
 
 // Between 55 and 125 degrees the dot product d = u.v loses little: theta = pi/2 - asin(d) with
-// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(53 deg), degree 5: absolute
-// theta error <= 2.1e-8 rad (3.3e-8 after fp32 rounding). Scaled by 1/w on the host.
-constexpr int kRTerms = 6;
-constexpr double kR[kRTerms] = {0.99999956256812916,  0.16669876877905515,   0.07433148849621074,
-                                0.050509827344902551, 0.0062717738364129879, 0.065395572657082512};
+// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(53 deg), degree 4: absolute
+// theta error <= 2.4e-7 rad (2.7e-7 after fp32 rounding), within the exact mode's window; a higher
+// degree would cost one more instruction per pair on nearly half the pairs. Scaled by 1/w on the
+// host.
+constexpr int kRTerms = 5;
+constexpr double kR[kRTerms] = {1.0000042503922144, 0.16644559569653503, 0.07818303909030544,
+                                0.026501255145352308, 0.071919159378340883};
 constexpr float kMidRad = 0.95993108859688125f;  // groups whose separations all lie in (55, 125) degrees use the dot form
 
 // Every code is the float 2^23 + (histogram entry), entry = floor(theta / w) (direct map, where
@@ -647,15 +649,14 @@ __device__ __forceinline__ float pair_code_fixed2(float xi, float yi, float zi, 
 // theta / w = P/2 - d R(d^2) / w, floored exactly by one fma rounded toward zero onto 2^23 + P/2
 // (the product of the two fp32 operands enters unrounded). Worst-case theta error: d carries
 // <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 2.7e-7 rad where sin theta >=
-// sin 53 deg, plus <= 1e-7 from the polynomial and its rounding.
+// sin 53 deg, plus <= 3.4e-7 from the polynomial and its rounding: <= 6.1e-7 in all.
 template <bool FINE = false>
 __device__ __forceinline__ float pair_code_mid(float xi, float yi, float zi, float xj, float yj, float zj,
                                                const BinParams& bp) {
 #define ACF_RC(k) (FINE ? bp.rc_f[k] : bp.rc[k])
   const float d = fmaf(zi, zj, fmaf(yi, yj, xi * xj));
   const float t = d * d;
-  float p = fmaf(ACF_RC(5), t, ACF_RC(4));
-  p = fmaf(p, t, ACF_RC(3));
+  float p = fmaf(ACF_RC(4), t, ACF_RC(3));
   p = fmaf(p, t, ACF_RC(2));
   p = fmaf(p, t, ACF_RC(1));
   p = fmaf(p, t, ACF_RC(0));
