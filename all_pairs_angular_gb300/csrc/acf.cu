@@ -160,27 +160,40 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   }
   bp.small = c->opt_range_forms ? 1 : 0;
   // Exact mode: S fractional bits in the bin code make a window of 2^-S bins around every edge,
-  // wider than the fp32 path's error there (3.5e-7 rad near 0 and 180 degrees, 8e-7 rad anywhere).
+  // wider than the fp32 path's error there.
   pl.exact = (pl.method == kChordPoly) ? c->opt_exact : 0;
   pl.exact_lo = (float)(c->opt_exact_below_deg * pi / 180.0);
   if (pl.exact) {
-    // bound on the fp32 path's error: vectors 1.2e-7 plus terms that grow with the separation, up
-    // to 8e-7 rad near 90 degrees; mode 1 only re-decides separations within exact_lo of 0 or 180
-    const double zone = std::min(1.0, c->opt_exact_below_deg / 90.0);
-    const double err = (pl.exact == 2) ? 8e-7 : 1.5e-7 + 6.5e-7 * zone;
-    int S = (int)std::floor(std::log2(w_rad / err));
+    // Worst-case fp32 error of each form (every rounding aligned): the full-range chord <= 1.25e-6
+    // rad (near 90 degrees), the short chord (theta' <= 72 deg) <= 1.05e-6, the dot form (55..125
+    // deg) <= 7e-7. Mode 1 only re-decides separations within exact_lo of 0 or 180 degrees, where
+    // the chord's error is err1(lo) (vectors, chord rounding ~ tan(theta'/2), polynomial, sqrt and
+    // 1/w ~ theta'). Each form's S is the largest whose window 2^-S bins covers its bound.
+    const double lo = std::min(c->opt_exact_below_deg, 90.0) * pi / 180.0;
+    const double err1 = 1.2e-7 / std::cos(lo / 2) + 6e-7 * std::tan(lo / 2) + 5e-8 + 3.5e-7 * lo;
+    const double err_full = (pl.exact == 2) ? 1.25e-6 : err1;
+    const double err_small = (pl.exact == 2) ? 1.05e-6 : err1;
+    const double err_mid = (pl.exact == 2) ? 7e-7 : err1;
     const int room = (int)std::floor(std::log2(8.0e6 / ((double)bp.entries + 2.0)));  // (entries+2) << S < 2^23
-    S = std::max(0, std::min(S, room));
+    auto shift_for = [&](double err) {
+      return std::max(0, std::min((int)std::floor(std::log2(w_rad / err)), room));
+    };
+    const int S = shift_for(err_full), Ss = shift_for(err_small), Sm = shift_for(err_mid);
     bp.fine_shift = S;
+    bp.fine_shift_small = Ss;
+    bp.fine_shift_mid = Sm;
     bp.inv_w_f = (float)(std::ldexp(1.0, S) / w_rad);
+    bp.inv_w_fs = (float)(std::ldexp(1.0, Ss) / w_rad);
     // fine codes carry a bias of one fine unit (see BinParams)
     bp.magic_f = 8388609.0f;
     if (pl.map == kDirect) {
       bp.magic_far_f = (float)(8388609.0 + std::ldexp(pr, S));
-      bp.magic_mid_f = (float)(8388609.0 + std::ldexp(pr / 2.0, S));
-      for (int k = 0; k < kRTerms; ++k) bp.rc_f[k] = (float)(std::ldexp(kR[k], S) / w_rad);
+      bp.magic_far_fs = (float)(8388609.0 + std::ldexp(pr, Ss));
+      bp.magic_mid_f = (float)(8388609.0 + std::ldexp(pr / 2.0, Sm));
+      for (int k = 0; k < kRTerms; ++k) bp.rc_f[k] = (float)(std::ldexp(kR[k], Sm) / w_rad);
     }
     bp.clamp_f = (float)std::ldexp((double)bp.clamp_c + 0.5, S);
+    bp.clamp_fs = (float)std::ldexp((double)bp.clamp_c + 0.5, Ss);
   }
   bp.kmax = (int)std::min<double>((double)nbins - 1.0, std::floor(P + 1e-9));
   // exact zone, as histogram entries: everything (mode 2), or separations within exact_lo of
@@ -490,7 +503,8 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
 }
 
 // Exact-mode queue slots for a histogram of `units` work units: every computed pair may be flagged
-// with probability ~2^(1-S); twice that, within bounds.
+// with probability up to 2^(1-S) (S of the full-range chord, the smallest); twice that, within
+// bounds. Overflow is not an error: those pairs keep their fp32 bin, and "exact_overflow" counts them.
 long long queue_slots(const Plan& pl, long long units) {
   // the queue is drained after every launch: it holds one launch's flagged pairs
   if (!pl.exact) return 0;

@@ -55,6 +55,9 @@ constexpr int kJJBatch = ACF_JJ_BATCH;
 #define ACF_JJ_BATCH_FINE 1
 #endif
 constexpr int kJJBatchFine = ACF_JJ_BATCH_FINE;  // the same for the exact-mode (flagging) loops
+#ifndef ACF_J_SHUFFLE
+#define ACF_J_SHUFFLE 0  // 1: j-vectors broadcast by warp shuffles instead of shared-memory loads
+#endif
 #ifndef ACF_ASM_LOP3
 #define ACF_ASM_LOP3 1  // write the two sign-bit logic ops as explicit lop3 (2 ops, not 3)
 #endif  // j-loop unroll of the full-chunk path
@@ -105,18 +108,25 @@ constexpr float kMidRad = 0.95993108859688125f;  // groups whose separations all
 struct BinParams {
   float magic_far;    // direct: 2^23 + P, the far-side (theta > 90 deg) constant of the chord form
   float magic_mid;    // direct, P even: 2^23 + P/2, the constant of the dot form
+  // Exact mode: each form has its own S, so that its window (2^-S bins) covers its own error bound:
+  // S (full-range and general chord, clamp map, masked units), S_small (short chord), S_mid (dot).
   float inv_w_f;      // exact mode: 2^S / w (fine code with S fractional bits)
+  float inv_w_fs;     // exact mode: 2^S_small / w
+  float magic_far_fs; // exact mode: 2^23 + P 2^S_small + 1
+  float clamp_fs;     // exact mode: (clamp_c + 0.5) * 2^S_small (clamp map)
   // The fine code is biased by one fine unit (every fine constant carries + 1), so a pair lies
   // within one fine unit of an edge exactly when its low S bits are 0 or 1.
   float magic_f;      // exact mode: 2^23 + 1
   float magic_far_f;  // exact mode: 2^23 + P 2^S + 1
-  float magic_mid_f;  // exact mode: 2^23 + (P/2) 2^S + 1
+  float magic_mid_f;  // exact mode: 2^23 + (P/2) 2^S_mid + 1
   float clamp_f;      // exact mode: (clamp_c + 0.5) * 2^S (clamp map)
   float rc[kRTerms];   // dot form: kR[k] / w
-  float rc_f[kRTerms]; // exact mode: kR[k] 2^S / w
+  float rc_f[kRTerms]; // exact mode: kR[k] 2^S_mid / w
   int mid;            // 1: groups between 55 and 125 degrees use the dot form
   int small;          // 1: groups whose theta' stays below 72 degrees use the degree-5 chord polynomial
   int fine_shift;     // exact mode: S
+  int fine_shift_small;  // exact mode: S_small
+  int fine_shift_mid;    // exact mode: S_mid
   int kmax;           // exact mode: highest bin a separation <= 180 degrees can reach
   unsigned int zone0, span0, zone1, span1;  // exact mode: entries e with e - zone <= span (unsigned) are re-decided
   float clamp_c;      // largest index (clamp map)
@@ -641,7 +651,7 @@ __device__ __forceinline__ float pair_code_fixed2(float xi, float yi, float zi, 
     const float t = fmaf(th, iws, h);
     const float tf = fmaf(th, iws_f, h_f);
     coarse = __float_as_uint(add_rz(fminf(t, bp.clamp_c), kMagic));
-    return add_rz(fminf(tf, bp.clamp_f), bp.magic_f);
+    return add_rz(fminf(tf, SMALL ? bp.clamp_fs : bp.clamp_f), bp.magic_f);
   }
 }
 
@@ -649,7 +659,7 @@ __device__ __forceinline__ float pair_code_fixed2(float xi, float yi, float zi, 
 // theta / w = P/2 - d R(d^2) / w, floored exactly by one fma rounded toward zero onto 2^23 + P/2
 // (the product of the two fp32 operands enters unrounded). Worst-case theta error: d carries
 // <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 2.7e-7 rad where sin theta >=
-// sin 53 deg, plus <= 3.4e-7 from the polynomial and its rounding: <= 6.1e-7 in all.
+// sin 53 deg, plus <= 4.3e-7 from the polynomial, its rounding and its scaling: <= 7e-7 in all.
 template <bool FINE = false>
 __device__ __forceinline__ float pair_code_mid(float xi, float yi, float zi, float xj, float yj, float zj,
                                                const BinParams& bp) {
@@ -751,14 +761,14 @@ struct FormTag {
 // A pair at one fine unit below an edge is counted one entry up; the fp64 re-decision moves it.
 template <bool F>
 __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint32_t base, uint32_t base_f, int shift,
-                                         uint32_t magic_bits, int i, int j, float xi, float yi, float zi, float4 v) {
+                                         int S, uint32_t magic_bits, int i, int j, float xi, float yi, float zi,
+                                         float4 v) {
   if (!F) {
     if (ACF_CHECK(cb - magic_bits < (uint32_t)p.bp.entries, 1, (long long)(cb - magic_bits), i,
                   __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
       red_shared_add((cb << shift) + base, p.inc);
     return false;
   } else {
-    const int S = p.bp.fine_shift;
     if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i,
                   __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
       red_shared_add(((cb >> S) << shift) + base_f, p.inc);
@@ -807,11 +817,10 @@ __device__ __noinline__ void push_flagged_call(QueueArgs q, uint32_t cb, uint32_
 #ifndef ACF_PUSH_NOINLINE
 #define ACF_PUSH_NOINLINE 0
 #endif
-__device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, uint32_t magic_bits, int i, int j,
+__device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, int S, uint32_t magic_bits, int i, int j,
                                              unsigned int* s_qcount, uint32_t base_f, int shift) {
-  const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc,
-                    p.bp.fine_shift};
-  const uint32_t e_cnt = (cb - magic_bits) >> p.bp.fine_shift;
+  const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc, S};
+  const uint32_t e_cnt = (cb - magic_bits) >> S;
   if (ACF_PUSH_NOINLINE) push_flagged_call(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
   else push_flagged_body(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
 }
@@ -906,6 +915,8 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   // exact mode: the fine code is 2^23 + (entry << S) + fraction; entry = (bits >> S) - (bits(2^23) >> S)
   const uint32_t base_f = (LAYOUT == kLane) ? hist_addr + lane * 4u - ((magic_bits >> p.bp.fine_shift) << 7)
                                             : hist_addr - ((magic_bits >> p.bp.fine_shift) << 2);
+  const uint32_t base_fm = (LAYOUT == kLane) ? hist_addr + lane * 4u - ((magic_bits >> p.bp.fine_shift_mid) << 7)
+                                             : hist_addr - ((magic_bits >> p.bp.fine_shift_mid) << 2);
   const int ni = (int)p.ni, nj = (int)p.nj;
 
   // tickets: the unit being computed (u), the one whose tile is in flight (un), and one fetched
@@ -996,6 +1007,18 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           // the general and the full-range fixed chord loops are rare once the caps pick the dot form
           // across 90 degrees and the short chord below 72: rolled
           constexpr int U = (F || X == 0 || X == 1) ? kJJUnrollFine : kJJUnroll;
+          // j-vector jj of this group: a shared-memory broadcast, or (measured alternative) one
+          // vector per lane held in registers and broadcast by three shuffles
+#if ACF_J_SHUFFLE
+          const float4 vl = tile[jbeg + lane];
+          auto jvec = [&](int jj) -> float4 {
+            const int src = jj - jbeg;
+            return make_float4(__shfl_sync(0xffffffffu, vl.x, src), __shfl_sync(0xffffffffu, vl.y, src),
+                               __shfl_sync(0xffffffffu, vl.z, src), 0.0f);
+          };
+#else
+          auto jvec = [&](int jj) -> float4 { return tile[jj]; };
+#endif
           auto code_of = [&](int k, float4 v) -> uint32_t {
             return __float_as_uint(
                 X == 2   ? pair_code_mid<F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp)
@@ -1003,14 +1026,17 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                 : X == 1 ? pair_code_fixed<MAP, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h, p.bp)
                          : pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
           };
+          // this form's fine shift, and the histogram base of its fine code (single-code loops)
+          const int SF = X == 2 ? p.bp.fine_shift_mid : (X == 3 ? p.bp.fine_shift_small : p.bp.fine_shift);
+          const uint32_t bf = X == 2 ? base_fm : base_f;
+          const uint32_t fmask = (1u << SF) - 1u;
           constexpr int B = F ? kJJBatchFine : kJJBatch;
           if constexpr ((F || U > 1) && B > 1) {
-            const uint32_t fmask = (1u << p.bp.fine_shift) - 1u;
 #pragma unroll 1
             for (int jj = jbeg; jj < jbeg + 32; jj += B) {
               float4 vv[B];
 #pragma unroll
-              for (int u = 0; u < B; ++u) vv[u] = tile[jj + u];
+              for (int u = 0; u < B; ++u) vv[u] = jvec(jj + u);
               uint32_t cb[B * K];
 #pragma unroll
               for (int u = 0; u < B; ++u)
@@ -1021,7 +1047,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               for (int u = 0; u < B; ++u)
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
-                  add_pair<F>(p, cb[u * K + k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
+                  add_pair<F>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
                               xi[k], yi[k], zi[k], vv[u]);
                   if (F) low = min(low, cb[u * K + k] & fmask);
                 }
@@ -1033,27 +1059,26 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                   uint32_t c = cb[0];
 #pragma unroll
                   for (int q = 1; q < B * K; ++q) c = (t == q) ? cb[q] : c;
-                  if ((c & fmask) <= 1u) push_flagged(p, c, magic_bits, i0 + (t % K) * 32 + lane, j0 + jj + t / K, s_qcount,
-                                                        base_f, SHIFT);
+                  if ((c & fmask) <= 1u)
+                    push_flagged(p, c, SF, magic_bits, i0 + (t % K) * 32 + lane, j0 + jj + t / K, s_qcount, bf, SHIFT);
                 }
               }
             }
             return;
           }
-          const uint32_t fmask = (1u << p.bp.fine_shift) - 1u;
           if constexpr (F && (X == 1 || X == 3)) {
             // fixed-sign chord with flags: the plain code addresses the histogram (as without flags),
             // the fine code, from the same theta', only decides the flag
 #pragma unroll 1
             for (int jj = jbeg; jj < jbeg + 32; ++jj) {
-              const float4 v = tile[jj];
+              const float4 v = jvec(jj);
               uint32_t cfs[K], ccs[K];
               uint32_t low = 0xFFFFFFFFu;
 #pragma unroll
               for (int k = 0; k < K; ++k) {
                 cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
                                                                         iws_c, h_c, p.bp, ccs[k]));
-                add_pair<false>(p, ccs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
+                add_pair<false>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
                                 zi[k], v);
                 low = min(low, cfs[k] & fmask);
               }
@@ -1067,13 +1092,13 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           }
 #pragma unroll U
           for (int jj = jbeg; jj < jbeg + 32; ++jj) {
-            const float4 v = tile[jj];
+            const float4 v = jvec(jj);
             uint32_t cbs[K];
             uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               cbs[k] = code_of(k, v);
-              add_pair<F>(p, cbs[k], base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
+              add_pair<F>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
                           v);
               if (F) low = min(low, cbs[k] & fmask);
             }
@@ -1082,7 +1107,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #pragma unroll
               for (int k = 0; k < K; ++k)
                 if ((cbs[k] & fmask) <= 1u)
-                  push_flagged(p, cbs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
+                  push_flagged(p, cbs[k], SF, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, bf, SHIFT);
             }
           }
         };
@@ -1110,9 +1135,11 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           else h_c = below ? 0.0f : 3.14159265358979323846f * p.bp.inv_w;
           float iws = iws_c, h = h_c;
           if (fine) {
-            iws = below ? p.bp.inv_w_f : -p.bp.inv_w_f;
-            if (MAP == kDirect) h = below ? p.bp.magic_f : p.bp.magic_far_f;
-            else h = below ? 0.0f : 3.14159265358979323846f * p.bp.inv_w_f;
+            const bool sm = (pc & kSmallBit) != 0;
+            const float iwf = sm ? p.bp.inv_w_fs : p.bp.inv_w_f;
+            iws = below ? iwf : -iwf;
+            if (MAP == kDirect) h = below ? p.bp.magic_f : (sm ? p.bp.magic_far_fs : p.bp.magic_far_f);
+            else h = below ? 0.0f : 3.14159265358979323846f * iwf;
           }
           if (pc & kSmallBit) {
             count_path(fine ? 8 : 7, 1u);
@@ -1148,8 +1175,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             for (int k = 0; k < K; ++k) {
               const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
               if (jj > thr[k] &&
-                  add_pair<F>(p, cb, base, base_f, SHIFT, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k], v))
-                push_flagged(p, cb, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
+                  add_pair<F>(p, cb, base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
+                              yi[k], zi[k], v))
+                push_flagged(p, cb, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
             }
           }
         };

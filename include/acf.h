@@ -13,12 +13,14 @@
  * [k w, (k+1) w); separations beyond nbins * w are clamped into the last bin, so every pair is
  * counted and a histogram always sums to n1 * n2.
  *
- * Precision contract: the kernels work in fp32 on unit vectors built in fp64. The computed
- * separation of every pair is within 1e-6 rad of the fp64 value of the formula above, so a pair
- * can land in a neighbouring bin only if its fp64 theta lies within 1e-6 rad of that bin edge.
- * In "exact" mode (option below; on by default, mode 2) pairs whose fp32 separation falls that
- * close to an edge are re-decided in fp64 from the same unit vectors, so every bin is the one the
- * fp64 formula gives (up to ~1e-15 relative): the histograms equal those of the fp64 definition.
+ * Precision: the kernels work in fp32 on unit vectors built in fp64. In the default exact mode 2
+ * every pair whose fp32 separation falls within its form's worst-case error of a bin edge is
+ * re-decided in fp64 from the same unit vectors, so every bin is the one the fp64 formula gives
+ * (up to ~1e-15 relative): the histograms equal those of the fp64 definition. Without it (exact
+ * modes 0 and 1), a pair can land in a neighbouring bin only if its fp64 theta lies near that edge:
+ * the worst-case error (every rounding aligned) is 7e-7 rad for the dot form used between 55 and
+ * 125 degrees, 1.05e-6 for the chord form below 72 degrees and 1.25e-6 near 90 degrees for the
+ * full-range chord form; the largest measured on millions of test pairs is 2.4e-7.
  *
  * Conventions for every entry point:
  *   - Array arguments marked "device" are caller-owned CUDA device pointers on the context's
@@ -84,7 +86,7 @@ int acf_set_stream(acf_ctx *ctx, void *cuda_stream);
  * symmetry". Either way sum(out) == n * n2 exactly.
  * n == 0 or n2 == 0 gives an all-zero histogram. Returns ACF_ERR_UNSUPPORTED when the
  * per-block shared-memory histogram does not fit: that needs min(nbins, 180/w + 1) <= 49152
- * (or, when 180/w is an integer, 180/w + 4 <= 49152).
+ * (or, when 180/w is an integer, 180/w + 2 <= 49152).
  */
 int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, const float *ra2, const float *dec2,
                   int64_t n2, double bin_width_deg, int32_t nbins, uint64_t *out);
@@ -95,15 +97,15 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  * device memory to another allocator (a framework's caching allocator) or latency-critical code
  * that cannot afford the implicit device synchronisation and driver work of an allocation.
  *
- * Same arguments, semantics and results as acf_histogram, but its scratch (unit vectors, block
- * rows, the chunk counter) lives in one file-scope device array of 16 MiB that the library
+ * Same arguments, semantics and results as acf_histogram, but its scratch (sorted unit vectors,
+ * caps, block rows, counters, the exact-mode queue) lives in one file-scope device array of 16 MiB that the library
  * reserves on every GPU that loads it, until the process exits. It calls no cudaMalloc, cudaFree
  * or other allocating routine.
  *   - Limit: about 61 bytes per galaxy of each catalog + ((blocks + 2) * nbins * 8) bytes must fit
  *     in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
  *     return ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need
- *     ~11 MB. In exact mode the rest of the array holds the queue of pairs to re-decide; pairs that
- *     do not fit keep their fp32 bin (still within the precision contract) and are counted by the
+ *     ~13 MB. In exact mode the rest of the array holds the queue of pairs to re-decide; pairs that
+ *     do not fit keep their fp32 bin (the precision of exact mode 0) and are counted by the
  *     "exact_overflow" info key.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
  *     make that first call before any stream capture.
