@@ -762,16 +762,16 @@ struct FormTag {
 template <bool F>
 __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint32_t base, uint32_t base_f, int shift,
                                          int S, uint32_t magic_bits, int i, int j, float xi, float yi, float zi,
-                                         float4 v) {
+                                         float4 v, uint32_t inc) {
   if (!F) {
     if (ACF_CHECK(cb - magic_bits < (uint32_t)p.bp.entries, 1, (long long)(cb - magic_bits), i,
                   __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
-      red_shared_add((cb << shift) + base, p.inc);
+      red_shared_add((cb << shift) + base, inc);
     return false;
   } else {
     if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i,
                   __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
-      red_shared_add(((cb >> S) << shift) + base_f, p.inc);
+      red_shared_add(((cb >> S) << shift) + base_f, inc);
     return (cb & ((1u << S) - 1u)) <= 1u;
   }
 }
@@ -918,6 +918,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   const uint32_t base_fm = (LAYOUT == kLane) ? hist_addr + lane * 4u - ((magic_bits >> p.bp.fine_shift_mid) << 7)
                                              : hist_addr - ((magic_bits >> p.bp.fine_shift_mid) << 2);
   const int ni = (int)p.ni, nj = (int)p.nj;
+  const uint32_t inc = p.inc;  // the histogram increment: 2 for DD/RR pairs i < j, 1 for DR
 
   // tickets: the unit being computed (u), the one whose tile is in flight (un), and one fetched
   // ahead by lane 0 while computing (its latency hides behind the unit)
@@ -1048,7 +1049,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
                   add_pair<F>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
-                              xi[k], yi[k], zi[k], vv[u]);
+                              xi[k], yi[k], zi[k], vv[u], inc);
                   if (F) low = min(low, cb[u * K + k] & fmask);
                 }
               // near-edge pairs are rare: one warp vote per batch; the lanes that hold one walk
@@ -1079,7 +1080,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                 cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
                                                                         iws_c, h_c, p.bp, ccs[k]));
                 add_pair<false>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
-                                zi[k], v);
+                                zi[k], v, inc);
                 low = min(low, cfs[k] & fmask);
               }
               if (__any_sync(0xffffffffu, low <= 1u)) {
@@ -1099,7 +1100,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             for (int k = 0; k < K; ++k) {
               cbs[k] = code_of(k, v);
               add_pair<F>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
-                          v);
+                          v, inc);
               if (F) low = min(low, cbs[k] & fmask);
             }
             // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
@@ -1176,7 +1177,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
               if (jj > thr[k] &&
                   add_pair<F>(p, cb, base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
-                              yi[k], zi[k], v))
+                              yi[k], zi[k], v, inc))
                 push_flagged(p, cb, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
             }
           }
