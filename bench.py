@@ -255,6 +255,7 @@ def run_ours(args, cat, workload, rank, world, local):
     # instructions the algorithm needs per step: one untimed step, reading each call's path counts
     ctx.set_option("kernel_timing", 0)
     alg_inst, alg_pairs = 0, 0
+    path_pairs = {}
     with torch.cuda.stream(stream):
         for call in (lambda: acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, None, None, 0, w, nb, dd),
                      lambda: acf.acf_histogram(ctx.handle, ra_d, dec_d, cat.n_d, ra_r, dec_r, cat.n_r, w, nb, dr),
@@ -264,12 +265,13 @@ def run_ours(args, cat, workload, rank, world, local):
                 n_pairs = ctx.info(key)
                 alg_inst += ipp * n_pairs
                 alg_pairs += n_pairs
+                path_pairs[key] = path_pairs.get(key, 0) + n_pairs
             masked = ctx.info("pairs_masked")
+            path_pairs["pairs_masked"] = path_pairs.get("pairs_masked", 0) + masked
             exact_on = sum(ctx.info(k) for k in ("pairs_fixed_exact", "pairs_general_exact", "pairs_small_exact",
                                                  "pairs_mid_exact")) > 0
             alg_inst += (INST_MASKED + (INST_MASKED_EXACT if exact_on else 0)) * masked
             alg_pairs += masked
-    path_mix = {k: ctx.info(k) for k in INST_PER_PATH}
     total_ms = sum(step_ms)
     total_ms_max, = reduce_max([total_ms], world)
     pairs = logical_pairs(cat.n_d, cat.n_r)
@@ -283,6 +285,7 @@ def run_ours(args, cat, workload, rank, world, local):
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
             "frac": (achieved / peak) if achieved else None, "traffic": recorded_traffic(workload),
             "inst_per_pair": alg_inst / max(alg_pairs, 1), "pairs_computed_per_step": alg_pairs,
+            "path_share": {k[len("pairs_"):]: round(v / max(alg_pairs, 1), 4) for k, v in path_pairs.items() if v},
             "pair_kernel_ms_per_launch": pair_ms / max(len(kt), 1),
             "pair_kernel_launches": len(kt),
             "peak_basis": f"{SMS} SMs x {LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz (maximum SM clock)"}
