@@ -51,10 +51,6 @@ constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact
 // j-galaxies per step of the hot loops: their tile loads first, then every code, then every atomic
 // (the atomics' memory clobber would otherwise keep the next tile load behind them)
 constexpr int kJJBatch = ACF_JJ_BATCH;
-#ifndef ACF_JJ_BATCH_FINE
-#define ACF_JJ_BATCH_FINE 1
-#endif
-constexpr int kJJBatchFine = ACF_JJ_BATCH_FINE;  // the same for the exact-mode (flagging) loops
 #ifndef ACF_J_SHUFFLE
 #define ACF_J_SHUFFLE 0  // 1: j-vectors broadcast by warp shuffles instead of shared-memory loads
 #endif
@@ -809,20 +805,11 @@ __device__ __forceinline__ void push_flagged_body(const QueueArgs& q, uint32_t c
     red_shared_add(a - (1u << shift), q.inc);
   }
 }
-// Out of line: the flagged path is rare, and one call per site keeps the hot loop bodies small.
-__device__ __noinline__ void push_flagged_call(QueueArgs q, uint32_t cb, uint32_t e_cnt, bool may_carry, int i, int j,
-                                               unsigned int* s_qcount, uint32_t base_f, int shift) {
-  push_flagged_body(q, cb, e_cnt, may_carry, i, j, s_qcount, base_f, shift);
-}
-#ifndef ACF_PUSH_NOINLINE
-#define ACF_PUSH_NOINLINE 0
-#endif
 __device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, int S, uint32_t magic_bits, int i, int j,
                                              unsigned int* s_qcount, uint32_t base_f, int shift) {
   const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc, S};
   const uint32_t e_cnt = (cb - magic_bits) >> S;
-  if (ACF_PUSH_NOINLINE) push_flagged_call(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
-  else push_flagged_body(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
+  push_flagged_body(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
 }
 // The same for a two-code loop: the count went to the plain code's entry.
 __device__ __forceinline__ void push_flagged2(const PairParams& p, uint32_t cb, uint32_t coarse, uint32_t magic_bits,
@@ -1031,8 +1018,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const int SF = X == 2 ? p.bp.fine_shift_mid : (X == 3 ? p.bp.fine_shift_small : p.bp.fine_shift);
           const uint32_t bf = X == 2 ? base_fm : base_f;
           const uint32_t fmask = (1u << SF) - 1u;
-          constexpr int B = F ? kJJBatchFine : kJJBatch;
-          if constexpr ((F || U > 1) && B > 1) {
+          if constexpr (!F && U > 1 && kJJBatch > 1) {
+            // plain loops: load kJJBatch j-vectors, then every code, then every atomic
+            constexpr int B = kJJBatch;
 #pragma unroll 1
             for (int jj = jbeg; jj < jbeg + 32; jj += B) {
               float4 vv[B];
@@ -1043,27 +1031,12 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               for (int u = 0; u < B; ++u)
 #pragma unroll
                 for (int k = 0; k < K; ++k) cb[u * K + k] = code_of(k, vv[u]);
-              uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of the batch
 #pragma unroll
               for (int u = 0; u < B; ++u)
 #pragma unroll
-                for (int k = 0; k < K; ++k) {
-                  add_pair<F>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
-                              xi[k], yi[k], zi[k], vv[u], inc);
-                  if (F) low = min(low, cb[u * K + k] & fmask);
-                }
-              // near-edge pairs are rare: one warp vote per batch; the lanes that hold one walk
-              // their batch once (the code picked by a select chain keeps the array in registers)
-              if (F && __any_sync(0xffffffffu, low <= 1u)) {
-#pragma unroll 1
-                for (int t = 0; t < B * K; ++t) {
-                  uint32_t c = cb[0];
-#pragma unroll
-                  for (int q = 1; q < B * K; ++q) c = (t == q) ? cb[q] : c;
-                  if ((c & fmask) <= 1u)
-                    push_flagged(p, c, SF, magic_bits, i0 + (t % K) * 32 + lane, j0 + jj + t / K, s_qcount, bf, SHIFT);
-                }
-              }
+                for (int k = 0; k < K; ++k)
+                  add_pair<false>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
+                                  xi[k], yi[k], zi[k], vv[u], inc);
             }
             return;
           }
