@@ -392,13 +392,11 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   p.qused = sc.qused;
   p.qflagged = sc.counters + 3;
   p.qcap = (unsigned int)std::min<long long>(sc.qcap, 0xFFFFFFFFll);
-  // each block owns a region of the queue (half the queue spread over the blocks of a launch, a
-  // power of two each; the queue is drained after every launch); blocks that flag more append to
-  // the spill region through the global counter
-  int qbatch_log2 = -1;
-  for (long long qb = sc.qcap / (2 * std::max<long long>(L.grid, 1)); qb > 0; qb >>= 1) ++qbatch_log2;
-  if (qbatch_log2 < 0) p.qcap = 0;  // too small to use
-  p.qbatch = qbatch_log2 >= 0 ? (1u << qbatch_log2) : 0u;
+  // each block owns a region of the queue: three quarters of the queue spread over the blocks of a
+  // launch, at least 1.5 times what a block flags on average (the queue is drained after every
+  // launch). Blocks that flag more append to the spill region through one global counter, which
+  // all blocks contend for, so the regions must hold nearly everything.
+  p.qbatch = (unsigned int)std::min<long long>((long long)p.qcap * 3 / 4 / std::max<long long>(L.grid, 1), 0x7FFFFFFFll);
   p.path_pairs = reinterpret_cast<unsigned long long*>(sc.counters + 16);
   if (p.qcap == 0) p.exact_mode = 0;
   p.vi = ci.v;
@@ -431,11 +429,13 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     }
     if (p.exact_mode) {
       // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
-      const int fblocks = c->num_sms * 8;
-      const size_t fsmem = (size_t)(3 * pl.bp.nbins + 2) * 8 + (size_t)L.grid * 4;
+      // parts x pair-grid blocks: each region is shared by `parts` blocks
+      const long long parts = std::max<long long>(1, (long long)c->num_sms * 8 / std::max<long long>(L.grid, 1));
+      const unsigned fblocks = (unsigned)(parts * L.grid);
+      const size_t fsmem = (size_t)(3 * pl.bp.nbins + 2) * 8;
       const bool fs = fsmem <= 48 * 1024;
 #define ACF_FIXUP(M, SM)                                                                                           \
-  fixup_kernel<M, SM><<<fblocks, 256, SM ? fsmem : 0, c->stream>>>(sc.queue, sc.qused, (int)L.grid, qbatch_log2,    \
+  fixup_kernel<M, SM><<<fblocks, 256, SM ? fsmem : 0, c->stream>>>(sc.queue, sc.qused, (int)L.grid, p.qbatch,       \
                                                                     sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T, \
                                                                     sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,  \
                                                                     sc.counters + 4)

@@ -156,7 +156,7 @@ struct PairParams {
   unsigned int* qused;                 // per block: slots of its own region in use
   unsigned int* qflagged;              // pairs flagged (for reporting)
   unsigned int qcap;                   // queue slots
-  unsigned int qbatch;                 // slots a block owns (a power of two)
+  unsigned int qbatch;                 // slots a block owns
   unsigned long long* path_pairs;      // pairs evaluated per path: chord fixed, chord general,
                                        // chord fixed+flag, chord general+flag, masked/ragged units,
                                        // dot form, dot form+flag, short chord, short chord+flag
@@ -1246,11 +1246,13 @@ __global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ 
 // starts empty again); the merge adds delta[] to the counts. Slots requested past the queue's end
 // are added to *overflow (those pairs kept their fp32 bin).
 // The queue holds pair_grid regions of qbatch slots (region b: qused[b] in use), then spill slots.
-// With SMEM the edge tables, the per-bin moves and the region use sit in shared memory (nbins up to
-// a few thousand); the moves reach delta[] once per block.
+// The grid is parts x pair_grid blocks: block x serves region x % pair_grid with its share
+// x / pair_grid of the parts, and every block takes a share of the spill slots. With SMEM the edge
+// tables and the per-bin moves sit in shared memory (nbins up to a few thousand); the moves reach
+// delta[] once per block.
 template <int MAP, bool SMEM>
 __global__ void __launch_bounds__(256) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
-                                                    int pair_grid, int qbatch_log2,
+                                                    int pair_grid, unsigned int qbatch,
                                                     const unsigned int* __restrict__ qspill, unsigned int qcap,
                                                     const double4* __restrict__ vi, const double4* __restrict__ vj,
                                                     const double* __restrict__ T, const double* __restrict__ U,
@@ -1262,36 +1264,33 @@ __global__ void __launch_bounds__(256) fixup_kernel(const uint4* __restrict__ qu
   const double* tT = T;
   const double* tU = U;
   unsigned long long* dl = delta;
-  const unsigned int* used = qused;
   if (SMEM) {
     double* sT = reinterpret_cast<double*>(fsm);
     double* sU = sT + (nb + 1);
     unsigned long long* sd = reinterpret_cast<unsigned long long*>(sU + (nb + 1));
-    unsigned int* su = reinterpret_cast<unsigned int*>(sd + nb);
     for (int k = threadIdx.x; k <= nb; k += blockDim.x) {
       sT[k] = T[k];
       sU[k] = U[k];
       if (k < nb) sd[k] = 0ull;
     }
-    for (int b = threadIdx.x; b < pair_grid; b += blockDim.x) su[b] = qused[b];
     tT = sT;
     tU = sU;
     dl = sd;
-    used = su;
   }
   if (threadIdx.x == 0) s_moved = 0u;
   __syncthreads();
-  const unsigned int qbatch = 1u << qbatch_log2;
-  const unsigned int nbatch = (unsigned int)pair_grid << qbatch_log2;
+  const unsigned int nbatch = (unsigned int)pair_grid * qbatch;
   const unsigned int spill = *qspill;
   const unsigned int room = qcap - nbatch;
   const unsigned int nspill = min(spill, room);
   if (blockIdx.x == 0 && threadIdx.x == 0 && spill > room) atomicAdd(overflow, spill - room);
-  const uint32_t magic_bits = __float_as_uint(kMagic);
   unsigned int my_moved = 0u;
-  for (unsigned int s = blockIdx.x * blockDim.x + threadIdx.x; s < nbatch + nspill; s += gridDim.x * blockDim.x) {
-    if (s < nbatch && (s & (qbatch - 1u)) >= used[s >> qbatch_log2]) continue;  // unused slot of a region
-    const uint4 rec = queue[s];
+  const unsigned int region = blockIdx.x % (unsigned)pair_grid;
+  const unsigned int part = blockIdx.x / (unsigned)pair_grid, parts = gridDim.x / (unsigned)pair_grid;
+  const unsigned int nused = qbatch ? min(qused[region], qbatch) : 0u;
+  const unsigned int nmine = part < parts ? nused : 0u;  // blocks past the last whole part take spill only
+  const unsigned int step = parts * blockDim.x;
+  auto redo = [&](const uint4 rec) {
     const double4 a = vi[rec.x], b = vj[rec.y];
     int e = (int)rec.w;  // the entry the pair's count went to
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
@@ -1315,7 +1314,11 @@ __global__ void __launch_bounds__(256) fixup_kernel(const uint4* __restrict__ qu
       atomicAdd(dl + k, (unsigned long long)inc);
       ++my_moved;
     }
-  }
+  };
+  // this block's share of its region, then its share of the spill slots
+  for (unsigned int t = part * blockDim.x + threadIdx.x; t < nmine; t += step) redo(queue[region * qbatch + t]);
+  for (unsigned int t = blockIdx.x * blockDim.x + threadIdx.x; t < nspill; t += gridDim.x * blockDim.x)
+    redo(queue[nbatch + t]);
   for (int o = 16; o > 0; o >>= 1) my_moved += __shfl_xor_sync(0xffffffffu, my_moved, o);
   if ((threadIdx.x & 31) == 0 && my_moved) atomicAdd(&s_moved, my_moved);
   __syncthreads();
