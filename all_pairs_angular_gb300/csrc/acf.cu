@@ -257,13 +257,15 @@ PairKernelFn pick_kernel(const Plan& pl) {
 // Device buffers of one histogram call, carved out of one scratch region.
 struct CatBufs {
   float4* v = nullptr;       // unit vectors in spatial order (fp32)
+  float4* lo = nullptr;      // what fp32 leaves of the fp64 components (double-single with v)
   double4* v64 = nullptr;    // the same in fp64 (exact re-decision)
   float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
 };
 struct Scratch {
   unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue spill slots handed out (this launch),
-                                       // [2] moved pairs, [3] flagged pairs, [4] queue overflow;
+                                       // [2] moved pairs, [3] flagged pairs, [4] queue overflow,
+                                       // [5] pairs the fix-up redid in fp64;
                                        // bytes 64..135: pairs per path (u64)
   unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
   unsigned int* key1 = nullptr;        // sort: keys after the first pass
@@ -274,11 +276,16 @@ struct Scratch {
   unsigned long long* delta = nullptr; // exact mode: count moves of the fp64 re-decision, per bin
   double* T = nullptr;                 // exact mode: edge tables, nbins + 1 each
   double* U = nullptr;
+  float2* Tds = nullptr;               // the same as double-single (hi, lo) pairs
+  float2* Uds = nullptr;
   uint4* queue = nullptr;
   unsigned int* qused = nullptr;       // per pair-kernel block: slots of its queue region in use
   long long qcap = 0;
 };
 
+// the fix-up's shared moves and tables at most: eight 256-thread blocks per SM still fit, since the
+// kernel waits on loads and needs every warp it can get
+constexpr size_t kFixupSmemMax = 24 * 1024;
 constexpr long long kQueueCapMin = 1ll << 20;  // flagged pairs the workspace can hold: 16 MB ..
 constexpr long long kQueueCapMax = 1ll << 28;  // .. 4 GB
 
@@ -293,6 +300,7 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   auto cat = [&](long long m, CatBufs& cb) {
     const long long ch = (m + 127) / 128;
     cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
+    cb.lo = reinterpret_cast<float4*>(take((size_t)m * 16));
     cb.v64 = reinterpret_cast<double4*>(take((size_t)m * 32));
     cb.cap32 = reinterpret_cast<float4*>(take((size_t)ch * 4 * 16));
     cb.cap128 = reinterpret_cast<float4*>(take((size_t)ch * 16));
@@ -312,6 +320,8 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   r.delta = reinterpret_cast<unsigned long long*>(take((size_t)nbins * 8));
   r.T = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
   r.U = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
+  r.Tds = reinterpret_cast<float2*>(take((size_t)(nbins + 1) * 8));
+  r.Uds = reinterpret_cast<float2*>(take((size_t)(nbins + 1) * 8));
   r.qcap = qcap;
   r.qused = reinterpret_cast<unsigned int*>(take((size_t)grid * 4));
   r.queue = reinterpret_cast<uint4*>(take((size_t)qcap * 16));
@@ -340,7 +350,7 @@ int prepare_catalog(acf_ctx* c, const float* ra, const float* dec, long long n, 
                                                                  s.key0);
   ACF_LAUNCHED(c);
   const long long vblocks = std::min<long long>((n + 255) / 256, (long long)c->num_sms * 8);
-  vectors_kernel<<<(unsigned)vblocks, 256, 0, c->stream>>>(ra, dec, s.key0, n, cb.v, cb.v64);
+  vectors_kernel<<<(unsigned)vblocks, 256, 0, c->stream>>>(ra, dec, s.key0, n, cb.v, cb.lo, cb.v64);
   ACF_LAUNCHED(c);
   const long long warps = (n + 127) / 128;
   caps_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, c->stream>>>(cb.v, n, cb.cap32, cb.cap128);
@@ -374,6 +384,36 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
   const double per_unit = (pl.layout == kLane ? 1.0 : 32.0) * kK * kJT * inc;
   L.per_launch = (long long)std::floor(4294967295.0 / per_unit);
   if (c->opt_units_per_launch > 0) L.per_launch = std::min(L.per_launch, c->opt_units_per_launch);
+  return ACF_OK;
+}
+
+// Every pair a launch flagged near an edge is re-decided exactly; its count moves if the bin differs.
+// parts x pair-grid blocks, each region shared by `parts` blocks. The per-bin moves (int32 per
+// block) and, when they fit too, the double-single edge tables go to shared memory if small.
+int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& p, const Scratch& sc,
+                 const CatBufs& ci, const CatBufs& cj) {
+  const long long parts = std::max<long long>(1, (long long)c->num_sms * 8 / std::max<long long>(L.grid, 1));
+  const unsigned fblocks = (unsigned)(parts * L.grid);
+  const int nb = pl.bp.nbins;
+  const size_t moves = ((size_t)nb * 4 + 15) & ~(size_t)15, tables = (size_t)(nb + 1) * 16;
+  const int level = moves + tables <= kFixupSmemMax ? 2 : (moves <= kFixupSmemMax ? 1 : 0);
+  const size_t fsmem = level == 2 ? moves + tables : (level == 1 ? moves : 0);
+#define ACF_FIXUP(M, SM)                                                                                       \
+  fixup_kernel<M, SM><<<fblocks, 256, fsmem, c->stream>>>(sc.queue, sc.qused, (int)L.grid, p.qbatch, sc.counters + 1, \
+                                                          p.qcap, ci.v, ci.lo, cj.v, cj.lo, ci.v64, cj.v64, sc.T,     \
+                                                          sc.U, sc.Tds, sc.Uds, pl.bp, p.inc, sc.delta,               \
+                                                          sc.counters + 2, sc.counters + 4, sc.counters + 5)
+  if (pl.map == kDirect) {
+    if (level == 2) ACF_FIXUP(kDirect, 2);
+    else if (level == 1) ACF_FIXUP(kDirect, 1);
+    else ACF_FIXUP(kDirect, 0);
+  } else {
+    if (level == 2) ACF_FIXUP(kClamp, 2);
+    else if (level == 1) ACF_FIXUP(kClamp, 1);
+    else ACF_FIXUP(kClamp, 0);
+  }
+#undef ACF_FIXUP
+  ACF_LAUNCHED(c);
   return ACF_OK;
 }
 
@@ -428,26 +468,8 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
       c->ev_used += 2;
     }
     if (p.exact_mode) {
-      // every pair flagged near an edge is re-decided in fp64; its count moves if the bin differs
-      // parts x pair-grid blocks: each region is shared by `parts` blocks
-      const long long parts = std::max<long long>(1, (long long)c->num_sms * 8 / std::max<long long>(L.grid, 1));
-      const unsigned fblocks = (unsigned)(parts * L.grid);
-      const size_t fsmem = (size_t)(3 * pl.bp.nbins + 2) * 8;
-      const bool fs = fsmem <= 48 * 1024;
-#define ACF_FIXUP(M, SM)                                                                                           \
-  fixup_kernel<M, SM><<<fblocks, 256, SM ? fsmem : 0, c->stream>>>(sc.queue, sc.qused, (int)L.grid, p.qbatch,       \
-                                                                    sc.counters + 1, p.qcap, ci.v64, cj.v64, sc.T, \
-                                                                    sc.U, pl.bp, p.inc, sc.delta, sc.counters + 2,  \
-                                                                    sc.counters + 4)
-      if (pl.map == kDirect) {
-        if (fs) ACF_FIXUP(kDirect, true);
-        else ACF_FIXUP(kDirect, false);
-      } else {
-        if (fs) ACF_FIXUP(kClamp, true);
-        else ACF_FIXUP(kClamp, false);
-      }
-#undef ACF_FIXUP
-      ACF_LAUNCHED(c);
+      const int frc = launch_fixup(c, pl, L, p, sc, ci, cj);
+      if (frc) return frc;
     }
   }
 #ifdef ACF_DEBUG_BOUNDS
@@ -496,7 +518,7 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
     if (rc) return rc;
   }
   if (pl.exact && sc.qcap > 0) {
-    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U);
+    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U, sc.Tds, sc.Uds);
     ACF_LAUNCHED(c);
   }
   return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc, out);
@@ -555,7 +577,7 @@ int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_
   if ((rc = prepare_catalog(c, ra_d, dec_d, n_d, sc, sc.a)) || (rc = prepare_catalog(c, ra_r, dec_r, n_r, sc, sc.b)))
     return rc;
   if (pl.exact && sc.qcap > 0) {
-    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U);
+    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U, sc.Tds, sc.Uds);
     ACF_LAUNCHED(c);
   }
   if ((rc = histogram_vectors(c, sc.a, n_d, sc.a, n_d, true, pl, Ldd, sc, dd)) ||
@@ -799,9 +821,10 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
       *v = (long long)h[k];
       return ACF_OK;
     }
-  if (!strcmp(key, "exact_flagged") || !strcmp(key, "exact_moved") || !strcmp(key, "exact_overflow")) {
+  if (!strcmp(key, "exact_flagged") || !strcmp(key, "exact_moved") || !strcmp(key, "exact_overflow") ||
+      !strcmp(key, "exact_redone_fp64")) {
     // synchronises the stream; counts of the last histogram call
-    unsigned int h[5] = {0, 0, 0, 0, 0};
+    unsigned int h[6] = {0, 0, 0, 0, 0, 0};
     if (c->last_counters && c->last_qcap > 0) {
       if (cudaSetDevice(c->device) != cudaSuccess || cudaStreamSynchronize(c->stream) != cudaSuccess ||
           cudaMemcpy(h, c->last_counters, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -809,6 +832,7 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
     }
     if (!strcmp(key, "exact_flagged")) *v = h[3];
     else if (!strcmp(key, "exact_moved")) *v = h[2];
+    else if (!strcmp(key, "exact_redone_fp64")) *v = h[5];
     else *v = h[4];  // slots requested past the end, over all launches
     return ACF_OK;
   }
@@ -921,7 +945,7 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
-                "(about 61 bytes per galaxy of each catalog plus (%lld blocks + 2) x nbins x 8 bytes); use acf_histogram",
+                "(about 77 bytes per galaxy of each catalog plus (%lld blocks + 2) x nbins x 8 bytes); use acf_histogram",
                 need, kNoAllocScratchBytes, L.grid);
   void* scratch = nullptr;
   rc = noalloc_scratch(c, c->device, &scratch);

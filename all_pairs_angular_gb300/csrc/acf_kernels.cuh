@@ -440,15 +440,19 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(
 
 // Unit vectors in sorted order, as fp32 (pair kernel) and fp64 (exact re-decision of flagged
 // pairs): position p holds input galaxy order[p].
+// v_out is the fp32 rounding of each fp64 component and lo_out the fp32 rounding of what remains
+// (|x - hi - lo| <= 2^-48 |x|): together a double-single copy for the fix-up's first pass.
 __global__ void vectors_kernel(const float* __restrict__ ra, const float* __restrict__ dec,
                                const unsigned int* __restrict__ order, long long n, float4* __restrict__ v_out,
-                               double4* __restrict__ v64_out) {
+                               float4* __restrict__ lo_out, double4* __restrict__ v64_out) {
   for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n; p += (long long)gridDim.x * blockDim.x) {
     const unsigned int src = order[p];
     if (ACF_CHECK(src < (unsigned long long)n, 5, p, src)) {
       double x, y, z;
       unit64(ra[src], dec[src], x, y, z);
-      v_out[p] = make_float4((float)x, (float)y, (float)z, 0.0f);
+      const float hx = (float)x, hy = (float)y, hz = (float)z;
+      v_out[p] = make_float4(hx, hy, hz, 0.0f);
+      lo_out[p] = make_float4((float)(x - (double)hx), (float)(y - (double)hy), (float)(z - (double)hz), 0.0f);
       v64_out[p] = make_double4(x, y, z, 0.0);
     }
   }
@@ -1232,100 +1236,223 @@ __global__ void omega_kernel(const unsigned long long* __restrict__ dd, const un
 // Edge thresholds of the exact re-decision, in fp64: bin k starts where the difference chord
 // reaches T[k] = 4 sin^2(k w / 2), or, for pairs past 90 degrees, where the sum chord falls to
 // U[k] = 4 cos^2(k w / 2).
-__global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ T, double* __restrict__ U) {
+__global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ T, double* __restrict__ U,
+                                  float2* __restrict__ Tds, float2* __restrict__ Uds) {
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k <= nbins; k += gridDim.x * blockDim.x) {
     double sh, ch;
     sincos(0.5 * w_rad * k, &sh, &ch);
-    T[k] = 4.0 * sh * sh;
-    U[k] = 4.0 * ch * ch;
+    const double t = 4.0 * sh * sh, u = 4.0 * ch * ch;
+    T[k] = t;
+    U[k] = u;
+    // double-single copies: hi = fp32 rounding, lo = fp32 rounding of the rest
+    const float th = (float)t, uh = (float)u;
+    Tds[k] = make_float2(th, (float)(t - (double)th));
+    Uds[k] = make_float2(uh, (float)(u - (double)uh));
   }
 }
 
-// Re-decide every queued pair in fp64 from the fp64 unit vectors and record the move of its count
-// if the fast code put it in a neighbouring bin. Runs after every pair-kernel launch (the queue then
-// starts empty again); the merge adds delta[] to the counts. Slots requested past the queue's end
-// are added to *overflow (those pairs kept their fp32 bin).
+// ------------------------------------------------------------------ exact re-decision
+
+// Knuth's TwoSum: s + t == a + b exactly (round-to-nearest; the _rn intrinsics keep the compiler from
+// contracting or reordering these operations).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& t) {
+  s = __fadd_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  const float av = __fsub_rn(s, bv);
+  t = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
+}
+
+// q = |a + sg b|^2 (sg = -1: the difference chord, +1: the sum chord) of two double-single vectors
+// (hi + lo), returned as qh + ql. Error against the same q of the fp64 vectors that hi + lo round:
+//  - representation: |hi + lo - x| <= 2^-48 per component, so <= 2^-47 on each component of a + sg b;
+//  - components: lo + sg lo' (error <= 2^-47), the TwoSum remainder plus that (error <= 2^-46), then
+//    an exact TwoSum: <= 2^-45 in all per component, so <= 2 sqrt(3) 2^-45 |d| = 9.8e-14 |d| on q;
+//  - squares: exact product and remainder (fma), 2 dh dl rounded and dl^2 dropped: <= 2^-46 q;
+//  - the sum of the eight small terms: <= 2^-44 q.
+__device__ __forceinline__ void ds_chord2(float4 ah, float4 al, float4 bh, float4 bl, float sg, float& qh, float& ql) {
+  const float a_h[3] = {ah.x, ah.y, ah.z}, a_l[3] = {al.x, al.y, al.z};
+  const float b_h[3] = {bh.x, bh.y, bh.z}, b_l[3] = {bl.x, bl.y, bl.z};
+  float p[3], small = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    float s, t, dh, dl;
+    two_sum(a_h[c], sg * b_h[c], s, t);  // sg * b is exact
+    const float v = __fadd_rn(t, __fadd_rn(a_l[c], sg * b_l[c]));
+    two_sum(s, v, dh, dl);
+    p[c] = __fmul_rn(dh, dh);
+    const float e = __fmaf_rn(dh, dh, -p[c]);  // dh^2 - p exactly
+    small = __fadd_rn(small, __fadd_rn(e, __fmul_rn(2.0f * dh, dl)));
+  }
+  float s1, t1, s2, t2;
+  two_sum(p[0], p[1], s1, t1);
+  two_sum(s1, p[2], s2, t2);
+  small = __fadd_rn(small, __fadd_rn(t1, t2));
+  two_sum(s2, small, qh, ql);
+}
+
+// Side of q = qh + ql against a double-single table value: +1 above, -1 below, 0 within eps (then
+// only the fp64 re-decision can tell). qh - th is exact when the two are within a factor of 2.
+__device__ __forceinline__ int ds_side(float qh, float ql, float2 t, float eps) {
+  const float d = __fadd_rn(__fsub_rn(qh, t.x), __fsub_rn(ql, t.y));
+  return d > eps ? 1 : (d < -eps ? -1 : 0);
+}
+
+constexpr int kFixupILP = 3;  // queued pairs a fix-up thread loads at once
+
+// Re-decide every queued pair exactly and record the move of its count if the fast code put it in a
+// neighbouring bin. Runs after every pair-kernel launch (the queue then starts empty again); the
+// merge adds delta[] to the counts. Slots requested past the queue's end are added to *overflow
+// (those pairs kept their fp32 bin).
+// The decision is the fp64 one: the chord q of the fp64 unit vectors against the fp64 edge tables
+// T[k] = 4 sin^2(k w / 2) (bins whose lower edge is up to 90 degrees, difference chord) or
+// U[k] = 4 cos^2(k w / 2) (the others, sum chord), each exact enough where the other loses relative
+// precision. A double-single pass (fp32 hi + lo, about 48 bits) takes it first: where it lies farther
+// than its error bound from a table value it decides as the fp64 comparison would; within that bound
+// (about 1e-13 relative, against a flagged pair's 1e-6 rad window) the pair is redone in fp64.
 // The queue holds pair_grid regions of qbatch slots (region b: qused[b] in use), then spill slots.
 // The grid is parts x pair_grid blocks: block x serves region x % pair_grid with its share
-// x / pair_grid of the parts, and every block takes a share of the spill slots. With SMEM the edge
-// tables and the per-bin moves sit in shared memory (nbins up to a few thousand); the moves reach
-// delta[] once per block.
-template <int MAP, bool SMEM>
-__global__ void __launch_bounds__(256) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
+// x / pair_grid of the parts, and every block takes a share of the spill slots.
+// SMEM 2: the double-single tables and per-bin moves in shared memory; 1: the moves only; 0: neither.
+// Shared moves reach delta[] once per block.
+template <int MAP, int SMEM>
+__global__ void __launch_bounds__(256, 3) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
                                                     int pair_grid, unsigned int qbatch,
                                                     const unsigned int* __restrict__ qspill, unsigned int qcap,
+                                                    const float4* __restrict__ hi_i, const float4* __restrict__ lo_i,
+                                                    const float4* __restrict__ hi_j, const float4* __restrict__ lo_j,
                                                     const double4* __restrict__ vi, const double4* __restrict__ vj,
                                                     const double* __restrict__ T, const double* __restrict__ U,
+                                                    const float2* __restrict__ Tds, const float2* __restrict__ Uds,
                                                     BinParams bp, unsigned int inc, unsigned long long* __restrict__ delta,
-                                                    unsigned int* __restrict__ moved, unsigned int* __restrict__ overflow) {
+                                                    unsigned int* __restrict__ moved, unsigned int* __restrict__ overflow,
+                                                    unsigned int* __restrict__ redone) {
   extern __shared__ __align__(16) unsigned char fsm[];
-  __shared__ unsigned int s_moved;
+  __shared__ unsigned int s_moved, s_redone;
   const int nb = bp.nbins;
-  const double* tT = T;
-  const double* tU = U;
-  unsigned long long* dl = delta;
-  if (SMEM) {
-    double* sT = reinterpret_cast<double*>(fsm);
-    double* sU = sT + (nb + 1);
-    unsigned long long* sd = reinterpret_cast<unsigned long long*>(sU + (nb + 1));
+  const float2* tT = Tds;
+  const float2* tU = Uds;
+  int* sd = nullptr;
+  if (SMEM >= 1) {
+    sd = reinterpret_cast<int*>(fsm);
+    for (int k = threadIdx.x; k < nb; k += blockDim.x) sd[k] = 0;
+  }
+  if (SMEM == 2) {
+    float2* sT = reinterpret_cast<float2*>(fsm + (((size_t)nb * 4 + 15) & ~(size_t)15));
+    float2* sU = sT + (nb + 1);
     for (int k = threadIdx.x; k <= nb; k += blockDim.x) {
-      sT[k] = T[k];
-      sU[k] = U[k];
-      if (k < nb) sd[k] = 0ull;
+      sT[k] = Tds[k];
+      sU[k] = Uds[k];
     }
     tT = sT;
     tU = sU;
-    dl = sd;
   }
-  if (threadIdx.x == 0) s_moved = 0u;
+  if (threadIdx.x == 0) s_moved = s_redone = 0u;
   __syncthreads();
   const unsigned int nbatch = (unsigned int)pair_grid * qbatch;
   const unsigned int spill = *qspill;
   const unsigned int room = qcap - nbatch;
   const unsigned int nspill = min(spill, room);
   if (blockIdx.x == 0 && threadIdx.x == 0 && spill > room) atomicAdd(overflow, spill - room);
-  unsigned int my_moved = 0u;
+  unsigned int my_moved = 0u, my_redone = 0u;
   const unsigned int region = blockIdx.x % (unsigned)pair_grid;
   const unsigned int part = blockIdx.x / (unsigned)pair_grid, parts = gridDim.x / (unsigned)pair_grid;
   const unsigned int nused = qbatch ? min(qused[region], qbatch) : 0u;
   const unsigned int nmine = part < parts ? nused : 0u;  // blocks past the last whole part take spill only
   const unsigned int step = parts * blockDim.x;
-  auto redo = [&](const uint4 rec) {
-    const double4 a = vi[rec.x], b = vj[rec.y];
+  // re-decide one queued pair from its double-single vectors (ah + al, bh + bl)
+  auto redo = [&](const uint4 rec, float4 ah, float4 al, float4 bh, float4 bl) {
     int e = (int)rec.w;  // the entry the pair's count went to
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     const int kf = entry_to_bin<MAP>(e, bp);
-    int k = kf > bp.kmax ? bp.kmax : kf;
-    // bins up to 90 degrees compare the difference chord with T, the others the sum chord with U
-    // (both exact enough near 90 degrees, each where the other loses relative precision)
-    if (tT[k] <= 2.0) {
-      const double dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z;
-      const double q = dx * dx + dy * dy + dz * dz;
-      while (k > 0 && q < tT[k]) --k;
-      while (k < bp.kmax && q >= tT[k + 1]) ++k;
-    } else {
-      const double dx = a.x + b.x, dy = a.y + b.y, dz = a.z + b.z;
-      const double q = dx * dx + dy * dy + dz * dz;
-      while (k > 0 && q > tU[k]) --k;
-      while (k < bp.kmax && q <= tU[k + 1]) ++k;
+    const int k0 = kf > bp.kmax ? bp.kmax : kf;
+    const bool diff = tT[k0].x <= 2.0f;  // the side, from the table both passes share
+    int k = k0;
+    bool sure = true;
+    {
+      float qh, ql;
+      ds_chord2(ah, al, bh, bl, diff ? -1.0f : 1.0f, qh, ql);
+      // the bound on ds_chord2's error (|d| = sqrt(q); sqrt.approx is within 2^-22 relative), plus
+      // the tables' 2^-48 and the fp64 computation's 2^-50 relative
+      const float eps = 1.5e-13f * sqrt_approx(qh) + 3e-13f * qh;
+      if (diff) {
+        // lower edge: q >= T[k]; upper edge: q < T[k + 1]
+        for (int c; k > 0 && (c = ds_side(qh, ql, tT[k], eps)) <= 0; --k) if (!c) { sure = false; break; }
+        if (sure)
+          for (int c; k < bp.kmax && (c = ds_side(qh, ql, tT[k + 1], eps)) >= 0; ++k) if (!c) { sure = false; break; }
+      } else {
+        // lower edge: q <= U[k]; upper edge: q > U[k + 1]
+        for (int c; k > 0 && (c = ds_side(qh, ql, tU[k], eps)) >= 0; --k) if (!c) { sure = false; break; }
+        if (sure)
+          for (int c; k < bp.kmax && (c = ds_side(qh, ql, tU[k + 1], eps)) <= 0; ++k) if (!c) { sure = false; break; }
+      }
+    }
+    if (!sure) {
+      // too close to an edge for the double-single bound: the same comparisons in fp64
+      ++my_redone;
+      const double4 a = vi[rec.x], b = vj[rec.y];
+      k = k0;
+      if (diff) {
+        const double dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z;
+        const double q = dx * dx + dy * dy + dz * dz;
+        while (k > 0 && q < T[k]) --k;
+        while (k < bp.kmax && q >= T[k + 1]) ++k;
+      } else {
+        const double dx = a.x + b.x, dy = a.y + b.y, dz = a.z + b.z;
+        const double q = dx * dx + dy * dy + dz * dz;
+        while (k > 0 && q > U[k]) --k;
+        while (k < bp.kmax && q <= U[k + 1]) ++k;
+      }
     }
     if (k != kf) {
-      atomicAdd(dl + kf, (unsigned long long)(-(long long)inc));
-      atomicAdd(dl + k, (unsigned long long)inc);
+      if (SMEM >= 1) {
+        atomicAdd(sd + kf, -(int)inc);
+        atomicAdd(sd + k, (int)inc);
+      } else {
+        atomicAdd(delta + kf, (unsigned long long)(-(long long)inc));
+        atomicAdd(delta + k, (unsigned long long)inc);
+      }
       ++my_moved;
     }
   };
+  // slots first, first + stride, ... below n of queue[base ..]: kFixupILP records per thread at a
+  // time, all loads issued before any arithmetic (the loads are what this kernel waits for)
+  auto run = [&](unsigned int base, unsigned int n, unsigned int first, unsigned int stride) {
+    for (unsigned int t = first; t < n; t += kFixupILP * stride) {
+      uint4 rec[kFixupILP];
+      bool ok[kFixupILP];
+#pragma unroll
+      for (int u = 0; u < kFixupILP; ++u) {
+        ok[u] = t + u * stride < n;
+        rec[u] = ok[u] ? queue[base + t + u * stride] : make_uint4(0u, 0u, 0u, 0u);
+      }
+      float4 ah[kFixupILP], al[kFixupILP], bh[kFixupILP], bl[kFixupILP];
+#pragma unroll
+      for (int u = 0; u < kFixupILP; ++u) {
+        ah[u] = hi_i[rec[u].x];
+        al[u] = lo_i[rec[u].x];
+        bh[u] = hi_j[rec[u].y];
+        bl[u] = lo_j[rec[u].y];
+      }
+#pragma unroll
+      for (int u = 0; u < kFixupILP; ++u)
+        if (ok[u]) redo(rec[u], ah[u], al[u], bh[u], bl[u]);
+    }
+  };
   // this block's share of its region, then its share of the spill slots
-  for (unsigned int t = part * blockDim.x + threadIdx.x; t < nmine; t += step) redo(queue[region * qbatch + t]);
-  for (unsigned int t = blockIdx.x * blockDim.x + threadIdx.x; t < nspill; t += gridDim.x * blockDim.x)
-    redo(queue[nbatch + t]);
-  for (int o = 16; o > 0; o >>= 1) my_moved += __shfl_xor_sync(0xffffffffu, my_moved, o);
+  run(region * qbatch, nmine, part * blockDim.x + threadIdx.x, step);
+  run(nbatch, nspill, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+  for (int o = 16; o > 0; o >>= 1) {
+    my_moved += __shfl_xor_sync(0xffffffffu, my_moved, o);
+    my_redone += __shfl_xor_sync(0xffffffffu, my_redone, o);
+  }
   if ((threadIdx.x & 31) == 0 && my_moved) atomicAdd(&s_moved, my_moved);
+  if ((threadIdx.x & 31) == 0 && my_redone) atomicAdd(&s_redone, my_redone);
   __syncthreads();
   if (threadIdx.x == 0 && s_moved) atomicAdd(moved, s_moved);
-  if (SMEM) {
+  if (threadIdx.x == 0 && s_redone) atomicAdd(redone, s_redone);
+  if (SMEM >= 1) {
     for (int k = threadIdx.x; k < nb; k += blockDim.x)
-      if (dl[k]) atomicAdd(delta + k, dl[k]);
+      if (sd[k]) atomicAdd(delta + k, (unsigned long long)(long long)sd[k]);
   }
 }
 

@@ -101,7 +101,7 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  * caps, block rows, counters, the exact-mode queue) lives in one file-scope device array of 16 MiB that the library
  * reserves on every GPU that loads it, until the process exits. It calls no cudaMalloc, cudaFree
  * or other allocating routine.
- *   - Limit: about 61 bytes per galaxy of each catalog + ((blocks + 2) * nbins * 8) bytes must fit
+ *   - Limit: about 77 bytes per galaxy of each catalog + ((blocks + 2) * nbins * 8) bytes must fit
  *     in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
  *     return ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need
  *     ~13 MB. In exact mode the rest of the array holds the queue of pairs to re-decide; pairs that
@@ -207,6 +207,8 @@ int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
  *   "pairs_small", "pairs_small_exact"  the degree-5 chord form, without and with flagging
  *   "exact_flagged"  pairs flagged for re-decision;  "exact_moved"  of those, pairs moved a bin;
  *   "exact_overflow"  flagged pairs that did not fit in the queue (kept their fp32 bin)
+ *   "exact_redone_fp64"  flagged pairs the double-single first pass of the re-decision could not
+ *                    settle (within ~1e-13 relative of an edge), decided again in fp64
  * Unknown keys return ACF_ERR_ARG.
  */
 int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
