@@ -104,9 +104,11 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  *   - Limit: about 77 bytes per galaxy of each catalog + ((blocks + 2) * nbins * 8) bytes must fit
  *     in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
  *     return ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need
- *     ~13 MB. In exact mode the rest of the array holds the queue of pairs to re-decide; pairs that
- *     do not fit keep their fp32 bin (the precision of exact mode 0) and are counted by the
- *     "exact_overflow" info key.
+ *     ~16.3 MB. In exact mode the rest of the array holds the queue of pairs to re-decide (there
+ *     about 30k pairs, against ~4.9M flagged in that DR histogram); pairs that do not fit keep
+ *     their fp32 bin (the precision of exact mode 0) and are counted by the "exact_overflow" info
+ *     key. Exact results need a queue that holds one launch's flagged pairs: catalogs of a few
+ *     tens of thousands of galaxies at 0.25 degree bins.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
  *     make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's contents; the
