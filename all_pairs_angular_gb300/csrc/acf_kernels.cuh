@@ -45,6 +45,20 @@ constexpr int kJJUnroll = ACF_JJ_UNROLL;
 #define ACF_JJ_UNROLL_FINE 1
 #endif
 constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact-mode (fine code) loops
+// Flag test per j: 1 = OR of per-pair tests "biased fraction bits above bit 0 all zero"; 0 = a
+// running minimum of the biased fractions compared with 1 (measured alternative: 12.62 against
+// 12.47 ms of pair kernels per 100k step)
+#ifndef ACF_FLAG_PRED
+#define ACF_FLAG_PRED 1
+#endif
+// Fix-up: queued pairs a thread loads at once, and the blocks per SM its registers must allow
+// (measured: 2 and 4 alike, 4 and 2 slower on fine bins)
+#ifndef ACF_FIXUP_ILP
+#define ACF_FIXUP_ILP 3
+#endif
+#ifndef ACF_FIXUP_MINB
+#define ACF_FIXUP_MINB 3
+#endif
 #ifndef ACF_JJ_BATCH
 #define ACF_JJ_BATCH 2
 #endif
@@ -1052,15 +1066,20 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               const float4 v = jvec(jj);
               uint32_t cfs[K], ccs[K];
               uint32_t low = 0xFFFFFFFFu;
+              bool fl = false;
 #pragma unroll
               for (int k = 0; k < K; ++k) {
                 cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
                                                                         iws_c, h_c, p.bp, ccs[k]));
                 add_pair<false>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
                                 zi[k], v, inc);
+#if ACF_FLAG_PRED
+                fl |= (cfs[k] & (fmask & ~1u)) == 0u;
+#else
                 low = min(low, cfs[k] & fmask);
+#endif
               }
-              if (__any_sync(0xffffffffu, low <= 1u)) {
+              if (__any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
 #pragma unroll
                 for (int k = 0; k < K; ++k)
                   if ((cfs[k] & fmask) <= 1u) push_flagged2(p, cfs[k], ccs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
@@ -1073,15 +1092,20 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             const float4 v = jvec(jj);
             uint32_t cbs[K];
             uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
+            bool fl = false;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               cbs[k] = code_of(k, v);
               add_pair<F>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
                           v, inc);
+#if ACF_FLAG_PRED
+              if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
+#else
               if (F) low = min(low, cbs[k] & fmask);
+#endif
             }
             // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
-            if (F && __any_sync(0xffffffffu, low <= 1u)) {
+            if (F && __any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
 #pragma unroll
               for (int k = 0; k < K; ++k)
                 if ((cbs[k] & fmask) <= 1u)
@@ -1297,7 +1321,7 @@ __device__ __forceinline__ int ds_side(float qh, float ql, float2 t, float eps) 
   return d > eps ? 1 : (d < -eps ? -1 : 0);
 }
 
-constexpr int kFixupILP = 3;  // queued pairs a fix-up thread loads at once
+constexpr int kFixupILP = ACF_FIXUP_ILP;  // queued pairs a fix-up thread loads at once
 
 // Re-decide every queued pair exactly and record the move of its count if the fast code put it in a
 // neighbouring bin. Runs after every pair-kernel launch (the queue then starts empty again); the
@@ -1315,7 +1339,7 @@ constexpr int kFixupILP = 3;  // queued pairs a fix-up thread loads at once
 // SMEM 2: the double-single tables and per-bin moves in shared memory; 1: the moves only; 0: neither.
 // Shared moves reach delta[] once per block.
 template <int MAP, int SMEM>
-__global__ void __launch_bounds__(256, 3) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
+__global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
                                                     int pair_grid, unsigned int qbatch,
                                                     const unsigned int* __restrict__ qspill, unsigned int qcap,
                                                     const float4* __restrict__ hi_i, const float4* __restrict__ lo_i,

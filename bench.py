@@ -37,11 +37,11 @@ UNIT = "Gpairs/s"
 # shared atomic); where the caps fix the sign of the dot product the dot, the sign operation and the
 # constant choice drop out (18); where every theta' stays below 72 degrees the polynomial is of
 # degree 5 instead of 7 (16); the dot form for groups between 55 and 125 degrees is 11 (dot, square,
-# degree-4 polynomial, rounding fma, address, atomic). Exact-mode flagging adds 3.25: the fine code
-# (a second rounding fma, or a shift of the one code), the fraction mask, a 3-input running minimum
-# shared by 2 pairs, and one warp vote with its compare and branch per j (4 pairs per lane).
-INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 21.25, "pairs_general_exact": 28.25,
-                 "pairs_mid": 11, "pairs_mid_exact": 14.25, "pairs_small": 16, "pairs_small_exact": 19.25}
+# degree-4 polynomial, rounding fma, address, atomic). Exact-mode flagging adds 3: the fine code
+# (a second rounding fma, or a shift of the one code), the masked zero test of its fraction, a
+# 3-input predicate OR shared by 2 pairs, and one warp vote with its branch per j (4 pairs per lane).
+INST_PER_PATH = {"pairs_fixed": 18, "pairs_general": 25, "pairs_fixed_exact": 21, "pairs_general_exact": 28,
+                 "pairs_mid": 11, "pairs_mid_exact": 14, "pairs_small": 16, "pairs_small_exact": 19}
 INST_MASKED = 25  # diagonal / ragged units run the general loop on every computed pair
 INST_MASKED_EXACT = 4  # and with flags: fine-code shift, fraction mask, test, branch per pair
 SMS, LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
