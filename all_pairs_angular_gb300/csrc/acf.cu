@@ -214,9 +214,13 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   // copy. 1024 threads (32 warps, one block per SM) when everything fits, else 512.
   const size_t lane_hist = (size_t)bp.entries * 32 * 4;
   const size_t block_hist = (size_t)((bp.entries * 4 + 15) & ~15);
+  // (option 3, built with -DACF_U16_HIST=1 and exact mode 0 only: two copies of 16-bit counters)
+  const size_t block16_hist = (size_t)((2 * ((bp.entries + 1) / 2) * 4 + 15) & ~15);
   int layout = c->opt_layout;
   if (layout == 0) layout = (lane_hist + 16 * kWarpTileBytes <= kMaxSmem) ? kLane : kBlock;
-  const size_t hist_bytes = (layout == kLane) ? lane_hist : block_hist;
+  if (layout == kBlock16 && (!ACF_U16_HIST || pl.exact))
+    return fail(c, ACF_ERR_UNSUPPORTED, "layout 3 (16-bit counters) needs a build with ACF_U16_HIST and exact mode 0");
+  const size_t hist_bytes = (layout == kLane) ? lane_hist : (layout == kBlock16 ? block16_hist : block_hist);
   int threads = c->opt_threads;
   if (threads == 0) threads = (hist_bytes + 32 * kWarpTileBytes <= kMaxSmem) ? 1024 : 512;
   if (threads != 512 && threads != 1024) return fail(c, ACF_ERR_ARG, "threads must be 512 or 1024");
@@ -225,7 +229,8 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   pl.smem = hist_bytes + (size_t)(threads / 32) * kWarpTileBytes;
   if (pl.smem > kMaxSmem)
     return fail(c, ACF_ERR_UNSUPPORTED, "%s histogram of %d entries with %d threads needs %zu bytes of shared memory",
-                layout == kLane ? "lane-private" : "block-shared", bp.entries, threads, pl.smem);
+                layout == kLane ? "lane-private" : (layout == kBlock16 ? "16-bit block-shared" : "block-shared"),
+                bp.entries, threads, pl.smem);
   return ACF_OK;
 }
 
@@ -242,6 +247,12 @@ PairKernelFn pick_kernel(const Plan& pl) {
   ACF_PICK(512, kLane, kClamp, kChordPoly)
   ACF_PICK(512, kBlock, kDirect, kChordPoly)
   ACF_PICK(512, kBlock, kClamp, kChordPoly)
+#if ACF_U16_HIST
+  ACF_PICK(1024, kBlock16, kDirect, kChordPoly)
+  ACF_PICK(1024, kBlock16, kClamp, kChordPoly)
+  ACF_PICK(512, kBlock16, kDirect, kChordPoly)
+  ACF_PICK(512, kBlock16, kClamp, kChordPoly)
+#endif
   ACF_PICK(1024, kLane, kClamp, kDotAcos)
   ACF_PICK(1024, kBlock, kClamp, kDotAcos)
   ACF_PICK(512, kLane, kClamp, kDotAcos)
@@ -761,7 +772,7 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
     if (v != kChordPoly && v != kDotAcos && v != kDotFastAcos) return fail(c, ACF_ERR_ARG, "bin_method must be 0, 1 or 2");
     c->opt_method = (int)v;
   } else if (!strcmp(key, "layout")) {
-    if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "layout must be 0, 1 or 2");
+    if (v < 0 || v > 3) return fail(c, ACF_ERR_ARG, "layout must be 0, 1, 2 or 3");
     c->opt_layout = (int)v;
   } else if (!strcmp(key, "exact")) {
     if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "exact must be 0, 1 or 2");

@@ -73,7 +73,12 @@ constexpr int kJJBatch = ACF_JJ_BATCH;
 #endif  // j-loop unroll of the full-chunk path
 constexpr float kMagic = 8388608.0f;  // 2^23: adding it with round-toward-zero floors into the mantissa
 
-enum Layout { kLane = 1, kBlock = 2 };
+// kBlock16: two block-shared copies of 16-bit counters packed in pairs (a measured alternative for
+// fine binning, built with -DACF_U16_HIST=1, exact mode 0 only)
+enum Layout { kLane = 1, kBlock = 2, kBlock16 = 3 };
+#ifndef ACF_U16_HIST
+#define ACF_U16_HIST 0
+#endif
 enum BinMap { kDirect = 0, kClamp = 1 };
 enum Method { kChordPoly = 0, kDotAcos = 1, kDotFastAcos = 2 };
 
@@ -232,6 +237,23 @@ __device__ __forceinline__ float fma_rz(float a, float b, float c) { return __fm
 
 __device__ __forceinline__ void red_shared_add(uint32_t addr, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Add v to the 16-bit counter at shared byte address a16 (two counters per 32-bit word, so the add
+// goes to the word). The thread whose add takes the counter from below 0x8000 to 0x8000 or more
+// takes 0x8000 back out and returns true: its caller adds 0x8000 to the counter's bin elsewhere.
+// Adds in flight meanwhile only raise the counter further, and stay far below 0x8000 in total, so
+// the counter never carries into its neighbour.
+__device__ __forceinline__ bool add_u16(uint32_t a16, uint32_t v) {
+  const uint32_t word = a16 & ~3u, sh = (a16 & 2u) * 8u;
+  uint32_t old;
+  asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(word), "r"(v << sh) : "memory");
+  const uint32_t h = (old >> sh) & 0xFFFFu;
+  if (h < 0x8000u && h + v >= 0x8000u) {
+    red_shared_add(word, 0u - (0x8000u << sh));
+    return true;
+  }
+  return false;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr) {
@@ -773,14 +795,22 @@ struct FormTag {
 // fractional bits, biased by one unit: the entry is the code's integer part. Returns whether the
 // pair lies within one fine unit of an edge (biased fraction 0 or 1); such pairs go to push_flagged.
 // A pair at one fine unit below an edge is counted one entry up; the fp64 re-decision moves it.
-template <bool F>
+// shift 1 is the kBlock16 layout: 16-bit counters, whose overflow goes to the block's row.
+template <bool F, int MAP>
 __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint32_t base, uint32_t base_f, int shift,
                                          int S, uint32_t magic_bits, int i, int j, float xi, float yi, float zi,
                                          float4 v, uint32_t inc) {
   if (!F) {
     if (ACF_CHECK(cb - magic_bits < (uint32_t)p.bp.entries, 1, (long long)(cb - magic_bits), i,
-                  __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
-      red_shared_add((cb << shift) + base, inc);
+                  __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j)) {
+      if (shift == 1) {
+        if (add_u16((cb << 1) + base, inc))
+          atomicAdd(p.partial + (size_t)blockIdx.x * p.bp.nbins + entry_to_bin<MAP>((int)(cb - magic_bits), p.bp),
+                    0x8000ull);
+      } else {
+        red_shared_add((cb << shift) + base, inc);
+      }
+    }
     return false;
   } else {
     if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i,
@@ -871,6 +901,18 @@ __device__ __forceinline__ void flush_hist(const PairParams& p, uint32_t* hist, 
       if (lane == 0 && v && ACF_CHECK(entry_to_bin<MAP>(e, p.bp) < p.bp.nbins, 3, e, entry_to_bin<MAP>(e, p.bp)))
         atomicAdd(row + entry_to_bin<MAP>(e, p.bp), v);
     }
+  } else if (LAYOUT == kBlock16) {
+    const int words = (p.bp.entries + 1) / 2;  // per copy
+    for (int e = threadIdx.x; e < p.bp.entries; e += THREADS) {
+      const int sh = (e & 1) * 16;
+      const unsigned long long v = ((hist[e >> 1] >> sh) & 0xFFFFu) + ((hist[words + (e >> 1)] >> sh) & 0xFFFFu);
+      if (v && ACF_CHECK(entry_to_bin<MAP>(e, p.bp) < p.bp.nbins, 3, e, entry_to_bin<MAP>(e, p.bp)))
+        atomicAdd(row + entry_to_bin<MAP>(e, p.bp), v);
+    }
+    if (zero) {
+      __syncthreads();
+      for (int w = threadIdx.x; w < 2 * words; w += THREADS) hist[w] = 0;
+    }
   } else {
     for (int e = threadIdx.x; e < p.bp.entries; e += THREADS) {
       const unsigned long long v = hist[e];
@@ -900,7 +942,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   // (kept here, not in registers, to leave the hot loops all the registers)
   __shared__ unsigned int s_paths[WARPS][9];
   __shared__ float4 s_icap[WARPS];
-  const int words = (LAYOUT == kLane) ? p.bp.entries * 32 : p.bp.entries;
+  const int words = (LAYOUT == kLane) ? p.bp.entries * 32 : (LAYOUT == kBlock16 ? 2 * ((p.bp.entries + 1) / 2) : p.bp.entries);
   for (int w = tid; w < words; w += THREADS) hist[w] = 0;
   unsigned long long* row = p.partial + (size_t)blockIdx.x * p.bp.nbins;
   if (!p.accumulate)
@@ -915,8 +957,12 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   // every code is the float 2^23 + entry (the mirror offset is already inside the code)
   const uint32_t magic_bits = __float_as_uint(kMagic);
   // address of entry e in this lane's copy = (code bits << shift) + base
-  const uint32_t base = (LAYOUT == kLane) ? hist_addr + lane * 4u - (magic_bits << 7) : hist_addr - (magic_bits << 2);
-  constexpr int SHIFT = (LAYOUT == kLane) ? 7 : 2;
+  // kBlock16: the first half of the warps adds to copy 0, the second half to copy 1 (2 bytes a counter)
+  const uint32_t copy16 = (LAYOUT == kBlock16 && warp >= WARPS / 2) ? (uint32_t)((p.bp.entries + 1) / 2) * 4u : 0u;
+  const uint32_t base = (LAYOUT == kLane)     ? hist_addr + lane * 4u - (magic_bits << 7)
+                        : (LAYOUT == kBlock16) ? hist_addr + copy16 - (magic_bits << 1)
+                                               : hist_addr - (magic_bits << 2);
+  constexpr int SHIFT = (LAYOUT == kLane) ? 7 : (LAYOUT == kBlock16 ? 1 : 2);
   // exact mode: the fine code is 2^23 + (entry << S) + fraction; entry = (bits >> S) - (bits(2^23) >> S)
   const uint32_t base_f = (LAYOUT == kLane) ? hist_addr + lane * 4u - ((magic_bits >> p.bp.fine_shift) << 7)
                                             : hist_addr - ((magic_bits >> p.bp.fine_shift) << 2);
@@ -1053,7 +1099,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               for (int u = 0; u < B; ++u)
 #pragma unroll
                 for (int k = 0; k < K; ++k)
-                  add_pair<false>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
+                  add_pair<false, MAP>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
                                   xi[k], yi[k], zi[k], vv[u], inc);
             }
             return;
@@ -1071,7 +1117,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               for (int k = 0; k < K; ++k) {
                 cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
                                                                         iws_c, h_c, p.bp, ccs[k]));
-                add_pair<false>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
+                add_pair<false, MAP>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
                                 zi[k], v, inc);
 #if ACF_FLAG_PRED
                 fl |= (cfs[k] & (fmask & ~1u)) == 0u;
@@ -1096,7 +1142,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
               cbs[k] = code_of(k, v);
-              add_pair<F>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
+              add_pair<F, MAP>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
                           v, inc);
 #if ACF_FLAG_PRED
               if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
@@ -1177,7 +1223,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             for (int k = 0; k < K; ++k) {
               const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
               if (jj > thr[k] &&
-                  add_pair<F>(p, cb, base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
+                  add_pair<F, MAP>(p, cb, base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
                               yi[k], zi[k], v, inc))
                 push_flagged(p, cb, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
             }

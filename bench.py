@@ -213,6 +213,8 @@ def run_ours(args, cat, workload, rank, world, local):
     stream = torch.cuda.Stream(dev)
     ctx = acf.Context(local, stream)
     ctx.set_option("kernel_timing", 1)
+    for k, v in parse_options(args.option).items():
+        ctx.set_option(k, v)
     w, nb = cat.bin_width_deg, cat.nbins
     with torch.cuda.stream(stream):
         ra_d = torch.from_numpy(cat.ra_d).to(dev)
@@ -328,12 +330,15 @@ def run_ours(args, cat, workload, rank, world, local):
             "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak",
             # the pages' number is for two 100k catalogs in 0.25-degree bins only
-            "vs_baseline": value / (pairs / (PAGE_KERNEL_MS / 1e3) / 1e9) if args.config == 1 else None,
+            # (and with the default options only)
+            "vs_baseline": (value / (pairs / (PAGE_KERNEL_MS / 1e3) / 1e9)
+                            if args.config == 1 and not args.option else None),
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": workload, "n_d": cat.n_d, "n_r": cat.n_r, "bin_width_deg": w, "nbins": nb,
                        "l2": "flushed between timed steps (256 MiB device write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "grid": ctx.info("grid"), "threads": ctx.info("threads"), "layout": ctx.info("layout")},
+                       "grid": ctx.info("grid"), "threads": ctx.info("threads"), "layout": ctx.info("layout"),
+                       **({"options": parse_options(args.option)} if args.option else {})},
             "evaluated_gpairs_per_s": world * evals * args.steps / (total_ms_max / 1e3) / 1e9,
             "roofline": roof, "cpu_baseline": cb,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -354,6 +359,8 @@ def run_profile(args, cat):
 
     dev = torch.device("cuda", 0)
     ctx = acf.Context(0)
+    for k, v in parse_options(args.option).items():
+        ctx.set_option(k, v)
     w, nb = cat.bin_width_deg, cat.nbins
     t = {k: torch.from_numpy(getattr(cat, k)).to(dev) for k in ("ra_d", "dec_d", "ra_r", "dec_r")}
     out = [torch.empty(nb, dtype=torch.int64, device=dev) for _ in range(3)]
@@ -457,6 +464,17 @@ def run_ablation(args, cat) -> int:
     return 0
 
 
+def parse_options(items) -> dict:
+    """["exact=0", "layout=3"] -> {"exact": 0, "layout": 3}"""
+    out = {}
+    for it in items:
+        k, sep, v = it.partition("=")
+        if not sep or not k:
+            raise SystemExit(f"--option wants KEY=VALUE, got {it!r}")
+        out[k] = int(v)
+    return out
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,6 +485,8 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-rows", type=int, default=2000, help="rows per family for the CPU baseline (0: skip)")
     ap.add_argument("--ref-rows", type=int, default=200, help="rows per family per reference-arm step")
     ap.add_argument("--profile", action="store_true", help="one warm-up step + one step only (for ncu)")
+    ap.add_argument("--option", action="append", default=[], metavar="KEY=VALUE",
+                    help="a library option (acf_set_option) for the timed run, e.g. exact=0; repeatable")
     ap.add_argument("--ablation", action="store_true",
                     help="the page's ladder and one-change variants of the library, timed and checked")
     args = ap.parse_args(argv)

@@ -174,7 +174,9 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    2 = dot product + the arccos polynomial of Abramowitz and Stegun 4.4.45 (the
  *                        approximate mode: error up to 6.7e-5 rad, so many pairs near edges move;
  *                        sums stay exact). Methods 1 and 2 take no exact mode and no range forms.
- *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram
+ *   "layout"         0 = automatic, 1 = lane-private copies, 2 = one block-shared histogram,
+ *                    3 = two block-shared copies of 16-bit counters (only in a library built with
+ *                        -DACF_U16_HIST=1, and only with "exact" 0; ACF_ERR_UNSUPPORTED otherwise)
  *   "exact"          0 = fp32 bins only (precision contract above);
  *                    1 = re-decide in fp64 the pairs within ~1e-6 rad of an edge whose separation is
  *                        below "exact_below_deg" or above 180 minus it;

@@ -50,3 +50,11 @@ def test_max_over_two_gloo_ranks():
     for p in ps:
         p.join(timeout=60)
     assert res[0] == res[1] == [2.0, 10.0]
+
+
+def test_option_arguments_parse_to_library_options():
+    import bench
+    assert bench.parse_options([]) == {}
+    assert bench.parse_options(["exact=0", "layout=3"]) == {"exact": 0, "layout": 3}
+    with pytest.raises(SystemExit):
+        bench.parse_options(["exact"])

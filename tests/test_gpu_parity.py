@@ -320,6 +320,28 @@ def test_exact_mode_2_equals_oracle_bin_for_bin(acf, ctx, w, nb):
         ctx.set_option("exact", DEFAULT_EXACT)
 
 
+def test_pairs_exactly_on_edges_take_the_fp64_fallback(acf, ctx):
+    # Equator galaxies 15 arcmin apart and meridian galaxies 15 arcmin apart: every separation is a
+    # whole number of 0.25-degree bins, so every pair lies exactly on an edge. The fp32 code flags
+    # them, the double-single pass cannot settle them (q equals the edge value to far below its
+    # error bound), and the fp64 re-decision decides. A pair exactly on an edge may land on either
+    # side within the rounding of the fp64 formula, which the edge rule allows.
+    ra_eq = (7.5 + 15.0 * np.arange(200)).astype(np.float32)
+    dec_eq = np.zeros(200, np.float32)
+    dec_mer = (-2970.0 + 15.0 * np.arange(396)).astype(np.float32)
+    ra_mer = np.full(396, 1000.0, np.float32)
+    ctx.set_option("exact", 2)
+    try:
+        for ra, dec in ((ra_eq, dec_eq), (ra_mer, dec_mer)):
+            _compare(acf, ctx, ra, dec, None, None, 0.25, 720)
+            flagged, redone = ctx.info("exact_flagged"), ctx.info("exact_redone_fp64")
+            n = len(ra)
+            assert redone > 0 and redone <= flagged
+            assert flagged >= n * (n - 1) // 2 // 2  # most of the off-diagonal pairs are on an edge
+    finally:
+        ctx.set_option("exact", DEFAULT_EXACT)
+
+
 def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
     c = synth.catalogs(4000, 3100, 12, 30.0, seed=15)
     ctx.set_option("exact", 0)

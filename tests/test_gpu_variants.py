@@ -1,0 +1,104 @@
+"""Measured alternatives that stay behind compile switches, held to the same parity bar.
+
+- ACF_U16_HIST=1 adds layout 3: two block-shared copies of 16-bit counters, whose overflow is
+  carried into the block's u64 row. In exact mode 0 its histograms must equal those of the 32-bit
+  block-shared layout bit for bit. That includes a 5 x 5 degree field in 0.01-degree bins, where
+  single bins pass 0x8000 counts per copy many times over.
+- ACF_J_SHUFFLE=1 broadcasts the j-vectors by warp shuffles instead of shared-memory loads. In the
+  default exact mode 2 its histograms must equal the fp64 oracle's bin for bin.
+
+Each variant is built on the spot and exercised in a child process, which loads it through
+ACF_LIB.
+"""
+import concurrent.futures
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+from all_pairs_angular_gb300 import build as acf_build
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+VARIANTS = {"u16": ["-DACF_U16_HIST=1"], "shuffle": ["-DACF_J_SHUFFLE=1"]}
+
+
+@pytest.fixture(scope="module")
+def libs():
+    acf_build.build()  # the default library first (its build directory and staleness check)
+    out = {k: os.path.join(acf_build.BUILD_DIR, f"libacf_{k}.so") for k in VARIANTS}
+    with concurrent.futures.ThreadPoolExecutor(len(VARIANTS)) as ex:
+        futs = [ex.submit(acf_build.build, out=out[k], extra=flags) for k, flags in VARIANTS.items()]
+        for f in futs:
+            f.result()
+    return out
+
+
+def _child(lib, code):
+    env = dict(os.environ, ACF_LIB=lib)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+U16_CODE = r"""
+import json, numpy as np, torch, synth
+import all_pairs_angular_gb300 as acf
+ctx = acf.Context(0)
+ctx.set_option("exact", 0)
+res = {}
+for name, c in (("small-field", synth.config(2)), ("mixed", synth.catalogs(30000, 20000, 8, 60.0, seed=41))):
+    t = {k: torch.from_numpy(getattr(c, k)).cuda() for k in ("ra_d", "dec_d", "ra_r", "dec_r")}
+    h = {}
+    for lay in (2, 3):
+        ctx.set_option("layout", lay)
+        dd = acf.as_uint64(ctx.histogram(t["ra_d"], t["dec_d"], bin_width_deg=0.01, nbins=18000))
+        dr = acf.as_uint64(ctx.histogram(t["ra_d"], t["dec_d"], t["ra_r"], t["dec_r"], bin_width_deg=0.01, nbins=18000))
+        torch.cuda.synchronize()
+        h[lay] = (dd, dr, ctx.info("layout"))
+    res[name] = {"equal": bool(np.array_equal(h[2][0], h[3][0]) and np.array_equal(h[2][1], h[3][1])),
+                 "layout": h[3][2], "max_dd": int(h[3][0].max()), "sum_dd": int(h[3][0].sum()),
+                 "n_d": c.n_d}
+ctx.set_option("layout", 3)
+ctx.set_option("exact", 2)
+try:
+    ctx.histogram(t["ra_d"], t["dec_d"], bin_width_deg=0.01, nbins=18000)
+    res["exact_refused"] = False
+except Exception:
+    res["exact_refused"] = True
+print(json.dumps(res))
+"""
+
+
+def test_u16_counters_equal_32_bit_counters(libs):
+    res = _child(libs["u16"], U16_CODE)
+    for name in ("small-field", "mixed"):
+        r = res[name]
+        assert r["layout"] == 3 and r["equal"], res
+        assert r["sum_dd"] == r["n_d"] ** 2
+    # 100k galaxies in a 5x5 degree field: bins far above what one 16-bit counter can hold
+    assert res["small-field"]["max_dd"] > 152 * 2 * 0x8000
+    assert res["exact_refused"]
+
+
+SHUFFLE_CODE = r"""
+import json, numpy as np, torch, synth, oracle
+import all_pairs_angular_gb300 as acf
+ctx = acf.Context(0)
+c = synth.catalogs(3000, 2500, 10, 30.0, seed=43)
+ok = []
+for args in ((c.ra_d, c.dec_d, None, None), (c.ra_d, c.dec_d, c.ra_r, c.dec_r)):
+    g = acf.as_uint64(ctx.histogram(*args, bin_width_deg=0.25, nbins=720))
+    torch.cuda.synchronize()
+    o = oracle.histogram(*args, 0.25, 720)
+    ok.append(bool(np.array_equal(g, o.hist)))
+print(json.dumps({"equal": ok}))
+"""
+
+
+def test_shuffle_broadcast_equals_oracle_in_exact_mode(libs):
+    res = _child(libs["shuffle"], SHUFFLE_CODE)
+    assert res["equal"] == [True, True], res
