@@ -269,7 +269,7 @@ PairKernelFn pick_kernel(const Plan& pl) {
 struct CatBufs {
   float4* v = nullptr;       // unit vectors in spatial order (fp32)
   float4* lo = nullptr;      // what fp32 leaves of the fp64 components (double-single with v)
-  double4* v64 = nullptr;    // the same in fp64 (exact re-decision)
+  double4_32a* v64 = nullptr;    // the same in fp64 (exact re-decision)
   float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
 };
@@ -312,7 +312,7 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
     const long long ch = (m + 127) / 128;
     cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
     cb.lo = reinterpret_cast<float4*>(take((size_t)m * 16));
-    cb.v64 = reinterpret_cast<double4*>(take((size_t)m * 32));
+    cb.v64 = reinterpret_cast<double4_32a*>(take((size_t)m * 32));
     cb.cap32 = reinterpret_cast<float4*>(take((size_t)ch * 4 * 16));
     cb.cap128 = reinterpret_cast<float4*>(take((size_t)ch * 16));
   };

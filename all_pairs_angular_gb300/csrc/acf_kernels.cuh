@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(
 // (|x - hi - lo| <= 2^-48 |x|): together a double-single copy for the fix-up's first pass.
 __global__ void vectors_kernel(const float* __restrict__ ra, const float* __restrict__ dec,
                                const unsigned int* __restrict__ order, long long n, float4* __restrict__ v_out,
-                               float4* __restrict__ lo_out, double4* __restrict__ v64_out) {
+                               float4* __restrict__ lo_out, double4_32a* __restrict__ v64_out) {
   for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n; p += (long long)gridDim.x * blockDim.x) {
     const unsigned int src = order[p];
     if (ACF_CHECK(src < (unsigned long long)n, 5, p, src)) {
@@ -489,7 +489,7 @@ __global__ void vectors_kernel(const float* __restrict__ ra, const float* __rest
       const float hx = (float)x, hy = (float)y, hz = (float)z;
       v_out[p] = make_float4(hx, hy, hz, 0.0f);
       lo_out[p] = make_float4((float)(x - (double)hx), (float)(y - (double)hy), (float)(z - (double)hz), 0.0f);
-      v64_out[p] = make_double4(x, y, z, 0.0);
+      v64_out[p] = make_double4_32a(x, y, z, 0.0);
     }
   }
 }
@@ -1102,9 +1102,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                   add_pair<false, MAP>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
                                   xi[k], yi[k], zi[k], vv[u], inc);
             }
-            return;
-          }
-          if constexpr (F && (X == 1 || X == 3)) {
+          } else if constexpr (F && (X == 1 || X == 3)) {
             // fixed-sign chord with flags: the plain code addresses the histogram (as without flags),
             // the fine code, from the same theta', only decides the flag
 #pragma unroll 1
@@ -1131,31 +1129,31 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                   if ((cfs[k] & fmask) <= 1u) push_flagged2(p, cfs[k], ccs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
               }
             }
-            return;
-          }
+          } else {
 #pragma unroll U
-          for (int jj = jbeg; jj < jbeg + 32; ++jj) {
-            const float4 v = jvec(jj);
-            uint32_t cbs[K];
-            uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
-            bool fl = false;
+            for (int jj = jbeg; jj < jbeg + 32; ++jj) {
+              const float4 v = jvec(jj);
+              uint32_t cbs[K];
+              uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
+              bool fl = false;
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-              cbs[k] = code_of(k, v);
-              add_pair<F, MAP>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
-                          v, inc);
+              for (int k = 0; k < K; ++k) {
+                cbs[k] = code_of(k, v);
+                add_pair<F, MAP>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
+                            v, inc);
 #if ACF_FLAG_PRED
-              if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
+                if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
 #else
-              if (F) low = min(low, cbs[k] & fmask);
+                if (F) low = min(low, cbs[k] & fmask);
 #endif
-            }
-            // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
-            if (F && __any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
+              }
+              // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
+              if (F && __any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
 #pragma unroll
-              for (int k = 0; k < K; ++k)
-                if ((cbs[k] & fmask) <= 1u)
-                  push_flagged(p, cbs[k], SF, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, bf, SHIFT);
+                for (int k = 0; k < K; ++k)
+                  if ((cbs[k] & fmask) <= 1u)
+                    push_flagged(p, cbs[k], SF, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, bf, SHIFT);
+              }
             }
           }
         };
@@ -1390,7 +1388,7 @@ __global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4*
                                                     const unsigned int* __restrict__ qspill, unsigned int qcap,
                                                     const float4* __restrict__ hi_i, const float4* __restrict__ lo_i,
                                                     const float4* __restrict__ hi_j, const float4* __restrict__ lo_j,
-                                                    const double4* __restrict__ vi, const double4* __restrict__ vj,
+                                                    const double4_32a* __restrict__ vi, const double4_32a* __restrict__ vj,
                                                     const double* __restrict__ T, const double* __restrict__ U,
                                                     const float2* __restrict__ Tds, const float2* __restrict__ Uds,
                                                     BinParams bp, unsigned int inc, unsigned long long* __restrict__ delta,
@@ -1459,7 +1457,7 @@ __global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4*
     if (!sure) {
       // too close to an edge for the double-single bound: the same comparisons in fp64
       ++my_redone;
-      const double4 a = vi[rec.x], b = vj[rec.y];
+      const double4_32a a = vi[rec.x], b = vj[rec.y];
       k = k0;
       if (diff) {
         const double dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z;
