@@ -56,6 +56,8 @@ struct acf_ctx {
   // options
   int opt_threads = 0, opt_ctas = 0, opt_method = kChordPoly, opt_layout = 0, opt_timing = 0;
   long long opt_units_per_launch = 0;
+  long long opt_workspace_limit = 0;   // bytes a workspace may grow to (0: no limit)
+  long long inject_launch_error = 0;   // fault injection: the n-th kernel launch from now reports an error
   int opt_exact = 2;              // 0 off, 1 near 0 and 180 degrees, 2 everywhere
   double opt_exact_below_deg = 20.0;
   int opt_range_forms = 1;        // 1: cheaper forms where the caps bound the separations
@@ -93,18 +95,27 @@ int cuda_fail(acf_ctx* c, cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail((c), e_, #call); \
   } while (0)
 
-// Check a kernel launch just made on context c and count it.
-#define ACF_LAUNCHED(c)                   \
-  do {                                    \
-    ACF_CUDA((c), cudaGetLastError());    \
-    ++(c)->kernel_launches;               \
+// Check a kernel launch just made on context c and count it. With the option
+// "inject_launch_error" n, the n-th launch from then on is reported as failed (host-side fault
+// injection: the launch itself ran normally and nothing touches the device).
+#define ACF_LAUNCHED(c)                                                                                   \
+  do {                                                                                                    \
+    ACF_CUDA((c), cudaGetLastError());                                                                    \
+    ++(c)->kernel_launches;                                                                               \
+    if ((c)->inject_launch_error > 0 && --(c)->inject_launch_error == 0)                                  \
+      return fail((c), ACF_ERR_CUDA, "injected launch failure (option inject_launch_error) after launch %lld", \
+                  (c)->kernel_launches);                                                                  \
   } while (0)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int ensure(acf_ctx* c, Workspace& w, size_t bytes) {
   if (bytes <= w.bytes) return ACF_OK;
-  size_t want = std::max(bytes, w.bytes + w.bytes / 2);
+  const size_t limit = c->opt_workspace_limit > 0 ? (size_t)c->opt_workspace_limit : SIZE_MAX;
+  if (bytes > limit)
+    return fail(c, ACF_ERR_NOMEM, "a workspace of %zu bytes exceeds the limit of %zu bytes (option workspace_limit)",
+                bytes, limit);
+  size_t want = std::min(std::max(bytes, w.bytes + w.bytes / 2), limit);
   if (w.ptr) {
     ACF_CUDA(c, cudaStreamSynchronize(c->stream));
     ACF_CUDA(c, cudaFree(w.ptr));
@@ -789,6 +800,12 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "units_per_launch")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "units_per_launch must be >= 0");
     c->opt_units_per_launch = v;
+  } else if (!strcmp(key, "workspace_limit")) {
+    if (v < 0) return fail(c, ACF_ERR_ARG, "workspace_limit must be >= 0");
+    c->opt_workspace_limit = v;
+  } else if (!strcmp(key, "inject_launch_error")) {
+    if (v < 0) return fail(c, ACF_ERR_ARG, "inject_launch_error must be >= 0");
+    c->inject_launch_error = v;
   } else if (!strcmp(key, "kernel_timing")) {
     c->opt_timing = v ? 1 : 0;
     if (c->opt_timing && c->ev.empty()) {

@@ -194,6 +194,12 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *   "units_per_launch"  cap on work units (128 x 128 pairs) per pair-kernel launch; 0 = automatic
  *                    (large problems are always split so that no 32-bit shared counter can wrap)
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
+ *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
+ *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
+ *   "inject_launch_error"  fault injection for tests, on the host only: the n-th kernel launch from
+ *                    now on is reported as failed (ACF_ERR_CUDA, "injected" in the message) and the
+ *                    call returns at once; the launch itself ran normally, the device is untouched,
+ *                    and the next call works as usual (0 = off, default; it resets after firing)
  * Unknown keys and out-of-range values return ACF_ERR_ARG and leave the option unchanged.
  */
 int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
