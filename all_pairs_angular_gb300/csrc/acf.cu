@@ -295,7 +295,7 @@ struct Scratch {
   unsigned int* counts = nullptr;      // sort: digit counts per tile, then their offsets
   CatBufs a, b;                        // b only for cross-correlations
   unsigned long long* partial = nullptr;
-  unsigned long long* delta = nullptr; // exact mode: count moves of the fp64 re-decision, per bin
+  unsigned long long* delta = nullptr; // exact mode: count moves of the exact re-decision, per bin
   double* T = nullptr;                 // exact mode: edge tables, nbins + 1 each
   double* U = nullptr;
   float2* Tds = nullptr;               // the same as double-single (hi, lo) pairs

@@ -27,8 +27,9 @@
 //   * persistent blocks whose warps take 128 x 128-pair work units from a global ticket (only the
 //     upper triangle for DD/RR); per-block counts go to per-block uint64 rows that a final kernel
 //     reduces;
-//   * optionally (exact mode), pairs whose fast code lies within a fine unit of a bin edge are
-//     queued and re-decided in fp64 after the merge.
+//   * in exact mode (the default), pairs whose fast code lies within a fine unit of a bin edge are
+//     queued and re-decided after every launch: in double-single fp32 where that settles them,
+//     else in fp64.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -172,7 +173,7 @@ struct PairParams {
                                        // block b owns slots [b qbatch, (b + 1) qbatch), then a shared
                                        // spill region from gridDim.x qbatch on
   unsigned int* qspill;                // spill slots handed out
-  unsigned int* qused;                 // per block: slots of its own region in use
+  unsigned int* qused;                 // per block: slots of its own region in use (at most qbatch)
   unsigned int* qflagged;              // pairs flagged (for reporting)
   unsigned int qcap;                   // queue slots
   unsigned int qbatch;                 // slots a block owns
@@ -794,7 +795,7 @@ struct FormTag {
 // Add one pair to the shared histogram. With F (exact mode) the code carries fine_shift extra
 // fractional bits, biased by one unit: the entry is the code's integer part. Returns whether the
 // pair lies within one fine unit of an edge (biased fraction 0 or 1); such pairs go to push_flagged.
-// A pair at one fine unit below an edge is counted one entry up; the fp64 re-decision moves it.
+// A pair at one fine unit below an edge is counted one entry up; the exact re-decision moves it.
 // shift 1 is the kBlock16 layout: 16-bit counters, whose overflow goes to the block's row.
 template <bool F, int MAP>
 __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint32_t base, uint32_t base_f, int shift,
@@ -820,7 +821,7 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
   }
 }
 
-// Queue a near-edge pair for the fp64 re-decision if its entry lies in the exact zone (a function
+// Queue a near-edge pair for the exact re-decision if its entry lies in the exact zone (a function
 // of the pair's own code, so the set of re-decided pairs does not depend on grouping or order).
 // A pair that is not queued (outside the zone, or the queue is full) keeps its fp32 bin: if the
 // one-unit bias carried it into the next entry (biased fraction 0), its count moves back.
@@ -1280,7 +1281,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const unsigned 
   __syncthreads();
   if (warp == 0 && k < nbins) {
     unsigned long long t = (k == 0) ? self_pairs : 0ull;
-    if (delta) t += delta[k];  // exact mode: counts moved by the fp64 re-decision (two's complement)
+    if (delta) t += delta[k];  // exact mode: counts moved by the exact re-decision (two's complement)
 #pragma unroll
     for (int w = 0; w < kMergeWarps; ++w) t += acc[w][lane];
     out[k] = t;

@@ -139,11 +139,41 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def code_only(text: str) -> str:
+    """C++/CUDA source without comments, trailing blanks and empty lines (what the compiler sees)."""
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        ch = text[i]
+        if quote:
+            out.append(ch)
+            if ch == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 1
+            elif ch == quote:
+                quote = None
+        elif ch in "\"'":
+            quote = ch
+            out.append(ch)
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+            continue
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            continue
+        else:
+            out.append(ch)
+        i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments excluded), to tie recorded ncu counters to them."""
     h = hashlib.sha256()
     for rel in ("all_pairs_angular_gb300/csrc/acf_kernels.cuh", "all_pairs_angular_gb300/csrc/acf.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -58,3 +58,13 @@ def test_option_arguments_parse_to_library_options():
     assert bench.parse_options(["exact=0", "layout=3"]) == {"exact": 0, "layout": 3}
     with pytest.raises(SystemExit):
         bench.parse_options(["exact"])
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    import bench
+    a = 'int f() { return 1; } // one\n/* block */\nconst char* s = "a//b";\n'
+    b = 'int f() { return 1; }\n\n// another comment\nconst char* s = "a//b";   \n'
+    c = 'int f() { return 2; }\nconst char* s = "a//b";\n'
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert '"a//b"' in bench.code_only(a)
