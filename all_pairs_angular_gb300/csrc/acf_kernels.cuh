@@ -46,6 +46,11 @@ constexpr int kJJUnroll = ACF_JJ_UNROLL;
 #define ACF_JJ_UNROLL_FINE 1
 #endif
 constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact-mode (fine code) loops
+#ifndef ACF_JJ_UNROLL_FINE2
+#define ACF_JJ_UNROLL_FINE2 1
+#endif
+constexpr int kJJUnrollFine2 = ACF_JJ_UNROLL_FINE2;  // and of the two-code (fixed-sign chord) ones
+// (both measured slower unrolled twice: the queue code then no longer fits the instruction cache)
 // Flag test per j: 1 = OR of per-pair tests "biased fraction bits above bit 0 all zero"; 0 = a
 // running minimum of the biased fractions compared with 1 (measured alternative: 12.62 against
 // 12.47 ms of pair kernels per 100k step)
@@ -1106,7 +1111,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           } else if constexpr (F && (X == 1 || X == 3)) {
             // fixed-sign chord with flags: the plain code addresses the histogram (as without flags),
             // the fine code, from the same theta', only decides the flag
-#pragma unroll 1
+#pragma unroll kJJUnrollFine2
             for (int jj = jbeg; jj < jbeg + 32; ++jj) {
               const float4 v = jvec(jj);
               uint32_t cfs[K], ccs[K];
