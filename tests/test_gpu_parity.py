@@ -342,6 +342,32 @@ def test_pairs_exactly_on_edges_take_the_fp64_fallback(acf, ctx):
         ctx.set_option("exact", DEFAULT_EXACT)
 
 
+def test_largest_histogram_that_fits_and_the_next_is_refused(acf, ctx):
+    # The block-shared histogram (512 threads, 16 warps' 4 KB j-tiles) fills the shared memory at
+    # 41,216 entries. Direct map (180/w integral): P + 2 entries, so P = 41214 is the largest; clamp
+    # map: nbins entries when nbins <= floor(P) + 1. Both must still equal the oracle bin for bin
+    # (exact mode 2); one entry more must be refused, and the context must keep working.
+    c = synth.catalogs(1500, 1200, 6, 60.0, seed=71)
+    lib = acf.load()
+    ctx.set_option("exact", 2)
+    try:
+        for w, nb in ((180.0 / 41214, 41214), (180.0 / 41189.9, 41190)):
+            for args in ((c.ra_d, c.dec_d, None, None), (c.ra_d, c.dec_d, c.ra_r, c.dec_r)):
+                g, o, rep = _compare(acf, ctx, *args, w, nb)
+                assert np.array_equal(g, o.hist), (w, nb, rep)
+            assert ctx.info("hist_entries") in (41216, 41190) and ctx.info("threads") == 512
+        ra, dec = torch.from_numpy(c.ra_d).cuda(), torch.from_numpy(c.dec_d).cuda()
+        for w, nb in ((180.0 / 41216, 41216), (180.0 / 41300.5, 41217)):
+            out = torch.empty(nb, dtype=torch.int64, device="cuda")
+            rc = lib.acf_histogram(ctx.handle, ra.data_ptr(), dec.data_ptr(), c.n_d, None, None, 0, w, nb,
+                                   out.data_ptr())
+            assert rc == acf.ACF_ERR_UNSUPPORTED, (w, nb, rc)
+            assert "shared memory" in acf.acf_last_error(ctx.handle)
+        _compare(acf, ctx, c.ra_d, c.dec_d, None, None, 0.25, 720)
+    finally:
+        ctx.set_option("exact", DEFAULT_EXACT)
+
+
 def test_exact_mode_off_still_meets_edge_rule(acf, ctx):
     c = synth.catalogs(4000, 3100, 12, 30.0, seed=15)
     ctx.set_option("exact", 0)
