@@ -22,7 +22,8 @@ using namespace acf;
 namespace {
 
 constexpr int kK = 4;                          // i-galaxies per thread (32 * kK == kJT)
-constexpr int kMaxEntries = 49152;             // histogram entries a block can hold (192 KB)
+constexpr int kMaxEntries = 49152;             // entries a code may address (the shared-memory plan
+                                               // binds first: 41,216 beside 512 threads' tiles)
 constexpr size_t kWarpTileBytes = 2 * kJT * sizeof(float4);  // one warp's double-buffered j-tile
 constexpr size_t kMaxSmem = 232448 - 2048;  // dynamic shared memory per block: 227 KB less the pair kernel's static arrays
 constexpr int kMaxTimed = 4096;
