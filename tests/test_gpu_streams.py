@@ -1,0 +1,102 @@
+"""Stream semantics of the C ABI: calls are stream-ordered and asynchronous on the context's stream.
+
+- Two contexts on two streams, with all their work in flight at once, give the same histograms as
+  one context run alone.
+- acf_set_stream moves a context to another stream between calls.
+- A warmed-up acf_correlate (its workspace already allocated) can be captured into a CUDA graph
+  and replayed. The replays give the captured call's results.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.fixture(scope="module")
+def data(acf):
+    a = synth.catalogs(6000, 5000, 10, 30.0, seed=81)
+    b = synth.catalogs(4000, 4500, 6, 60.0, seed=82)
+    ref = {}
+    ctx = acf.Context(0)
+    for name, c in (("a", a), ("b", b)):
+        t = tuple(map(_dev, (c.ra_d, c.dec_d, c.ra_r, c.dec_r)))
+        out = ctx.correlate(*t, 0.25, 720)
+        torch.cuda.synchronize()
+        ref[name] = (t, [acf.as_uint64(h).copy() for h in out[:3]], out[3].cpu().numpy())
+    ctx.close()
+    return ref
+
+
+def test_two_contexts_on_two_streams_at_once(acf, data):
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    c1, c2 = acf.Context(0, s1), acf.Context(0, s2)
+    try:
+        outs = []
+        for _ in range(3):  # several rounds, nothing synchronised in between
+            with torch.cuda.stream(s1):
+                o1 = c1.correlate(*data["a"][0], 0.25, 720)
+            with torch.cuda.stream(s2):
+                o2 = c2.correlate(*data["b"][0], 0.25, 720)
+            outs.append((o1, o2))
+        torch.cuda.synchronize()
+        for o1, o2 in outs:
+            for o, name in ((o1, "a"), (o2, "b")):
+                for h, r in zip(o[:3], data[name][1]):
+                    assert np.array_equal(acf.as_uint64(h), r)
+                assert np.allclose(o[3].cpu().numpy(), data[name][2], rtol=0, atol=0, equal_nan=True)
+    finally:
+        c1.close()
+        c2.close()
+
+
+def test_set_stream_moves_a_context(acf, data):
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ctx = acf.Context(0, s1)
+    try:
+        with torch.cuda.stream(s1):
+            o1 = ctx.correlate(*data["a"][0], 0.25, 720)
+        s2.wait_stream(s1)
+        acf.acf_set_stream(ctx.handle, s2)
+        ctx.stream = s2
+        with torch.cuda.stream(s2):
+            o2 = ctx.correlate(*data["b"][0], 0.25, 720)
+        torch.cuda.synchronize()
+        for o, name in ((o1, "a"), (o2, "b")):
+            for h, r in zip(o[:3], data[name][1]):
+                assert np.array_equal(acf.as_uint64(h), r)
+    finally:
+        ctx.close()
+
+
+def test_correlate_captured_in_a_cuda_graph(acf, data):
+    s = torch.cuda.Stream()
+    ctx = acf.Context(0, s)
+    try:
+        t, ref, ref_om = data["a"]
+        outs = tuple(torch.empty(720, dtype=torch.int64, device="cuda") for _ in range(3)) + (
+            torch.empty(720, dtype=torch.float64, device="cuda"),)
+        with torch.cuda.stream(s):
+            ctx.correlate(*t, 0.25, 720, out=outs)  # warm-up: allocates the workspace
+        s.synchronize()
+        for o in outs:
+            o.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            ctx.correlate(*t, 0.25, 720, out=outs)
+        for _ in range(3):
+            for o in outs:
+                o.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            for h, r in zip(outs[:3], ref):
+                assert np.array_equal(acf.as_uint64(h), r)
+            assert np.allclose(outs[3].cpu().numpy(), ref_om, rtol=0, atol=0, equal_nan=True)
+    finally:
+        ctx.close()
