@@ -57,13 +57,18 @@ constexpr int kJJUnrollFine2 = ACF_JJ_UNROLL_FINE2;  // and of the two-code (fix
 #ifndef ACF_FLAG_PRED
 #define ACF_FLAG_PRED 1
 #endif
-// Fix-up: queued pairs a thread loads at once, and the blocks per SM its registers must allow
-// (measured: 2 and 4 alike, 4 and 2 slower on fine bins)
+// Fix-up: queued pairs a thread loads at once, the blocks per SM its registers must allow, and
+// whether the next records load while the current pairs are decided. Measured per step (100k;
+// fine-200k): 2, 4, prefetch 12.94 and 111.6 ms; 3, 3, no prefetch 12.99 and 112.0; 3, 3, prefetch
+// 12.96 and 115.1 (spills); 4, 2, no prefetch slower on fine bins.
 #ifndef ACF_FIXUP_ILP
-#define ACF_FIXUP_ILP 3
+#define ACF_FIXUP_ILP 2
 #endif
 #ifndef ACF_FIXUP_MINB
-#define ACF_FIXUP_MINB 3
+#define ACF_FIXUP_MINB 4
+#endif
+#ifndef ACF_FIXUP_PREFETCH
+#define ACF_FIXUP_PREFETCH 1
 #endif
 #ifndef ACF_JJ_BATCH
 #define ACF_JJ_BATCH 2
@@ -1491,14 +1496,17 @@ __global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4*
   // slots first, first + stride, ... below n of queue[base ..]: kFixupILP records per thread at a
   // time, all loads issued before any arithmetic (the loads are what this kernel waits for)
   auto run = [&](unsigned int base, unsigned int n, unsigned int first, unsigned int stride) {
-    for (unsigned int t = first; t < n; t += kFixupILP * stride) {
-      uint4 rec[kFixupILP];
-      bool ok[kFixupILP];
+    uint4 rec[kFixupILP];
+    bool ok[kFixupILP];
+    auto fetch = [&](unsigned int t, uint4* r, bool* o) {
 #pragma unroll
       for (int u = 0; u < kFixupILP; ++u) {
-        ok[u] = t + u * stride < n;
-        rec[u] = ok[u] ? queue[base + t + u * stride] : make_uint4(0u, 0u, 0u, 0u);
+        o[u] = t + u * stride < n;
+        r[u] = o[u] ? queue[base + t + u * stride] : make_uint4(0u, 0u, 0u, 0u);
       }
+    };
+    fetch(first, rec, ok);
+    for (unsigned int t = first; t < n; t += kFixupILP * stride) {
       float4 ah[kFixupILP], al[kFixupILP], bh[kFixupILP], bl[kFixupILP];
 #pragma unroll
       for (int u = 0; u < kFixupILP; ++u) {
@@ -1507,9 +1515,24 @@ __global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4*
         bh[u] = hi_j[rec[u].y];
         bl[u] = lo_j[rec[u].y];
       }
+#if ACF_FIXUP_PREFETCH
+      // the next records load while these pairs are decided
+      uint4 nrec[kFixupILP];
+      bool nok[kFixupILP];
+      fetch(t + kFixupILP * stride, nrec, nok);
+#endif
 #pragma unroll
       for (int u = 0; u < kFixupILP; ++u)
         if (ok[u]) redo(rec[u], ah[u], al[u], bh[u], bl[u]);
+#if ACF_FIXUP_PREFETCH
+#pragma unroll
+      for (int u = 0; u < kFixupILP; ++u) {
+        rec[u] = nrec[u];
+        ok[u] = nok[u];
+      }
+#else
+      fetch(t + kFixupILP * stride, rec, ok);
+#endif
     }
   };
   // this block's share of its region, then its share of the spill slots
