@@ -178,14 +178,14 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   if (pl.exact) {
     // Worst-case fp32 error of each form (every rounding aligned): the full-range chord <= 1.25e-6
     // rad (near 90 degrees), the short chord (theta' <= 72 deg) <= 1.05e-6, the dot form (55..125
-    // deg) <= 7e-7. Mode 1 only re-decides separations within exact_lo of 0 or 180 degrees, where
+    // deg) <= 6e-7. Mode 1 only re-decides separations within exact_lo of 0 or 180 degrees, where
     // the chord's error is err1(lo) (vectors, chord rounding ~ tan(theta'/2), polynomial, sqrt and
     // 1/w ~ theta'). Each form's S is the largest whose window 2^-S bins covers its bound.
     const double lo = std::min(c->opt_exact_below_deg, 90.0) * pi / 180.0;
     const double err1 = 1.2e-7 / std::cos(lo / 2) + 6e-7 * std::tan(lo / 2) + 5e-8 + 3.5e-7 * lo;
     const double err_full = (pl.exact == 2) ? 1.25e-6 : err1;
     const double err_small = (pl.exact == 2) ? 1.05e-6 : err1;
-    const double err_mid = (pl.exact == 2) ? 7e-7 : err1;
+    const double err_mid = (pl.exact == 2) ? 6e-7 : err1;
     const int room = (int)std::floor(std::log2(8.0e6 / ((double)bp.entries + 2.0)));  // (entries+2) << S < 2^23
     auto shift_for = [&](double err) {
       return std::max(0, std::min((int)std::floor(std::log2(w_rad / err)), room));

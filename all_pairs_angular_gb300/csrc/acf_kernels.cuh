@@ -120,13 +120,13 @@ __device__ constexpr float kS0 = 0.99999908438480867f, kS1 = 0.08335094100319942
 constexpr float kSmallRad = 1.2566370614359172f;  // 72 degrees
 
 // Between 55 and 125 degrees the dot product d = u.v loses little: theta = pi/2 - asin(d) with
-// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(53 deg), degree 4: absolute
-// theta error <= 2.4e-7 rad (2.7e-7 after fp32 rounding), within the exact mode's window; a higher
+// asin(d) = d * R(d^2). R fitted by fit_asin_mid.py on d^2 <= cos^2(54.5 deg), degree 4: absolute
+// theta error <= 1.5e-7 rad (also after fp32 rounding), within the exact mode's window; a higher
 // degree would cost one more instruction per pair on nearly half the pairs. Scaled by 1/w on the
 // host.
 constexpr int kRTerms = 5;
-constexpr double kR[kRTerms] = {1.0000042503922144, 0.16644559569653503, 0.07818303909030544,
-                                0.026501255145352308, 0.071919159378340883};
+constexpr double kR[kRTerms] = {1.0000027330813104, 0.16651326659029475, 0.077385369858043895,
+                                0.0299281303350203, 0.067072790014221492};
 constexpr float kMidRad = 0.95993108859688125f;  // groups whose separations all lie in (55, 125) degrees use the dot form
 
 // Every code is the float 2^23 + (histogram entry), entry = floor(theta / w) (direct map, where
@@ -705,8 +705,9 @@ __device__ __forceinline__ float pair_code_fixed2(float xi, float yi, float zi, 
 // The dot form, for pairs whose caps put theta in (55, 125) degrees (direct map, P even):
 // theta / w = P/2 - d R(d^2) / w, floored exactly by one fma rounded toward zero onto 2^23 + P/2
 // (the product of the two fp32 operands enters unrounded). Worst-case theta error: d carries
-// <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 2.7e-7 rad where sin theta >=
-// sin 53 deg, plus <= 4.3e-7 from the polynomial, its rounding and its scaling: <= 7e-7 in all.
+// <= 2.1e-7 from the fp32 vectors and the dot product, i.e. <= 2.6e-7 rad where sin theta >=
+// sin 55 deg, plus <= 3.2e-7 from the polynomial (fit 1.6e-7, Horner 1e-7) and its scaling
+// (5.7e-8): <= 6e-7 in all.
 template <bool FINE = false>
 __device__ __forceinline__ float pair_code_mid(float xi, float yi, float zi, float xj, float yj, float zj,
                                                const BinParams& bp) {

@@ -3,13 +3,14 @@
 There the dot product d = u.v of two unit vectors determines theta without loss: theta =
 pi/2 - asin(d), and asin(d) = d * R(d^2) with R(t) = asin(sqrt t)/sqrt t analytic on [0, 1).
 The kernel only uses this form when the caps of both groups prove |d| < cos(55 deg), so R is
-fitted on t in [0, cos^2(53 deg)] (two degrees of margin), with degree 4 (error 2.4e-7 rad, inside
-the kernel's precision budget; degree 5 gives 2.1e-8 for one more instruction per pair). We minimise the largest ABSOLUTE error
+fitted on t in [0, cos^2(54.5 deg)] (half a degree of margin, far above the fp32 error of d), with
+degree 4 (error 1.5e-7 rad, also after rounding the coefficients to fp32, inside the kernel's
+precision budget; degree 5 gives about 1e-8 for one more instruction per pair). We minimise the largest ABSOLUTE error
 of d * R(d^2) (= the error in theta, radians) by Lawson's iteratively reweighted least squares on a
 Chebyshev grid, with R evaluated in 40-digit arithmetic. Prints the coefficients (lowest degree
 first) and the worst theta error before and after rounding them to fp32.
 
-Run: python fit_asin_mid.py [degree [theta_fit_deg]]   (defaults: 4 53)
+Run: python fit_asin_mid.py [degree [theta_fit_deg]]   (defaults: 4 54.5)
 """
 import sys
 
@@ -19,7 +20,7 @@ import numpy as np
 mp.mp.dps = 40
 DEG = int(sys.argv[1]) if len(sys.argv) > 1 else 4
 N = 6000
-THETA_FIT_DEG = float(sys.argv[2]) if len(sys.argv) > 2 else 53.0
+THETA_FIT_DEG = float(sys.argv[2]) if len(sys.argv) > 2 else 54.5
 
 
 def r_exact(t):

@@ -19,7 +19,7 @@
  * but those within ~1e-13 relative of the edge, which are redone in fp64), so every bin is the one
  * the fp64 formula gives (up to ~1e-15 relative): the histograms equal those of the fp64 definition. Without it (exact
  * modes 0 and 1), a pair can land in a neighbouring bin only if its fp64 theta lies near that edge:
- * the worst-case error (every rounding aligned) is 7e-7 rad for the dot form used between 55 and
+ * the worst-case error (every rounding aligned) is 6e-7 rad for the dot form used between 55 and
  * 125 degrees, 1.05e-6 for the chord form below 72 degrees and 1.25e-6 near 90 degrees for the
  * full-range chord form; the largest measured on millions of test pairs is 2.4e-7.
  *

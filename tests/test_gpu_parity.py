@@ -304,10 +304,10 @@ def test_split_launches_accumulate(acf, ctx, layout):
         ctx.set_option("layout", 0)
 
 
-# widths chosen so the edge windows are tight for a form: 180/2176 deg leaves the dot form a
-# window only 1% wider than its worst-case error (S = 11), 0.1478 deg the full-range chord (clamp
-# map, S = 11) 0.4% wider
-@pytest.mark.parametrize("w,nb", [(0.25, 720), (0.35, 515), (0.01, 18000), (0.25, 1440), (180.0 / 2176, 2176),
+# widths chosen so the edge windows are tight for a form: 180/2556 deg leaves the dot form a
+# window only 0.02% wider than its worst-case error of 6e-7 rad (S = 11), 0.1478 deg the full-range
+# chord (clamp map, S = 11) 0.4% wider
+@pytest.mark.parametrize("w,nb", [(0.25, 720), (0.35, 515), (0.01, 18000), (0.25, 1440), (180.0 / 2556, 2556),
                                   (0.1478, 1218)])
 def test_exact_mode_2_equals_oracle_bin_for_bin(acf, ctx, w, nb):
     c = synth.catalogs(4000, 3100, 12, 30.0, seed=14)
