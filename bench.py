@@ -370,6 +370,9 @@ def run_ours(args, cat, workload, rank, world, local):
                        "grid": ctx.info("grid"), "threads": ctx.info("threads"), "layout": ctx.info("layout"),
                        **({"options": parse_options(args.option)} if args.option else {})},
             "evaluated_gpairs_per_s": world * evals * args.steps / (total_ms_max / 1e3) / 1e9,
+            # per-step spread on rank 0 (the pages' protocol reports the median and the minimum)
+            "step_ms_stats": {"first": step_ms[0], "median": statistics.median(step_ms), "min": min(step_ms),
+                              "max": max(step_ms)},
             "roofline": roof, "cpu_baseline": cb,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": 1e3 * e2e_total / args.steps},
