@@ -390,18 +390,25 @@ def test_coincident_galaxies_overflow_the_queue_and_stay_exact(acf, ctx):
         ctx.set_option("exact", DEFAULT_EXACT)
 
 
+@pytest.mark.parametrize("line", ["equator", "meridian"])
 @pytest.mark.parametrize("w,nb", [(0.25, 720), (0.01, 18000)])
-def test_dense_equator_sweep_across_every_edge(acf, ctx, w, nb):
-    # 128 copies of the point (0, 0) against 172,800 equator points every 1/8 arcmin around the
-    # circle: every separation is min(ra, 21600 - ra) exactly, a dense sweep over every edge, with
-    # the i-set a single point so the caps put whole j-groups on each form (dot form, short and
-    # full chords, both sides of 90 degrees). The only pairs within 1e-6 rad of an edge are those
-    # exactly on it (the grid step is 3.6e-5 rad), so the edge-flux check leaves room for nothing
-    # else. That holds in exact mode 2 and, given its error bounds, in mode 0 too.
-    ra_a = np.zeros(128, np.float32)
-    dec_a = np.zeros(128, np.float32)
-    ra_b = (np.arange(172_800) / 8.0).astype(np.float32)
-    dec_b = np.zeros(172_800, np.float32)
+def test_dense_sweep_across_every_edge(acf, ctx, w, nb, line):
+    # equator: 128 copies of the point (0, 0) against 172,800 equator points every 1/8 arcmin around
+    # the circle, separations min(ra, 21600 - ra); meridian: 128 copies of the south pole against
+    # 86,401 points every 1/8 arcmin from pole to pole on one meridian, separations dec + 5400.
+    # Every separation is exact, a dense sweep over every edge, with the i-set a single point so the
+    # caps put whole j-groups on each form (dot form, short and full chords, both sides of 90
+    # degrees). The only pairs within 1e-6 rad of an edge are those exactly on it (the grid step is
+    # 3.6e-5 rad), so the edge-flux check leaves room for nothing else. That holds in exact mode 2
+    # and, given its error bounds, in mode 0 too.
+    if line == "equator":
+        ra_a, dec_a = np.zeros(128, np.float32), np.zeros(128, np.float32)
+        ra_b = (np.arange(172_800) / 8.0).astype(np.float32)
+        dec_b = np.zeros(172_800, np.float32)
+    else:
+        ra_a, dec_a = np.zeros(128, np.float32), np.full(128, -5400.0, np.float32)
+        dec_b = (-5400.0 + np.arange(86_401) / 8.0).astype(np.float32)
+        ra_b = np.zeros(86_401, np.float32)
     o = oracle.histogram(ra_a, dec_a, ra_b, dec_b, w, nb)
     on_edge = o.near_below.sum() + o.near_above.sum()
     assert on_edge <= 2 * 128 * (2 * nb)  # only pairs exactly on an edge lie within 1e-6 rad of one
@@ -413,7 +420,7 @@ def test_dense_equator_sweep_across_every_edge(acf, ctx, w, nb):
         finally:
             ctx.set_option("exact", DEFAULT_EXACT)
         rep = check.edge_flux(g, o.hist, o.near_below, o.near_above)
-        assert int(g.sum()) == 128 * 172_800
+        assert int(g.sum()) == 128 * len(ra_b)
         assert rep.ok, (exact, str(rep))
 
 
