@@ -249,16 +249,22 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
 typedef void (*PairKernelFn)(const PairParams);
 
 PairKernelFn pick_kernel(const Plan& pl) {
+  // the block-shared histogram in exact mode 2 takes the build without the plain loops
+  const int layout = (pl.layout == kBlock && pl.exact == 2 && pl.method == kChordPoly) ? kBlockExact : pl.layout;
 #define ACF_PICK(T, L, M, X) \
-  if (pl.threads == T && pl.layout == L && pl.map == M && pl.method == X) return pair_kernel<kK, T, L, M, X>;
+  if (pl.threads == T && layout == L && pl.map == M && pl.method == X) return pair_kernel<kK, T, L, M, X>;
   ACF_PICK(1024, kLane, kDirect, kChordPoly)
   ACF_PICK(1024, kLane, kClamp, kChordPoly)
   ACF_PICK(1024, kBlock, kDirect, kChordPoly)
   ACF_PICK(1024, kBlock, kClamp, kChordPoly)
+  ACF_PICK(1024, kBlockExact, kDirect, kChordPoly)
+  ACF_PICK(1024, kBlockExact, kClamp, kChordPoly)
   ACF_PICK(512, kLane, kDirect, kChordPoly)
   ACF_PICK(512, kLane, kClamp, kChordPoly)
   ACF_PICK(512, kBlock, kDirect, kChordPoly)
   ACF_PICK(512, kBlock, kClamp, kChordPoly)
+  ACF_PICK(512, kBlockExact, kDirect, kChordPoly)
+  ACF_PICK(512, kBlockExact, kClamp, kChordPoly)
 #if ACF_U16_HIST
   ACF_PICK(1024, kBlock16, kDirect, kChordPoly)
   ACF_PICK(1024, kBlock16, kClamp, kChordPoly)

@@ -85,8 +85,10 @@ constexpr int kJJBatch = ACF_JJ_BATCH;
 constexpr float kMagic = 8388608.0f;  // 2^23: adding it with round-toward-zero floors into the mantissa
 
 // kBlock16: two block-shared copies of 16-bit counters packed in pairs (a measured alternative for
-// fine binning, built with -DACF_U16_HIST=1, exact mode 0 only)
-enum Layout { kLane = 1, kBlock = 2, kBlock16 = 3 };
+// fine binning, built with -DACF_U16_HIST=1, exact mode 0 only). kBlockExact: kBlock for exact mode
+// 2, whose every group takes the flagging loops, built without the plain ones (measured faster on
+// fine bins; the lane-private layout measured slower that way).
+enum Layout { kLane = 1, kBlock = 2, kBlock16 = 3, kBlockExact = 4 };
 #ifndef ACF_U16_HIST
 #define ACF_U16_HIST 0
 #endif
@@ -1178,10 +1180,10 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         for (int g = 0; g < kJT / 32; ++g) {
           const int pc = __shfl_sync(0xffffffffu, pc_lane, g);
           const int path = pc & 3;
-          const bool fine = (pc & kExactBit) != 0;
+          const bool fine = LAYOUT == kBlockExact || (pc & kExactBit) != 0;
           if (pc & kMidBit) {
             count_path(fine ? 6 : 5, 1u);
-            if (fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
             else run(FormTag<2>(), FineTag<false>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
             continue;
           }
@@ -1201,16 +1203,16 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           }
           if (pc & kSmallBit) {
             count_path(fine ? 8 : 7, 1u);
-            if (fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
             else run(FormTag<3>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
             continue;
           }
           count_path(path == kGeneral ? (fine ? 3 : 1) : (fine ? 2 : 0), 1u);
           if (path == kGeneral) {
-            if (fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
             else run(FormTag<0>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
           } else {
-            if (fine) run(FormTag<1>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<1>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
             else run(FormTag<1>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
           }
         }
@@ -1239,7 +1241,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             }
           }
         };
-        if (p.exact_mode && METHOD == kChordPoly) edge(FineTag<true>());
+        if ((LAYOUT == kBlockExact || p.exact_mode) && METHOD == kChordPoly) edge(FineTag<true>());
         else edge(FineTag<false>());
         count_path(4, (unsigned int)jn);
       }
