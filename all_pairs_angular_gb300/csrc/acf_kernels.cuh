@@ -58,14 +58,15 @@ constexpr int kJJUnrollFine2 = ACF_JJ_UNROLL_FINE2;  // and of the two-code (fix
 #define ACF_FLAG_PRED 1
 #endif
 // Fix-up: queued pairs a thread loads at once, the blocks per SM its registers must allow, and
-// whether the next records load while the current pairs are decided. Measured per step (100k;
-// fine-200k): 2, 4, prefetch 12.94 and 111.6 ms; 3, 3, no prefetch 12.99 and 112.0; 3, 3, prefetch
-// 12.96 and 115.1 (spills); 4, 2, no prefetch slower on fine bins.
+// whether the next records load while the current pairs are decided. Measured per fine-200k step:
+// 1, 8, prefetch 97.7 ms (32 registers); 2, 4, prefetch 98.1; 1, 6, prefetch 100.9; earlier, before
+// a refit that cut its flags: 2, 4, prefetch 111.6; 3, 3, no prefetch 112.0; 3, 3, prefetch 115.1
+// (spills). All alike on the 100k step.
 #ifndef ACF_FIXUP_ILP
-#define ACF_FIXUP_ILP 2
+#define ACF_FIXUP_ILP 1
 #endif
 #ifndef ACF_FIXUP_MINB
-#define ACF_FIXUP_MINB 4
+#define ACF_FIXUP_MINB 8
 #endif
 #ifndef ACF_FIXUP_PREFETCH
 #define ACF_FIXUP_PREFETCH 1
