@@ -269,8 +269,9 @@ def run_ours(args, cat, workload, rank, world, local):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         barrier(world)
         torch.cuda.synchronize(dev)
-        clock_log = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else None
+        # the raw nvidia-smi samples go to a file only when ACF_CLOCK_LOG_DIR names a folder
+        log_dir = os.environ.get("ACF_CLOCK_LOG_DIR", "")
+        clock_log = os.path.join(log_dir, f"clocks_rank{rank}.csv") if log_dir and os.path.isdir(log_dir) else None
         launched_before = ctx.info("kernel_launches")
         with ClockSampler(local, clock_log) as clk:
             for s in range(args.steps):
