@@ -68,3 +68,21 @@ def test_kernel_hash_ignores_comments_but_not_code():
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only(a) != bench.code_only(c)
     assert '"a//b"' in bench.code_only(a)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the reference arm times the fp64 oracle on the host cores; it needs no GPU
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3", "--ref-rows", "10"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 3
+    assert line["unit"] == "Gpairs/s" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"].startswith("pages-shape-100k")
