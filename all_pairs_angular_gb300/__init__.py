@@ -26,7 +26,9 @@ ACF_ERR_CUDA = -4
 EXPORTED = ["acf_version", "acf_create", "acf_destroy", "acf_last_error", "acf_set_stream", "acf_histogram",
             "acf_omega", "acf_correlate", "acf_correlate_host", "acf_pair_bins", "acf_set_option", "acf_get_info",
             "acf_kernel_times", "acf_histogram_noalloc", "acf_fp32_peak", "acf_read_catalog", "acf_free_catalog",
-            "acf_write_omega", "acf_ladder"]
+            "acf_write_omega", "acf_ladder", "acf_plan_info"]
+PLAN_INFO_FIELDS = ("bin_map", "entries", "layout", "threads", "smem_bytes", "fine_shift", "fine_shift_small",
+                    "fine_shift_mid", "dot_form", "short_chord", "kmax", "exact")
 
 _lib = None
 
@@ -71,6 +73,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "acf_get_info": (ci, [vp, ctypes.c_char_p, ctypes.POINTER(i64)]),
         "acf_kernel_times": (ci, [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]),
         "acf_fp32_peak": (ci, [vp, i64, ctypes.POINTER(f64), ctypes.POINTER(ctypes.c_float)]),
+        "acf_plan_info": (ci, [f64, i32, i32, ctypes.POINTER(i64)]),
         "acf_read_catalog": (ci, [ctypes.c_char_p, ctypes.POINTER(ctypes.POINTER(ctypes.c_float)),
                                   ctypes.POINTER(ctypes.POINTER(ctypes.c_float)), ctypes.POINTER(i64),
                                   ctypes.c_char_p, i32]),
@@ -187,6 +190,16 @@ def acf_fp32_peak(ctx: int, iters: int = 1 << 16) -> tuple[float, float]:
     t0 = ctypes.c_float()
     _check(ctx, load().acf_fp32_peak(ctx, int(iters), ctypes.byref(rate), ctypes.byref(t0)))
     return rate.value, t0.value
+
+
+def acf_plan_info(bin_width_deg: float, nbins: int, exact: int = 2) -> dict:
+    """The plan acf_histogram would make for this binning (host only, no device): a dict keyed by
+    PLAN_INFO_FIELDS. Raises AcfError with the library's status for unsupported binnings."""
+    info = (ctypes.c_int64 * len(PLAN_INFO_FIELDS))()
+    rc = load().acf_plan_info(float(bin_width_deg), int(nbins), int(exact), info)
+    if rc != ACF_OK:
+        raise AcfError(rc, "acf_plan_info(%r, %r, %r)" % (bin_width_deg, nbins, exact))
+    return dict(zip(PLAN_INFO_FIELDS, (int(v) for v in info)))
 
 
 def acf_read_catalog(path: str) -> tuple[np.ndarray, np.ndarray]:

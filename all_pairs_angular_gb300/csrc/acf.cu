@@ -656,6 +656,22 @@ const char* acf_version(void) { return "acf 0.1 sm_103a bounds-checked"; }
 const char* acf_version(void) { return "acf 0.1 sm_103a"; }
 #endif
 
+int acf_plan_info(double bin_width_deg, int32_t nbins, int32_t exact, int64_t* info) {
+  if (!info || exact < 0 || exact > 2) return ACF_ERR_ARG;
+  acf_ctx host;  // default options and no device: make_plan only reads options
+  host.opt_exact = exact;
+  Plan pl;
+  const int rc = make_plan(&host, bin_width_deg, nbins, pl);
+  if (rc) return rc;
+  const BinParams& bp = pl.bp;
+  const int64_t v[ACF_PLAN_INFO_FIELDS] = {pl.map,           bp.entries,           pl.layout,          pl.threads,
+                                           (int64_t)pl.smem, pl.exact ? bp.fine_shift : 0,
+                                           pl.exact ? bp.fine_shift_small : 0,
+                                           pl.exact ? bp.fine_shift_mid : 0, bp.mid, bp.small, bp.kmax, pl.exact};
+  for (int k = 0; k < ACF_PLAN_INFO_FIELDS; ++k) info[k] = v[k];
+  return ACF_OK;
+}
+
 int acf_create(acf_ctx** out, int device, void* cuda_stream) {
   if (!out) return ACF_ERR_ARG;
   *out = nullptr;

@@ -206,6 +206,21 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
 int acf_set_option(acf_ctx *ctx, const char *key, int64_t value);
 
 /*
+ * The plan acf_histogram would make for a binning, with default options and the given exact mode
+ * (0, 1 or 2), worked out on the host alone: no context, no device, no CUDA call. Writes
+ * ACF_PLAN_INFO_FIELDS values to info: [0] bin map (0 direct: 180/w an integer; 1 clamp),
+ * [1] histogram entries, [2] layout (1 lane-private copies, 2 one block-shared histogram),
+ * [3] pair-kernel threads per block, [4] its dynamic shared memory in bytes, [5] [6] [7] the fine
+ * bits S of the exact-mode window for the full-range chord, the short chord and the dot form (0
+ * without exact mode), [8] dot form on, [9] short chord on, [10] the last bin index a separation
+ * up to 180 degrees reaches, [11] the exact mode the method allows.
+ * Returns ACF_ERR_ARG (bad width, nbins <= 0, info NULL, exact outside 0..2) or
+ * ACF_ERR_UNSUPPORTED (a histogram larger than the shared memory holds) like acf_histogram.
+ */
+#define ACF_PLAN_INFO_FIELDS 12
+int acf_plan_info(double bin_width_deg, int32_t nbins, int32_t exact, int64_t *info);
+
+/*
  * Read back facts about the last acf_histogram call. Keys: "grid", "threads", "ctas_per_sm",
  * "units", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
  * "pairs_evaluated", "launches" (pair-kernel launches the call was split into),
