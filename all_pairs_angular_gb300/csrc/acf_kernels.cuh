@@ -17,7 +17,7 @@
 //     theta'^2 = q * P(q) with a polynomial P (degree 5 where theta' < 72 deg, else 7), then one
 //     sqrt.approx;
 //   * between 55 and 125 degrees the dot product itself is precise enough: theta = pi/2 - d R(d^2)
-//     with a degree-7 polynomial R and no square root (14 instead of 18 instructions per pair);
+//     with a degree-4 polynomial R and no square root (11 instead of 18 instructions per pair);
 //   * the bin index comes from exact float rounding (one fma rounded toward zero onto 2^23 + c)
 //     instead of acos, multiply and float-to-int conversion;
 //   * each histogram lives in shared memory as 32 lane-private copies (word = bin*32 + lane), so a
