@@ -248,9 +248,16 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
 
 typedef void (*PairKernelFn)(const PairParams);
 
-PairKernelFn pick_kernel(const Plan& pl) {
+// small: units of one 32-galaxy j-group (lane-private layout, 1024 threads, chord method only)
+PairKernelFn pick_kernel(const Plan& pl, bool small) {
   // the block-shared histogram in exact mode 2 takes the build without the plain loops
   const int layout = (pl.layout == kBlock && pl.exact == 2 && pl.method == kChordPoly) ? kBlockExact : pl.layout;
+  if (small) {
+    if (pl.threads == 1024 && layout == kLane && pl.method == kChordPoly)
+      return pl.map == kDirect ? pair_kernel<kK, 1024, kLane, kDirect, kChordPoly, 1>
+                               : pair_kernel<kK, 1024, kLane, kClamp, kChordPoly, 1>;
+    return nullptr;
+  }
 #define ACF_PICK(T, L, M, X) \
   if (pl.threads == T && layout == L && pl.map == M && pl.method == X) return pair_kernel<kK, T, L, M, X>;
   ACF_PICK(1024, kLane, kDirect, kChordPoly)
@@ -391,26 +398,33 @@ struct Launch {
   PairKernelFn fn = nullptr;
   int ctas = 0;
   long long grid = 0, units = 0, rows = 0, cols = 0, per_launch = 0;
+  bool small = false;  // units of one j-group (four per chunk pair)
 };
+
+// Below this many chunk-pair units per resident warp a problem takes units of one j-group.
+constexpr double kSmallUnitsPerWarp = 2.0;
 
 // Persistent grid: every SM gets as many blocks as can be resident (one, normally).
 int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym, Launch& L) {
-  L.fn = pick_kernel(pl);
+  L.rows = (ni + kJT - 1) / kJT;
+  L.cols = (nj + kJT - 1) / kJT;
+  const long long chunk_units = sym ? L.rows * L.cols - L.rows * (L.rows - 1) / 2 : L.rows * L.cols;
+  // few chunk pairs for the warps of the whole GPU: four units per chunk pair, if a kernel exists
+  L.small = chunk_units < kSmallUnitsPerWarp * c->num_sms * (pl.threads / 32) && pick_kernel(pl, true) != nullptr;
+  L.fn = pick_kernel(pl, L.small);
   if (!L.fn) return fail(c, ACF_ERR_UNSUPPORTED, "no kernel for this plan");
   ACF_CUDA(c, cudaFuncSetAttribute(L.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
   int occ = 0;
   ACF_CUDA(c, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, L.fn, pl.threads, pl.smem));
   if (occ <= 0) return fail(c, ACF_ERR_UNSUPPORTED, "pair kernel cannot be resident (smem %zu)", pl.smem);
   L.ctas = c->opt_ctas > 0 ? std::min(c->opt_ctas, occ) : occ;
-  L.rows = (ni + kJT - 1) / kJT;
-  L.cols = (nj + kJT - 1) / kJT;
-  L.units = sym ? L.rows * L.cols - L.rows * (L.rows - 1) / 2 : L.rows * L.cols;
+  L.units = L.small ? 4 * chunk_units : chunk_units;
   L.grid = std::min<long long>((long long)c->num_sms * L.ctas, std::max<long long>(L.units, 1));
   // One unit adds at most kK*kJT*inc to a lane-private 32-bit counter (32 times that to a
   // block-shared one). Even if one block took every unit of a launch, no counter may wrap, so
   // large problems are split into launches that add into the same block rows.
   const double inc = sym ? 2.0 : 1.0;
-  const double per_unit = (pl.layout == kLane ? 1.0 : 32.0) * kK * kJT * inc;
+  const double per_unit = (pl.layout == kLane ? 1.0 : 32.0) * kK * (L.small ? 32 : kJT) * inc;
   L.per_launch = (long long)std::floor(4294967295.0 / per_unit);
   if (c->opt_units_per_launch > 0) L.per_launch = std::min(L.per_launch, c->opt_units_per_launch);
   return ACF_OK;

@@ -943,7 +943,9 @@ __device__ __forceinline__ void flush_hist(const PairParams& p, uint32_t* hist, 
 // take units from a global ticket independently and never wait for each other inside the loop:
 // each streams its own double-buffered j-tiles with cp.async and synchronises only with
 // __syncwarp. All warps of the block add into one shared histogram (lane-private copies).
-template <int K, int THREADS, int LAYOUT, int MAP, int METHOD>
+// GROUPS 1 (small problems): a unit is one 32-galaxy j-group of such a pair of chunks, four units
+// per chunk pair, so that few galaxies still spread over many warps.
+template <int K, int THREADS, int LAYOUT, int MAP, int METHOD, int GROUPS = 4>
 __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   static_assert(32 * K == kJT, "an i-set and a j-chunk have the same size");
   constexpr int WARPS = THREADS / 32;
@@ -1005,8 +1007,18 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     cp_async_commit();
   };
   if (u < p.unit_end) {
-    int r, c;
-    unit_coords(p, u, r, c);
+    // unit -> (i-set row, j-chunk column, j-group when a unit is one group)
+    auto unit_of = [&](long long uu, int& r_, int& c_, int& g_) {
+      if constexpr (GROUPS == 1) {
+        unit_coords(p, uu >> 2, r_, c_);
+        g_ = (int)(uu & 3);
+      } else {
+        unit_coords(p, uu, r_, c_);
+        g_ = 0;
+      }
+    };
+    int r, c, gs;
+    unit_of(u, r, c, gs);
     load_tile(c, 0);
     float xi[K], yi[K], zi[K];
     if (lane < 9) s_paths[warp][lane] = 0u;
@@ -1019,9 +1031,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       if (lane == 0) s_paths[warp][slot] += n;
     };
     while (true) {
-      int rn = 0, cn = 0;
+      int rn = 0, cn = 0, gsn = 0;
       if (un < p.unit_end) {
-        unit_coords(p, un, rn, cn);
+        unit_of(un, rn, cn, gsn);
         load_tile(cn, buf ^ 1);
       } else {
         cp_async_commit();
@@ -1178,7 +1190,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           pc_lane = choose_path(s_icap[warp], __ldg(p.jcap32 + c * (kJT / 32) + lane), p.exact_mode, p.exact_lo,
                                 MAP == kDirect ? p.bp.mid : 0, p.bp.small);
 #pragma unroll 1
-        for (int g = 0; g < kJT / 32; ++g) {
+        for (int g = GROUPS == 1 ? gs : 0; g < (GROUPS == 1 ? gs + 1 : kJT / 32); ++g) {
           const int pc = __shfl_sync(0xffffffffu, pc_lane, g);
           const int path = pc & 3;
           const bool fine = LAYOUT == kBlockExact || (pc & kExactBit) != 0;
@@ -1230,7 +1242,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         auto edge = [&](auto fine) {
           constexpr bool F = decltype(fine)::value;
 #pragma unroll 1
-          for (int jj = 0; jj < jn; ++jj) {
+          for (int jj = GROUPS == 1 ? gs * 32 : 0; jj < (GROUPS == 1 ? min(jn, gs * 32 + 32) : jn); ++jj) {
             const float4 v = tile[jj];
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -1244,13 +1256,14 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         };
         if ((LAYOUT == kBlockExact || p.exact_mode) && METHOD == kChordPoly) edge(FineTag<true>());
         else edge(FineTag<false>());
-        count_path(4, (unsigned int)jn);
+        count_path(4, GROUPS == 1 ? (unsigned int)max(0, min(jn, gs * 32 + 32) - gs * 32) : (unsigned int)jn);
       }
       __syncwarp();  // every lane is done with this buffer before the next prefetch refills it
       if (un >= p.unit_end) break;
       u = un;
       r = rn;
       c = cn;
+      gs = gsn;
       un = p.unit_begin + __shfl_sync(0xffffffffu, ta, 0);
       buf ^= 1;
     }
