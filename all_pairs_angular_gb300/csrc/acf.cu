@@ -63,11 +63,12 @@ struct acf_ctx {
   double opt_exact_below_deg = 20.0;
   int opt_range_forms = 1;        // 1: cheaper forms where the caps bound the separations
   int opt_pair_bins_form = 0;     // acf_pair_bins: 0 full-range chord form, 1 the range forms by own u.v
+  int opt_unit_groups = 0;        // j-groups per work unit: 0 automatic, 4 (chunk pairs) or 1 (small problems)
   unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
   long long last_qcap = 0;
   // info about the last histogram
   long long info_grid = 0, info_threads = 0, info_ctas = 0, info_chunks = 0, info_layout = 0, info_map = 0,
-            info_entries = 0, info_smem = 0, info_pairs = 0, info_flush = 0;
+            info_entries = 0, info_smem = 0, info_pairs = 0, info_flush = 0, info_groups = 0;
   long long kernel_launches = 0;  // kernels this context has launched, over its lifetime
   // kernel timing
   std::vector<cudaEvent_t> ev;  // pairs (start, stop)
@@ -410,7 +411,8 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
   L.cols = (nj + kJT - 1) / kJT;
   const long long chunk_units = sym ? L.rows * L.cols - L.rows * (L.rows - 1) / 2 : L.rows * L.cols;
   // few chunk pairs for the warps of the whole GPU: four units per chunk pair, if a kernel exists
-  L.small = chunk_units < kSmallUnitsPerWarp * c->num_sms * (pl.threads / 32) && pick_kernel(pl, true) != nullptr;
+  const bool few = chunk_units < kSmallUnitsPerWarp * c->num_sms * (pl.threads / 32);
+  L.small = (c->opt_unit_groups == 1 || (c->opt_unit_groups == 0 && few)) && pick_kernel(pl, true) != nullptr;
   L.fn = pick_kernel(pl, L.small);
   if (!L.fn) return fail(c, ACF_ERR_UNSUPPORTED, "no kernel for this plan");
   ACF_CUDA(c, cudaFuncSetAttribute(L.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
@@ -538,6 +540,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   c->last_counters = sc.counters;
   c->last_qcap = p.exact_mode ? p.qcap : 0;
   c->info_grid = L.grid;
+  c->info_groups = L.small ? 1 : 4;
   c->info_threads = pl.threads;
   c->info_ctas = L.ctas;
   c->info_chunks = L.units;
@@ -837,6 +840,9 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "units_per_launch")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "units_per_launch must be >= 0");
     c->opt_units_per_launch = v;
+  } else if (!strcmp(key, "unit_groups")) {
+    if (v != 0 && v != 1 && v != 4) return fail(c, ACF_ERR_ARG, "unit_groups must be 0, 1 or 4");
+    c->opt_unit_groups = (int)v;
   } else if (!strcmp(key, "workspace_limit")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "workspace_limit must be >= 0");
     c->opt_workspace_limit = v;
@@ -865,7 +871,8 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
   } t[] = {{"grid", c->info_grid},       {"threads", c->info_threads},   {"ctas_per_sm", c->info_ctas},
            {"units", c->info_chunks},   {"layout", c->info_layout},     {"bin_map", c->info_map},
            {"hist_entries", c->info_entries}, {"smem_bytes", c->info_smem}, {"pairs_evaluated", c->info_pairs},
-           {"launches", c->info_flush},  {"kernel_launches", c->kernel_launches}};
+           {"launches", c->info_flush},  {"kernel_launches", c->kernel_launches},
+           {"unit_groups", c->info_groups}};
   for (auto& e : t)
     if (!strcmp(e.k, key)) {
       *v = e.val;

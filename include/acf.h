@@ -194,6 +194,10 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    bounded block would use for that pair's own dot product
  *   "units_per_launch"  cap on work units (128 x 128 pairs) per pair-kernel launch; 0 = automatic
  *                    (large problems are always split so that no 32-bit shared counter can wrap)
+ *   "unit_groups"    j-groups of 32 galaxies per work unit: 0 = automatic (default: 1 when the
+ *                    problem has fewer than two 128 x 128 chunk pairs per resident warp), 4 = a
+ *                    whole chunk pair, 1 = one j-group (lane-private layout, 1024 threads and the
+ *                    chord method only; otherwise 4)
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
  *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
  *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
@@ -224,7 +228,8 @@ int acf_plan_info(double bin_width_deg, int32_t nbins, int32_t exact, int64_t *i
  * Read back facts about the last acf_histogram call. Keys: "grid", "threads", "ctas_per_sm",
  * "units", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
  * "pairs_evaluated", "launches" (pair-kernel launches the call was split into),
- * "kernel_launches" (kernels this context has launched since acf_create, all entry points).
+ * "kernel_launches" (kernels this context has launched since acf_create, all entry points),
+ * "unit_groups" (4: units of a 128 x 128 chunk pair; 1: of one 32-galaxy j-group).
  * These keys synchronise the context's stream and read device counters of the last call:
  *   "pairs_fixed", "pairs_general"  pairs evaluated on the fixed-sign and general loops
  *   "pairs_fixed_exact", "pairs_general_exact"  the same loops with edge flagging (exact mode)

@@ -32,7 +32,10 @@ def main() -> int:
     bad = 0
     cases += [(3000, 2500, 0.25, 720, 0, 0, 10), (3000, 2500, 0.01, 18000, 0, 0, 10), (3000, 2500, 0.35, 515, 0, 0, 10),
               (3000, 2500, 0.25, 720, 0, 0, 20)]
-    for n1, n2, w, nb, layout, threads, method in cases:
+    # every case with the automatic unit choice (small catalogs: one j-group per unit), then the
+    # chunk-pair units forced
+    cases = [cs + (g,) for g in (0, 4) for cs in cases]
+    for n1, n2, w, nb, layout, threads, method, groups in cases:
         # method 10 / 20: chord method with exact mode 2 / 0
         exact = {10: 2, 20: 0}.get(method, 1)
         method = 0 if method >= 10 else method
@@ -40,13 +43,14 @@ def main() -> int:
         ctx.set_option("layout", layout)
         ctx.set_option("threads", threads)
         ctx.set_option("bin_method", method)
+        ctx.set_option("unit_groups", groups)
         c = synth.catalogs(n1, n2, 5 if n1 > 10 else 0, 30.0, seed=n1 * 7 + n2)
         for args in ((c.ra_d, c.dec_d, None, None), (c.ra_d, c.dec_d, c.ra_r, c.dec_r)):
             try:
                 g = ctx.histogram(*args, bin_width_deg=w, nbins=nb)
                 torch.cuda.synchronize()
             except acf.AcfError as e:
-                print("VIOLATION", (n1, n2, w, nb, layout, threads, method), e, flush=True)
+                print("VIOLATION", (n1, n2, w, nb, layout, threads, method, groups), e, flush=True)
                 bad += 1
                 continue
             gh = acf.as_uint64(g)
@@ -55,7 +59,8 @@ def main() -> int:
             ok = rep.ok if method == 0 else int(gh.sum()) == int(o.hist.sum())
             if exact == 2:
                 ok = ok and np.array_equal(gh, o.hist)
-            print("case", (n1, n2, w, nb, layout, threads, method, exact), "ok" if ok else "MISMATCH " + str(rep),
+            print("case", (n1, n2, w, nb, layout, threads, method, exact, ctx.info("unit_groups")),
+                  "ok" if ok else "MISMATCH " + str(rep),
                   flush=True)
             bad += 0 if ok else 1
     ctx.close()

@@ -1,6 +1,6 @@
 """Seeded random cases against the oracle: catalog sizes, clustering, bin widths (with 180/w an
 integer, odd or even, or not), bin counts that stop short of 180 degrees or run past it, and the
-three exact modes. Every case must pass the edge-flux rule and sum to n1*n2. In exact mode 2 every
+three exact modes, with the automatic work units or chunk-pair units forced. Every case must pass the edge-flux rule and sum to n1*n2. In exact mode 2 every
 case must equal the oracle bin for bin, except where a pair lies within 1e-15 relative of an edge;
 none does in practice.
 """
@@ -37,7 +37,8 @@ def _case(k):
     sigma = float(rng.choice([1.0, 30.0, 300.0]))
     exact = int(rng.choice([0, 1, 2]))
     patch = float(rng.choice([0.0, 0.0, 300.0]))
-    return n1, n2, w, nb, clumps, sigma, exact, patch, k
+    groups = int(rng.choice([0, 4]))  # automatic units (one j-group for these sizes), or chunk pairs
+    return n1, n2, w, nb, clumps, sigma, exact, patch, k, groups
 
 
 @pytest.fixture(scope="module")
@@ -49,11 +50,12 @@ def ctx(acf):
 
 @pytest.mark.parametrize("k", range(N_CASES))
 def test_random_case(acf, ctx, k):
-    n1, n2, w, nb, clumps, sigma, exact, patch, seed = _case(k)
+    n1, n2, w, nb, clumps, sigma, exact, patch, seed, groups = _case(k)
     c = synth.catalogs(n1, max(n2, 1), clumps, sigma, seed=500 + seed, patch_arcmin=patch)
     ra1, dec1 = c.ra_d, c.dec_d
     ra2, dec2 = (c.ra_r[:n2], c.dec_r[:n2]) if n2 else (None, None)
     ctx.set_option("exact", exact)
+    ctx.set_option("unit_groups", groups)
     try:
         try:
             g = acf.as_uint64(ctx.histogram(ra1, dec1, ra2, dec2, bin_width_deg=w, nbins=nb))
@@ -71,6 +73,7 @@ def test_random_case(acf, ctx, k):
         torch.cuda.synchronize()
     finally:
         ctx.set_option("exact", 2)
+        ctx.set_option("unit_groups", 0)
     o = oracle.histogram(ra1, dec1, ra2, dec2, w, nb)
     m = n2 if n2 else n1
     assert int(g.sum()) == n1 * m
