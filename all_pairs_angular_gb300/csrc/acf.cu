@@ -64,6 +64,7 @@ struct acf_ctx {
   int opt_range_forms = 1;        // 1: cheaper forms where the caps bound the separations
   int opt_pair_bins_form = 0;     // acf_pair_bins: 0 full-range chord form, 1 the range forms by own u.v
   int opt_unit_groups = 0;        // j-groups per work unit: 0 automatic, 4 (chunk pairs) or 1 (small problems)
+  long long opt_exact_queue = 0;  // exact-mode queue records: 0 automatic, else this many (tests of overflow)
   unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
   long long last_qcap = 0;
   // info about the last histogram
@@ -300,9 +301,9 @@ struct CatBufs {
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
 };
 struct Scratch {
-  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue spill slots handed out (this launch),
-                                       // [2] moved pairs, [3] flagged pairs, [4] queue overflow,
-                                       // [5] pairs the fix-up redid in fp64;
+  unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue spill records handed out (this launch),
+                                       // [2] moved pairs, [3] flagged pairs, [4] flagged pairs without a
+                                       // record slot, [5] pairs the fix-up redid in fp64;
                                        // bytes 64..135: pairs per path (u64)
   unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
   unsigned int* key1 = nullptr;        // sort: keys after the first pass
@@ -315,16 +316,18 @@ struct Scratch {
   double* U = nullptr;
   float2* Tds = nullptr;               // the same as double-single (hi, lo) pairs
   float2* Uds = nullptr;
-  uint4* queue = nullptr;
-  unsigned int* qused = nullptr;       // per pair-kernel block: slots of its queue region in use
+  uint2* qhdr = nullptr;               // exact mode: flag records, headers ..
+  uint4* qmask = nullptr;              // .. and lane ballots
+  unsigned int* qused = nullptr;       // per pair-kernel warp: records of its queue region in use
   long long qcap = 0;
 };
 
-// the fix-up's shared moves and tables at most: eight 256-thread blocks per SM still fit, since the
+// the fix-up's shared moves and tables at most: several 256-thread blocks per SM still fit, since the
 // kernel waits on loads and needs every warp it can get
 constexpr size_t kFixupSmemMax = 24 * 1024;
-constexpr long long kQueueCapMin = 1ll << 20;  // flagged pairs the workspace can hold: 16 MB ..
-constexpr long long kQueueCapMax = 1ll << 28;  // .. 4 GB
+constexpr long long kQueueCapMin = 1ll << 20;  // flag records the workspace can hold: 24 MB ..
+constexpr long long kQueueCapMax = 1ll << 28;  // .. 6 GB
+constexpr size_t kRecordBytes = sizeof(uint2) + sizeof(uint4);
 
 // Lay the buffers out from `base` (nullptr: only measure). Returns the bytes needed.
 size_t carve(char* base, long long n, long long nj, bool sym, long long grid, int nbins, long long qcap, Scratch* s) {
@@ -360,8 +363,9 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   r.Tds = reinterpret_cast<float2*>(take((size_t)(nbins + 1) * 8));
   r.Uds = reinterpret_cast<float2*>(take((size_t)(nbins + 1) * 8));
   r.qcap = qcap;
-  r.qused = reinterpret_cast<unsigned int*>(take((size_t)grid * 4));
-  r.queue = reinterpret_cast<uint4*>(take((size_t)qcap * 16));
+  r.qused = reinterpret_cast<unsigned int*>(take((size_t)grid * 32 * 4));  // up to 32 warps per block
+  r.qhdr = reinterpret_cast<uint2*>(take((size_t)qcap * sizeof(uint2)));
+  r.qmask = reinterpret_cast<uint4*>(take((size_t)qcap * sizeof(uint4)));
   return off;
 }
 
@@ -433,21 +437,41 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
 }
 
 // Every pair a launch flagged near an edge is re-decided exactly; its count moves if the bin differs.
-// parts x pair-grid blocks, each region shared by `parts` blocks. The per-bin moves (int32 per
-// block) and, when they fit too, the double-single edge tables go to shared memory if small.
+// One fix-up warp per pair-kernel warp (queue region). The per-bin moves (int32 per block) and, when
+// they fit too, the double-single edge tables go to shared memory if small.
 int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& p, const Scratch& sc,
                  const CatBufs& ci, const CatBufs& cj) {
-  const long long parts = std::max<long long>(1, (long long)c->num_sms * 8 / std::max<long long>(L.grid, 1));
-  const unsigned fblocks = (unsigned)(parts * L.grid);
+  const long long regions = L.grid * (pl.threads / 32);
+  const unsigned fblocks = (unsigned)((regions + kFixupThreads / 32 - 1) / (kFixupThreads / 32));
   const int nb = pl.bp.nbins;
   const size_t moves = ((size_t)nb * 4 + 15) & ~(size_t)15, tables = (size_t)(nb + 1) * 16;
   const int level = moves + tables <= kFixupSmemMax ? 2 : (moves <= kFixupSmemMax ? 1 : 0);
   const size_t fsmem = level == 2 ? moves + tables : (level == 1 ? moves : 0);
-#define ACF_FIXUP(M, SM)                                                                                       \
-  fixup_kernel<M, SM><<<fblocks, 256, fsmem, c->stream>>>(sc.queue, sc.qused, (int)L.grid, p.qbatch, sc.counters + 1, \
-                                                          p.qcap, ci.v, ci.lo, cj.v, cj.lo, ci.v64, cj.v64, sc.T,     \
-                                                          sc.U, sc.Tds, sc.Uds, pl.bp, p.inc, sc.delta,               \
-                                                          sc.counters + 2, sc.counters + 4, sc.counters + 5)
+  FixupParams f;
+  f.qhdr = sc.qhdr;
+  f.qmask = sc.qmask;
+  f.qused = sc.qused;
+  f.qspill = sc.counters + 1;
+  f.regions = (unsigned)regions;
+  f.qbatch = p.qbatch;
+  f.qcap = p.qcap;
+  f.hi_i = ci.v;
+  f.lo_i = ci.lo;
+  f.hi_j = cj.v;
+  f.lo_j = cj.lo;
+  f.vi = ci.v64;
+  f.vj = cj.v64;
+  f.T = sc.T;
+  f.U = sc.U;
+  f.Tds = sc.Tds;
+  f.Uds = sc.Uds;
+  f.bp = pl.bp;
+  f.inc = p.inc;
+  f.delta = sc.delta;
+  f.moved = sc.counters + 2;
+  f.redone = sc.counters + 5;
+  f.flagged = sc.counters + 3;
+#define ACF_FIXUP(M, SM) fixup_kernel<M, SM><<<fblocks, kFixupThreads, fsmem, c->stream>>>(f)
   if (pl.map == kDirect) {
     if (level == 2) ACF_FIXUP(kDirect, 2);
     else if (level == 1) ACF_FIXUP(kDirect, 1);
@@ -472,16 +496,19 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   PairParams p;
   p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
   p.exact_lo = pl.exact_lo;
-  p.queue = sc.queue;
+  p.qhdr = sc.qhdr;
+  p.qmask = sc.qmask;
   p.qspill = sc.counters + 1;
   p.qused = sc.qused;
   p.qflagged = sc.counters + 3;
+  p.qoverflow = sc.counters + 4;
   p.qcap = (unsigned int)std::min<long long>(sc.qcap, 0xFFFFFFFFll);
-  // each block owns a region of the queue: three quarters of the queue spread over the blocks of a
-  // launch, at least 1.5 times what a block flags on average (the queue is drained after every
-  // launch). Blocks that flag more append to the spill region through one global counter, which
-  // all blocks contend for, so the regions must hold nearly everything.
-  p.qbatch = (unsigned int)std::min<long long>((long long)p.qcap * 3 / 4 / std::max<long long>(L.grid, 1), 0x7FFFFFFFll);
+  // each warp owns a region of the queue: two thirds of the queue spread over the warps of a launch,
+  // at least what a warp records on average (the queue is drained after every launch). Warps that
+  // record more append to the spill region through one global counter, which all warps contend
+  // for, so the regions must hold nearly everything.
+  p.qbatch = (unsigned int)std::min<long long>((long long)p.qcap * 2 / 3 / std::max<long long>(L.grid * (pl.threads / 32), 1),
+                                               0x7FFFFFFFll);
   p.path_pairs = reinterpret_cast<unsigned long long*>(sc.counters + 16);
   if (p.qcap == 0) p.exact_mode = 0;
   p.vi = ci.v;
@@ -570,15 +597,18 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
   return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc, out);
 }
 
-// Exact-mode queue slots for a histogram of `units` work units: every computed pair may be flagged
-// with probability up to 2^(1-S) (S of the full-range chord, the smallest); twice that, within
-// bounds. Overflow is not an error: those pairs keep their fp32 bin, and "exact_overflow" counts them.
-long long queue_slots(const Plan& pl, long long units) {
+// Exact-mode queue records for a histogram of `units` work units: every computed pair may be flagged
+// with probability up to 2^(1-S) (S of the full-range chord, the smallest), and a record holds at
+// least one flagged pair: twice that. A record stands for one warp and one j, so there are never more
+// than pairs / 128 of them: where flags are that dense, one and a half times that. Within bounds.
+// Overflow is not an error: those pairs keep their fp32 bin, and "exact_overflow" counts them.
+long long queue_slots(const acf_ctx* c, const Plan& pl, long long units) {
   // the queue is drained after every launch: it holds one launch's flagged pairs
   if (!pl.exact) return 0;
+  if (c->opt_exact_queue > 0) return c->opt_exact_queue;
   const double pairs = (double)units * kJT * kJT;
-  return (long long)std::min<double>(kQueueCapMax,
-                                     std::max<double>(kQueueCapMin, 4.0 * pairs * std::ldexp(1.0, -pl.bp.fine_shift)));
+  const double want = std::min(4.0 * pairs * std::ldexp(1.0, -pl.bp.fine_shift), 1.5 * pairs / kJT);
+  return (long long)std::min<double>(kQueueCapMax, std::max<double>(kQueueCapMin, want));
 }
 
 int launch_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t* rr, int32_t nbins, int64_t n_d,
@@ -613,7 +643,7 @@ int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_
       (rc = plan_launch(c, pl, n_r, n_r, true, Lrr)))
     return rc;
   const long long grid = std::max(Ldd.grid, std::max(Ldr.grid, Lrr.grid));
-  const long long qcap = queue_slots(pl, std::max(std::min(Ldd.units, Ldd.per_launch),
+  const long long qcap = queue_slots(c, pl, std::max(std::min(Ldd.units, Ldd.per_launch),
                                                   std::max(std::min(Ldr.units, Ldr.per_launch),
                                                            std::min(Lrr.units, Lrr.per_launch))));
   rc = ensure(c, c->ws, carve(nullptr, n_d, n_r, false, grid, nbins, qcap, nullptr));
@@ -655,7 +685,7 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const long long qcap = queue_slots(pl, std::min(L.units, L.per_launch));
+  const long long qcap = queue_slots(c, pl, std::min(L.units, L.per_launch));
   rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, qcap, nullptr));
   if (rc) return rc;
   Scratch sc;
@@ -843,6 +873,9 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "unit_groups")) {
     if (v != 0 && v != 1 && v != 4) return fail(c, ACF_ERR_ARG, "unit_groups must be 0, 1 or 4");
     c->opt_unit_groups = (int)v;
+  } else if (!strcmp(key, "exact_queue")) {
+    if (v < 0 || v > kQueueCapMax) return fail(c, ACF_ERR_ARG, "exact_queue must be 0..2^28");
+    c->opt_exact_queue = v;
   } else if (!strcmp(key, "workspace_limit")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "workspace_limit must be >= 0");
     c->opt_workspace_limit = v;
@@ -972,16 +1005,49 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx_id[kMaxDevices] = {};  // the context the cached address belongs to
 
-// Device address of the static scratch on `device` (which must be current); set up on first use.
+// Unique ID of the calling thread's current CUDA context (0 if it cannot be read). A device reset
+// (cudaDeviceReset) destroys the primary context and a new one gets a new ID, even if the driver
+// hands out the same handle again. The two driver functions are resolved through the runtime, so
+// the library does not link the driver library itself.
+unsigned long long current_context_id() {
+  typedef int (*GetCurrentFn)(void**);
+  typedef int (*GetIdFn)(void*, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrentFn>(f1);
+      get_id = reinterpret_cast<GetIdFn>(f2);
+    }
+    resolved = true;
+  }
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Device address of the static scratch on `device` (which must be current). Looked up on the first
+// call on a device, and again whenever that device's context has changed since (after a device
+// reset the module is loaded anew, possibly elsewhere).
 int noalloc_scratch(acf_ctx* c, int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return fail(c, ACF_ERR_UNSUPPORTED, "device %d out of range", device);
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[device]) {
+  const unsigned long long id = current_context_id();
+  if (!g_noalloc_ptr[device] || id == 0 || id != g_noalloc_ctx_id[device]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetSymbolAddress(g_noalloc_scratch)");
     g_noalloc_ptr[device] = p;
+    g_noalloc_ctx_id[device] = id;
   }
   *out = g_noalloc_ptr[device];
   return ACF_OK;
@@ -1012,8 +1078,9 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
   const size_t need = carve(nullptr, n, nj, sym, L.grid, nbins, 0, nullptr);
-  // the exact-mode queue takes whatever the static array has left
-  const long long qcap = pl.exact && need < kNoAllocScratchBytes ? (long long)((kNoAllocScratchBytes - need) / 16) - 16 : 0;
+  // the exact-mode queue takes whatever the static array has left (minus the alignment of its two parts)
+  const long long qcap =
+      pl.exact && need + 1024 < kNoAllocScratchBytes ? (long long)((kNoAllocScratchBytes - need - 1024) / kRecordBytes) : 0;
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "

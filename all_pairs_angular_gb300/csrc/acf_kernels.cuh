@@ -43,33 +43,26 @@ constexpr int kJT = 128;  // j-galaxies per shared-memory chunk
 #endif
 constexpr int kJJUnroll = ACF_JJ_UNROLL;
 #ifndef ACF_JJ_UNROLL_FINE
-#define ACF_JJ_UNROLL_FINE 1
+#define ACF_JJ_UNROLL_FINE 2
 #endif
 constexpr int kJJUnrollFine = ACF_JJ_UNROLL_FINE;  // j-loop unroll of the exact-mode (fine code) loops
 #ifndef ACF_JJ_UNROLL_FINE2
-#define ACF_JJ_UNROLL_FINE2 1
+#define ACF_JJ_UNROLL_FINE2 2
 #endif
 constexpr int kJJUnrollFine2 = ACF_JJ_UNROLL_FINE2;  // and of the two-code (fixed-sign chord) ones
-// (both measured slower unrolled twice: the queue code then no longer fits the instruction cache)
+// (with a queue push per flagged pair both measured slower unrolled twice: that push code no longer
+// fit the instruction cache; with one flag record per j it does, and twice is faster: 4.02 against
+// 4.23 ms per 100k DR-sized launch, 2.47 against 2.55 ms per fine-binning launch)
 // Flag test per j: 1 = OR of per-pair tests "biased fraction bits above bit 0 all zero"; 0 = a
 // running minimum of the biased fractions compared with 1 (measured alternative: 12.62 against
 // 12.47 ms of pair kernels per 100k step)
 #ifndef ACF_FLAG_PRED
 #define ACF_FLAG_PRED 1
 #endif
-// Fix-up: queued pairs a thread loads at once, the blocks per SM its registers must allow, and
-// whether the next records load while the current pairs are decided. Measured per fine-200k step:
-// 1, 8, prefetch 97.7 ms (32 registers); 2, 4, prefetch 98.1; 1, 6, prefetch 100.9; earlier, before
-// a refit that cut its flags: 2, 4, prefetch 111.6; 3, 3, no prefetch 112.0; 3, 3, prefetch 115.1
-// (spills). All alike on the 100k step.
-#ifndef ACF_FIXUP_ILP
-#define ACF_FIXUP_ILP 1
-#endif
+// Fix-up: the blocks per SM its registers must allow (it waits on loads and wants every warp it can
+// get).
 #ifndef ACF_FIXUP_MINB
-#define ACF_FIXUP_MINB 8
-#endif
-#ifndef ACF_FIXUP_PREFETCH
-#define ACF_FIXUP_PREFETCH 1
+#define ACF_FIXUP_MINB 4
 #endif
 #ifndef ACF_JJ_BATCH
 #define ACF_JJ_BATCH 2
@@ -182,14 +175,17 @@ struct PairParams {
   long long igroups;                   // number of 32-galaxy groups of the i catalog
   int exact_mode;                      // 0 off, 1 groups that may hold separations < theta_lo or > 180 - theta_lo, 2 all
   float exact_lo;                      // theta_lo in radians
-  uint4* queue;                        // exact mode: flagged pairs (sorted i, sorted j, fine code bits, 0):
-                                       // block b owns slots [b qbatch, (b + 1) qbatch), then a shared
-                                       // spill region from gridDim.x qbatch on
+  // exact mode: the queue of flag records, one per (warp i-set, j) holding a flagged pair (see
+  // push_record): warp w of block b (region g = b * warps + w) owns slots [g qbatch, (g + 1) qbatch),
+  // then a shared spill region follows all regions
+  uint2* qhdr;                         // (sorted j, i-set row | path code << 24)
+  uint4* qmask;                        // per i-vector slot k of the lanes: the ballot of flagged lanes
   unsigned int* qspill;                // spill slots handed out
-  unsigned int* qused;                 // per block: slots of its own region in use (at most qbatch)
+  unsigned int* qused;                 // per region: records the warp wrote (its own slots, then spill)
   unsigned int* qflagged;              // pairs flagged (for reporting)
+  unsigned int* qoverflow;             // flagged pairs whose record found no slot (kept their fp32 bin)
   unsigned int qcap;                   // queue slots
-  unsigned int qbatch;                 // slots a block owns
+  unsigned int qbatch;                 // slots a warp owns
   unsigned long long* path_pairs;      // pairs evaluated per path: chord fixed, chord general,
                                        // chord fixed+flag, chord general+flag, masked/ragged units,
                                        // dot form, dot form+flag, short chord, short chord+flag
@@ -797,6 +793,34 @@ __device__ __forceinline__ int choose_path(float4 a, float4 b, int mode, float l
   return path;
 }
 
+// The registers of a fixed-sign chord loop (see pair_code_fixed) for a group of path code pc: ns =
+// -sign of u.v, the scale and constant of the plain code (iws_c, h_c) and of the code the loop
+// bins or flags with (iws, h: the fine ones when `fine`, S_small bits for a short-chord group).
+// The pair kernel and the exact re-decision derive them here alike, so that the re-decision
+// recomputes a flagged pair's codes bit for bit.
+struct ChordConsts {
+  float ns, iws, h, iws_c, h_c;
+};
+template <int MAP>
+__device__ __forceinline__ ChordConsts chord_consts(int pc, bool fine, const BinParams& bp) {
+  const bool below = (pc & 3) == kBelow90;
+  ChordConsts c;
+  c.ns = below ? -1.0f : 1.0f;
+  c.iws_c = below ? bp.inv_w : -bp.inv_w;
+  if (MAP == kDirect) c.h_c = below ? kMagic : bp.magic_far;
+  else c.h_c = below ? 0.0f : 3.14159265358979323846f * bp.inv_w;
+  c.iws = c.iws_c;
+  c.h = c.h_c;
+  if (fine) {
+    const bool sm = (pc & kSmallBit) != 0;
+    const float iwf = sm ? bp.inv_w_fs : bp.inv_w_f;
+    c.iws = below ? iwf : -iwf;
+    if (MAP == kDirect) c.h = below ? bp.magic_f : (sm ? bp.magic_far_fs : bp.magic_far_f);
+    else c.h = below ? 0.0f : 3.14159265358979323846f * iwf;
+  }
+  return c;
+}
+
 template <bool F>
 struct FineTag {
   static constexpr bool value = F;
@@ -808,7 +832,8 @@ struct FormTag {
 
 // Add one pair to the shared histogram. With F (exact mode) the code carries fine_shift extra
 // fractional bits, biased by one unit: the entry is the code's integer part. Returns whether the
-// pair lies within one fine unit of an edge (biased fraction 0 or 1); such pairs go to push_flagged.
+// pair lies within one fine unit of an edge (biased fraction 0 or 1); such pairs are recorded
+// (push_record).
 // A pair at one fine unit below an edge is counted one entry up; the exact re-decision moves it.
 // shift 1 is the kBlock16 layout: 16-bit counters, whose overflow goes to the block's row.
 template <bool F, int MAP>
@@ -835,51 +860,57 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
   }
 }
 
-// Queue a near-edge pair for the exact re-decision if its entry lies in the exact zone (a function
-// of the pair's own code, so the set of re-decided pairs does not depend on grouping or order).
-// A pair that is not queued (outside the zone, or the queue is full) keeps its fp32 bin: if the
-// one-unit bias carried it into the next entry (biased fraction 0), its count moves back.
-struct QueueArgs {
-  uint4* queue;
-  unsigned int* qspill;
-  unsigned int qcap, qbatch, zone0, span0, zone1, span1, inc;
-  int fine_shift;
-};
-// cb is the pair's fine code; e_cnt the entry its count went to: the fine code's integer part
-// (single-code loops, where the bias may have carried) or the plain code's (two-code loops, may_carry
-// false). The queue record keeps both, so the re-decision moves the count from where it is.
-__device__ __forceinline__ void push_flagged_body(const QueueArgs& q, uint32_t cb, uint32_t e_cnt, bool may_carry, int i,
-                                                  int j, unsigned int* s_qcount, uint32_t base_f, int shift) {
-  const int S = q.fine_shift;
-  const uint32_t e = e_cnt;
-  bool queued = false;
-  if (e - q.zone0 <= q.span0 || e - q.zone1 <= q.span1) {
-    // a slot of this block's own region (shared-memory counter), or past it a spill slot
-    const unsigned int local = atomicAdd(s_qcount, 1u);
-    const unsigned int slot = local < q.qbatch ? blockIdx.x * q.qbatch + local : gridDim.x * q.qbatch + atomicAdd(q.qspill, 1u);
-    if (slot < q.qcap) {
-      q.queue[slot] = make_uint4((unsigned)i, (unsigned)j, cb, e_cnt);
-      queued = true;
+// Exact mode: record, for the re-decision, a j whose pairs with the warp's i-set hold at least one
+// flagged pair (a fine code within one fine unit of an edge). One record per warp and j: the header
+// (j, the i-set row r, the group's path code pc) and for each i-vector slot k the ballot of the lanes
+// whose pair (i = 32 (K r + k) + lane, j) is flagged. The re-decision recomputes each such pair's
+// codes from the same vectors with the same device code (the path code fixes the form), so that
+// the record need not carry them. The warp's records go to its own region of the queue at its
+// cursor `cur` (the same value in every lane; no atomic), and past the region's end to slots of the
+// spill region (one global counter). Called by every lane. Returns whether the record found a slot;
+// if not, its pairs keep their fp32 bins and are counted as flagged and as overflow.
+static_assert(kJT == 128, "a flag record holds four 32-lane ballots");
+__device__ __forceinline__ bool push_record(const PairParams& p, unsigned int region, unsigned int& cur, int r, int j, int pc,
+                                            uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3) {
+  const bool lead = (threadIdx.x & 31) == 0;
+  const uint2 hdr = make_uint2((unsigned)j, (unsigned)r | ((unsigned)pc << 24));
+  if (cur < p.qbatch) {
+    if (lead) {
+      const size_t slot = (size_t)region * p.qbatch + cur;
+      p.qhdr[slot] = hdr;
+      p.qmask[slot] = make_uint4(m0, m1, m2, m3);
+    }
+    ++cur;
+    return true;
+  }
+  ++cur;
+  bool ok = false;
+  if (lead) {
+    // spill slots start after every warp's region
+    const unsigned int regions = gridDim.x * (blockDim.x >> 5);
+    const unsigned long long slot = (unsigned long long)regions * p.qbatch + atomicAdd(p.qspill, 1u);
+    if (slot < p.qcap) {
+      p.qhdr[slot] = hdr;
+      p.qmask[slot] = make_uint4(m0, m1, m2, m3);
+      ok = true;
+    } else {
+      const unsigned int n = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
+      atomicAdd(p.qoverflow, n);
+      atomicAdd(p.qflagged, n);
     }
   }
-  if (!queued && may_carry && (cb & ((1u << S) - 1u)) == 0u) {
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// A flagged pair of a single-code loop that is not re-decided keeps its fp32 bin: if the one-unit
+// bias carried it into the next entry (biased fraction 0), its count moves back. cb is its fine code
+// (S fractional bits), base_f/shift the histogram addressing of the loop.
+__device__ __forceinline__ void carry_back(uint32_t cb, int S, uint32_t base_f, int shift, uint32_t inc) {
+  if ((cb & ((1u << S) - 1u)) == 0u) {
     const uint32_t a = ((cb >> S) << shift) + base_f;
-    red_shared_add(a, 0u - q.inc);
-    red_shared_add(a - (1u << shift), q.inc);
+    red_shared_add(a, 0u - inc);
+    red_shared_add(a - (1u << shift), inc);
   }
-}
-__device__ __forceinline__ void push_flagged(const PairParams& p, uint32_t cb, int S, uint32_t magic_bits, int i, int j,
-                                             unsigned int* s_qcount, uint32_t base_f, int shift) {
-  const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc, S};
-  const uint32_t e_cnt = (cb - magic_bits) >> S;
-  push_flagged_body(q, cb, e_cnt, true, i, j, s_qcount, base_f, shift);
-}
-// The same for a two-code loop: the count went to the plain code's entry.
-__device__ __forceinline__ void push_flagged2(const PairParams& p, uint32_t cb, uint32_t coarse, uint32_t magic_bits,
-                                              int i, int j, unsigned int* s_qcount) {
-  const QueueArgs q{p.queue, p.qspill, p.qcap, p.qbatch, p.bp.zone0, p.bp.span0, p.bp.zone1, p.bp.span1, p.inc,
-                    p.bp.fine_shift};
-  push_flagged_body(q, cb, coarse - magic_bits, false, i, j, s_qcount, 0u, 0);
 }
 
 // ------------------------------------------------------------------ pair kernel
@@ -954,7 +985,6 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   float4* my_tiles = reinterpret_cast<float4*>(smem) + warp * 2 * kJT;  // [2][kJT] per warp
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + WARPS * 2 * kJT * sizeof(float4));
 
-  __shared__ unsigned int s_qcount[1];  // exact mode: pairs this block flagged
   // per warp: j-groups run on each path (see path_pairs), and the cap of the warp's current i-set
   // (kept here, not in registers, to leave the hot loops all the registers)
   __shared__ unsigned int s_paths[WARPS][9];
@@ -964,9 +994,6 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
   unsigned long long* row = p.partial + (size_t)blockIdx.x * p.bp.nbins;
   if (!p.accumulate)
     for (int k = tid; k < p.bp.nbins; k += THREADS) row[k] = 0ull;
-  if (tid == 0) {
-    s_qcount[0] = 0u;
-  }
   __syncthreads();
 
   const uint32_t hist_addr = (uint32_t)__cvta_generic_to_shared(hist);
@@ -987,6 +1014,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                                              : hist_addr - ((magic_bits >> p.bp.fine_shift_mid) << 2);
   const int ni = (int)p.ni, nj = (int)p.nj;
   const uint32_t inc = p.inc;  // the histogram increment: 2 for DD/RR pairs i < j, 1 for DR
+  // exact mode: this warp's region of the flag-record queue and its cursor there (warp-uniform)
+  const unsigned int region = blockIdx.x * WARPS + warp;
+  unsigned int cur = 0u;
 
   // tickets: the unit being computed (u), the one whose tile is in flight (un), and one fetched
   // ahead by lane 0 while computing (its latency hides behind the unit)
@@ -1079,7 +1109,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         // instruction cache.
         // (ns, iws, h): sign, scale and constant of a fixed-sign chord loop (fine ones when F);
         // (iws_c, h_c): the plain scale and constant, for the two-code fine loops
-        auto run = [&](auto form, auto fine, int jbeg, float ns, float iws, float h, float iws_c, float h_c) {
+        auto run = [&](auto form, auto fine, int jbeg, int pc, float ns, float iws, float h, float iws_c, float h_c) {
           constexpr int X = decltype(form)::value;  // 0 chord general, 1 chord fixed sign, 2 dot form,
                                                     // 3 short chord (fixed sign)
           constexpr bool F = decltype(fine)::value;
@@ -1151,9 +1181,11 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #endif
               }
               if (__any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
-#pragma unroll
-                for (int k = 0; k < K; ++k)
-                  if ((cfs[k] & fmask) <= 1u) push_flagged2(p, cfs[k], ccs[k], magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount);
+                // the count went to the plain code's entry: nothing to move back without a record
+                (void)push_record(p, region, cur, r, j0 + jj, pc, __ballot_sync(0xffffffffu, (cfs[0] & fmask) <= 1u),
+                                  __ballot_sync(0xffffffffu, (cfs[1] & fmask) <= 1u),
+                                  __ballot_sync(0xffffffffu, (cfs[2] & fmask) <= 1u),
+                                  __ballot_sync(0xffffffffu, (cfs[3] & fmask) <= 1u));
               }
             }
           } else {
@@ -1176,10 +1208,13 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               }
               // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
               if (F && __any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
+                if (!push_record(p, region, cur, r, j0 + jj, pc, __ballot_sync(0xffffffffu, (cbs[0] & fmask) <= 1u),
+                                 __ballot_sync(0xffffffffu, (cbs[1] & fmask) <= 1u),
+                                 __ballot_sync(0xffffffffu, (cbs[2] & fmask) <= 1u),
+                                 __ballot_sync(0xffffffffu, (cbs[3] & fmask) <= 1u))) {
 #pragma unroll
-                for (int k = 0; k < K; ++k)
-                  if ((cbs[k] & fmask) <= 1u)
-                    push_flagged(p, cbs[k], SF, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, bf, SHIFT);
+                  for (int k = 0; k < K; ++k) carry_back(cbs[k], SF, bf, SHIFT, inc);
+                }
               }
             }
           }
@@ -1196,37 +1231,25 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const bool fine = LAYOUT == kBlockExact || (pc & kExactBit) != 0;
           if (pc & kMidBit) {
             count_path(fine ? 6 : 5, 1u);
-            if (LAYOUT == kBlockExact || fine) run(FormTag<2>(), FineTag<true>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
-            else run(FormTag<2>(), FineTag<false>(), g * 32, 0.f, 0.f, 0.f, 0.f, 0.f);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<2>(), FineTag<true>(), g * 32, pc, 0.f, 0.f, 0.f, 0.f, 0.f);
+            else run(FormTag<2>(), FineTag<false>(), g * 32, pc, 0.f, 0.f, 0.f, 0.f, 0.f);
             continue;
           }
-          const bool below = path == kBelow90;
-          const float ns = below ? -1.0f : 1.0f;
-          const float iws_c = below ? p.bp.inv_w : -p.bp.inv_w;
-          float h_c;
-          if (MAP == kDirect) h_c = below ? kMagic : p.bp.magic_far;
-          else h_c = below ? 0.0f : 3.14159265358979323846f * p.bp.inv_w;
-          float iws = iws_c, h = h_c;
-          if (fine) {
-            const bool sm = (pc & kSmallBit) != 0;
-            const float iwf = sm ? p.bp.inv_w_fs : p.bp.inv_w_f;
-            iws = below ? iwf : -iwf;
-            if (MAP == kDirect) h = below ? p.bp.magic_f : (sm ? p.bp.magic_far_fs : p.bp.magic_far_f);
-            else h = below ? 0.0f : 3.14159265358979323846f * iwf;
-          }
+          const ChordConsts cc = chord_consts<MAP>(pc, fine, p.bp);
+          const float ns = cc.ns, iws = cc.iws, h = cc.h, iws_c = cc.iws_c, h_c = cc.h_c;
           if (pc & kSmallBit) {
             count_path(fine ? 8 : 7, 1u);
-            if (LAYOUT == kBlockExact || fine) run(FormTag<3>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
-            else run(FormTag<3>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<3>(), FineTag<true>(), g * 32, pc, ns, iws, h, iws_c, h_c);
+            else run(FormTag<3>(), FineTag<false>(), g * 32, pc, ns, iws, h, iws_c, h_c);
             continue;
           }
           count_path(path == kGeneral ? (fine ? 3 : 1) : (fine ? 2 : 0), 1u);
           if (path == kGeneral) {
-            if (LAYOUT == kBlockExact || fine) run(FormTag<0>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
-            else run(FormTag<0>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<0>(), FineTag<true>(), g * 32, pc, ns, iws, h, iws_c, h_c);
+            else run(FormTag<0>(), FineTag<false>(), g * 32, pc, ns, iws, h, iws_c, h_c);
           } else {
-            if (LAYOUT == kBlockExact || fine) run(FormTag<1>(), FineTag<true>(), g * 32, ns, iws, h, iws_c, h_c);
-            else run(FormTag<1>(), FineTag<false>(), g * 32, ns, iws, h, iws_c, h_c);
+            if (LAYOUT == kBlockExact || fine) run(FormTag<1>(), FineTag<true>(), g * 32, pc, ns, iws, h, iws_c, h_c);
+            else run(FormTag<1>(), FineTag<false>(), g * 32, pc, ns, iws, h, iws_c, h_c);
           }
         }
       } else {
@@ -1239,18 +1262,29 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           const int tt = p.sym ? i - j0 : -1;
           thr[k] = (i >= ni) ? 0x7fffffff : max(-1, min(tt, kJT));
         }
+        // (flagged pairs are recorded with the general chord's path code, kGeneral: the form this loop uses)
         auto edge = [&](auto fine) {
           constexpr bool F = decltype(fine)::value;
 #pragma unroll 1
           for (int jj = GROUPS == 1 ? gs * 32 : 0; jj < (GROUPS == 1 ? min(jn, gs * 32 + 32) : jn); ++jj) {
             const float4 v = tile[jj];
+            uint32_t cbs[K];
+            bool fk[K];
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-              const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
-              if (jj > thr[k] &&
-                  add_pair<F, MAP>(p, cb, base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k],
-                              yi[k], zi[k], v, inc))
-                push_flagged(p, cb, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane, j0 + jj, s_qcount, base_f, SHIFT);
+              cbs[k] = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
+              fk[k] = jj > thr[k] &&
+                      add_pair<F, MAP>(p, cbs[k], base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane,
+                                       j0 + jj, xi[k], yi[k], zi[k], v, inc);
+            }
+            if (F && __any_sync(0xffffffffu, fk[0] || fk[1] || fk[2] || fk[3])) {
+              if (!push_record(p, region, cur, r, j0 + jj, kGeneral, __ballot_sync(0xffffffffu, fk[0]),
+                               __ballot_sync(0xffffffffu, fk[1]), __ballot_sync(0xffffffffu, fk[2]),
+                               __ballot_sync(0xffffffffu, fk[3]))) {
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+                  if (fk[k]) carry_back(cbs[k], p.bp.fine_shift, base_f, SHIFT, inc);
+              }
             }
           }
         };
@@ -1277,12 +1311,9 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       }
     }
   }
+  // the records of this warp's own region (the fix-up reads that many)
+  if (p.exact_mode && lane == 0) p.qused[region] = min(cur, p.qbatch);
   __syncthreads();
-  if (p.exact_mode && tid == 0) {
-    // the slots of this block's own region in use, and its flags for reporting
-    p.qused[blockIdx.x] = min(s_qcount[0], p.qbatch);
-    atomicAdd(p.qflagged, s_qcount[0]);
-  }
   flush_hist<K, THREADS, LAYOUT, MAP, METHOD>(p, hist, false);
 }
 
@@ -1393,40 +1424,88 @@ __device__ __forceinline__ int ds_side(float qh, float ql, float2 t, float eps) 
   return d > eps ? 1 : (d < -eps ? -1 : 0);
 }
 
-constexpr int kFixupILP = ACF_FIXUP_ILP;  // queued pairs a fix-up thread loads at once
+// The codes a pair-kernel loop computed for a recorded pair (a = its i-vector, b = its j-vector, fp32
+// as the kernel read them), from the record's path code: the fine code cb with its S fractional bits,
+// the entry e_cnt its count went to, and whether the loop was a single-code one (whose entry is the
+// fine code's integer part, which the one-unit bias may have carried one entry up). The same device
+// functions as the loops, with the same constants, so every value is bit for bit the kernel's.
+template <int MAP>
+__device__ __forceinline__ void recorded_codes(int pc, float4 a, float4 b, const BinParams& bp, uint32_t& cb,
+                                               uint32_t& e_cnt, bool& single, int& S) {
+  const uint32_t magic_bits = __float_as_uint(kMagic);
+  if (pc & kMidBit) {
+    cb = __float_as_uint(pair_code_mid<true>(a.x, a.y, a.z, b.x, b.y, b.z, bp));
+    S = bp.fine_shift_mid;
+    e_cnt = (cb - magic_bits) >> S;
+    single = true;
+  } else if ((pc & 3) == kGeneral) {
+    cb = __float_as_uint(pair_code<MAP, kChordPoly, true>(a.x, a.y, a.z, b.x, b.y, b.z, bp));
+    S = bp.fine_shift;
+    e_cnt = (cb - magic_bits) >> S;
+    single = true;
+  } else {
+    const ChordConsts c = chord_consts<MAP>(pc, true, bp);
+    uint32_t coarse;
+    if (pc & kSmallBit) {
+      cb = __float_as_uint(
+          pair_code_fixed2<MAP, true>(a.x, a.y, a.z, b.x, b.y, b.z, c.ns, c.iws, c.h, c.iws_c, c.h_c, bp, coarse));
+      S = bp.fine_shift_small;
+    } else {
+      cb = __float_as_uint(
+          pair_code_fixed2<MAP, false>(a.x, a.y, a.z, b.x, b.y, b.z, c.ns, c.iws, c.h, c.iws_c, c.h_c, bp, coarse));
+      S = bp.fine_shift;
+    }
+    e_cnt = coarse - magic_bits;
+    single = false;
+  }
+}
 
-// Re-decide every queued pair exactly and record the move of its count if the fast code put it in a
-// neighbouring bin. Runs after every pair-kernel launch (the queue then starts empty again); the
-// merge adds delta[] to the counts. Slots requested past the queue's end are added to *overflow
-// (those pairs kept their fp32 bin).
+struct FixupParams {
+  const uint2* qhdr;                  // flag records (see push_record)
+  const uint4* qmask;
+  const unsigned int* qused;          // per pair-kernel warp: records of its region
+  const unsigned int* qspill;         // spill records handed out
+  unsigned int regions;               // pair-kernel warps (regions)
+  unsigned int qbatch, qcap;          // records per region, records in all
+  const float4 *hi_i, *lo_i, *hi_j, *lo_j;  // fp32 vectors (as the pair kernel read them) and remainders
+  const double4_32a *vi, *vj;         // fp64 vectors
+  const double *T, *U;                // fp64 edge tables
+  const float2 *Tds, *Uds;            // the same as double-single pairs
+  BinParams bp;
+  unsigned int inc;                   // histogram increment of the pair kernel's launch
+  unsigned long long* delta;          // per-bin moves (two's complement)
+  unsigned int* moved;                // pairs moved
+  unsigned int* redone;               // pairs decided again in fp64
+  unsigned int* flagged;              // pairs re-decided (flagged and recorded)
+};
+
+// Re-decide every flagged pair of the records a pair-kernel launch wrote, exactly, and record the
+// move of its count if the fast code put it in a neighbouring bin. Runs after every pair-kernel
+// launch (the queue then starts empty again); the merge adds delta[] to the counts.
 // The decision is the fp64 one: the chord q of the fp64 unit vectors against the fp64 edge tables
 // T[k] = 4 sin^2(k w / 2) (bins whose lower edge is up to 90 degrees, difference chord) or
 // U[k] = 4 cos^2(k w / 2) (the others, sum chord), each exact enough where the other loses relative
 // precision. A double-single pass (fp32 hi + lo, about 48 bits) takes it first: where it lies farther
 // than its error bound from a table value it decides as the fp64 comparison would; within that bound
 // (about 1e-13 relative, against a flagged pair's 1e-6 rad window) the pair is redone in fp64.
-// The queue holds pair_grid regions of qbatch slots (region b: qused[b] in use), then spill slots.
-// The grid is parts x pair_grid blocks: block x serves region x % pair_grid with its share
-// x / pair_grid of the parts, and every block takes a share of the spill slots.
+// Pairs outside the exact zone (mode 1) keep their fp32 bin; a single-code loop's count that the bias
+// carried one entry up moves back.
+// The queue holds one region of qbatch records per pair-kernel warp (region g: qused[g] in use), then
+// spill records. Fix-up warp g takes region g, whose records came from one pair-kernel warp in order
+// (consecutive records share an i-set, and mostly a path code), and a share of the spill records.
 // SMEM 2: the double-single tables and per-bin moves in shared memory; 1: the moves only; 0: neither.
 // Shared moves reach delta[] once per block.
+constexpr int kFixupThreads = 256;
 template <int MAP, int SMEM>
-__global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4* __restrict__ queue, const unsigned int* __restrict__ qused,
-                                                    int pair_grid, unsigned int qbatch,
-                                                    const unsigned int* __restrict__ qspill, unsigned int qcap,
-                                                    const float4* __restrict__ hi_i, const float4* __restrict__ lo_i,
-                                                    const float4* __restrict__ hi_j, const float4* __restrict__ lo_j,
-                                                    const double4_32a* __restrict__ vi, const double4_32a* __restrict__ vj,
-                                                    const double* __restrict__ T, const double* __restrict__ U,
-                                                    const float2* __restrict__ Tds, const float2* __restrict__ Uds,
-                                                    BinParams bp, unsigned int inc, unsigned long long* __restrict__ delta,
-                                                    unsigned int* __restrict__ moved, unsigned int* __restrict__ overflow,
-                                                    unsigned int* __restrict__ redone) {
+__global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(const FixupParams f) {
+  static_assert(kFixupThreads == 8 * 32, "one pair list per warp");
   extern __shared__ __align__(16) unsigned char fsm[];
-  __shared__ unsigned int s_moved, s_redone;
+  __shared__ unsigned int s_moved, s_redone, s_flagged;
+  __shared__ uint4 s_list[8][32];  // per warp: (i, j, path code) of the pairs of one round
+  const BinParams& bp = f.bp;
   const int nb = bp.nbins;
-  const float2* tT = Tds;
-  const float2* tU = Uds;
+  const float2* tT = f.Tds;
+  const float2* tU = f.Uds;
   int* sd = nullptr;
   if (SMEM >= 1) {
     sd = reinterpret_cast<int*>(fsm);
@@ -1436,28 +1515,31 @@ __global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4*
     float2* sT = reinterpret_cast<float2*>(fsm + (((size_t)nb * 4 + 15) & ~(size_t)15));
     float2* sU = sT + (nb + 1);
     for (int k = threadIdx.x; k <= nb; k += blockDim.x) {
-      sT[k] = Tds[k];
-      sU[k] = Uds[k];
+      sT[k] = f.Tds[k];
+      sU[k] = f.Uds[k];
     }
     tT = sT;
     tU = sU;
   }
-  if (threadIdx.x == 0) s_moved = s_redone = 0u;
+  if (threadIdx.x == 0) s_moved = s_redone = s_flagged = 0u;
   __syncthreads();
-  const unsigned int nbatch = (unsigned int)pair_grid * qbatch;
-  const unsigned int spill = *qspill;
-  const unsigned int room = qcap - nbatch;
-  const unsigned int nspill = min(spill, room);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && spill > room) atomicAdd(overflow, spill - room);
-  unsigned int my_moved = 0u, my_redone = 0u;
-  const unsigned int region = blockIdx.x % (unsigned)pair_grid;
-  const unsigned int part = blockIdx.x / (unsigned)pair_grid, parts = gridDim.x / (unsigned)pair_grid;
-  const unsigned int nused = qbatch ? min(qused[region], qbatch) : 0u;
-  const unsigned int nmine = part < parts ? nused : 0u;  // blocks past the last whole part take spill only
-  const unsigned int step = parts * blockDim.x;
-  // re-decide one queued pair from its double-single vectors (ah + al, bh + bl)
-  auto redo = [&](const uint4 rec, float4 ah, float4 al, float4 bh, float4 bl) {
-    int e = (int)rec.w;  // the entry the pair's count went to
+  const unsigned long long nbatch = (unsigned long long)f.regions * f.qbatch;
+  const unsigned int nspill = nbatch < f.qcap ? (unsigned int)min((unsigned long long)*f.qspill, f.qcap - nbatch) : 0u;
+  unsigned int my_moved = 0u, my_redone = 0u, my_flagged = 0u;
+  // move one count between bins (k_from -> k_to)
+  auto move = [&](int k_from, int k_to) {
+    if (k_from == k_to) return;
+    if (SMEM >= 1) {
+      atomicAdd(sd + k_from, -(int)f.inc);
+      atomicAdd(sd + k_to, (int)f.inc);
+    } else {
+      atomicAdd(f.delta + k_from, (unsigned long long)(-(long long)f.inc));
+      atomicAdd(f.delta + k_to, (unsigned long long)f.inc);
+    }
+    ++my_moved;
+  };
+  // re-decide pair (i, j), whose count went to entry e, from its double-single vectors
+  auto redo = [&](int e, int i, int j, float4 ah, float4 al, float4 bh, float4 bl) {
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     const int kf = entry_to_bin<MAP>(e, bp);
     const int k0 = kf > bp.kmax ? bp.kmax : kf;
@@ -1485,88 +1567,116 @@ __global__ void __launch_bounds__(256, ACF_FIXUP_MINB) fixup_kernel(const uint4*
     if (!sure) {
       // too close to an edge for the double-single bound: the same comparisons in fp64
       ++my_redone;
-      const double4_32a a = vi[rec.x], b = vj[rec.y];
+      const double4_32a a = f.vi[i], b = f.vj[j];
       k = k0;
       if (diff) {
         const double dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z;
         const double q = dx * dx + dy * dy + dz * dz;
-        while (k > 0 && q < T[k]) --k;
-        while (k < bp.kmax && q >= T[k + 1]) ++k;
+        while (k > 0 && q < f.T[k]) --k;
+        while (k < bp.kmax && q >= f.T[k + 1]) ++k;
       } else {
         const double dx = a.x + b.x, dy = a.y + b.y, dz = a.z + b.z;
         const double q = dx * dx + dy * dy + dz * dz;
-        while (k > 0 && q > U[k]) --k;
-        while (k < bp.kmax && q <= U[k + 1]) ++k;
+        while (k > 0 && q > f.U[k]) --k;
+        while (k < bp.kmax && q <= f.U[k + 1]) ++k;
       }
     }
-    if (k != kf) {
-      if (SMEM >= 1) {
-        atomicAdd(sd + kf, -(int)inc);
-        atomicAdd(sd + k, (int)inc);
-      } else {
-        atomicAdd(delta + kf, (unsigned long long)(-(long long)inc));
-        atomicAdd(delta + k, (unsigned long long)inc);
-      }
-      ++my_moved;
+    move(kf, k);
+  };
+  // one flagged pair: i, j and the path code of the group that computed it
+  auto pair = [&](int i, int j, int pc) {
+    ++my_flagged;
+    const float4 ah = f.hi_i[i], al = f.lo_i[i], bh = f.hi_j[j], bl = f.lo_j[j];
+    uint32_t cb, e;
+    bool single;
+    int S;
+    recorded_codes<MAP>(pc, ah, bh, bp, cb, e, single, S);
+    if (e - bp.zone0 <= bp.span0 || e - bp.zone1 <= bp.span1) {
+      redo((int)e, i, j, ah, al, bh, bl);
+    } else if (single && (cb & ((1u << S) - 1u)) == 0u) {
+      // outside the exact zone: the fp32 bin stands, minus the bias's carry
+      const int ec = (int)e < bp.entries ? (int)e : bp.entries - 1;
+      move(entry_to_bin<MAP>(ec, bp), entry_to_bin<MAP>(ec > 0 ? ec - 1 : 0, bp));
     }
   };
-  // slots first, first + stride, ... below n of queue[base ..]: kFixupILP records per thread at a
-  // time, all loads issued before any arithmetic (the loads are what this kernel waits for)
-  auto run = [&](unsigned int base, unsigned int n, unsigned int first, unsigned int stride) {
-    uint4 rec[kFixupILP];
-    bool ok[kFixupILP];
-    auto fetch = [&](unsigned int t, uint4* r, bool* o) {
-#pragma unroll
-      for (int u = 0; u < kFixupILP; ++u) {
-        o[u] = t + u * stride < n;
-        r[u] = o[u] ? queue[base + t + u * stride] : make_uint4(0u, 0u, 0u, 0u);
+  // Each lane walks its own sequence of records (base + first, + stride, ...), holding the flagged
+  // pairs of one record that are still to do (the next record already loading). Per round the warp
+  // packs up to 32 of those pairs into its list, in lane order (a warp scan of the lanes' counts
+  // gives each lane its slots), and then every lane decides one pair of the list: the lanes stay
+  // converged however the pairs spread over the records.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4* list = s_list[warp];
+  auto run = [&](unsigned long long base, unsigned int n, unsigned int first, unsigned int stride) {
+    unsigned int t = first;
+    uint2 hn = make_uint2(0u, 0u), h = make_uint2(0u, 0u);
+    uint4 mn = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t m[4] = {0u, 0u, 0u, 0u};  // pairs of the current record still to do
+    bool has_next = t < n;
+    if (has_next) {
+      hn = f.qhdr[base + t];
+      mn = f.qmask[base + t];
+      t += stride;
+    }
+    while (true) {
+      if ((m[0] | m[1] | m[2] | m[3]) == 0u && has_next) {
+        h = hn;
+        m[0] = mn.x; m[1] = mn.y; m[2] = mn.z; m[3] = mn.w;
+        has_next = t < n;
+        if (has_next) {
+          hn = f.qhdr[base + t];
+          mn = f.qmask[base + t];
+          t += stride;
+        }
       }
-    };
-    fetch(first, rec, ok);
-    for (unsigned int t = first; t < n; t += kFixupILP * stride) {
-      float4 ah[kFixupILP], al[kFixupILP], bh[kFixupILP], bl[kFixupILP];
+      const unsigned int cnt = __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
+      unsigned int incl = cnt;
 #pragma unroll
-      for (int u = 0; u < kFixupILP; ++u) {
-        ah[u] = hi_i[rec[u].x];
-        al[u] = lo_i[rec[u].x];
-        bh[u] = hi_j[rec[u].y];
-        bl[u] = lo_j[rec[u].y];
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-#if ACF_FIXUP_PREFETCH
-      // the next records load while these pairs are decided
-      uint4 nrec[kFixupILP];
-      bool nok[kFixupILP];
-      fetch(t + kFixupILP * stride, nrec, nok);
-#endif
+      const unsigned int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (total == 0u) break;  // a lane with a record left always has a pair to do
+      unsigned int slot = incl - cnt;
+      if (slot < 32u) {
+        const int j = (int)h.x, r = (int)(h.y & 0xFFFFFFu), pc = (int)(h.y >> 24);
 #pragma unroll
-      for (int u = 0; u < kFixupILP; ++u)
-        if (ok[u]) redo(rec[u], ah[u], al[u], bh[u], bl[u]);
-#if ACF_FIXUP_PREFETCH
-#pragma unroll
-      for (int u = 0; u < kFixupILP; ++u) {
-        rec[u] = nrec[u];
-        ok[u] = nok[u];
+        for (int k = 0; k < 4; ++k) {
+          while (m[k] && slot < 32u) {
+            const int b = __ffs(m[k]) - 1;
+            m[k] &= m[k] - 1u;
+            list[slot++] = make_uint4((unsigned)((r * 4 + k) * 32 + b), (unsigned)j, (unsigned)pc, 0u);
+          }
+        }
       }
-#else
-      fetch(t + kFixupILP * stride, rec, ok);
-#endif
+      __syncwarp();
+      if ((unsigned)lane < total) {
+        const uint4 e = list[lane];
+        pair((int)e.x, (int)e.y, (int)e.z);
+      }
+      __syncwarp();
     }
   };
-  // this block's share of its region, then its share of the spill slots
-  run(region * qbatch, nmine, part * blockDim.x + threadIdx.x, step);
-  run(nbatch, nspill, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+  // this warp's region, then its share of the spill records
+  const unsigned int gw = blockIdx.x * (kFixupThreads / 32) + warp, nw = gridDim.x * (kFixupThreads / 32);
+  const unsigned int nmine = gw < f.regions ? min(f.qused[gw], f.qbatch) : 0u;
+  run((unsigned long long)gw * f.qbatch, nmine, lane, 32);
+  run(nbatch, nspill, gw * 32 + lane, nw * 32);
   for (int o = 16; o > 0; o >>= 1) {
     my_moved += __shfl_xor_sync(0xffffffffu, my_moved, o);
     my_redone += __shfl_xor_sync(0xffffffffu, my_redone, o);
+    my_flagged += __shfl_xor_sync(0xffffffffu, my_flagged, o);
   }
-  if ((threadIdx.x & 31) == 0 && my_moved) atomicAdd(&s_moved, my_moved);
-  if ((threadIdx.x & 31) == 0 && my_redone) atomicAdd(&s_redone, my_redone);
+  if (lane == 0 && my_moved) atomicAdd(&s_moved, my_moved);
+  if (lane == 0 && my_redone) atomicAdd(&s_redone, my_redone);
+  if (lane == 0 && my_flagged) atomicAdd(&s_flagged, my_flagged);
   __syncthreads();
-  if (threadIdx.x == 0 && s_moved) atomicAdd(moved, s_moved);
-  if (threadIdx.x == 0 && s_redone) atomicAdd(redone, s_redone);
+  if (threadIdx.x == 0 && s_moved) atomicAdd(f.moved, s_moved);
+  if (threadIdx.x == 0 && s_redone) atomicAdd(f.redone, s_redone);
+  if (threadIdx.x == 0 && s_flagged) atomicAdd(f.flagged, s_flagged);
   if (SMEM >= 1) {
     for (int k = threadIdx.x; k < nb; k += blockDim.x)
-      if (sd[k]) atomicAdd(delta + k, (unsigned long long)(long long)sd[k]);
+      if (sd[k]) atomicAdd(f.delta + k, (unsigned long long)(long long)sd[k]);
   }
 }
 

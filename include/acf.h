@@ -105,13 +105,17 @@ int acf_histogram(acf_ctx *ctx, const float *ra, const float *dec, int64_t n, co
  *   - Limit: about 77 bytes per galaxy of each catalog + ((blocks + 2) * nbins * 8) bytes must fit
  *     in 16 MiB, blocks being the persistent grid (one per SM: 152 on a GB300); larger requests
  *     return ACF_ERR_UNSUPPORTED with the sizes in the message. Two 100k catalogs at 720 bins need
- *     ~16.3 MB. In exact mode the rest of the array holds the queue of pairs to re-decide (there
- *     about 30k pairs, against ~4.9M flagged in that DR histogram); pairs that do not fit keep
- *     their fp32 bin (the precision of exact mode 0) and are counted by the "exact_overflow" info
- *     key. Exact results need a queue that holds one launch's flagged pairs: catalogs of a few
- *     tens of thousands of galaxies at 0.25 degree bins.
+ *     ~16.3 MB. In exact mode the rest of the array holds the queue of pairs to re-decide.
+ *     Exact results need a queue that holds one launch's flagged pairs: catalogs of a few tens of
+ *     thousands of galaxies at 0.25 degree bins. When the queue overflows (the "exact_overflow"
+ *     info key is then > 0; e.g. two 60k catalogs), the pairs that did not fit keep their fp32 bin:
+ *     the rule that a pair moves to a neighbouring bin only within 1e-6 rad of its edge is then met
+ *     in practice (largest measured error 2.4e-7 rad) but not proven (worst-case bounds up to
+ *     1.25e-6 rad), sums stay exact, and because which pairs fit depends on the order in which
+ *     blocks fill the queue, such results can differ from run to run.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture. The address is looked up again when the
+ *     device's context has changed (e.g. after cudaDeviceReset).
  *   - Every call on a device shares the one array, which keeps the last call's contents; the
  *     kernels re-initialise everything they read. Calls whose work overlaps on the GPU (other
  *     streams, other host threads or contexts) race on it and must be serialised by the caller.
@@ -198,6 +202,10 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    problem has fewer than two 128 x 128 chunk pairs per resident warp), 4 = a
  *                    whole chunk pair, 1 = one j-group (lane-private layout, 1024 threads and the
  *                    chord method only; otherwise 4)
+ *   "exact_queue"    records of the exact-mode queue (one per warp i-set and j holding a flagged
+ *                    pair): 0 = automatic (default: enough for one launch at twice the worst-case flag
+ *                    rate), else exactly this many, up to 2^28. A smaller queue can overflow; its
+ *                    pairs then keep their fp32 bins (see "exact_overflow")
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
  *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
  *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
@@ -237,7 +245,7 @@ int acf_plan_info(double bin_width_deg, int32_t nbins, int32_t exact, int64_t *i
  *   "pairs_mid", "pairs_mid_exact"  the dot form (55..125 degrees), without and with flagging
  *   "pairs_small", "pairs_small_exact"  the degree-5 chord form, without and with flagging
  *   "exact_flagged"  pairs flagged for re-decision;  "exact_moved"  of those, pairs moved a bin;
- *   "exact_overflow"  flagged pairs that did not fit in the queue (kept their fp32 bin)
+ *   "exact_overflow"  flagged pairs whose record did not fit in the queue (kept their fp32 bin)
  *   "exact_redone_fp64"  flagged pairs the double-single first pass of the re-decision could not
  *                    settle (within ~1e-13 relative of an edge), decided again in fp64
  * Unknown keys return ACF_ERR_ARG.

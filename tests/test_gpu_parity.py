@@ -371,23 +371,27 @@ def test_largest_histogram_that_fits_and_the_next_is_refused(acf, ctx):
 def test_coincident_galaxies_overflow_the_queue_and_stay_exact(acf, ctx):
     # 2000 copies of one galaxy and 2000 of another 10.3 degrees away: 8M ordered pairs at
     # separation 0 and 8M at 10.3 degrees (bin 41 of 0.25). Every pair at separation 0 lies within
-    # one fine unit above the edge at 0 and is flagged. That is 4M unordered pairs, against a queue
-    # of 2^20 slots, so most overflow. An overflowed pair keeps its fp32 bin, which is exact here,
-    # and the overflow is reported.
+    # one fine unit above the edge at 0 and is flagged: 4M unordered pairs, in flag records of up to
+    # 128 pairs each. With the automatic queue they all fit; with a queue of 1000 records most
+    # overflow. An overflowed pair keeps its fp32 bin, which is exact here, and the overflow is
+    # reported.
     ra = np.concatenate([np.full(2000, 600.0), np.full(2000, 600.0)]).astype(np.float32)
     dec = np.concatenate([np.full(2000, 100.0), np.full(2000, 100.0 + 618.0)]).astype(np.float32)
+    expect = np.zeros(720, np.uint64)
+    expect[0] = 2 * 2000 * 2000
+    expect[int(618.0 / 15.0)] = 2 * 2000 * 2000
     ctx.set_option("exact", 2)
     try:
-        g = acf.as_uint64(ctx.histogram(ra, dec, bin_width_deg=0.25, nbins=720))
-        torch.cuda.synchronize()
-        expect = np.zeros(720, np.uint64)
-        expect[0] = 2 * 2000 * 2000
-        expect[int(618.0 / 15.0)] = 2 * 2000 * 2000
-        assert np.array_equal(g, expect)
-        assert ctx.info("exact_flagged") >= 2 * 1999 * 1000
-        assert ctx.info("exact_overflow") > 0
+        for cap in (0, 1000):
+            ctx.set_option("exact_queue", cap)
+            g = acf.as_uint64(ctx.histogram(ra, dec, bin_width_deg=0.25, nbins=720))
+            torch.cuda.synchronize()
+            assert np.array_equal(g, expect), cap
+            assert ctx.info("exact_flagged") >= 2 * 1999 * 1000
+            assert (ctx.info("exact_overflow") > 0) == (cap > 0), cap
     finally:
         ctx.set_option("exact", DEFAULT_EXACT)
+        ctx.set_option("exact_queue", 0)
 
 
 @pytest.mark.parametrize("line", ["equator", "meridian"])
