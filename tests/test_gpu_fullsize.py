@@ -3,10 +3,12 @@
 - The pages' shape (two 100k catalogs) and the 5x5 degree field: every bin against the oracle's
   stored full histograms (tests/golden/, written by make_golden.py from oracle/ only), after
   proving the regenerated catalogs are the ones the golden files were computed from.
-- The 1M and the fine-binning (200k, 18,000 bins) workloads: the oracle cannot do all pairs in a
-  test, so 2000 seeded random rows of each family are checked pair-exactly (the GPU histogram of
-  those rows against the full catalog vs the oracle's), and the full-size histograms are checked
-  for their exact totals (n1*n2) and the DD split identity.
+- The fine-binning workload (two 200k catalogs, 18,000 bins of 0.01 degrees): every bin against the
+  oracle's stored full histograms too (the oracle needs minutes for it, so it ran once, offline).
+- The 1M and the fine-binning workloads: 2000 seeded random rows of each family are checked
+  against the oracle's edge rule (the GPU histogram of those rows against the full catalog vs the
+  oracle's), and the full-size histograms are checked for their exact totals (n1*n2) and the DD
+  split identity.
 """
 import json
 import os
@@ -80,6 +82,34 @@ def test_full_histograms_match_golden_oracle(acf, ctx, idx, exact):
         for fam in ("DD", "DR", "RR"):
             assert np.array_equal(gpu[fam], np.array(g[fam]["hist"], np.uint64)), fam
         assert float(dev.max()) == 0.0
+
+
+def test_fine_binning_full_histograms_match_golden_oracle(acf, ctx):
+    # two 200k catalogs in 18,000 bins of 0.01 degrees through acf_correlate, as bench.py --config 4
+    # times it (exact mode 2, the default): every bin of DD, DR and RR equals the oracle's stored full
+    # histograms. This is where the exact mode works hardest: about 1.2% of the pairs lie within
+    # their form's window of an edge and are re-decided.
+    with open(os.path.join(GOLDEN, "config4_oracle.json")) as f:
+        g = json.load(f)
+    c = synth.config(4)
+    assert c.digest() == g["digest"], "regenerated catalogs differ from the ones the golden file was made from"
+    assert (g["nbins"], g["bin_width_deg"]) == (18000, 0.01)
+    ra_d, dec_d, ra_r, dec_r = map(_dev, (c.ra_d, c.dec_d, c.ra_r, c.dec_r))
+    dd, dr, rr, om = ctx.correlate(ra_d, dec_d, ra_r, dec_r, c.bin_width_deg, c.nbins)
+    torch.cuda.synchronize()
+    assert ctx.info("exact_overflow") == 0
+    gpu = {"DD": acf.as_uint64(dd), "DR": acf.as_uint64(dr), "RR": acf.as_uint64(rr)}
+    for fam, n in (("DD", c.n_d ** 2), ("DR", c.n_d * c.n_r), ("RR", c.n_r ** 2)):
+        ref = np.array(g[fam]["hist"], np.uint64)
+        assert int(ref.sum()) == n
+        diff = np.flatnonzero(gpu[fam] != ref)
+        assert diff.size == 0, f"{fam}: {diff.size} bins differ, first {diff[:5]}"
+    # omega of the oracle's counts (the file stores only the histograms at this binning)
+    om = om.cpu().numpy()
+    ref_om = oracle.omega(*(np.array(g[f]["hist"], np.uint64) for f in ("DD", "DR", "RR")), c.n_d, c.n_r)
+    assert np.array_equal(np.isnan(om), np.isnan(ref_om))
+    ok = ~np.isnan(ref_om)
+    assert np.allclose(om[ok], ref_om[ok], rtol=1e-12, atol=1e-15)
 
 
 def _row_sample_check(acf, ctx, c, rows, seed):

@@ -3,7 +3,8 @@
 - ACF_U16_HIST=1 adds layout 3: two block-shared copies of 16-bit counters, whose overflow is
   carried into the block's u64 row. In exact mode 0 its histograms must equal those of the 32-bit
   block-shared layout bit for bit. That includes a 5 x 5 degree field in 0.01-degree bins, where
-  single bins pass 0x8000 counts per copy many times over.
+  single bins pass 0x8000 counts per copy many times over. Row samples in the same layout are
+  also held to the oracle's edge rule, one of them dense enough that every block's counters carry.
 - ACF_J_SHUFFLE=1 broadcasts the j-vectors by warp shuffles instead of shared-memory loads. In the
   default exact mode 2 its histograms must equal the fp64 oracle's bin for bin.
 
@@ -62,7 +63,23 @@ for name, c in (("small-field", synth.config(2)), ("mixed", synth.catalogs(30000
     res[name] = {"equal": bool(np.array_equal(h[2][0], h[3][0]) and np.array_equal(h[2][1], h[3][1])),
                  "layout": h[3][2], "max_dd": int(h[3][0].max()), "sum_dd": int(h[3][0].sum()),
                  "n_d": c.n_d}
+# against the oracle: row samples of each catalog against the whole other one, in the 16-bit layout,
+# judged by the edge rule. The dense case (100k galaxies in a 0.3-degree patch, 4000 rows) puts
+# more than 0x8000 counts of one bin into every block's counters, so their carries are exercised.
+import oracle
+from oracle import check
 ctx.set_option("layout", 3)
+dense = synth.catalogs(100000, 0, 0, 0.0, seed=47, patch_arcmin=18.0)
+for name, c, rows in (("small-field", synth.config(2), 2000), ("mixed", synth.catalogs(30000, 20000, 8, 60.0, seed=41), 2000),
+                      ("dense", dense, 4000)):
+    idx = synth.sample_rows(c.n_d, rows, 7)
+    ra2, dec2 = (c.ra_r, c.dec_r) if c.n_r else (c.ra_d, c.dec_d)
+    g = acf.as_uint64(ctx.histogram(c.ra_d[idx], c.dec_d[idx], ra2, dec2, bin_width_deg=0.01, nbins=18000))
+    torch.cuda.synchronize()
+    o = oracle.histogram(c.ra_d[idx], c.dec_d[idx], ra2, dec2, 0.01, 18000)
+    rep = check.edge_flux(g, o.hist, o.near_below, o.near_above)
+    res.setdefault("oracle", {})[name] = {"ok": bool(rep.ok), "layout": ctx.info("layout"), "max_bin": int(g.max()),
+                                          "sum": int(g.sum()), "pairs": int(rows) * len(ra2), "grid": ctx.info("grid")}
 ctx.set_option("exact", 2)
 try:
     ctx.histogram(t["ra_d"], t["dec_d"], bin_width_deg=0.01, nbins=18000)
@@ -82,6 +99,11 @@ def test_u16_counters_equal_32_bit_counters(libs):
     # 100k galaxies in a 5x5 degree field: bins far above what one 16-bit counter can hold
     assert res["small-field"]["max_dd"] > 152 * 2 * 0x8000
     assert res["exact_refused"]
+    # row samples against the oracle, within the edge rule, every pair counted
+    for name, r in res["oracle"].items():
+        assert r["ok"] and r["layout"] == 3 and r["sum"] == r["pairs"], (name, r)
+    d = res["oracle"]["dense"]
+    assert d["max_bin"] > d["grid"] * 2 * 0x8000, d  # on average past 0x8000 in both copies of every block
 
 
 SHUFFLE_CODE = r"""

@@ -5,7 +5,8 @@ afford the device synchronisation an allocation brings) get their scratch from t
 static 16 MiB device array. This file checks, through the C ABI, that two calls in a row give
 exactly the counts of the allocating entry point (histogram counts are integers, so the tolerance
 is zero), that its results obey the oracle's edge rule, and that requests larger than the static
-array are refused with a clear error. It is named to run last so that a run stopping at the first
+array are refused with a clear error. When the static array's exact-mode queue overflows, the
+call still succeeds, reports the shortfall and keeps the totals and the edge rule. It is named to run last so that a run stopping at the first
 failure has already run every other test.
 """
 import numpy as np
@@ -58,4 +59,26 @@ def test_no_alloc_matches_allocating_entry_point_twice(acf):
     acf.acf_histogram_noalloc(ctx.handle, ra_r, dec_r, c.n_r, None, None, 0, w, nb, got)
     torch.cuda.synchronize()
     assert torch.equal(ref, got)
+    ctx.close()
+
+
+def test_no_alloc_queue_overflow_keeps_sums_and_edge_rule(acf):
+    # Two 60k catalogs fit the static array (about 10 MB of vectors, caps and block rows), but the
+    # ~6 MB left for the exact-mode queue holds far fewer pairs than their DR histogram flags near
+    # bin edges. The pairs that do not fit keep their fp32 bin: the call still succeeds, reports the
+    # shortfall, keeps every total exact and stays within the edge rule against the oracle.
+    ctx = acf.Context(0)
+    c = synth.catalogs(60000, 60000, 20, 30.0, seed=17)
+    ra_d, dec_d, ra_r, dec_r = map(_dev, (c.ra_d, c.dec_d, c.ra_r, c.dec_r))
+    w, nb = 0.25, 720
+    got = torch.full((nb,), -1, dtype=torch.int64, device="cuda")
+    acf.acf_histogram_noalloc(ctx.handle, ra_d, dec_d, c.n_d, ra_r, dec_r, c.n_r, w, nb, got)
+    torch.cuda.synchronize()
+    overflow, flagged = ctx.info("exact_overflow"), ctx.info("exact_flagged")
+    assert overflow > 0 and flagged > overflow, (overflow, flagged)
+    g = acf.as_uint64(got)
+    assert int(g.sum()) == c.n_d * c.n_r
+    o = oracle.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, w, nb)
+    rep = check.edge_flux(g, o.hist, o.near_below, o.near_above)
+    assert rep.ok, rep
     ctx.close()
