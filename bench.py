@@ -177,9 +177,23 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str) -> float | None:
-    """dram read+write bytes per pair-kernel launch from the committed ncu summary, if it was
-    captured from the current kernel source."""
+# How each arm treats the L2 cache between timed steps: one statement, the same in both arms'
+# `config`, so that the two lines describe the same workload
+L2_NOTE = "GPU arm: L2 flushed between timed steps (256 MiB device write); CPU reference arm: n/a"
+
+
+def bench_config(cat, workload: str, options: dict) -> dict:
+    """The workload as both arms report it (launch facts go to a separate `launch` object)."""
+    cfg = {"workload": workload, "n_d": cat.n_d, "n_r": cat.n_r, "bin_width_deg": cat.bin_width_deg,
+           "nbins": cat.nbins, "l2": L2_NOTE}
+    if options:
+        cfg["options"] = options
+    return cfg
+
+
+def recorded_counters(workload: str) -> dict | None:
+    """The committed ncu record of the pair kernel on this workload (per-launch DRAM bytes and
+    executed instructions), if it was captured from the current kernel source."""
     path = os.path.join(ROOT, "profiles", "pair_kernel_traffic.json")
     try:
         with open(path) as f:
@@ -188,7 +202,27 @@ def recorded_traffic(workload: str) -> float | None:
         return None
     if rec.get("kernel_source_hash") != kernel_source_hash() or rec.get("workload") != workload:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec
+
+
+def executed_roofline(rec: dict | None, pair_ms_per_step: float, alg_inst_per_step: float, peak: float) -> dict | None:
+    """The pair kernel's fraction of the issue roofline on the basis of the instructions it really
+    executed (ncu smsp__thread_inst_executed.sum of the DD, DR and RR launches of one step, from
+    the committed record) over the event-timed pair-kernel time of a step."""
+    if not rec or pair_ms_per_step <= 0:
+        return None
+    per = rec.get("per_launch", {})
+    try:
+        inst = sum(float(per[f]["thread_inst_executed"]) for f in ("DD", "DR", "RR"))
+    except (KeyError, TypeError, ValueError):
+        return None
+    achieved = inst / (pair_ms_per_step / 1e3) / 1e12
+    out = {"basis": "executed thread-instructions per step (ncu smsp__thread_inst_executed.sum, committed record)",
+           "thread_inst_per_step": inst, "achieved": achieved, "frac": achieved / peak,
+           "inst_overhead": inst / alg_inst_per_step if alg_inst_per_step else None}
+    if "issue_active_pct" in rec:
+        out["ncu_issue_active_pct"] = rec["issue_active_pct"]
+    return out
 
 
 def cpu_baseline(cat, rows: int, seed: int, threads: int = 0) -> dict:
@@ -226,8 +260,7 @@ def run_reference(args, cat, workload, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload, "n_d": cat.n_d, "n_r": cat.n_r, "bin_width_deg": cat.bin_width_deg,
-                       "nbins": cat.nbins, "l2": "n/a (CPU)"},
+            "config": bench_config(cat, workload, {}),
             "cpu_baseline": cb, "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -315,13 +348,18 @@ def run_ours(args, cat, workload, rank, world, local):
     clocks = clk.summary()
     peak = SMS * LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12  # T thread-instructions / s at the maximum clock
     achieved = alg_inst * args.steps / (pair_ms / 1e3) / 1e12 if pair_ms > 0 else None
+    rec = recorded_counters(workload)
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
-            "frac": (achieved / peak) if achieved else None, "traffic": recorded_traffic(workload),
+            "frac": (achieved / peak) if achieved else None,
+            "frac_basis": "algorithmic instructions: a per-path instruction model (bench.py INST_PER_PATH) "
+                          "times the kernel's own per-path pair counters, over event-timed pair-kernel time",
+            "traffic": rec.get("dram_bytes_per_launch") if rec else None,
             "inst_per_pair": alg_inst / max(alg_pairs, 1), "pairs_computed_per_step": alg_pairs,
             "path_share": {k[len("pairs_"):]: round(v / max(alg_pairs, 1), 4) for k, v in path_pairs.items() if v},
             "pair_kernel_ms_per_launch": pair_ms / max(len(kt), 1),
             "pair_kernel_launches": len(kt),
             "peak_basis": f"{SMS} SMs x {LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz (maximum SM clock)"}
+    roof["executed"] = executed_roofline(rec, pair_ms / args.steps, alg_inst, peak)
     if clocks.get("sm_mhz"):
         roof["frac_at_observed_clock"] = achieved / (SMS * LANES_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12)
     # the FP32 issue ceiling measured on this GPU in this run (independent FMA chains)
@@ -365,11 +403,9 @@ def run_ours(args, cat, workload, rank, world, local):
             "vs_baseline": (value / (pairs / (PAGE_KERNEL_MS / 1e3) / 1e9)
                             if args.config == 1 and not args.option else None),
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload, "n_d": cat.n_d, "n_r": cat.n_r, "bin_width_deg": w, "nbins": nb,
-                       "l2": "flushed between timed steps (256 MiB device write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "grid": ctx.info("grid"), "threads": ctx.info("threads"), "layout": ctx.info("layout"),
-                       **({"options": parse_options(args.option)} if args.option else {})},
+            "config": bench_config(cat, workload, parse_options(args.option)),
+            "launch": {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "grid": ctx.info("grid"), "threads": ctx.info("threads"), "layout": ctx.info("layout")},
             "evaluated_gpairs_per_s": world * evals * args.steps / (total_ms_max / 1e3) / 1e9,
             # per-step spread on rank 0 (the pages' protocol reports the median and the minimum)
             "step_ms_stats": {"first": step_ms[0], "median": statistics.median(step_ms), "min": min(step_ms),

@@ -86,3 +86,19 @@ def test_reference_arm_prints_the_contract_line():
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("pages-shape-100k")
+    # both arms print the same workload description (launch facts go elsewhere in our arm)
+    import synth
+    c = synth.config(1)
+    assert line["config"] == bench.bench_config(c, line["config"]["workload"], {})
+    assert "grid" not in line["config"] and "threads" not in line["config"]
+
+
+def test_executed_roofline_from_a_record():
+    rec = {"per_launch": {"DD": {"thread_inst_executed": 1.0e11}, "DR": {"thread_inst_executed": 2.0e11},
+                          "RR": {"thread_inst_executed": 1.0e11}}, "issue_active_pct": 88.0}
+    # 4e11 instructions in 10 ms = 40 T inst/s
+    r = bench.executed_roofline(rec, 10.0, 3.2e11, 40.0)
+    assert r["achieved"] == pytest.approx(40.0) and r["frac"] == pytest.approx(1.0)
+    assert r["inst_overhead"] == pytest.approx(1.25) and r["ncu_issue_active_pct"] == 88.0
+    assert bench.executed_roofline(None, 10.0, 1.0, 40.0) is None
+    assert bench.executed_roofline({"per_launch": {"DD": {}}}, 10.0, 1.0, 40.0) is None
