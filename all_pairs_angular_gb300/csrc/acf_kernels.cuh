@@ -656,9 +656,10 @@ __device__ __forceinline__ float pair_code_fixed(float xi, float yi, float zi, f
   if (MAP == kDirect) {
     return fma_rz(th, iws, h);
   } else {
-    // theta / w = th * iws + h with h = 0 (near side) or pi / w (far side); iws = -1/w there
+    // theta / w = th * iws + h with h = 0 (near side) or pi / w (far side); iws = -1/w there; the
+    // fine clamp is in units of the form's own window (S_small fine bits for the short chord)
     const float t = fmaf(th, iws, h);
-    return add_rz(fminf(t, FINE ? bp.clamp_f : bp.clamp_c), FINE ? bp.magic_f : kMagic);
+    return add_rz(fminf(t, FINE ? (SMALL ? bp.clamp_fs : bp.clamp_f) : bp.clamp_c), FINE ? bp.magic_f : kMagic);
   }
 }
 
@@ -1389,32 +1390,44 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& t) {
   t = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
 }
 
-// q = |a + sg b|^2 (sg = -1: the difference chord, +1: the sum chord) of two double-single vectors
-// (hi + lo), returned as qh + ql. Error against the same q of the fp64 vectors that hi + lo round:
-//  - representation: |hi + lo - x| <= 2^-48 per component, so <= 2^-47 on each component of a + sg b;
-//  - components: lo + sg lo' (error <= 2^-47), the TwoSum remainder plus that (error <= 2^-46), then
-//    an exact TwoSum: <= 2^-45 in all per component, so <= 2 sqrt(3) 2^-45 |d| = 9.8e-14 |d| on q;
-//  - squares: exact product and remainder (fma), 2 dh dl rounded and dl^2 dropped: <= 2^-46 q;
-//  - the sum of the eight small terms: <= 2^-44 q.
-__device__ __forceinline__ void ds_chord2(float4 ah, float4 al, float4 bh, float4 bl, float sg, float& qh, float& ql) {
+// The dot product of two double-single unit vectors (hi + lo), returned as dh + dl. Error against
+// the dot product of the fp64 vectors that hi + lo round (|a|, |b| = 1):
+//  - representation: |hi + lo - x| <= 2^-48 |x| per component, so <= 2^-47 on the dot product;
+//  - products: hi hi' as the fp32 product plus its exact fma remainder; the three cross terms (and
+//    lo lo') added to that remainder by fma, each rounding <= 2^-24 of a remainder below 3 2^-24 of
+//    the component's product: <= 9 2^-48 over the three components; the remainders' two fp32 sums
+//    <= 6 2^-48;
+//  - the sum: two exact TwoSums, then two fp32 adds of their remainders and the products'
+//    (below 8 2^-24 in all): <= 13 2^-48; the final TwoSum is exact.
+// In all <= 30 2^-48 = 1.07e-13.
+constexpr float kDotErr = 1.07e-13f;
+__device__ __forceinline__ void ds_dot(float4 ah, float4 al, float4 bh, float4 bl, float& dh, float& dl) {
   const float a_h[3] = {ah.x, ah.y, ah.z}, a_l[3] = {al.x, al.y, al.z};
   const float b_h[3] = {bh.x, bh.y, bh.z}, b_l[3] = {bl.x, bl.y, bl.z};
-  float p[3], small = 0.0f;
+  float p[3], r = 0.0f;
 #pragma unroll
   for (int c = 0; c < 3; ++c) {
-    float s, t, dh, dl;
-    two_sum(a_h[c], sg * b_h[c], s, t);  // sg * b is exact
-    const float v = __fadd_rn(t, __fadd_rn(a_l[c], sg * b_l[c]));
-    two_sum(s, v, dh, dl);
-    p[c] = __fmul_rn(dh, dh);
-    const float e = __fmaf_rn(dh, dh, -p[c]);  // dh^2 - p exactly
-    small = __fadd_rn(small, __fadd_rn(e, __fmul_rn(2.0f * dh, dl)));
+    p[c] = __fmul_rn(a_h[c], b_h[c]);
+    float e = __fmaf_rn(a_h[c], b_h[c], -p[c]);  // exact
+    e = __fmaf_rn(a_h[c], b_l[c], e);
+    e = __fmaf_rn(a_l[c], b_h[c], e);
+    e = __fmaf_rn(a_l[c], b_l[c], e);
+    r = c == 0 ? e : __fadd_rn(r, e);
   }
   float s1, t1, s2, t2;
   two_sum(p[0], p[1], s1, t1);
   two_sum(s1, p[2], s2, t2);
-  small = __fadd_rn(small, __fadd_rn(t1, t2));
-  two_sum(s2, small, qh, ql);
+  two_sum(s2, __fadd_rn(r, __fadd_rn(t1, t2)), dh, dl);
+}
+
+// The chord q = |a + sg b|^2 = 2 + 2 sg (a.b) of two unit vectors (sg = -1: the difference chord,
+// +1: the sum chord) from their double-single dot product, as qh + ql. 2 + 2 sg dh is split exactly
+// by TwoSum; the one rounding of its remainder plus 2 sg dl is below 2^-24 of 6 2^-24. With the dot
+// product's error: |q - exact| <= 2 kDotErr + 2.2e-14.
+__device__ __forceinline__ void ds_chord_from_dot(float dh, float dl, float sg, float& qh, float& ql) {
+  float t;
+  two_sum(2.0f, 2.0f * sg * dh, qh, t);
+  ql = __fadd_rn(t, 2.0f * sg * dl);
 }
 
 // Side of q = qh + ql against a double-single table value: +1 above, -1 below, 0 within eps (then
@@ -1538,8 +1551,9 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     }
     ++my_moved;
   };
-  // re-decide pair (i, j), whose count went to entry e, from its double-single vectors
-  auto redo = [&](int e, int i, int j, float4 ah, float4 al, float4 bh, float4 bl) {
+  // re-decide pair (i, j), whose count went to entry e, from the double-single dot product of its
+  // vectors (dh + dl)
+  auto redo = [&](int e, int i, int j, float dh, float dl) {
     e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
     const int kf = entry_to_bin<MAP>(e, bp);
     const int k0 = kf > bp.kmax ? bp.kmax : kf;
@@ -1548,10 +1562,11 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     bool sure = true;
     {
       float qh, ql;
-      ds_chord2(ah, al, bh, bl, diff ? -1.0f : 1.0f, qh, ql);
-      // the bound on ds_chord2's error (|d| = sqrt(q); sqrt.approx is within 2^-22 relative), plus
-      // the tables' 2^-48 and the fp64 computation's 2^-50 relative
-      const float eps = 1.5e-13f * sqrt_approx(qh) + 3e-13f * qh;
+      ds_chord_from_dot(dh, dl, diff ? -1.0f : 1.0f, qh, ql);
+      // the bound on q's error (2 kDotErr + 2.2e-14), plus the double-single tables' 2^-48 relative
+      // (T, U <= 4), the fp64 computation's own rounding (<= 2.2e-15) and the rounding of the side
+      // test's remainder difference (<= 2.9e-14): 2.8e-13, with some margin
+      const float eps = 4e-13f;
       if (diff) {
         // lower edge: q >= T[k]; upper edge: q < T[k + 1]
         for (int c; k > 0 && (c = ds_side(qh, ql, tT[k], eps)) <= 0; --k) if (!c) { sure = false; break; }
@@ -1592,7 +1607,9 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     int S;
     recorded_codes<MAP>(pc, ah, bh, bp, cb, e, single, S);
     if (e - bp.zone0 <= bp.span0 || e - bp.zone1 <= bp.span1) {
-      redo((int)e, i, j, ah, al, bh, bl);
+      float dh, dl;
+      ds_dot(ah, al, bh, bl, dh, dl);
+      redo((int)e, i, j, dh, dl);
     } else if (single && (cb & ((1u << S) - 1u)) == 0u) {
       // outside the exact zone: the fp32 bin stands, minus the bias's carry
       const int ec = (int)e < bp.entries ? (int)e : bp.entries - 1;
