@@ -249,6 +249,27 @@ __device__ __forceinline__ void red_shared_add(uint32_t addr, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// ACF_MATCH_AGG=1 builds (a measured alternative for the block-shared histogram): lanes of a warp
+// that add to the same counter are grouped by __match_any_sync and the group's lowest lane adds the
+// group's total, so a warp issues one red per distinct counter instead of one per lane.
+#ifndef ACF_MATCH_AGG
+#define ACF_MATCH_AGG 0
+#endif
+// Add v (the same in every lane) to the shared counter at byte address a; `aggregate` selects the
+// warp aggregation (block-shared layouts, in ACF_MATCH_AGG builds).
+__device__ __forceinline__ void hist_add(uint32_t a, uint32_t v, bool aggregate) {
+#if ACF_MATCH_AGG
+  if (aggregate) {
+    const uint32_t peers = __match_any_sync(__activemask(), a);
+    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) red_shared_add(a, v * (uint32_t)__popc(peers));
+    return;
+  }
+#else
+  (void)aggregate;
+#endif
+  red_shared_add(a, v);
+}
+
 // Add v to the 16-bit counter at shared byte address a16 (two counters per 32-bit word, so the add
 // goes to the word). The thread whose add takes the counter from below 0x8000 to 0x8000 or more
 // takes 0x8000 back out and returns true: its caller adds 0x8000 to the counter's bin elsewhere.
@@ -849,14 +870,14 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
           atomicAdd(p.partial + (size_t)blockIdx.x * p.bp.nbins + entry_to_bin<MAP>((int)(cb - magic_bits), p.bp),
                     0x8000ull);
       } else {
-        red_shared_add((cb << shift) + base, inc);
+        hist_add((cb << shift) + base, inc, shift == 2);
       }
     }
     return false;
   } else {
     if (ACF_CHECK(((cb - magic_bits) >> S) < (uint32_t)p.bp.entries, 6, (long long)((cb - magic_bits) >> S), i,
                   __uint_as_float(cb), xi, yi, zi, v.x, v.y, v.z, (float)j))
-      red_shared_add(((cb >> S) << shift) + base_f, inc);
+      hist_add(((cb >> S) << shift) + base_f, inc, shift == 2);
     return (cb & ((1u << S) - 1u)) <= 1u;
   }
 }
@@ -864,7 +885,7 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
 // Exact mode: record, for the re-decision, a j whose pairs with the warp's i-set hold at least one
 // flagged pair (a fine code within one fine unit of an edge). One record per warp and j: the header
 // (j, the i-set row r, the group's path code pc) and for each i-vector slot k the ballot of the lanes
-// whose pair (i = 32 (K r + k) + lane, j) is flagged. The re-decision recomputes each such pair's
+// whose pair (i = kJT r + islot(k, lane), j) is flagged. The re-decision recomputes each such pair's
 // codes from the same vectors with the same device code (the path code fixes the form), so that
 // the record need not carry them. The warp's records go to its own region of the queue at its
 // cursor `cur` (the same value in every lane; no atomic), and past the region's end to slots of the
@@ -915,6 +936,19 @@ __device__ __forceinline__ void carry_back(uint32_t cb, int S, uint32_t base_f, 
 }
 
 // ------------------------------------------------------------------ pair kernel
+
+// Which galaxy of a warp's i-set (kJT = 32 K consecutive sorted galaxies) lane `lane` holds in its
+// slot k. ACF_ISPREAD 1: lane l holds galaxies K l .. K l + K - 1, so that the 32 lanes of one slot
+// spread over the whole i-set and their separations to one j over more bins (fewer lanes adding to
+// the same counter of a block-shared histogram at once); 0: lane l holds l, l + 32, ... The pairs, the
+// caps and the forms are the same either way.
+#ifndef ACF_ISPREAD
+#define ACF_ISPREAD 1
+#endif
+template <int K>
+__device__ __forceinline__ int islot(int k, int lane) {
+  return ACF_ISPREAD ? lane * K + k : k * 32 + lane;
+}
 
 // Map unit u to (i-set row r, j-chunk column c). For DD/RR row r holds columns r .. cols-1 and
 // starts at S(r) = r*cols - r*(r-1)/2.
@@ -1075,7 +1109,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
       if (r != cur_r) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          int i = i0 + k * 32 + lane;
+          int i = i0 + islot<K>(k, lane);
           i = i < ni ? i : ni - 1;
           const float4 v = __ldg(p.vi + i);
           xi[k] = v.x;
@@ -1157,7 +1191,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               for (int u = 0; u < B; ++u)
 #pragma unroll
                 for (int k = 0; k < K; ++k)
-                  add_pair<false, MAP>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj + u,
+                  add_pair<false, MAP>(p, cb[u * K + k], base, bf, SHIFT, SF, magic_bits, i0 + islot<K>(k, lane), j0 + jj + u,
                                   xi[k], yi[k], zi[k], vv[u], inc);
             }
           } else if constexpr (F && (X == 1 || X == 3)) {
@@ -1173,7 +1207,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
               for (int k = 0; k < K; ++k) {
                 cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
                                                                         iws_c, h_c, p.bp, ccs[k]));
-                add_pair<false, MAP>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k],
+                add_pair<false, MAP>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + islot<K>(k, lane), j0 + jj, xi[k], yi[k],
                                 zi[k], v, inc);
 #if ACF_FLAG_PRED
                 fl |= (cfs[k] & (fmask & ~1u)) == 0u;
@@ -1199,7 +1233,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
 #pragma unroll
               for (int k = 0; k < K; ++k) {
                 cbs[k] = code_of(k, v);
-                add_pair<F, MAP>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + k * 32 + lane, j0 + jj, xi[k], yi[k], zi[k],
+                add_pair<F, MAP>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + islot<K>(k, lane), j0 + jj, xi[k], yi[k], zi[k],
                             v, inc);
 #if ACF_FLAG_PRED
                 if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
@@ -1259,7 +1293,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         int thr[K];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-          const int i = i0 + k * 32 + lane;
+          const int i = i0 + islot<K>(k, lane);
           const int tt = p.sym ? i - j0 : -1;
           thr[k] = (i >= ni) ? 0x7fffffff : max(-1, min(tt, kJT));
         }
@@ -1275,7 +1309,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             for (int k = 0; k < K; ++k) {
               cbs[k] = __float_as_uint(pair_code<MAP, METHOD, F>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
               fk[k] = jj > thr[k] &&
-                      add_pair<F, MAP>(p, cbs[k], base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + k * 32 + lane,
+                      add_pair<F, MAP>(p, cbs[k], base, base_f, SHIFT, p.bp.fine_shift, magic_bits, i0 + islot<K>(k, lane),
                                        j0 + jj, xi[k], yi[k], zi[k], v, inc);
             }
             if (F && __any_sync(0xffffffffu, fk[0] || fk[1] || fk[2] || fk[3])) {
@@ -1662,7 +1696,7 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
           while (m[k] && slot < 32u) {
             const int b = __ffs(m[k]) - 1;
             m[k] &= m[k] - 1u;
-            list[slot++] = make_uint4((unsigned)((r * 4 + k) * 32 + b), (unsigned)j, (unsigned)pc, 0u);
+            list[slot++] = make_uint4((unsigned)(r * kJT + islot<kJT / 32>(k, b)), (unsigned)j, (unsigned)pc, 0u);
           }
         }
       }

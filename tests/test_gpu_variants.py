@@ -7,6 +7,9 @@
   also held to the oracle's edge rule, one of them dense enough that every block's counters carry.
 - ACF_J_SHUFFLE=1 broadcasts the j-vectors by warp shuffles instead of shared-memory loads. In the
   default exact mode 2 its histograms must equal the fp64 oracle's bin for bin.
+- ACF_MATCH_AGG=1 aggregates the block-shared histogram's increments per warp with __match_any_sync
+  (one red per distinct counter). In exact mode 2 its histograms must equal the oracle's bin for bin,
+  at 0.01-degree bins (block-shared by default) and at 0.25 degrees with the layout forced.
 
 Each variant is built on the spot and exercised in a child process, which loads it through
 ACF_LIB.
@@ -24,7 +27,7 @@ from all_pairs_angular_gb300 import build as acf_build
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-VARIANTS = {"u16": ["-DACF_U16_HIST=1"], "shuffle": ["-DACF_J_SHUFFLE=1"]}
+VARIANTS = {"u16": ["-DACF_U16_HIST=1"], "shuffle": ["-DACF_J_SHUFFLE=1"], "match": ["-DACF_MATCH_AGG=1"]}
 
 
 @pytest.fixture(scope="module")
@@ -124,3 +127,27 @@ print(json.dumps({"equal": ok}))
 def test_shuffle_broadcast_equals_oracle_in_exact_mode(libs):
     res = _child(libs["shuffle"], SHUFFLE_CODE)
     assert res["equal"] == [True, True], res
+
+
+MATCH_CODE = r"""
+import json, numpy as np, torch, synth, oracle
+import all_pairs_angular_gb300 as acf
+ctx = acf.Context(0)
+c = synth.catalogs(4000, 3000, 20, 3.0, seed=45, patch_arcmin=300.0)
+res = []
+for w, nb, lay in ((0.01, 18000, 0), (0.25, 720, 2)):
+    ctx.set_option("layout", lay)
+    for args in ((c.ra_d, c.dec_d, None, None), (c.ra_d, c.dec_d, c.ra_r, c.dec_r)):
+        g = acf.as_uint64(ctx.histogram(*args, bin_width_deg=w, nbins=nb))
+        torch.cuda.synchronize()
+        o = oracle.histogram(*args, w, nb)
+        res.append({"w": w, "layout": ctx.info("layout"), "equal": bool(np.array_equal(g, o.hist)),
+                    "flagged": ctx.info("exact_flagged")})
+print(json.dumps(res))
+"""
+
+
+def test_match_aggregation_equals_oracle_in_exact_mode(libs):
+    res = _child(libs["match"], MATCH_CODE)
+    assert all(r["equal"] and r["layout"] == 2 for r in res), res
+    assert all(r["flagged"] > 0 for r in res), res
