@@ -299,16 +299,16 @@ struct CatBufs {
   double4_32a* v64 = nullptr;    // the same in fp64 (exact re-decision)
   float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
+  unsigned int* key0 = nullptr;    // sort: cell keys in input order, at the end the order
+  unsigned int* key1 = nullptr;    // sort: keys after the first pass
+  unsigned int* idx1 = nullptr;    // sort: input indices after the first pass
+  unsigned int* counts = nullptr;  // sort: digit counts per tile, then their offsets
 };
 struct Scratch {
   unsigned int* counters = nullptr;    // [0] unit ticket, [1] queue spill records handed out (this launch),
                                        // [2] moved pairs, [3] flagged pairs, [4] flagged pairs without a
                                        // record slot, [5] pairs the fix-up redid in fp64;
                                        // bytes 64..135: pairs per path (u64)
-  unsigned int* key0 = nullptr;        // sort: cell keys in input order (shared by both catalogs)
-  unsigned int* key1 = nullptr;        // sort: keys after the first pass
-  unsigned int* idx1 = nullptr;        // sort: input indices after the first pass
-  unsigned int* counts = nullptr;      // sort: digit counts per tile, then their offsets
   CatBufs a, b;                        // b only for cross-correlations
   unsigned long long* partial = nullptr;
   unsigned long long* delta = nullptr; // exact mode: count moves of the exact re-decision, per bin
@@ -339,6 +339,11 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   };
   auto cat = [&](long long m, CatBufs& cb) {
     const long long ch = (m + 127) / 128;
+    const long long tiles = (m + kSortTile - 1) / kSortTile;
+    cb.key0 = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
+    cb.key1 = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
+    cb.idx1 = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
+    cb.counts = reinterpret_cast<unsigned int*>(take((size_t)tiles * kSortDigits * 4));
     cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
     cb.lo = reinterpret_cast<float4*>(take((size_t)m * 16));
     cb.v64 = reinterpret_cast<double4_32a*>(take((size_t)m * 32));
@@ -348,12 +353,6 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   Scratch t;
   Scratch& r = s ? *s : t;
   r.counters = reinterpret_cast<unsigned int*>(take(256));
-  const long long msort = std::max(n, sym ? n : nj);
-  const long long tiles = (msort + kSortTile - 1) / kSortTile;
-  r.key0 = reinterpret_cast<unsigned int*>(take((size_t)msort * 4));
-  r.key1 = reinterpret_cast<unsigned int*>(take((size_t)msort * 4));
-  r.idx1 = reinterpret_cast<unsigned int*>(take((size_t)msort * 4));
-  r.counts = reinterpret_cast<unsigned int*>(take((size_t)tiles * kSortDigits * 4));
   cat(n, r.a);
   if (!sym) cat(nj, r.b);
   r.partial = reinterpret_cast<unsigned long long*>(take((size_t)grid * (size_t)nbins * 8));
@@ -369,32 +368,51 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   return off;
 }
 
-// Unit vectors of one catalog in spatial order (a stable radix sort on the cell key: low 8 bits,
-// then high 7; then the fp64 vectors in that order), with their caps.
-int prepare_catalog(acf_ctx* c, const float* ra, const float* dec, long long n, const Scratch& s, const CatBufs& cb) {
-  const long long tiles = (n + kSortTile - 1) / kSortTile;
-  const unsigned grid = (unsigned)tiles;
-  const long long m = tiles * kSortDigits;
-  sort_count_kernel<<<grid, kSortThreads, 0, c->stream>>>(ra, dec, nullptr, s.key0, n, 0, (int)tiles, s.counts);
+// Unit vectors of one or two catalogs in spatial order (a stable radix sort on the cell key: low 8
+// bits, then high 7; then the fp64 vectors in that order), with their caps. Both catalogs of a
+// cross-correlation go through the same eight launches (blockIdx.y selects the catalog).
+int prepare_catalogs(acf_ctx* c, int count, const float* const ra[2], const float* const dec[2], const long long n[2],
+                     const CatBufs* const cb[2]) {
+  PrepBatch b;
+  std::memset(&b, 0, sizeof b);
+  int tiles_max = 0;
+  long long n_max = 0;
+  for (int k = 0; k < count; ++k) {
+    PrepCat& C = b.c[k];
+    C.ra = ra[k];
+    C.dec = dec[k];
+    C.n = n[k];
+    C.tiles = (int)((n[k] + kSortTile - 1) / kSortTile);
+    C.key0 = cb[k]->key0;
+    C.key1 = cb[k]->key1;
+    C.idx1 = cb[k]->idx1;
+    C.counts = cb[k]->counts;
+    C.v = cb[k]->v;
+    C.lo = cb[k]->lo;
+    C.v64 = cb[k]->v64;
+    C.cap32 = cb[k]->cap32;
+    C.cap128 = cb[k]->cap128;
+    tiles_max = std::max(tiles_max, C.tiles);
+    n_max = std::max(n_max, n[k]);
+  }
+  const dim3 tiles_grid((unsigned)tiles_max, (unsigned)count), one(1, (unsigned)count);
+  sort_count_kernel<true><<<tiles_grid, kSortThreads, 0, c->stream>>>(b, 0);
   ACF_LAUNCHED(c);
-  scan_kernel<<<1, 1024, 0, c->stream>>>(s.counts, m);
+  scan_kernel<<<one, 1024, 0, c->stream>>>(b);
   ACF_LAUNCHED(c);
-  sort_scatter_kernel<false><<<grid, kSortThreads, 0, c->stream>>>(s.key0, nullptr, n, 0, (int)tiles, s.counts, s.key1,
-                                                                  s.idx1);
+  sort_scatter_kernel<false><<<tiles_grid, kSortThreads, 0, c->stream>>>(b, 0);
   ACF_LAUNCHED(c);
-  sort_count_kernel<<<grid, kSortThreads, 0, c->stream>>>(ra, dec, s.key1, nullptr, n, 8, (int)tiles, s.counts);
+  sort_count_kernel<false><<<tiles_grid, kSortThreads, 0, c->stream>>>(b, 8);
   ACF_LAUNCHED(c);
-  scan_kernel<<<1, 1024, 0, c->stream>>>(s.counts, m);
+  scan_kernel<<<one, 1024, 0, c->stream>>>(b);
   ACF_LAUNCHED(c);
-  // the final order (sorted position -> input index) reuses key0, which pass 2 no longer reads
-  sort_scatter_kernel<true><<<grid, kSortThreads, 0, c->stream>>>(s.key1, s.idx1, n, 8, (int)tiles, s.counts, nullptr,
-                                                                 s.key0);
+  sort_scatter_kernel<true><<<tiles_grid, kSortThreads, 0, c->stream>>>(b, 8);
   ACF_LAUNCHED(c);
-  const long long vblocks = std::min<long long>((n + 255) / 256, (long long)c->num_sms * 8);
-  vectors_kernel<<<(unsigned)vblocks, 256, 0, c->stream>>>(ra, dec, s.key0, n, cb.v, cb.lo, cb.v64);
+  const long long vblocks = std::min<long long>((n_max + 255) / 256, (long long)c->num_sms * 8 / count);
+  vectors_kernel<<<dim3((unsigned)std::max<long long>(vblocks, 1), (unsigned)count), 256, 0, c->stream>>>(b);
   ACF_LAUNCHED(c);
-  const long long warps = (n + 127) / 128;
-  caps_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, c->stream>>>(cb.v, n, cb.cap32, cb.cap128);
+  const long long warps = (n_max + 127) / 128;
+  caps_kernel<<<dim3((unsigned)((warps * 32 + 255) / 256), (unsigned)count), 256, 0, c->stream>>>(b);
   ACF_LAUNCHED(c);
   return ACF_OK;
 }
@@ -584,12 +602,12 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
 // and (exact mode) re-decide the flagged pairs.
 int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, const float* ra2, const float* dec2,
                  long long nj, bool sym, const Plan& pl, const Launch& L, const Scratch& sc, uint64_t* out) {
-  int rc = prepare_catalog(c, ra, dec, n, sc, sc.a);
+  const float* const ras[2] = {ra, ra2};
+  const float* const decs[2] = {dec, dec2};
+  const long long ns[2] = {n, nj};
+  const CatBufs* const cbs[2] = {&sc.a, &sc.b};
+  int rc = prepare_catalogs(c, sym ? 1 : 2, ras, decs, ns, cbs);
   if (rc) return rc;
-  if (!sym) {
-    rc = prepare_catalog(c, ra2, dec2, nj, sc, sc.b);
-    if (rc) return rc;
-  }
   if (pl.exact && sc.qcap > 0) {
     edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U, sc.Tds, sc.Uds);
     ACF_LAUNCHED(c);
@@ -650,8 +668,13 @@ int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_
   if (rc) return rc;
   Scratch sc;
   carve(static_cast<char*>(c->ws.ptr), n_d, n_r, false, grid, nbins, qcap, &sc);
-  if ((rc = prepare_catalog(c, ra_d, dec_d, n_d, sc, sc.a)) || (rc = prepare_catalog(c, ra_r, dec_r, n_r, sc, sc.b)))
-    return rc;
+  {
+    const float* const ras[2] = {ra_d, ra_r};
+    const float* const decs[2] = {dec_d, dec_r};
+    const long long ns[2] = {n_d, n_r};
+    const CatBufs* const cbs[2] = {&sc.a, &sc.b};
+    if ((rc = prepare_catalogs(c, 2, ras, decs, ns, cbs))) return rc;
+  }
   if (pl.exact && sc.qcap > 0) {
     edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U, sc.Tds, sc.Uds);
     ACF_LAUNCHED(c);

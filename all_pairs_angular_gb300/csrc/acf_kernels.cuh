@@ -394,37 +394,62 @@ constexpr int kSortRounds = 8;
 constexpr int kSortTile = kSortThreads * kSortRounds;  // elements per tile (one block)
 constexpr int kSortDigits = 256;
 
-// Digit counts of one tile. Pass 1 (keys_in == nullptr) also computes every galaxy's cell key.
-__global__ void __launch_bounds__(kSortThreads) sort_count_kernel(const float* __restrict__ ra,
-                                                                  const float* __restrict__ dec,
-                                                                  const unsigned int* __restrict__ keys_in,
-                                                                  unsigned int* __restrict__ keys_out, long long n,
-                                                                  int shift, int ntiles, unsigned int* __restrict__ counts) {
+// One catalog's preparation: its input, its sort scratch and its outputs. The preparation kernels
+// take up to two catalogs at once (PrepBatch, blockIdx.y selects the catalog), so that both catalogs
+// of a cross-correlation are sorted and converted by the same launches.
+struct PrepCat {
+  const float* ra;        // input, arcminutes
+  const float* dec;
+  long long n;
+  int tiles;              // sort tiles of kSortTile galaxies
+  unsigned int* key0;     // sort: cell keys in input order; at the end the order (position -> input index)
+  unsigned int* key1;     // sort: keys after the first pass
+  unsigned int* idx1;     // sort: input indices after the first pass
+  unsigned int* counts;   // sort: digit counts per tile, then their offsets
+  float4* v;              // outputs: fp32 vectors, their remainders, fp64 vectors, caps
+  float4* lo;
+  double4_32a* v64;
+  float4* cap32;
+  float4* cap128;
+};
+struct PrepBatch {
+  PrepCat c[2];
+};
+
+// Digit counts of one tile. Pass 1 (PASS1) also computes every galaxy's cell key. Digits at bit
+// `shift`.
+template <bool PASS1>
+__global__ void __launch_bounds__(kSortThreads) sort_count_kernel(const PrepBatch b, int shift) {
+  const PrepCat& C = b.c[blockIdx.y];
+  if ((int)blockIdx.x >= C.tiles) return;
   __shared__ unsigned int h[kSortDigits];
   for (int d = threadIdx.x; d < kSortDigits; d += kSortThreads) h[d] = 0u;
   __syncthreads();
   const long long base = (long long)blockIdx.x * kSortTile;
   for (int r = 0; r < kSortRounds; ++r) {
     const long long i = base + r * kSortThreads + threadIdx.x;
-    if (i < n) {
+    if (i < C.n) {
       unsigned int k;
-      if (keys_in) {
-        k = keys_in[i];
+      if (PASS1) {
+        k = cell_key(C.ra[i], C.dec[i]);
+        C.key0[i] = k;
       } else {
-        k = cell_key(ra[i], dec[i]);
-        keys_out[i] = k;
+        k = C.key1[i];
       }
       atomicAdd(&h[(k >> shift) & (kSortDigits - 1)], 1u);
     }
   }
   __syncthreads();
-  for (int d = threadIdx.x; d < kSortDigits; d += kSortThreads) counts[(size_t)d * ntiles + blockIdx.x] = h[d];
+  for (int d = threadIdx.x; d < kSortDigits; d += kSortThreads) C.counts[(size_t)d * C.tiles + blockIdx.x] = h[d];
 }
 
-// In-place exclusive prefix sum of m counts, one block of 1024 threads: rounds of 1024
-// consecutive values (coalesced loads), each scanned with warp shuffles and the 32 warp totals,
-// plus the carry.
-__global__ void __launch_bounds__(1024) scan_kernel(unsigned int* __restrict__ v, long long m) {
+// In-place exclusive prefix sum of a catalog's tiles * kSortDigits counts, one block of 1024 threads
+// per catalog: rounds of 1024 consecutive values (coalesced loads), each scanned with warp shuffles
+// and the 32 warp totals, plus the carry.
+__global__ void __launch_bounds__(1024) scan_kernel(const PrepBatch b) {
+  const PrepCat& C = b.c[blockIdx.y];
+  unsigned int* __restrict__ v = C.counts;
+  const long long m = (long long)C.tiles * kSortDigits;
   __shared__ unsigned int warp_sum[32];
   __shared__ unsigned int carry;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -462,17 +487,19 @@ __global__ void __launch_bounds__(1024) scan_kernel(unsigned int* __restrict__ v
 // Stable scatter of one tile. Element i of the tile goes to offset(digit, tile) + the number of
 // earlier elements of the tile with the same digit: rounds of 256 in input order; within a round a
 // warp ranks its lanes with __match_any_sync, and the warps' per-digit totals rank the warps.
-// Pass 1 (FINAL = false) moves (key, input index); pass 2 only the input index.
+// Pass 1 (FINAL = false) moves (key, input index) from key0 to key1/idx1; pass 2 moves only the
+// input index, from idx1 into key0 (the order; pass 2 no longer reads key0).
 template <bool FINAL>
-__global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(
-    const unsigned int* __restrict__ keys_in, const unsigned int* __restrict__ idx_in, long long n, int shift,
-    int ntiles, const unsigned int* __restrict__ offsets, unsigned int* __restrict__ keys_out,
-    unsigned int* __restrict__ idx_out) {
+__global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(const PrepBatch b, int shift) {
+  const PrepCat& C = b.c[blockIdx.y];
+  if ((int)blockIdx.x >= C.tiles) return;
+  const unsigned int* __restrict__ keys_in = FINAL ? C.key1 : C.key0;
+  const long long n = C.n;
   constexpr int W = kSortThreads / 32;
   __shared__ unsigned int running[kSortDigits];      // elements of each digit placed by earlier rounds
   __shared__ unsigned int wcount[W][kSortDigits];    // this round: elements of each digit per warp
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  for (int d = t; d < kSortDigits; d += kSortThreads) running[d] = offsets[(size_t)d * ntiles + blockIdx.x];
+  for (int d = t; d < kSortDigits; d += kSortThreads) running[d] = C.counts[(size_t)d * C.tiles + blockIdx.x];
   const long long base = (long long)blockIdx.x * kSortTile;
   const unsigned int lt = (1u << lane) - 1u;
   for (int r = 0; r < kSortRounds; ++r) {
@@ -490,8 +517,12 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(
       unsigned int pos = running[dig] + rank;
       for (int w = 0; w < warp; ++w) pos += wcount[w][dig];
       if (ACF_CHECK(pos < (unsigned long long)n, 5, i, pos)) {
-        idx_out[pos] = FINAL ? idx_in[i] : (unsigned int)i;
-        if (!FINAL) keys_out[pos] = key;
+        if (FINAL) {
+          C.key0[pos] = C.idx1[i];
+        } else {
+          C.idx1[pos] = (unsigned int)i;
+          C.key1[pos] = key;
+        }
       }
     }
     __syncthreads();
@@ -506,21 +537,20 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(
 }
 
 // Unit vectors in sorted order, as fp32 (pair kernel) and fp64 (exact re-decision of flagged
-// pairs): position p holds input galaxy order[p].
-// v_out is the fp32 rounding of each fp64 component and lo_out the fp32 rounding of what remains
-// (|x - hi - lo| <= 2^-48 |x|): together a double-single copy for the fix-up's first pass.
-__global__ void vectors_kernel(const float* __restrict__ ra, const float* __restrict__ dec,
-                               const unsigned int* __restrict__ order, long long n, float4* __restrict__ v_out,
-                               float4* __restrict__ lo_out, double4_32a* __restrict__ v64_out) {
-  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n; p += (long long)gridDim.x * blockDim.x) {
-    const unsigned int src = order[p];
-    if (ACF_CHECK(src < (unsigned long long)n, 5, p, src)) {
+// pairs): position p holds input galaxy order[p] (key0 after the sort).
+// v is the fp32 rounding of each fp64 component and lo the fp32 rounding of what remains
+// (|x - hi - lo| <= 2^-48 |x|): together a double-single copy for the fix-up.
+__global__ void vectors_kernel(const PrepBatch b) {
+  const PrepCat& C = b.c[blockIdx.y];
+  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < C.n; p += (long long)gridDim.x * blockDim.x) {
+    const unsigned int src = C.key0[p];
+    if (ACF_CHECK(src < (unsigned long long)C.n, 5, p, src)) {
       double x, y, z;
-      unit64(ra[src], dec[src], x, y, z);
+      unit64(C.ra[src], C.dec[src], x, y, z);
       const float hx = (float)x, hy = (float)y, hz = (float)z;
-      v_out[p] = make_float4(hx, hy, hz, 0.0f);
-      lo_out[p] = make_float4((float)(x - (double)hx), (float)(y - (double)hy), (float)(z - (double)hz), 0.0f);
-      v64_out[p] = make_double4_32a(x, y, z, 0.0);
+      C.v[p] = make_float4(hx, hy, hz, 0.0f);
+      C.lo[p] = make_float4((float)(x - (double)hx), (float)(y - (double)hy), (float)(z - (double)hz), 0.0f);
+      C.v64[p] = make_double4_32a(x, y, z, 0.0);
     }
   }
 }
@@ -531,8 +561,12 @@ constexpr float kCapMargin = 2e-5f;
 
 // One warp per 128 sorted galaxies: the cap of each 32-galaxy group and of the whole chunk.
 // Empty groups get radius 4 (> pi), which no decision can use.
-__global__ void caps_kernel(const float4* __restrict__ v, long long n, float4* __restrict__ cap32,
-                            float4* __restrict__ cap128) {
+__global__ void caps_kernel(const PrepBatch b) {
+  const PrepCat& C = b.c[blockIdx.y];
+  const float4* __restrict__ v = C.v;
+  const long long n = C.n;
+  float4* __restrict__ cap32 = C.cap32;
+  float4* __restrict__ cap128 = C.cap128;
   const int lane = threadIdx.x & 31;
   const long long chunk = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const long long nchunks = (n + 127) / 128;
@@ -1543,12 +1577,18 @@ struct FixupParams {
 // SMEM 2: the double-single tables and per-bin moves in shared memory; 1: the moves only; 0: neither.
 // Shared moves reach delta[] once per block.
 constexpr int kFixupThreads = 256;
+// Fix-up: pairs a lane decides per round (their vector loads all in flight together): 2 measured
+// 0.54 against 0.63 ms per fine-binning fix-up launch (19 against 16 threads per instruction)
+#ifndef ACF_FIXUP_PAIRS
+#define ACF_FIXUP_PAIRS 2
+#endif
+constexpr int kFixupPairs = ACF_FIXUP_PAIRS;
 template <int MAP, int SMEM>
 __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(const FixupParams f) {
   static_assert(kFixupThreads == 8 * 32, "one pair list per warp");
   extern __shared__ __align__(16) unsigned char fsm[];
   __shared__ unsigned int s_moved, s_redone, s_flagged;
-  __shared__ uint4 s_list[8][32];  // per warp: (i, j, path code) of the pairs of one round
+  __shared__ uint4 s_list[8][32 * kFixupPairs];  // per warp: (i, j, path code, 0) of the pairs of one round
   const BinParams& bp = f.bp;
   const int nb = bp.nbins;
   const float2* tT = f.Tds;
@@ -1632,10 +1672,9 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     }
     move(kf, k);
   };
-  // one flagged pair: i, j and the path code of the group that computed it
-  auto pair = [&](int i, int j, int pc) {
+  // one flagged pair (i, j, path code pc of the group that computed it) and its vectors
+  auto pair = [&](int i, int j, int pc, float4 ah, float4 al, float4 bh, float4 bl) {
     ++my_flagged;
-    const float4 ah = f.hi_i[i], al = f.lo_i[i], bh = f.hi_j[j], bl = f.lo_j[j];
     uint32_t cb, e;
     bool single;
     int S;
@@ -1652,9 +1691,10 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
   };
   // Each lane walks its own sequence of records (base + first, + stride, ...), holding the flagged
   // pairs of one record that are still to do (the next record already loading). Per round the warp
-  // packs up to 32 of those pairs into its list, in lane order (a warp scan of the lanes' counts
-  // gives each lane its slots), and then every lane decides one pair of the list: the lanes stay
-  // converged however the pairs spread over the records.
+  // packs up to 32 kFixupPairs of those pairs into its list, in lane order (a warp scan of the lanes'
+  // counts gives each lane its slots), and then every lane decides kFixupPairs pairs of the list,
+  // their vectors all loading before the first is decided: the lanes stay converged however the
+  // pairs spread over the records.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint4* list = s_list[warp];
   auto run = [&](unsigned long long base, unsigned int n, unsigned int first, unsigned int stride) {
@@ -1688,12 +1728,13 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
       }
       const unsigned int total = __shfl_sync(0xffffffffu, incl, 31);
       if (total == 0u) break;  // a lane with a record left always has a pair to do
+      constexpr unsigned int L = 32u * kFixupPairs;  // list length
       unsigned int slot = incl - cnt;
-      if (slot < 32u) {
+      if (slot < L) {
         const int j = (int)h.x, r = (int)(h.y & 0xFFFFFFu), pc = (int)(h.y >> 24);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          while (m[k] && slot < 32u) {
+          while (m[k] && slot < L) {
             const int b = __ffs(m[k]) - 1;
             m[k] &= m[k] - 1u;
             list[slot++] = make_uint4((unsigned)(r * kJT + islot<kJT / 32>(k, b)), (unsigned)j, (unsigned)pc, 0u);
@@ -1701,10 +1742,22 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
         }
       }
       __syncwarp();
-      if ((unsigned)lane < total) {
-        const uint4 e = list[lane];
-        pair((int)e.x, (int)e.y, (int)e.z);
+      uint4 e[kFixupPairs];
+      float4 ah[kFixupPairs], al[kFixupPairs], bh[kFixupPairs], bl[kFixupPairs];
+#pragma unroll
+      for (int u = 0; u < kFixupPairs; ++u) {
+        const bool ok = (unsigned)(lane + 32 * u) < total;
+        e[u] = ok ? list[lane + 32 * u] : make_uint4(0u, 0u, 0u, 0xFFFFFFFFu);
+        if (ok) {
+          ah[u] = f.hi_i[e[u].x];
+          al[u] = f.lo_i[e[u].x];
+          bh[u] = f.hi_j[e[u].y];
+          bl[u] = f.lo_j[e[u].y];
+        }
       }
+#pragma unroll
+      for (int u = 0; u < kFixupPairs; ++u)
+        if (e[u].w == 0u) pair((int)e[u].x, (int)e[u].y, (int)e[u].z, ah[u], al[u], bh[u], bl[u]);
       __syncwarp();
     }
   };

@@ -495,9 +495,10 @@ def test_range_forms_on_off_and_where_they_apply(acf, ctx, w, nb, mid_expected):
 
 
 def test_kernel_launch_counter(acf, ctx):
-    """kernel_launches counts every kernel of a call: eight catalog-preparation kernels per catalog
-    (two radix-sort passes of count, scan and scatter, the vectors, the caps), the pair kernel and
-    the merge, plus the edge tables and the fix-up in exact mode."""
+    """kernel_launches counts every kernel of a call: eight catalog-preparation kernels (two radix-sort
+    passes of count, scan and scatter, the vectors, the caps), which prepare both catalogs of a
+    cross-correlation at once, the pair kernel and the merge, plus the edge tables and the fix-up in
+    exact mode."""
     c = synth.catalogs(3000, 2500, 12, 30.0, seed=17)
 
     def launched(fn):
@@ -507,9 +508,9 @@ def test_kernel_launch_counter(acf, ctx):
 
     assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2 + 2
     assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25,
-                                          nbins=720)) == 16 + 2 + 2
-    # the whole job: two catalogs prepared once, one edge table, three histograms, omega
-    assert launched(lambda: ctx.correlate(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)) == 16 + 1 + 3 * 3 + 1
+                                          nbins=720)) == 8 + 2 + 2
+    # the whole job: both catalogs prepared once, one edge table, three histograms, omega
+    assert launched(lambda: ctx.correlate(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720)) == 8 + 1 + 3 * 3 + 1
     ctx.set_option("exact", 0)
     try:
         assert launched(lambda: ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)) == 8 + 2
