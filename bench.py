@@ -412,7 +412,10 @@ def run_ours(args, cat, workload, rank, world, local):
                               "max": max(step_ms)},
             "roofline": roof, "cpu_baseline": cb,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": 1e3 * e2e_total / args.steps},
+                    "ms_per_step": 1e3 * e2e_total / args.steps,
+                    # host-timed, so a host hiccup shows here: the spread of the steps on rank 0
+                    "step_ms_stats": {"first": 1e3 * e2e_times[0], "median": 1e3 * statistics.median(e2e_times),
+                                      "min": 1e3 * min(e2e_times), "max": 1e3 * max(e2e_times)}},
             "gpu_launches": gpu_launches, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
