@@ -38,6 +38,7 @@ struct Plan {
   int layout = kLane;
   int threads = 256;
   size_t smem = 0;
+  bool grouped = false;  // exact mode 2 with the block-shared histogram: group records, no queue
 };
 
 struct Workspace {
@@ -240,6 +241,7 @@ int make_plan(acf_ctx* c, double w_deg, int nbins, Plan& pl) {
   if (threads != 512 && threads != 1024) return fail(c, ACF_ERR_ARG, "threads must be 512 or 1024");
   pl.layout = layout;
   pl.threads = threads;
+  pl.grouped = layout == kBlock && pl.exact == 2 && pl.method == kChordPoly;
   pl.smem = hist_bytes + (size_t)(threads / 32) * kWarpTileBytes;
   if (pl.smem > kMaxSmem)
     return fail(c, ACF_ERR_UNSUPPORTED, "%s histogram of %d entries with %d threads needs %zu bytes of shared memory",
@@ -295,7 +297,7 @@ PairKernelFn pick_kernel(const Plan& pl, bool small) {
 // Device buffers of one histogram call, carved out of one scratch region.
 struct CatBufs {
   float4* v = nullptr;       // unit vectors in spatial order (fp32)
-  float4* lo = nullptr;      // what fp32 leaves of the fp64 components (double-single with v)
+  DsVec* ds = nullptr;       // double-single vectors (v and what fp32 leaves of the fp64 components)
   double4_32a* v64 = nullptr;    // the same in fp64 (exact re-decision)
   float4* cap32 = nullptr;   // caps of 32-galaxy groups (4 per 128-chunk)
   float4* cap128 = nullptr;  // caps of 128-galaxy chunks
@@ -316,10 +318,14 @@ struct Scratch {
   double* U = nullptr;
   float2* Tds = nullptr;               // the same as double-single (hi, lo) pairs
   float2* Uds = nullptr;
+  int* kd = nullptr;                   // the last bin re-decided with T (difference chord)
   uint2* qhdr = nullptr;               // exact mode: flag records, headers ..
   uint4* qmask = nullptr;              // .. and lane ballots
   unsigned int* qused = nullptr;       // per pair-kernel warp: records of its queue region in use
   long long qcap = 0;
+  unsigned int* gbal = nullptr;        // exact mode with group records: lane ballots and records of
+  GroupRecord* grec = nullptr;         // .. gunits units (4 groups of 32 lanes each)
+  long long gunits = 0;
 };
 
 // the fix-up's shared moves and tables at most: several 256-thread blocks per SM still fit, since the
@@ -328,9 +334,11 @@ constexpr size_t kFixupSmemMax = 24 * 1024;
 constexpr long long kQueueCapMin = 1ll << 20;  // flag records the workspace can hold: 24 MB ..
 constexpr long long kQueueCapMax = 1ll << 28;  // .. 6 GB
 constexpr size_t kRecordBytes = sizeof(uint2) + sizeof(uint4);
+constexpr size_t kGroupUnitBytes = 4 * sizeof(unsigned int) + kJT * sizeof(GroupRecord);  // group records of a unit
 
 // Lay the buffers out from `base` (nullptr: only measure). Returns the bytes needed.
-size_t carve(char* base, long long n, long long nj, bool sym, long long grid, int nbins, long long qcap, Scratch* s) {
+size_t carve(char* base, long long n, long long nj, bool sym, long long grid, int nbins, long long qcap, long long gunits,
+             Scratch* s) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
     char* p = base ? base + off : nullptr;
@@ -345,7 +353,7 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
     cb.idx1 = reinterpret_cast<unsigned int*>(take((size_t)m * 4));
     cb.counts = reinterpret_cast<unsigned int*>(take((size_t)tiles * kSortDigits * 4));
     cb.v = reinterpret_cast<float4*>(take((size_t)m * 16));
-    cb.lo = reinterpret_cast<float4*>(take((size_t)m * 16));
+    cb.ds = reinterpret_cast<DsVec*>(take((size_t)m * sizeof(DsVec)));
     cb.v64 = reinterpret_cast<double4_32a*>(take((size_t)m * 32));
     cb.cap32 = reinterpret_cast<float4*>(take((size_t)ch * 4 * 16));
     cb.cap128 = reinterpret_cast<float4*>(take((size_t)ch * 16));
@@ -361,10 +369,14 @@ size_t carve(char* base, long long n, long long nj, bool sym, long long grid, in
   r.U = reinterpret_cast<double*>(take((size_t)(nbins + 1) * 8));
   r.Tds = reinterpret_cast<float2*>(take((size_t)(nbins + 1) * 8));
   r.Uds = reinterpret_cast<float2*>(take((size_t)(nbins + 1) * 8));
+  r.kd = reinterpret_cast<int*>(take(sizeof(int)));
   r.qcap = qcap;
   r.qused = reinterpret_cast<unsigned int*>(take((size_t)grid * 32 * 4));  // up to 32 warps per block
   r.qhdr = reinterpret_cast<uint2*>(take((size_t)qcap * sizeof(uint2)));
   r.qmask = reinterpret_cast<uint4*>(take((size_t)qcap * sizeof(uint4)));
+  r.gunits = gunits;
+  r.gbal = reinterpret_cast<unsigned int*>(take((size_t)gunits * 4 * sizeof(unsigned int)));
+  r.grec = reinterpret_cast<GroupRecord*>(take((size_t)gunits * kJT * sizeof(GroupRecord)));
   return off;
 }
 
@@ -388,7 +400,7 @@ int prepare_catalogs(acf_ctx* c, int count, const float* const ra[2], const floa
     C.idx1 = cb[k]->idx1;
     C.counts = cb[k]->counts;
     C.v = cb[k]->v;
-    C.lo = cb[k]->lo;
+    C.ds = cb[k]->ds;
     C.v64 = cb[k]->v64;
     C.cap32 = cb[k]->cap32;
     C.cap128 = cb[k]->cap128;
@@ -460,7 +472,13 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
 int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& p, const Scratch& sc,
                  const CatBufs& ci, const CatBufs& cj) {
   const long long regions = L.grid * (pl.threads / 32);
-  const unsigned fblocks = (unsigned)((regions + kFixupThreads / 32 - 1) / (kFixupThreads / 32));
+  // per-j records: one warp per region; group records: enough warps for the batches of 32 groups,
+  // as many blocks as are resident at once (they take batches from a ticket)
+  const long long ngroups = (p.unit_end - p.unit_begin) * 4;
+  const long long fwarps = pl.grouped ? std::min<long long>((ngroups + 31) / 32, (long long)c->num_sms * ACF_FIXUP_MINB *
+                                                                                    (kFixupThreads / 32))
+                                      : regions;
+  const unsigned fblocks = (unsigned)std::max<long long>(1, (fwarps + kFixupThreads / 32 - 1) / (kFixupThreads / 32));
   const int nb = pl.bp.nbins;
   const size_t moves = ((size_t)nb * 4 + 15) & ~(size_t)15, tables = (size_t)(nb + 1) * 16;
   const int level = moves + tables <= kFixupSmemMax ? 2 : (moves <= kFixupSmemMax ? 1 : 0);
@@ -473,32 +491,38 @@ int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& 
   f.regions = (unsigned)regions;
   f.qbatch = p.qbatch;
   f.qcap = p.qcap;
-  f.hi_i = ci.v;
-  f.lo_i = ci.lo;
-  f.hi_j = cj.v;
-  f.lo_j = cj.lo;
+  f.ds_i = ci.ds;
+  f.ds_j = cj.ds;
   f.vi = ci.v64;
   f.vj = cj.v64;
   f.T = sc.T;
   f.U = sc.U;
   f.Tds = sc.Tds;
   f.Uds = sc.Uds;
+  f.kd = sc.kd;
   f.bp = pl.bp;
   f.inc = p.inc;
   f.delta = sc.delta;
   f.moved = sc.counters + 2;
   f.redone = sc.counters + 5;
   f.flagged = sc.counters + 3;
-#define ACF_FIXUP(M, SM) fixup_kernel<M, SM><<<fblocks, kFixupThreads, fsmem, c->stream>>>(f)
+  f.gbal = sc.gbal;
+  f.grec = sc.grec;
+  f.ngroups = pl.grouped ? (unsigned long long)ngroups : 0ull;
+  f.gticket = sc.counters + 1;  // (the spill counter of per-j records; zero before every pair launch)
+#define ACF_FIXUP(M, SM, G) fixup_kernel<M, SM, G><<<fblocks, kFixupThreads, fsmem, c->stream>>>(f)
+#define ACF_FIXUP_LEVELS(M, G)      \
+  if (level == 2) ACF_FIXUP(M, 2, G); \
+  else if (level == 1) ACF_FIXUP(M, 1, G); \
+  else ACF_FIXUP(M, 0, G);
   if (pl.map == kDirect) {
-    if (level == 2) ACF_FIXUP(kDirect, 2);
-    else if (level == 1) ACF_FIXUP(kDirect, 1);
-    else ACF_FIXUP(kDirect, 0);
+    if (pl.grouped) { ACF_FIXUP_LEVELS(kDirect, true) }
+    else { ACF_FIXUP_LEVELS(kDirect, false) }
   } else {
-    if (level == 2) ACF_FIXUP(kClamp, 2);
-    else if (level == 1) ACF_FIXUP(kClamp, 1);
-    else ACF_FIXUP(kClamp, 0);
+    if (pl.grouped) { ACF_FIXUP_LEVELS(kClamp, true) }
+    else { ACF_FIXUP_LEVELS(kClamp, false) }
   }
+#undef ACF_FIXUP_LEVELS
 #undef ACF_FIXUP
   ACF_LAUNCHED(c);
   return ACF_OK;
@@ -510,9 +534,11 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   unsigned long long* partial = sc.partial;
   unsigned int* ticket = sc.counters;
   ACF_CUDA(c, cudaMemsetAsync(sc.counters, 0, 256, c->stream));  // ticket, queue, path counters
-  if (pl.exact && sc.qcap > 0) ACF_CUDA(c, cudaMemsetAsync(sc.delta, 0, (size_t)pl.bp.nbins * 8, c->stream));
+  // exact mode needs its queue (per-j records) or its group records
+  const bool exact_on = pl.exact && (pl.grouped ? sc.gunits > 0 : sc.qcap > 0);
+  if (exact_on) ACF_CUDA(c, cudaMemsetAsync(sc.delta, 0, (size_t)pl.bp.nbins * 8, c->stream));
   PairParams p;
-  p.exact_mode = sc.qcap > 0 ? pl.exact : 0;
+  p.exact_mode = exact_on ? pl.exact : 0;
   p.exact_lo = pl.exact_lo;
   p.qhdr = sc.qhdr;
   p.qmask = sc.qmask;
@@ -528,7 +554,11 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
   p.qbatch = (unsigned int)std::min<long long>((long long)p.qcap * 2 / 3 / std::max<long long>(L.grid * (pl.threads / 32), 1),
                                                0x7FFFFFFFll);
   p.path_pairs = reinterpret_cast<unsigned long long*>(sc.counters + 16);
-  if (p.qcap == 0) p.exact_mode = 0;
+  p.gbal = sc.gbal;
+  p.grec = sc.grec;
+  if (pl.grouped && sc.gunits < std::min(L.units, L.per_launch))
+    return fail(c, ACF_ERR_UNSUPPORTED, "group records for %lld units, a launch takes %lld", sc.gunits,
+                std::min(L.units, L.per_launch));
   p.vi = ci.v;
   p.vj = cj.v;
   p.icap32 = ci.cap32;
@@ -583,7 +613,7 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
                                                              reinterpret_cast<unsigned long long*>(out));
   ACF_LAUNCHED(c);
   c->last_counters = sc.counters;
-  c->last_qcap = p.exact_mode ? p.qcap : 0;
+  c->last_qcap = p.exact_mode ? (pl.grouped ? sc.gunits : (long long)p.qcap) : 0;
   c->info_grid = L.grid;
   c->info_groups = L.small ? 1 : 4;
   c->info_threads = pl.threads;
@@ -608,8 +638,9 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
   const CatBufs* const cbs[2] = {&sc.a, &sc.b};
   int rc = prepare_catalogs(c, sym ? 1 : 2, ras, decs, ns, cbs);
   if (rc) return rc;
-  if (pl.exact && sc.qcap > 0) {
-    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U, sc.Tds, sc.Uds);
+  if (pl.exact && (sc.qcap > 0 || sc.gunits > 0)) {
+    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, pl.bp.kmax, sc.T, sc.U,
+                                                                         sc.Tds, sc.Uds, sc.kd);
     ACF_LAUNCHED(c);
   }
   return histogram_vectors(c, sc.a, n, sym ? sc.a : sc.b, nj, sym, pl, L, sc, out);
@@ -622,12 +653,16 @@ int run_pipeline(acf_ctx* c, const float* ra, const float* dec, long long n, con
 // Overflow is not an error: those pairs keep their fp32 bin, and "exact_overflow" counts them.
 long long queue_slots(const acf_ctx* c, const Plan& pl, long long units) {
   // the queue is drained after every launch: it holds one launch's flagged pairs
-  if (!pl.exact) return 0;
+  if (!pl.exact || pl.grouped) return 0;
   if (c->opt_exact_queue > 0) return c->opt_exact_queue;
   const double pairs = (double)units * kJT * kJT;
   const double want = std::min(4.0 * pairs * std::ldexp(1.0, -pl.bp.fine_shift), 1.5 * pairs / kJT);
   return (long long)std::min<double>(kQueueCapMax, std::max<double>(kQueueCapMin, want));
 }
+
+// Group records (exact mode 2, block-shared histogram): every unit of a launch has its slots, so
+// they never overflow.
+long long group_units(const Plan& pl, long long units) { return pl.grouped ? units : 0; }
 
 int launch_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t* rr, int32_t nbins, int64_t n_d,
                  int64_t n_r, double* omega) {
@@ -661,13 +696,13 @@ int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_
       (rc = plan_launch(c, pl, n_r, n_r, true, Lrr)))
     return rc;
   const long long grid = std::max(Ldd.grid, std::max(Ldr.grid, Lrr.grid));
-  const long long qcap = queue_slots(c, pl, std::max(std::min(Ldd.units, Ldd.per_launch),
-                                                  std::max(std::min(Ldr.units, Ldr.per_launch),
-                                                           std::min(Lrr.units, Lrr.per_launch))));
-  rc = ensure(c, c->ws, carve(nullptr, n_d, n_r, false, grid, nbins, qcap, nullptr));
+  const long long units = std::max(std::min(Ldd.units, Ldd.per_launch),
+                                   std::max(std::min(Ldr.units, Ldr.per_launch), std::min(Lrr.units, Lrr.per_launch)));
+  const long long qcap = queue_slots(c, pl, units), gunits = group_units(pl, units);
+  rc = ensure(c, c->ws, carve(nullptr, n_d, n_r, false, grid, nbins, qcap, gunits, nullptr));
   if (rc) return rc;
   Scratch sc;
-  carve(static_cast<char*>(c->ws.ptr), n_d, n_r, false, grid, nbins, qcap, &sc);
+  carve(static_cast<char*>(c->ws.ptr), n_d, n_r, false, grid, nbins, qcap, gunits, &sc);
   {
     const float* const ras[2] = {ra_d, ra_r};
     const float* const decs[2] = {dec_d, dec_r};
@@ -675,8 +710,9 @@ int correlate_impl(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_
     const CatBufs* const cbs[2] = {&sc.a, &sc.b};
     if ((rc = prepare_catalogs(c, 2, ras, decs, ns, cbs))) return rc;
   }
-  if (pl.exact && sc.qcap > 0) {
-    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, sc.T, sc.U, sc.Tds, sc.Uds);
+  if (pl.exact && (sc.qcap > 0 || sc.gunits > 0)) {
+    edge_table_kernel<<<(pl.bp.nbins + 256) / 256, 256, 0, c->stream>>>(pl.w_rad, pl.bp.nbins, pl.bp.kmax, sc.T, sc.U,
+                                                                         sc.Tds, sc.Uds, sc.kd);
     ACF_LAUNCHED(c);
   }
   if ((rc = histogram_vectors(c, sc.a, n_d, sc.a, n_d, true, pl, Ldd, sc, dd)) ||
@@ -708,11 +744,12 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const long long qcap = queue_slots(c, pl, std::min(L.units, L.per_launch));
-  rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, qcap, nullptr));
+  const long long units = std::min(L.units, L.per_launch);
+  const long long qcap = queue_slots(c, pl, units), gunits = group_units(pl, units);
+  rc = ensure(c, c->ws, carve(nullptr, n, nj, sym, L.grid, nbins, qcap, gunits, nullptr));
   if (rc) return rc;
   Scratch sc;
-  carve(static_cast<char*>(c->ws.ptr), n, nj, sym, L.grid, nbins, qcap, &sc);
+  carve(static_cast<char*>(c->ws.ptr), n, nj, sym, L.grid, nbins, qcap, gunits, &sc);
   return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }
 
@@ -1100,14 +1137,21 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   Launch L;
   rc = plan_launch(c, pl, n, nj, sym, L);
   if (rc) return rc;
-  const size_t need = carve(nullptr, n, nj, sym, L.grid, nbins, 0, nullptr);
-  // the exact-mode queue takes whatever the static array has left (minus the alignment of its two parts)
-  const long long qcap =
-      pl.exact && need + 1024 < kNoAllocScratchBytes ? (long long)((kNoAllocScratchBytes - need - 1024) / kRecordBytes) : 0;
+  const size_t need = carve(nullptr, n, nj, sym, L.grid, nbins, 0, 0, nullptr);
+  // the exact-mode queue (or the group records) takes whatever the static array has left (minus the
+  // alignment of its two parts); group records take fewer units per launch to fit
+  const long long left = need + 1024 < kNoAllocScratchBytes ? (long long)(kNoAllocScratchBytes - need - 1024) : 0;
+  const long long qcap = pl.exact && !pl.grouped ? left / (long long)kRecordBytes : 0;
+  const long long gunits = pl.grouped ? std::min(std::min(L.units, L.per_launch), left / (long long)kGroupUnitBytes) : 0;
+  if (pl.grouped && gunits < 1 && need <= kNoAllocScratchBytes)
+    return fail(c, ACF_ERR_UNSUPPORTED,
+                "acf_histogram_noalloc: the static array has no room left for the exact mode's group records "
+                "(%zu of %zu bytes taken); use acf_histogram or exact mode 0", need, kNoAllocScratchBytes);
+  if (pl.grouped) L.per_launch = std::min(L.per_launch, gunits);
   if (need > kNoAllocScratchBytes)
     return fail(c, ACF_ERR_UNSUPPORTED,
                 "acf_histogram_noalloc needs %zu bytes of scratch but its static array holds %zu "
-                "(about 77 bytes per galaxy of each catalog plus (%lld blocks + 2) x nbins x 8 bytes); use acf_histogram",
+                "(about 93 bytes per galaxy of each catalog plus (%lld blocks + 2) x nbins x 8 bytes); use acf_histogram",
                 need, kNoAllocScratchBytes, L.grid);
   void* scratch = nullptr;
   rc = noalloc_scratch(c, c->device, &scratch);
@@ -1115,6 +1159,6 @@ extern "C" int acf_histogram_noalloc(acf_ctx* c, const float* ra, const float* d
   // Every byte the kernels read is rewritten first: the ticket and cell counters are cleared,
   // the preparation kernels write the vectors and caps, and the pair kernel zeroes its rows.
   Scratch sc;
-  carve(static_cast<char*>(scratch), n, nj, sym, L.grid, nbins, std::max(qcap, 0ll), &sc);
+  carve(static_cast<char*>(scratch), n, nj, sym, L.grid, nbins, std::max(qcap, 0ll), std::max(gunits, 0ll), &sc);
   return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }

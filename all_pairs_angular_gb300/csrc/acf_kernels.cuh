@@ -157,6 +157,14 @@ struct BinParams {
   int entries;        // histogram entries in shared memory
 };
 
+// Exact mode with a block-shared histogram (dense flags): the flags of one lane over one j-group,
+// 32 bytes. Word k holds, in bit b, the flag of the pair (i = kJT r + islot(k, lane), j = j + b);
+// pc is the group's path code.
+struct __align__(32) GroupRecord {
+  uint32_t w[4];
+  uint32_t r, j, pc, pad;
+};
+
 struct PairParams {
   const float4* __restrict__ vi;
   const float4* __restrict__ vj;
@@ -186,6 +194,11 @@ struct PairParams {
   unsigned int* qoverflow;             // flagged pairs whose record found no slot (kept their fp32 bin)
   unsigned int qcap;                   // queue slots
   unsigned int qbatch;                 // slots a warp owns
+  // exact mode with the block-shared histogram: group records instead (no queue, no overflow). Unit
+  // u of the launch, j-group g: gi = (u - unit_begin) * 4 + g; gbal[gi] = the ballot of the lanes
+  // whose record grec[gi * 32 + lane] holds a flag (the others are not written)
+  unsigned int* gbal;
+  GroupRecord* grec;
   unsigned long long* path_pairs;      // pairs evaluated per path: chord fixed, chord general,
                                        // chord fixed+flag, chord general+flag, masked/ragged units,
                                        // dot form, dot form+flag, short chord, short chord+flag
@@ -397,6 +410,36 @@ constexpr int kSortDigits = 256;
 // One catalog's preparation: its input, its sort scratch and its outputs. The preparation kernels
 // take up to two catalogs at once (PrepBatch, blockIdx.y selects the catalog), so that both catalogs
 // of a cross-correlation are sorted and converted by the same launches.
+// A unit vector as double-single components, 32 bytes (one sector): h = (hx, hy, hz, lx), l = (ly,
+// lz, 0, 0); hx = the fp32 rounding of the fp64 x, lx = the fp32 rounding of what it leaves.
+struct __align__(32) DsVec {
+  float4 h, l;
+};
+
+// One 256-bit load of a DsVec, as the hi (x, y, z) and lo (x, y, z) parts (w = 0).
+__device__ __forceinline__ void load_ds(const DsVec* p, float4& hi, float4& lo) {
+  float lx;
+  asm("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(lx), "=f"(lo.y), "=f"(lo.z), "=f"(hi.w), "=f"(lo.w)
+      : "l"(p));
+  lo.x = lx;
+}
+
+// One 256-bit store of a group record (its lane's flags, the i-set row, the group's first j, path).
+__device__ __forceinline__ void store_group_record(GroupRecord* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                                   uint32_t r, uint32_t j, uint32_t pc) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2), "r"(w3),
+               "r"(r), "r"(j), "r"(pc), "r"(0u)
+               : "memory");
+}
+
+// One 256-bit load of a group record: the flag words (m) and (r, j, pc, 0) (h).
+__device__ __forceinline__ void load_group_record(const GroupRecord* p, uint4& m, uint4& h) {
+  asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(m.x), "=r"(m.y), "=r"(m.z), "=r"(m.w), "=r"(h.x), "=r"(h.y), "=r"(h.z), "=r"(h.w)
+      : "l"(p));
+}
+
 struct PrepCat {
   const float* ra;        // input, arcminutes
   const float* dec;
@@ -406,8 +449,8 @@ struct PrepCat {
   unsigned int* key1;     // sort: keys after the first pass
   unsigned int* idx1;     // sort: input indices after the first pass
   unsigned int* counts;   // sort: digit counts per tile, then their offsets
-  float4* v;              // outputs: fp32 vectors, their remainders, fp64 vectors, caps
-  float4* lo;
+  float4* v;              // outputs: fp32 vectors, the double-single vectors, fp64 vectors, caps
+  DsVec* ds;
   double4_32a* v64;
   float4* cap32;
   float4* cap128;
@@ -549,7 +592,10 @@ __global__ void vectors_kernel(const PrepBatch b) {
       unit64(C.ra[src], C.dec[src], x, y, z);
       const float hx = (float)x, hy = (float)y, hz = (float)z;
       C.v[p] = make_float4(hx, hy, hz, 0.0f);
-      C.lo[p] = make_float4((float)(x - (double)hx), (float)(y - (double)hy), (float)(z - (double)hz), 0.0f);
+      DsVec d;
+      d.h = make_float4(hx, hy, hz, (float)(x - (double)hx));
+      d.l = make_float4((float)(y - (double)hy), (float)(z - (double)hz), 0.0f, 0.0f);
+      C.ds[p] = d;
       C.v64[p] = make_double4_32a(x, y, z, 0.0);
     }
   }
@@ -1171,6 +1217,18 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
         (void)ACF_CHECK(fabsf(v.x * v.x + v.y * v.y + v.z * v.z - 1.0f) < 1e-3f, 2, j0 + jj, u, v.x, v.y, v.z, (float)buf);
       }
 #endif
+      // group records (block-shared exact kernel): after each j-group, every lane with a flag writes
+      // its record and lane 0 the ballot of those lanes (for every group of every unit, so that the
+      // fix-up reads no stale ballot)
+      auto group_flush = [&](const uint32_t(&fw)[K], int g, int pc) {
+        static_assert(K == 4, "four flag words per record");
+        const bool any = (fw[0] | fw[1] | fw[2] | fw[3]) != 0u;
+        const unsigned int bal = __ballot_sync(0xffffffffu, any);
+        const size_t gi = (size_t)(u - p.unit_begin) * 4 + g;
+        if (any) store_group_record(p.grec + gi * 32 + lane, fw[0], fw[1], fw[2], fw[3], (uint32_t)r, (uint32_t)(j0 + g * 32),
+                                    (uint32_t)pc);
+        if (lane == 0) p.gbal[gi] = bal;
+      };
       if (full) {
         // one loop per (32-galaxy j-group, path); the path is uniform across the warp. The fixed
         // chord loops take the sign in registers (ns, iws, h); the dot-form loop needs no sign; the
@@ -1231,25 +1289,33 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
           } else if constexpr (F && (X == 1 || X == 3)) {
             // fixed-sign chord with flags: the plain code addresses the histogram (as without flags),
             // the fine code, from the same theta', only decides the flag
+            [[maybe_unused]] uint32_t fw[K] = {};  // group records: this lane's flag words over the group
+            [[maybe_unused]] uint32_t jbit = 1u;
 #pragma unroll kJJUnrollFine2
             for (int jj = jbeg; jj < jbeg + 32; ++jj) {
               const float4 v = jvec(jj);
               uint32_t cfs[K], ccs[K];
-              uint32_t low = 0xFFFFFFFFu;
-              bool fl = false;
+              [[maybe_unused]] uint32_t low = 0xFFFFFFFFu;
+              [[maybe_unused]] bool fl = false;
 #pragma unroll
               for (int k = 0; k < K; ++k) {
                 cfs[k] = __float_as_uint(pair_code_fixed2<MAP, X == 3>(xi[k], yi[k], zi[k], v.x, v.y, v.z, ns, iws, h,
                                                                         iws_c, h_c, p.bp, ccs[k]));
                 add_pair<false, MAP>(p, ccs[k], base, bf, SHIFT, SF, magic_bits, i0 + islot<K>(k, lane), j0 + jj, xi[k], yi[k],
                                 zi[k], v, inc);
+                if constexpr (LAYOUT == kBlockExact) {
+                  fw[k] |= (cfs[k] & (fmask & ~1u)) == 0u ? jbit : 0u;
+                } else {
 #if ACF_FLAG_PRED
-                fl |= (cfs[k] & (fmask & ~1u)) == 0u;
+                  fl |= (cfs[k] & (fmask & ~1u)) == 0u;
 #else
-                low = min(low, cfs[k] & fmask);
+                  low = min(low, cfs[k] & fmask);
 #endif
+                }
               }
-              if (__any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
+              if constexpr (LAYOUT == kBlockExact) {
+                jbit <<= 1;
+              } else if (__any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
                 // the count went to the plain code's entry: nothing to move back without a record
                 (void)push_record(p, region, cur, r, j0 + jj, pc, __ballot_sync(0xffffffffu, (cfs[0] & fmask) <= 1u),
                                   __ballot_sync(0xffffffffu, (cfs[1] & fmask) <= 1u),
@@ -1257,26 +1323,35 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                                   __ballot_sync(0xffffffffu, (cfs[3] & fmask) <= 1u));
               }
             }
+            if constexpr (LAYOUT == kBlockExact) group_flush(fw, jbeg / 32, pc);
           } else {
+            [[maybe_unused]] uint32_t fw[K] = {};  // group records (F): this lane's flag words over the group
+            [[maybe_unused]] uint32_t jbit = 1u;
 #pragma unroll U
             for (int jj = jbeg; jj < jbeg + 32; ++jj) {
               const float4 v = jvec(jj);
               uint32_t cbs[K];
-              uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
-              bool fl = false;
+              [[maybe_unused]] uint32_t low = 0xFFFFFFFFu;  // exact mode: smallest biased fraction of this j's pairs
+              [[maybe_unused]] bool fl = false;
 #pragma unroll
               for (int k = 0; k < K; ++k) {
                 cbs[k] = code_of(k, v);
                 add_pair<F, MAP>(p, cbs[k], base, bf, SHIFT, SF, magic_bits, i0 + islot<K>(k, lane), j0 + jj, xi[k], yi[k], zi[k],
                             v, inc);
+                if constexpr (F && LAYOUT == kBlockExact) {
+                  fw[k] |= (cbs[k] & (fmask & ~1u)) == 0u ? jbit : 0u;
+                } else {
 #if ACF_FLAG_PRED
-                if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
+                  if (F) fl |= (cbs[k] & (fmask & ~1u)) == 0u;
 #else
-                if (F) low = min(low, cbs[k] & fmask);
+                  if (F) low = min(low, cbs[k] & fmask);
 #endif
+                }
               }
-              // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
-              if (F && __any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
+              if constexpr (F && LAYOUT == kBlockExact) {
+                jbit <<= 1;
+              } else if (F && __any_sync(0xffffffffu, ACF_FLAG_PRED ? fl : low <= 1u)) {
+                // near-edge pairs are rare: one warp vote per j, then the queue for the lanes that need it
                 if (!push_record(p, region, cur, r, j0 + jj, pc, __ballot_sync(0xffffffffu, (cbs[0] & fmask) <= 1u),
                                  __ballot_sync(0xffffffffu, (cbs[1] & fmask) <= 1u),
                                  __ballot_sync(0xffffffffu, (cbs[2] & fmask) <= 1u),
@@ -1286,6 +1361,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
                 }
               }
             }
+            if constexpr (F && LAYOUT == kBlockExact) group_flush(fw, jbeg / 32, pc);
           }
         };
         // the four j-groups' paths, one per lane of lanes 0..3 (one pass of the decision per unit)
@@ -1357,8 +1433,29 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
             }
           }
         };
-        if ((LAYOUT == kBlockExact || p.exact_mode) && METHOD == kChordPoly) edge(FineTag<true>());
-        else edge(FineTag<false>());
+        if constexpr (LAYOUT == kBlockExact) {
+          // the same with group records: every group of the unit is flushed, the empty ones too
+#pragma unroll 1
+          for (int g = 0; g < kJT / 32; ++g) {
+            uint32_t fw[K] = {};
+#pragma unroll 1
+            for (int jj = g * 32; jj < min(jn, g * 32 + 32); ++jj) {
+              const float4 v = tile[jj];
+#pragma unroll
+              for (int k = 0; k < K; ++k) {
+                const uint32_t cb = __float_as_uint(pair_code<MAP, METHOD, true>(xi[k], yi[k], zi[k], v.x, v.y, v.z, p.bp));
+                if (jj > thr[k] && add_pair<true, MAP>(p, cb, base, base_f, SHIFT, p.bp.fine_shift, magic_bits,
+                                                       i0 + islot<K>(k, lane), j0 + jj, xi[k], yi[k], zi[k], v, inc))
+                  fw[k] |= 1u << (jj - g * 32);
+              }
+            }
+            group_flush(fw, g, kGeneral);
+          }
+        } else if (p.exact_mode && METHOD == kChordPoly) {
+          edge(FineTag<true>());
+        } else {
+          edge(FineTag<false>());
+        }
         count_path(4, GROUPS == 1 ? (unsigned int)max(0, min(jn, gs * 32 + 32) - gs * 32) : (unsigned int)jn);
       }
       __syncwarp();  // every lane is done with this buffer before the next prefetch refills it
@@ -1381,7 +1478,7 @@ __global__ void __launch_bounds__(THREADS, 1) pair_kernel(const PairParams p) {
     }
   }
   // the records of this warp's own region (the fix-up reads that many)
-  if (p.exact_mode && lane == 0) p.qused[region] = min(cur, p.qbatch);
+  if (LAYOUT != kBlockExact && p.exact_mode && lane == 0) p.qused[region] = min(cur, p.qbatch);
   __syncthreads();
   flush_hist<K, THREADS, LAYOUT, MAP, METHOD>(p, hist, false);
 }
@@ -1431,9 +1528,11 @@ __global__ void omega_kernel(const unsigned long long* __restrict__ dd, const un
 
 // Edge thresholds of the exact re-decision, in fp64: bin k starts where the difference chord
 // reaches T[k] = 4 sin^2(k w / 2), or, for pairs past 90 degrees, where the sum chord falls to
-// U[k] = 4 cos^2(k w / 2).
-__global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ T, double* __restrict__ U,
-                                  float2* __restrict__ Tds, float2* __restrict__ Uds) {
+// U[k] = 4 cos^2(k w / 2). The re-decision of a pair counted in bin k takes the difference chord
+// while the fp32 rounding of T[k] is at most 2; T rises with k up to kmax (k w <= 180 degrees), so
+// those bins are 0 .. kd, and kd is written too.
+__global__ void edge_table_kernel(double w_rad, int nbins, int kmax, double* __restrict__ T, double* __restrict__ U,
+                                  float2* __restrict__ Tds, float2* __restrict__ Uds, int* __restrict__ kd) {
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k <= nbins; k += gridDim.x * blockDim.x) {
     double sh, ch;
     sincos(0.5 * w_rad * k, &sh, &ch);
@@ -1444,6 +1543,15 @@ __global__ void edge_table_kernel(double w_rad, int nbins, double* __restrict__ 
     const float th = (float)t, uh = (float)u;
     Tds[k] = make_float2(th, (float)(t - (double)th));
     Uds[k] = make_float2(uh, (float)(u - (double)uh));
+    if (k <= kmax && th <= 2.0f) {
+      bool last = k == kmax;
+      if (!last) {
+        double sh1, ch1;
+        sincos(0.5 * w_rad * (k + 1), &sh1, &ch1);  // T[k + 1], as the thread of k + 1 computes it
+        last = (float)(4.0 * sh1 * sh1) > 2.0f;
+      }
+      if (last) *kd = k;
+    }
   }
 }
 
@@ -1548,10 +1656,16 @@ struct FixupParams {
   const unsigned int* qspill;         // spill records handed out
   unsigned int regions;               // pair-kernel warps (regions)
   unsigned int qbatch, qcap;          // records per region, records in all
-  const float4 *hi_i, *lo_i, *hi_j, *lo_j;  // fp32 vectors (as the pair kernel read them) and remainders
+  const DsVec *ds_i, *ds_j;           // double-single vectors (hi: the fp32 vectors the pair kernel read)
   const double4_32a *vi, *vj;         // fp64 vectors
   const double *T, *U;                // fp64 edge tables
   const float2 *Tds, *Uds;            // the same as double-single pairs
+  const int* kd;                      // the last bin whose lower edge the difference chord decides
+  // group records (GROUPED): the pair kernel's ballots and records, groups in all, batch dispenser
+  const unsigned int* gbal;
+  const GroupRecord* grec;
+  unsigned long long ngroups;
+  unsigned int* gticket;
   BinParams bp;
   unsigned int inc;                   // histogram increment of the pair kernel's launch
   unsigned long long* delta;          // per-bin moves (two's complement)
@@ -1571,9 +1685,11 @@ struct FixupParams {
 // (about 1e-13 relative, against a flagged pair's 1e-6 rad window) the pair is redone in fp64.
 // Pairs outside the exact zone (mode 1) keep their fp32 bin; a single-code loop's count that the bias
 // carried one entry up moves back.
-// The queue holds one region of qbatch records per pair-kernel warp (region g: qused[g] in use), then
-// spill records. Fix-up warp g takes region g, whose records came from one pair-kernel warp in order
-// (consecutive records share an i-set, and mostly a path code), and a share of the spill records.
+// Per-j records (GROUPED false): the queue holds one region of qbatch records per pair-kernel warp
+// (region g: qused[g] in use), then spill records. Fix-up warp g takes region g, whose records came
+// from one pair-kernel warp in order (consecutive records share an i-set, and mostly a path code),
+// and a share of the spill records. Group records (GROUPED true): warps take batches of 32 groups
+// from a ticket.
 // SMEM 2: the double-single tables and per-bin moves in shared memory; 1: the moves only; 0: neither.
 // Shared moves reach delta[] once per block.
 constexpr int kFixupThreads = 256;
@@ -1583,7 +1699,7 @@ constexpr int kFixupThreads = 256;
 #define ACF_FIXUP_PAIRS 2
 #endif
 constexpr int kFixupPairs = ACF_FIXUP_PAIRS;
-template <int MAP, int SMEM>
+template <int MAP, int SMEM, bool GROUPED>
 __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(const FixupParams f) {
   static_assert(kFixupThreads == 8 * 32, "one pair list per warp");
   extern __shared__ __align__(16) unsigned char fsm[];
@@ -1610,9 +1726,8 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
   }
   if (threadIdx.x == 0) s_moved = s_redone = s_flagged = 0u;
   __syncthreads();
-  const unsigned long long nbatch = (unsigned long long)f.regions * f.qbatch;
-  const unsigned int nspill = nbatch < f.qcap ? (unsigned int)min((unsigned long long)*f.qspill, f.qcap - nbatch) : 0u;
   unsigned int my_moved = 0u, my_redone = 0u, my_flagged = 0u;
+  const int kd = *f.kd;
   // move one count between bins (k_from -> k_to)
   auto move = [&](int k_from, int k_to) {
     if (k_from == k_to) return;
@@ -1625,32 +1740,37 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     }
     ++my_moved;
   };
-  // re-decide pair (i, j), whose count went to entry e, from the double-single dot product of its
-  // vectors (dh + dl)
-  auto redo = [&](int e, int i, int j, float dh, float dl) {
-    e = e < 0 ? 0 : (e >= bp.entries ? bp.entries - 1 : e);
-    const int kf = entry_to_bin<MAP>(e, bp);
-    const int k0 = kf > bp.kmax ? bp.kmax : kf;
-    const bool diff = tT[k0].x <= 2.0f;  // the side, from the table both passes share
+  // The bin of a flagged pair (i, j) whose count went to bin kf, from the double-single dot product
+  // of its vectors (dh + dl): k0 = kf (at most kmax) and the walk across the edges the pair lies
+  // beyond, starting from the table values at k0 and k0 + 1 (loaded before, together with the other
+  // pairs' of the round). The difference chord and T[] below 90 degrees (the side the table at k0
+  // gives), the sum chord and U[] above; on both sides the pair lies below edge k when
+  // sg (q - t_k) < 0 (sg = 1 with T, -1 with U: the sum chord falls as the separation grows).
+  auto decide = [&](int i, int j, int k0, float dh, float dl, float2 e_lo, float2 e_hi) {
+    const bool diff = k0 <= kd;
+    const float2* tb = diff ? tT : tU;
+    const int sg = diff ? 1 : -1;
+    float qh, ql;
+    ds_chord_from_dot(dh, dl, diff ? -1.0f : 1.0f, qh, ql);
+    // the bound on q's error (2 kDotErr + 2.2e-14), plus the double-single tables' 2^-48 relative
+    // (T, U <= 4), the fp64 computation's own rounding (<= 2.2e-15) and the rounding of the side
+    // test's remainder difference (<= 2.9e-14): 2.8e-13, with some margin
+    const float eps = 4e-13f;
     int k = k0;
     bool sure = true;
-    {
-      float qh, ql;
-      ds_chord_from_dot(dh, dl, diff ? -1.0f : 1.0f, qh, ql);
-      // the bound on q's error (2 kDotErr + 2.2e-14), plus the double-single tables' 2^-48 relative
-      // (T, U <= 4), the fp64 computation's own rounding (<= 2.2e-15) and the rounding of the side
-      // test's remainder difference (<= 2.9e-14): 2.8e-13, with some margin
-      const float eps = 4e-13f;
-      if (diff) {
-        // lower edge: q >= T[k]; upper edge: q < T[k + 1]
-        for (int c; k > 0 && (c = ds_side(qh, ql, tT[k], eps)) <= 0; --k) if (!c) { sure = false; break; }
-        if (sure)
-          for (int c; k < bp.kmax && (c = ds_side(qh, ql, tT[k + 1], eps)) >= 0; ++k) if (!c) { sure = false; break; }
-      } else {
-        // lower edge: q <= U[k]; upper edge: q > U[k + 1]
-        for (int c; k > 0 && (c = ds_side(qh, ql, tU[k], eps)) >= 0; --k) if (!c) { sure = false; break; }
-        if (sure)
-          for (int c; k < bp.kmax && (c = ds_side(qh, ql, tU[k + 1], eps)) <= 0; ++k) if (!c) { sure = false; break; }
+    int c = k > 0 ? sg * ds_side(qh, ql, e_lo, eps) : 1;
+    if (c <= 0) {
+      // below the lower edge (or too close to it to tell)
+      if (c == 0) sure = false;
+      else
+        for (--k; k > 0 && (c = sg * ds_side(qh, ql, tb[k], eps)) <= 0; --k) if (!c) { sure = false; break; }
+    } else if (k < bp.kmax) {
+      c = sg * ds_side(qh, ql, e_hi, eps);
+      if (c >= 0) {
+        // at or above the upper edge
+        if (c == 0) sure = false;
+        else
+          for (++k; k < bp.kmax && (c = sg * ds_side(qh, ql, tb[k + 1], eps)) >= 0; ++k) if (!c) { sure = false; break; }
       }
     }
     if (!sure) {
@@ -1670,74 +1790,81 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
         while (k < bp.kmax && q <= f.U[k + 1]) ++k;
       }
     }
-    move(kf, k);
+    return k;
   };
-  // one flagged pair (i, j, path code pc of the group that computed it) and its vectors
+  // one flagged pair (i, j, path code pc of the group that computed it) and its vectors: the codes
+  // the pair kernel computed; in the exact zone the pair is decided again (its first two edge values
+  // load while the dot product is summed), outside it (mode 1) the fp32 bin stands, less the carry
+  // of a single-code loop's bias
   auto pair = [&](int i, int j, int pc, float4 ah, float4 al, float4 bh, float4 bl) {
     ++my_flagged;
-    uint32_t cb, e;
+    uint32_t cb, en;
     bool single;
     int S;
-    recorded_codes<MAP>(pc, ah, bh, bp, cb, e, single, S);
-    if (e - bp.zone0 <= bp.span0 || e - bp.zone1 <= bp.span1) {
+    recorded_codes<MAP>(pc, ah, bh, bp, cb, en, single, S);
+    const int ec = (int)en < 0 ? 0 : ((int)en >= bp.entries ? bp.entries - 1 : (int)en);
+    const int kf = entry_to_bin<MAP>(ec, bp);
+    if (en - bp.zone0 <= bp.span0 || en - bp.zone1 <= bp.span1) {
+      const int k0 = kf > bp.kmax ? bp.kmax : kf;
+      const float2* tb = k0 <= kd ? tT : tU;
+      const float2 e_lo = tb[k0], e_hi = tb[k0 + 1];
       float dh, dl;
       ds_dot(ah, al, bh, bl, dh, dl);
-      redo((int)e, i, j, dh, dl);
+      move(kf, decide(i, j, k0, dh, dl, e_lo, e_hi));
     } else if (single && (cb & ((1u << S) - 1u)) == 0u) {
-      // outside the exact zone: the fp32 bin stands, minus the bias's carry
-      const int ec = (int)e < bp.entries ? (int)e : bp.entries - 1;
-      move(entry_to_bin<MAP>(ec, bp), entry_to_bin<MAP>(ec > 0 ? ec - 1 : 0, bp));
+      move(kf, entry_to_bin<MAP>(ec > 0 ? ec - 1 : 0, bp));
     }
   };
-  // Each lane walks its own sequence of records (base + first, + stride, ...), holding the flagged
-  // pairs of one record that are still to do (the next record already loading). Per round the warp
-  // packs up to 32 kFixupPairs of those pairs into its list, in lane order (a warp scan of the lanes'
-  // counts gives each lane its slots), and then every lane decides kFixupPairs pairs of the list,
-  // their vectors all loading before the first is decided: the lanes stay converged however the
-  // pairs spread over the records.
+  // Each lane walks its own sequence of records, holding the flagged pairs of one record that are
+  // still to do (the next record already loading; next(h, m) loads it as h = (i-set row, j, path
+  // code) and m = the four flag words, or returns false). Per round the warp packs up to
+  // 32 kFixupPairs of those pairs into its list (a warp scan of the lanes' counts gives each lane its
+  // slots), and then every lane decides the pairs at slots lane, lane + 32, ..., their vectors all
+  // loading before the first is decided: the lanes stay converged however the pairs spread over the
+  // records. Pairs of the dot form fill the list from the front, the chord forms' from the back, so
+  // that most 32-slot groups hold one form only (the two recompute their codes differently).
+  // Bit b of flag word k: per-j records, the pair (i = kJT row + islot(k, b), j); group records, the
+  // pair (i = kJT row + islot(k, lane), j + b) (the record of this lane of its group).
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint4* list = s_list[warp];
-  auto run = [&](unsigned long long base, unsigned int n, unsigned int first, unsigned int stride) {
-    unsigned int t = first;
-    uint2 hn = make_uint2(0u, 0u), h = make_uint2(0u, 0u);
-    uint4 mn = make_uint4(0u, 0u, 0u, 0u);
+  auto rounds = [&](auto next) {
+    uint4 hn = make_uint4(0u, 0u, 0u, 0u), h = hn, mn = hn;
     uint32_t m[4] = {0u, 0u, 0u, 0u};  // pairs of the current record still to do
-    bool has_next = t < n;
-    if (has_next) {
-      hn = f.qhdr[base + t];
-      mn = f.qmask[base + t];
-      t += stride;
-    }
+    bool has_next = next(hn, mn);
     while (true) {
       if ((m[0] | m[1] | m[2] | m[3]) == 0u && has_next) {
         h = hn;
         m[0] = mn.x; m[1] = mn.y; m[2] = mn.z; m[3] = mn.w;
-        has_next = t < n;
-        if (has_next) {
-          hn = f.qhdr[base + t];
-          mn = f.qmask[base + t];
-          t += stride;
-        }
+        has_next = next(hn, mn);
       }
-      const unsigned int cnt = __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
-      unsigned int incl = cnt;
+      const unsigned int pc = h.z;
+      const bool back = !(pc & kMidBit);
+      const unsigned int cnt = __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);  // <= 128
+      // dot-form counts in the low half, chord-form counts in the high half (totals <= 4096)
+      const unsigned int own = back ? cnt << 16 : cnt;
+      unsigned int incl = own;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const unsigned int total = __shfl_sync(0xffffffffu, incl, 31);
-      if (total == 0u) break;  // a lane with a record left always has a pair to do
+      const unsigned int tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (tot == 0u) break;  // a lane with a record left always has a pair to do
       constexpr unsigned int L = 32u * kFixupPairs;  // list length
-      unsigned int slot = incl - cnt;
-      if (slot < L) {
-        const int j = (int)h.x, r = (int)(h.y & 0xFFFFFFu), pc = (int)(h.y >> 24);
+      const unsigned int nfront = min(tot & 0xFFFFu, L), nback = min(tot >> 16, L - nfront);
+      {
+        const unsigned int ex = incl - own;
+        unsigned int r = back ? ex >> 16 : ex & 0xFFFFu;  // this lane's first pair among its form's
+        const unsigned int lim = back ? nback : nfront;
+        const unsigned int row = h.x, jr = h.y;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          while (m[k] && slot < L) {
+          while (m[k] && r < lim) {
             const int b = __ffs(m[k]) - 1;
             m[k] &= m[k] - 1u;
-            list[slot++] = make_uint4((unsigned)(r * kJT + islot<kJT / 32>(k, b)), (unsigned)j, (unsigned)pc, 0u);
+            const unsigned int i = row * kJT + islot<kJT / 32>(k, GROUPED ? lane : b);
+            list[back ? L - 1u - r : r] = make_uint4(i, GROUPED ? jr + b : jr, pc, 0u);
+            ++r;
           }
         }
       }
@@ -1746,26 +1873,62 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
       float4 ah[kFixupPairs], al[kFixupPairs], bh[kFixupPairs], bl[kFixupPairs];
 #pragma unroll
       for (int u = 0; u < kFixupPairs; ++u) {
-        const bool ok = (unsigned)(lane + 32 * u) < total;
-        e[u] = ok ? list[lane + 32 * u] : make_uint4(0u, 0u, 0u, 0xFFFFFFFFu);
+        const unsigned int s = lane + 32u * u;
+        const bool ok = s < nfront || s >= L - nback;
+        e[u] = ok ? list[s] : make_uint4(0u, 0u, 0u, 0xFFFFFFFFu);
         if (ok) {
-          ah[u] = f.hi_i[e[u].x];
-          al[u] = f.lo_i[e[u].x];
-          bh[u] = f.hi_j[e[u].y];
-          bl[u] = f.lo_j[e[u].y];
+          load_ds(f.ds_i + e[u].x, ah[u], al[u]);
+          load_ds(f.ds_j + e[u].y, bh[u], bl[u]);
         }
       }
+      __syncwarp();
 #pragma unroll
       for (int u = 0; u < kFixupPairs; ++u)
         if (e[u].w == 0u) pair((int)e[u].x, (int)e[u].y, (int)e[u].z, ah[u], al[u], bh[u], bl[u]);
-      __syncwarp();
     }
   };
-  // this warp's region, then its share of the spill records
-  const unsigned int gw = blockIdx.x * (kFixupThreads / 32) + warp, nw = gridDim.x * (kFixupThreads / 32);
-  const unsigned int nmine = gw < f.regions ? min(f.qused[gw], f.qbatch) : 0u;
-  run((unsigned long long)gw * f.qbatch, nmine, lane, 32);
-  run(nbatch, nspill, gw * 32 + lane, nw * 32);
+  if constexpr (GROUPED) {
+    // batches of 32 groups from a ticket; in each, lane l takes the records of lane l of the groups
+    // whose ballot holds l
+    while (true) {
+      unsigned int bt = 0u;
+      if (lane == 0) bt = atomicAdd(f.gticket, 1u);
+      const unsigned long long g0 = 32ull * __shfl_sync(0xffffffffu, bt, 0);
+      if (g0 >= f.ngroups) break;
+      const unsigned int bal = g0 + lane < f.ngroups ? f.gbal[g0 + lane] : 0u;
+      unsigned int mine = 0u;  // bit q: group g0 + q holds a record of this lane
+#pragma unroll 8
+      for (int l = 0; l < 32; ++l) {
+        const unsigned int x = __ballot_sync(0xffffffffu, (bal >> l) & 1u);
+        if (lane == l) mine = x;
+      }
+      rounds([&](uint4& hn, uint4& mn) {
+        if (!mine) return false;
+        const int q = __ffs(mine) - 1;
+        mine &= mine - 1u;
+        load_group_record(f.grec + (g0 + (unsigned)q) * 32 + lane, mn, hn);
+        return true;
+      });
+    }
+  } else {
+    // this warp's region, then its share of the spill records
+    const unsigned long long nbatch = (unsigned long long)f.regions * f.qbatch;
+    const unsigned int nspill = nbatch < f.qcap ? (unsigned int)min((unsigned long long)*f.qspill, f.qcap - nbatch) : 0u;
+    const unsigned int gw = blockIdx.x * (kFixupThreads / 32) + warp, nw = gridDim.x * (kFixupThreads / 32);
+    const unsigned int nmine = gw < f.regions ? min(f.qused[gw], f.qbatch) : 0u;
+    auto records = [&](unsigned long long base, unsigned int n, unsigned int t, unsigned int stride) {
+      rounds([&](uint4& hn, uint4& mn) {
+        if (t >= n) return false;
+        const uint2 q = f.qhdr[base + t];
+        mn = f.qmask[base + t];
+        hn = make_uint4(q.y & 0xFFFFFFu, q.x, q.y >> 24, 0u);
+        t += stride;
+        return true;
+      });
+    };
+    records((unsigned long long)gw * f.qbatch, nmine, lane, 32);
+    records(nbatch, nspill, gw * 32 + lane, nw * 32);
+  }
   for (int o = 16; o > 0; o >>= 1) {
     my_moved += __shfl_xor_sync(0xffffffffu, my_moved, o);
     my_redone += __shfl_xor_sync(0xffffffffu, my_redone, o);
