@@ -467,22 +467,23 @@ int plan_launch(acf_ctx* c, const Plan& pl, long long ni, long long nj, bool sym
 }
 
 // Every pair a launch flagged near an edge is re-decided exactly; its count moves if the bin differs.
-// One fix-up warp per pair-kernel warp (queue region). The per-bin moves (int32 per block) and, when
-// they fit too, the double-single edge tables go to shared memory if small.
+// The per-bin moves (int32 per block) and, when they fit too, the double-single edge tables go to
+// shared memory if small.
 int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& p, const Scratch& sc,
                  const CatBufs& ci, const CatBufs& cj) {
   const long long regions = L.grid * (pl.threads / 32);
-  // per-j records: one warp per region; group records: enough warps for the batches of 32 groups,
-  // as many blocks as are resident at once (they take batches from a ticket)
-  const long long ngroups = (p.unit_end - p.unit_begin) * 4;
-  const long long fwarps = pl.grouped ? std::min<long long>((ngroups + 31) / 32, (long long)c->num_sms * ACF_FIXUP_MINB *
-                                                                                    (kFixupThreads / 32))
-                                      : regions;
-  const unsigned fblocks = (unsigned)std::max<long long>(1, (fwarps + kFixupThreads / 32 - 1) / (kFixupThreads / 32));
   const int nb = pl.bp.nbins;
   const size_t moves = ((size_t)nb * 4 + 15) & ~(size_t)15, tables = (size_t)(nb + 1) * 16;
   const int level = moves + tables <= kFixupSmemMax ? 2 : (moves <= kFixupSmemMax ? 1 : 0);
   const size_t fsmem = level == 2 ? moves + tables : (level == 1 ? moves : 0);
+  constexpr int fwpb = kFixupThreads / 32;  // warps per block
+  // per-j records: one warp per region; group records: enough warps for the batches of groups,
+  // as many blocks as are resident at once (they take batches from a ticket)
+  const long long ngroups = (p.unit_end - p.unit_begin) * 4;
+  const long long fwarps = pl.grouped ? std::min<long long>((ngroups + kFixupBatch - 1) / kFixupBatch,
+                                                            (long long)c->num_sms * ACF_FIXUP_MINB * fwpb)
+                                      : regions;
+  const unsigned fblocks = (unsigned)std::max<long long>(1, (fwarps + fwpb - 1) / fwpb);
   FixupParams f;
   f.qhdr = sc.qhdr;
   f.qmask = sc.qmask;

@@ -1699,16 +1699,20 @@ constexpr int kFixupThreads = 256;
 #define ACF_FIXUP_PAIRS 2
 #endif
 constexpr int kFixupPairs = ACF_FIXUP_PAIRS;
+// Fix-up of group records: groups per ticket (a batch ends with the warp's last record of it, so
+// smaller batches shorten the launch's tail)
+constexpr int kFixupBatch = 8;
 template <int MAP, int SMEM, bool GROUPED>
 __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(const FixupParams f) {
-  static_assert(kFixupThreads == 8 * 32, "one pair list per warp");
+  constexpr int WARPS = kFixupThreads / 32;
   extern __shared__ __align__(16) unsigned char fsm[];
   __shared__ unsigned int s_moved, s_redone, s_flagged;
-  __shared__ uint4 s_list[8][32 * kFixupPairs];  // per warp: (i, j, path code, 0) of the pairs of one round
+  __shared__ uint4 s_list[WARPS][32 * kFixupPairs];  // per warp: (i, j, path code, 0) of the pairs of one round
   const BinParams& bp = f.bp;
   const int nb = bp.nbins;
   const float2* tT = f.Tds;
   const float2* tU = f.Uds;
+  const int kd = *f.kd;
   int* sd = nullptr;
   if (SMEM >= 1) {
     sd = reinterpret_cast<int*>(fsm);
@@ -1727,7 +1731,6 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
   if (threadIdx.x == 0) s_moved = s_redone = s_flagged = 0u;
   __syncthreads();
   unsigned int my_moved = 0u, my_redone = 0u, my_flagged = 0u;
-  const int kd = *f.kd;
   // move one count between bins (k_from -> k_to)
   auto move = [&](int k_from, int k_to) {
     if (k_from == k_to) return;
@@ -1888,20 +1891,21 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     }
   };
   if constexpr (GROUPED) {
-    // batches of 32 groups from a ticket; in each, lane l takes the records of lane l of the groups
-    // whose ballot holds l
+    // batches of kFixupBatch groups from a ticket (the next ticket fetched while a batch is done);
+    // in each, lane l takes the records of lane l of the groups whose ballot holds l
+    unsigned int bt = 0u;
+    if (lane == 0) bt = atomicAdd(f.gticket, 1u);
+    bt = __shfl_sync(0xffffffffu, bt, 0);
     while (true) {
-      unsigned int bt = 0u;
-      if (lane == 0) bt = atomicAdd(f.gticket, 1u);
-      const unsigned long long g0 = 32ull * __shfl_sync(0xffffffffu, bt, 0);
+      const unsigned long long g0 = (unsigned long long)kFixupBatch * bt;
       if (g0 >= f.ngroups) break;
-      const unsigned int bal = g0 + lane < f.ngroups ? f.gbal[g0 + lane] : 0u;
+      unsigned int bn = 0u;
+      if (lane == 0) bn = atomicAdd(f.gticket, 1u);
+      const unsigned int bal = lane < kFixupBatch && g0 + lane < f.ngroups ? f.gbal[g0 + lane] : 0u;
       unsigned int mine = 0u;  // bit q: group g0 + q holds a record of this lane
-#pragma unroll 8
-      for (int l = 0; l < 32; ++l) {
-        const unsigned int x = __ballot_sync(0xffffffffu, (bal >> l) & 1u);
-        if (lane == l) mine = x;
-      }
+#pragma unroll
+      for (int q = 0; q < kFixupBatch; ++q) mine |= ((__shfl_sync(0xffffffffu, bal, q) >> lane) & 1u) << q;
+      bt = __shfl_sync(0xffffffffu, bn, 0);
       rounds([&](uint4& hn, uint4& mn) {
         if (!mine) return false;
         const int q = __ffs(mine) - 1;
@@ -1914,7 +1918,7 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
     // this warp's region, then its share of the spill records
     const unsigned long long nbatch = (unsigned long long)f.regions * f.qbatch;
     const unsigned int nspill = nbatch < f.qcap ? (unsigned int)min((unsigned long long)*f.qspill, f.qcap - nbatch) : 0u;
-    const unsigned int gw = blockIdx.x * (kFixupThreads / 32) + warp, nw = gridDim.x * (kFixupThreads / 32);
+    const unsigned int gw = blockIdx.x * WARPS + warp, nw = gridDim.x * WARPS;
     const unsigned int nmine = gw < f.regions ? min(f.qused[gw], f.qbatch) : 0u;
     auto records = [&](unsigned long long base, unsigned int n, unsigned int t, unsigned int stride) {
       rounds([&](uint4& hn, uint4& mn) {

@@ -205,7 +205,10 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *   "exact_queue"    records of the exact-mode queue (one per warp i-set and j holding a flagged
  *                    pair): 0 = automatic (default: enough for one launch at twice the worst-case flag
  *                    rate), else exactly this many, up to 2^28. A smaller queue can overflow; its
- *                    pairs then keep their fp32 bins (see "exact_overflow")
+ *                    pairs then keep their fp32 bins (see "exact_overflow"). Plans with one
+ *                    block-shared histogram in exact mode 2 keep their flags in group records
+ *                    instead (a slot for every lane and j-group of a launch, so they never
+ *                    overflow) and ignore this option.
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
  *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
  *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
