@@ -1694,14 +1694,19 @@ struct FixupParams {
 // Shared moves reach delta[] once per block.
 constexpr int kFixupThreads = 256;
 // Fix-up: pairs a lane decides per round (their vector loads all in flight together): 2 measured
-// 0.54 against 0.63 ms per fine-binning fix-up launch (19 against 16 threads per instruction)
+// 0.54 against 0.63 ms per fine-binning fix-up launch (19 against 16 threads per instruction); with
+// group records 3 and 4 spill and are slower (fine-binning steps 70.6 and 76.3 against 65.2 ms, and
+// 67.2 / 74.9 ms with 3 blocks per SM)
 #ifndef ACF_FIXUP_PAIRS
 #define ACF_FIXUP_PAIRS 2
 #endif
 constexpr int kFixupPairs = ACF_FIXUP_PAIRS;
 // Fix-up of group records: groups per ticket (a batch ends with the warp's last record of it, so
-// smaller batches shorten the launch's tail)
-constexpr int kFixupBatch = 8;
+// smaller batches shorten the launch's tail; measured on fine bins: 4 and 16 groups slower than 8)
+#ifndef ACF_FIXUP_BATCH
+#define ACF_FIXUP_BATCH 8
+#endif
+constexpr int kFixupBatch = ACF_FIXUP_BATCH;
 template <int MAP, int SMEM, bool GROUPED>
 __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(const FixupParams f) {
   constexpr int WARPS = kFixupThreads / 32;
