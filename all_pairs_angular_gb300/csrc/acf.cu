@@ -580,17 +580,23 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     p.unit_end = std::min(L.units, ub + L.per_launch);
     p.accumulate = ub > 0 ? 1 : 0;
     if (ub > 0) ACF_CUDA(c, cudaMemsetAsync(ticket, 0, 8, c->stream));  // ticket and queue slots
+    // kernel_timing 1: events around the pair kernel; 2: around the fix-up
     const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
-    if (timed) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
+    if (timed && c->opt_timing == 1) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
     L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
     ACF_LAUNCHED(c);
-    if (timed) {
+    if (timed && c->opt_timing == 1) {
       ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
       c->ev_used += 2;
     }
     if (p.exact_mode) {
+      if (timed && c->opt_timing == 2) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
       const int frc = launch_fixup(c, pl, L, p, sc, ci, cj);
       if (frc) return frc;
+      if (timed && c->opt_timing == 2) {
+        ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
+        c->ev_used += 2;
+      }
     }
   }
 #ifdef ACF_DEBUG_BOUNDS
@@ -944,7 +950,8 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "inject_launch_error must be >= 0");
     c->inject_launch_error = v;
   } else if (!strcmp(key, "kernel_timing")) {
-    c->opt_timing = v ? 1 : 0;
+    if (v < 0 || v > 2) return fail(c, ACF_ERR_ARG, "kernel_timing must be 0, 1 or 2");
+    c->opt_timing = (int)v;
     if (c->opt_timing && c->ev.empty()) {
       ACF_CUDA(c, cudaSetDevice(c->device));
       c->ev.resize(2 * kMaxTimed);

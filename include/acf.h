@@ -209,7 +209,8 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    block-shared histogram in exact mode 2 keep their flags in group records
  *                    instead (a slot for every lane and j-group of a launch, so they never
  *                    overflow) and ignore this option.
- *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times)
+ *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times);
+ *                    2 = bracket every exact-mode fix-up launch instead; 0 = off (default)
  *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
  *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
  *   "inject_launch_error"  fault injection for tests, on the host only: the n-th kernel launch from
@@ -257,8 +258,9 @@ int acf_get_info(const acf_ctx *ctx, const char *key, int64_t *value);
 
 /*
  * With "kernel_timing" on: synchronise, write up to `cap` per-launch durations of the pair
- * kernel (milliseconds, CUDA events on the context stream) recorded since the last call into
- * ms[], set *count, and clear the record. At most 4096 launches are kept.
+ * kernel (option value 1) or of the exact-mode fix-up (value 2) (milliseconds, CUDA events on the
+ * context stream) recorded since the last call into ms[], set *count, and clear the record. At
+ * most 4096 launches are kept.
  */
 int acf_kernel_times(acf_ctx *ctx, float *ms, int32_t cap, int32_t *count);
 

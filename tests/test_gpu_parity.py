@@ -278,13 +278,25 @@ def test_acos_method_keeps_totals(acf, ctx):
 
 def test_kernel_timing_records_launches(acf, ctx):
     c = synth.catalogs(2000, 2000, 0, 0.0, seed=2)
-    ctx.set_option("kernel_timing", 1)
     try:
-        ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)
-        ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+        # 1: the pair kernels; 2: the exact-mode fix-ups (one after each pair launch), for the
+        # per-j records (720 bins) and the group records (18,000 bins, 3 launches forced)
+        for mode in (1, 2):
+            ctx.set_option("kernel_timing", mode)
+            ctx.histogram(c.ra_d, c.dec_d, bin_width_deg=0.25, nbins=720)
+            ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.25, nbins=720)
+            t = ctx.kernel_times()
+            assert len(t) == 2 and all(x > 0 for x in t), (mode, t)
+        ctx.set_option("units_per_launch", 50)
+        ctx.histogram(c.ra_d, c.dec_d, c.ra_r, c.dec_r, bin_width_deg=0.01, nbins=18000)
+        assert ctx.info("layout") == 2
+        launches = ctx.info("launches")
         t = ctx.kernel_times()
-        assert len(t) == 2 and all(x > 0 for x in t)
+        assert launches >= 3 and len(t) == launches and all(x > 0 for x in t), (launches, t)
+        with pytest.raises(acf.AcfError):
+            ctx.set_option("kernel_timing", 3)
     finally:
+        ctx.set_option("units_per_launch", 0)
         ctx.set_option("kernel_timing", 0)
 
 
