@@ -82,3 +82,31 @@ def test_no_alloc_queue_overflow_keeps_sums_and_edge_rule(acf):
     rep = check.edge_flux(g, o.hist, o.near_below, o.near_above)
     assert rep.ok, rep
     ctx.close()
+
+
+def test_no_alloc_group_records_split_launches(acf):
+    # 2000 bins of 0.09 deg take the block-shared histogram, whose exact mode keeps its flags in
+    # group records: a fixed slot for every lane and j-group of every unit of a launch. What the
+    # static array has left after two 20k catalogs and 152 block rows holds a few thousand units,
+    # so the call runs more, smaller launches than the allocating one; the histograms must still be
+    # equal to it and to the oracle, bin for bin.
+    ctx = acf.Context(0)
+    c = synth.catalogs(20000, 20000, 20, 30.0, seed=23)
+    ra_d, dec_d, ra_r, dec_r = map(_dev, (c.ra_d, c.dec_d, c.ra_r, c.dec_r))
+    w, nb = 0.09, 2000
+    for ra2, dec2, n2 in ((None, None, 0), (ra_r, dec_r, c.n_r)):
+        ref = torch.empty(nb, dtype=torch.int64, device="cuda")
+        got = torch.full((nb,), -1, dtype=torch.int64, device="cuda")
+        acf.acf_histogram(ctx.handle, ra_d, dec_d, c.n_d, ra2, dec2, n2, w, nb, ref)
+        launches_alloc = ctx.info("launches")
+        acf.acf_histogram_noalloc(ctx.handle, ra_d, dec_d, c.n_d, ra2, dec2, n2, w, nb, got)
+        torch.cuda.synchronize()
+        assert ctx.info("layout") == 2
+        assert ctx.info("launches") > launches_alloc, (ctx.info("launches"), launches_alloc)
+        assert ctx.info("exact_overflow") == 0
+        assert torch.equal(ref, got)
+        g = acf.as_uint64(got)
+        o = oracle.histogram(c.ra_d, c.dec_d, None if ra2 is None else c.ra_r, None if ra2 is None else c.dec_r,
+                             w, nb)
+        assert np.array_equal(g, o.hist)
+    ctx.close()
