@@ -46,6 +46,44 @@ struct Workspace {
   size_t bytes = 0;
 };
 
+// A call that repeats with the same arguments, options, stream and workspace replays a CUDA graph
+// of its launches instead of launching each kernel (see GraphCache).
+struct CallKey {
+  int entry = 0;  // 1 acf_correlate, 2 acf_histogram
+  const void* p[8] = {};
+  long long n[2] = {};
+  double w = 0.0;
+  int nbins = 0;
+  cudaStream_t stream = nullptr;
+  const void* ws = nullptr;
+  size_t ws_bytes = 0;
+  // the options that shape the launches
+  int threads = 0, ctas = 0, method = 0, layout = 0, exact = 0, range_forms = 0, unit_groups = 0;
+  long long units_per_launch = 0, exact_queue = 0;
+  double exact_below_deg = 0.0;
+  bool operator==(const CallKey& o) const {
+    return entry == o.entry && std::equal(p, p + 8, o.p) && n[0] == o.n[0] && n[1] == o.n[1] && w == o.w &&
+           nbins == o.nbins && stream == o.stream && ws == o.ws && ws_bytes == o.ws_bytes && threads == o.threads &&
+           ctas == o.ctas && method == o.method && layout == o.layout && exact == o.exact &&
+           range_forms == o.range_forms && unit_groups == o.unit_groups && units_per_launch == o.units_per_launch &&
+           exact_queue == o.exact_queue && exact_below_deg == o.exact_below_deg;
+  }
+};
+// What a call leaves for acf_get_info on the host side (restored when a graph stands in for it).
+struct CallInfo {
+  unsigned int* last_counters = nullptr;
+  long long last_qcap = 0, grid = 0, threads = 0, ctas = 0, chunks = 0, layout = 0, map = 0, entries = 0, smem = 0,
+            pairs = 0, flush = 0, groups = 0;
+};
+struct CachedGraph {
+  CallKey key;
+  cudaGraphExec_t exec = nullptr;
+  long long launches = 0;    // kernels in the graph
+  unsigned long long used = 0;  // last use (for eviction)
+  CallInfo info;             // the captured call's
+};
+constexpr int kGraphSlots = 4;
+
 }  // namespace
 
 struct acf_ctx {
@@ -66,6 +104,32 @@ struct acf_ctx {
   int opt_pair_bins_form = 0;     // acf_pair_bins: 0 full-range chord form, 1 the range forms by own u.v
   int opt_unit_groups = 0;        // j-groups per work unit: 0 automatic, 4 (chunk pairs) or 1 (small problems)
   long long opt_exact_queue = 0;  // exact-mode queue records: 0 automatic, else this many (tests of overflow)
+  int opt_graphs = 1;             // 1: repeated calls replay a CUDA graph of their launches
+  // graph replay: calls seen once (captured when they repeat) and the captured graphs
+  CallKey seen[kGraphSlots];
+  int seen_next = 0;
+  CachedGraph graphs[kGraphSlots];
+  unsigned long long graph_clock = 0;
+  long long graph_replays = 0;    // calls served by a graph
+  CallInfo info() const {
+    return CallInfo{last_counters, last_qcap, info_grid,  info_threads, info_ctas, info_chunks, info_layout,
+                    info_map,      info_entries, info_smem, info_pairs, info_flush, info_groups};
+  }
+  void set_info(const CallInfo& i) {
+    last_counters = i.last_counters;
+    last_qcap = i.last_qcap;
+    info_grid = i.grid;
+    info_threads = i.threads;
+    info_ctas = i.ctas;
+    info_chunks = i.chunks;
+    info_layout = i.layout;
+    info_map = i.map;
+    info_entries = i.entries;
+    info_smem = i.smem;
+    info_pairs = i.pairs;
+    info_flush = i.flush;
+    info_groups = i.groups;
+  }
   unsigned int* last_counters = nullptr;  // device counters of the last histogram (ticket, slots, moved, flagged)
   long long last_qcap = 0;
   // info about the last histogram
@@ -760,6 +824,91 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }
 
+// Graph replay of repeated calls. A call is eligible when the option is on, neither kernel timing
+// nor launch-error injection is asked for, the context has a stream of its own (the legacy default
+// stream cannot be captured) and the caller is not capturing that stream. The first call with a key
+// runs as usual (and sizes the workspace); when the same key comes again the call is captured into
+// a graph (its kernels do not run while it is captured), instantiated and launched, and later calls
+// with that key launch the graph. The results are those of the call: the graph holds the same
+// launches with the same arguments, and they read the inputs' current contents. run() is the call.
+template <class Run>
+int run_graphed(acf_ctx* c, CallKey key, Run run) {
+  bool eligible = c->opt_graphs && !c->opt_timing && c->inject_launch_error == 0 && c->stream != nullptr &&
+                  c->stream != cudaStreamLegacy && c->stream != cudaStreamPerThread;
+  if (eligible) {
+    ACF_CUDA(c, cudaSetDevice(c->device));
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    ACF_CUDA(c, cudaStreamIsCapturing(c->stream, &st));
+    eligible = st == cudaStreamCaptureStatusNone;
+  }
+  if (!eligible) return run();
+  key.stream = c->stream;
+  key.threads = c->opt_threads;
+  key.ctas = c->opt_ctas;
+  key.method = c->opt_method;
+  key.layout = c->opt_layout;
+  key.exact = c->opt_exact;
+  key.range_forms = c->opt_range_forms;
+  key.unit_groups = c->opt_unit_groups;
+  key.units_per_launch = c->opt_units_per_launch;
+  key.exact_queue = c->opt_exact_queue;
+  key.exact_below_deg = c->opt_exact_below_deg;
+  key.ws = c->ws.ptr;
+  key.ws_bytes = c->ws.bytes;
+  for (CachedGraph& g : c->graphs)
+    if (g.exec && g.key == key) {
+      ACF_CUDA(c, cudaGraphLaunch(g.exec, c->stream));
+      g.used = ++c->graph_clock;
+      c->kernel_launches += g.launches;
+      ++c->graph_replays;
+      c->set_info(g.info);
+      return ACF_OK;
+    }
+  int seen = -1;
+  for (int k = 0; k < kGraphSlots; ++k)
+    if (c->seen[k] == key) seen = k;
+  if (seen < 0) {
+    const int rc = run();
+    if (rc == ACF_OK) {
+      key.ws = c->ws.ptr;  // as the call left the workspace
+      key.ws_bytes = c->ws.bytes;
+      c->seen[c->seen_next] = key;
+      c->seen_next = (c->seen_next + 1) % kGraphSlots;
+    }
+    return rc;
+  }
+  c->seen[seen] = CallKey();  // captured once, whatever the outcome
+  const long long before = c->kernel_launches;
+  if (cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return run();
+  }
+  const int rc = run();
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (rc == ACF_OK && e == cudaSuccess && graph && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) exec = nullptr;
+  if (graph) cudaGraphDestroy(graph);
+  if (!exec) {
+    // not capturable after all (or the call failed while captured): run it as usual
+    cudaGetLastError();
+    c->kernel_launches = before;
+    return run();
+  }
+  CachedGraph* slot = &c->graphs[0];
+  for (CachedGraph& g : c->graphs)
+    if (!g.exec || (slot->exec && g.used < slot->used)) slot = &g;
+  if (slot->exec) cudaGraphExecDestroy(slot->exec);
+  slot->key = key;
+  slot->exec = exec;
+  slot->launches = c->kernel_launches - before;
+  slot->used = ++c->graph_clock;
+  slot->info = c->info();
+  ACF_CUDA(c, cudaGraphLaunch(exec, c->stream));
+  ++c->graph_replays;
+  return ACF_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -810,6 +959,8 @@ void acf_destroy(acf_ctx* c) {
   if (c->ws.ptr) cudaFree(c->ws.ptr);
   if (c->io.ptr) cudaFree(c->io.ptr);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+  for (CachedGraph& g : c->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
   delete c;
 }
 
@@ -825,7 +976,16 @@ int acf_set_stream(acf_ctx* c, void* s) {
 
 int acf_histogram(acf_ctx* c, const float* ra, const float* dec, int64_t n, const float* ra2, const float* dec2,
                   int64_t n2, double w_deg, int32_t nbins, uint64_t* out) {
-  return histogram_impl(c, ra, dec, n, ra2, dec2, n2, w_deg, nbins, out);
+  if (!c) return ACF_ERR_ARG;
+  CallKey k;
+  k.entry = 2;
+  const void* p[8] = {ra, dec, ra2, dec2, out, nullptr, nullptr, nullptr};
+  std::copy(p, p + 8, k.p);
+  k.n[0] = n;
+  k.n[1] = n2;
+  k.w = w_deg;
+  k.nbins = nbins;
+  return run_graphed(c, k, [&] { return histogram_impl(c, ra, dec, n, ra2, dec2, n2, w_deg, nbins, out); });
 }
 
 int acf_omega(acf_ctx* c, const uint64_t* dd, const uint64_t* dr, const uint64_t* rr, int32_t nbins, int64_t n_d,
@@ -841,7 +1001,15 @@ int acf_correlate(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_d
                   const float* dec_r, int64_t n_r, double w_deg, int32_t nbins, uint64_t* dd, uint64_t* dr, uint64_t* rr,
                   double* omega) {
   if (!c) return ACF_ERR_ARG;
-  return correlate_impl(c, ra_d, dec_d, n_d, ra_r, dec_r, n_r, w_deg, nbins, dd, dr, rr, omega);
+  CallKey k;
+  k.entry = 1;
+  const void* p[8] = {ra_d, dec_d, ra_r, dec_r, dd, dr, rr, omega};
+  std::copy(p, p + 8, k.p);
+  k.n[0] = n_d;
+  k.n[1] = n_r;
+  k.w = w_deg;
+  k.nbins = nbins;
+  return run_graphed(c, k, [&] { return correlate_impl(c, ra_d, dec_d, n_d, ra_r, dec_r, n_r, w_deg, nbins, dd, dr, rr, omega); });
 }
 
 int acf_correlate_host(acf_ctx* c, const float* ra_d, const float* dec_d, int64_t n_d, const float* ra_r,
@@ -943,6 +1111,9 @@ int acf_set_option(acf_ctx* c, const char* key, int64_t v) {
   } else if (!strcmp(key, "exact_queue")) {
     if (v < 0 || v > kQueueCapMax) return fail(c, ACF_ERR_ARG, "exact_queue must be 0..2^28");
     c->opt_exact_queue = v;
+  } else if (!strcmp(key, "graphs")) {
+    if (v != 0 && v != 1) return fail(c, ACF_ERR_ARG, "graphs must be 0 or 1");
+    c->opt_graphs = (int)v;
   } else if (!strcmp(key, "workspace_limit")) {
     if (v < 0) return fail(c, ACF_ERR_ARG, "workspace_limit must be >= 0");
     c->opt_workspace_limit = v;
@@ -973,6 +1144,7 @@ int acf_get_info(const acf_ctx* c, const char* key, int64_t* v) {
            {"units", c->info_chunks},   {"layout", c->info_layout},     {"bin_map", c->info_map},
            {"hist_entries", c->info_entries}, {"smem_bytes", c->info_smem}, {"pairs_evaluated", c->info_pairs},
            {"launches", c->info_flush},  {"kernel_launches", c->kernel_launches},
+           {"graph_replays", c->graph_replays},
            {"unit_groups", c->info_groups}};
   for (auto& e : t)
     if (!strcmp(e.k, key)) {

@@ -211,6 +211,15 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    overflow) and ignore this option.
  *   "kernel_timing"  1 = bracket every pair-kernel launch with CUDA events (see acf_kernel_times);
  *                    2 = bracket every exact-mode fix-up launch instead; 0 = off (default)
+ *   "graphs"         1 = an acf_correlate or acf_histogram call that repeats an earlier one (the
+ *                    same pointers, sizes, binning, options, stream and workspace) replays a CUDA
+ *                    graph of its launches: captured the second time the call comes (its kernels
+ *                    run from the graph), launched as one graph from then on; the four most
+ *                    recent such calls are kept (default). The results, and what acf_get_info
+ *                    reports, are those of the call; the inputs' current contents are read.
+ *                    Calls go launch by launch while "kernel_timing" or "inject_launch_error" is
+ *                    set, on the legacy default stream (NULL), and while the caller captures the
+ *                    context's stream. 0 = every call launches its kernels one by one
  *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
  *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
  *   "inject_launch_error"  fault injection for tests, on the host only: the n-th kernel launch from
@@ -240,7 +249,9 @@ int acf_plan_info(double bin_width_deg, int32_t nbins, int32_t exact, int64_t *i
  * Read back facts about the last acf_histogram call. Keys: "grid", "threads", "ctas_per_sm",
  * "units", "layout", "bin_map" (0 mirror, 1 clamp), "hist_entries", "smem_bytes",
  * "pairs_evaluated", "launches" (pair-kernel launches the call was split into),
- * "kernel_launches" (kernels this context has launched since acf_create, all entry points),
+ * "kernel_launches" (kernels this context has launched since acf_create, all entry points; a
+ * graph replay counts the kernels in the graph), "graph_replays" (calls served by a graph, see
+ * the option "graphs"),
  * "unit_groups" (4: units of a 128 x 128 chunk pair; 1: of one 32-galaxy j-group).
  * These keys synchronise the context's stream and read device counters of the last call:
  *   "pairs_fixed", "pairs_general"  pairs evaluated on the fixed-sign and general loops

@@ -5,6 +5,10 @@
 - acf_set_stream moves a context to another stream between calls.
 - A warmed-up acf_correlate (its workspace already allocated) can be captured into a CUDA graph
   and replayed. The replays give the captured call's results.
+- The library's own graph replay of repeated calls (option "graphs"): the same results and launch
+  counts as calls launched one by one, the inputs' current contents read, acf_get_info describing
+  the replayed call, and calls launched one by one again when an option changes, kernel timing is
+  on or the option is off.
 """
 import numpy as np
 import pytest
@@ -98,5 +102,84 @@ def test_correlate_captured_in_a_cuda_graph(acf, data):
             for h, r in zip(outs[:3], ref):
                 assert np.array_equal(acf.as_uint64(h), r)
             assert np.allclose(outs[3].cpu().numpy(), ref_om, rtol=0, atol=0, equal_nan=True)
+    finally:
+        ctx.close()
+
+
+def test_repeated_calls_replay_a_graph(acf, data):
+    s = torch.cuda.Stream()
+    ctx = acf.Context(0, s)
+    try:
+        t, ref, ref_om = data["a"]
+        with torch.cuda.stream(s):
+            outs = tuple(torch.empty(720, dtype=torch.int64, device="cuda") for _ in range(3)) + (
+                torch.empty(720, dtype=torch.float64, device="cuda"),)
+
+        def call():
+            with torch.cuda.stream(s):
+                for o in outs:
+                    o.zero_()
+                k0 = ctx.info("kernel_launches")
+                ctx.correlate(*t, 0.25, 720, out=outs)
+            s.synchronize()
+            return ctx.info("kernel_launches") - k0
+
+        def check(r=ref, om=ref_om):
+            for h, x in zip(outs[:3], r):
+                assert np.array_equal(acf.as_uint64(h), x)
+            assert np.allclose(outs[3].cpu().numpy(), om, rtol=0, atol=0, equal_nan=True)
+
+        base = ctx.info("graph_replays")
+        launches = []
+        for _ in range(4):  # the first call runs as usual, the second is captured, then replays
+            launches.append(call())
+            check()
+        assert ctx.info("graph_replays") - base == 3
+        assert len(set(launches)) == 1, launches
+        assert ctx.info("layout") == 1 and ctx.info("launches") == 1 and ctx.info("exact_flagged") > 0
+
+        # the graph reads the inputs' current contents: other catalogs of the same sizes
+        c2 = synth.catalogs(6000, 5000, 4, 90.0, seed=83)
+        t2 = tuple(map(_dev, (c2.ra_d, c2.dec_d, c2.ra_r, c2.dec_r)))
+        ref_ctx = acf.Context(0)
+        o2 = ref_ctx.correlate(*t2, 0.25, 720)
+        torch.cuda.synchronize()
+        ref2 = [acf.as_uint64(h).copy() for h in o2[:3]]
+        om2 = o2[3].cpu().numpy()
+        ref_ctx.close()
+        with torch.cuda.stream(s):
+            for dst, src in zip(t, t2):
+                dst.copy_(src)
+        n0 = ctx.info("graph_replays")
+        call()
+        assert ctx.info("graph_replays") == n0 + 1
+        check(ref2, om2)
+        # the fixture's inputs back in place (other tests share them)
+        a = synth.catalogs(6000, 5000, 10, 30.0, seed=81)
+        with torch.cuda.stream(s):
+            for dst, src in zip(t, (a.ra_d, a.dec_d, a.ra_r, a.dec_r)):
+                dst.copy_(torch.from_numpy(np.ascontiguousarray(src)).cuda())
+
+        # another option: launched one by one, then captured when it repeats; the first graph stays
+        ctx.set_option("exact", 0)
+        n0 = ctx.info("graph_replays")
+        call()
+        call()
+        assert ctx.info("graph_replays") == n0 + 1 and ctx.info("exact_flagged") == 0
+        ctx.set_option("exact", 2)
+        call()
+        assert ctx.info("graph_replays") == n0 + 2
+        check()
+
+        # kernel timing, or the option off: every kernel launched by itself
+        for key, v in (("kernel_timing", 1), ("graphs", 0)):
+            ctx.set_option(key, v)
+            n0 = ctx.info("graph_replays")
+            assert call() == launches[0]
+            check()
+            assert ctx.info("graph_replays") == n0
+            if key == "kernel_timing":
+                assert len(ctx.kernel_times()) == 3  # DD, DR, RR: every pair kernel timed
+            ctx.set_option(key, 1 - v)
     finally:
         ctx.close()
