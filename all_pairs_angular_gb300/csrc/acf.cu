@@ -49,7 +49,7 @@ struct Workspace {
 // A call that repeats with the same arguments, options, stream and workspace replays a CUDA graph
 // of its launches instead of launching each kernel (see GraphCache).
 struct CallKey {
-  int entry = 0;  // 1 acf_correlate, 2 acf_histogram
+  int entry = 0;  // 1 acf_correlate, 2 acf_histogram, 3 acf_correlate_host
   const void* p[8] = {};
   long long n[2] = {};
   double w = 0.0;
@@ -57,13 +57,16 @@ struct CallKey {
   cudaStream_t stream = nullptr;
   const void* ws = nullptr;
   size_t ws_bytes = 0;
+  const void* io = nullptr;  // acf_correlate_host's device staging
+  size_t io_bytes = 0;
   // the options that shape the launches
   int threads = 0, ctas = 0, method = 0, layout = 0, exact = 0, range_forms = 0, unit_groups = 0;
   long long units_per_launch = 0, exact_queue = 0;
   double exact_below_deg = 0.0;
   bool operator==(const CallKey& o) const {
     return entry == o.entry && std::equal(p, p + 8, o.p) && n[0] == o.n[0] && n[1] == o.n[1] && w == o.w &&
-           nbins == o.nbins && stream == o.stream && ws == o.ws && ws_bytes == o.ws_bytes && threads == o.threads &&
+           nbins == o.nbins && stream == o.stream && ws == o.ws && ws_bytes == o.ws_bytes && io == o.io &&
+           io_bytes == o.io_bytes && threads == o.threads &&
            ctas == o.ctas && method == o.method && layout == o.layout && exact == o.exact &&
            range_forms == o.range_forms && unit_groups == o.unit_groups && units_per_launch == o.units_per_launch &&
            exact_queue == o.exact_queue && exact_below_deg == o.exact_below_deg;
@@ -855,6 +858,8 @@ int run_graphed(acf_ctx* c, CallKey key, Run run) {
   key.exact_below_deg = c->opt_exact_below_deg;
   key.ws = c->ws.ptr;
   key.ws_bytes = c->ws.bytes;
+  key.io = c->io.ptr;
+  key.io_bytes = c->io.bytes;
   for (CachedGraph& g : c->graphs)
     if (g.exec && g.key == key) {
       ACF_CUDA(c, cudaGraphLaunch(g.exec, c->stream));
@@ -1034,16 +1039,45 @@ int acf_correlate_host(acf_ctx* c, const float* ra_d, const float* dec_d, int64_
   uint64_t* d_dr = reinterpret_cast<uint64_t*>(h + bh);
   uint64_t* d_rr = reinterpret_cast<uint64_t*>(h + 2 * bh);
   double* d_om = reinterpret_cast<double*>(h + 3 * bh);
-  ACF_CUDA(c, cudaMemcpyAsync(d_ra_d, ra_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
-  ACF_CUDA(c, cudaMemcpyAsync(d_dec_d, dec_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
-  ACF_CUDA(c, cudaMemcpyAsync(d_ra_r, ra_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
-  ACF_CUDA(c, cudaMemcpyAsync(d_dec_r, dec_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
-  if ((rc = correlate_impl(c, d_ra_d, d_dec_d, n_d, d_ra_r, d_dec_r, n_r, w_deg, nbins, d_dd, d_dr, d_rr, d_om)))
-    return rc;
-  ACF_CUDA(c, cudaMemcpyAsync(dd, d_dd, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
-  ACF_CUDA(c, cudaMemcpyAsync(dr, d_dr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
-  ACF_CUDA(c, cudaMemcpyAsync(rr, d_rr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
-  ACF_CUDA(c, cudaMemcpyAsync(omega, d_om, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+  auto body = [&]() -> int {
+    ACF_CUDA(c, cudaMemcpyAsync(d_ra_d, ra_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
+    ACF_CUDA(c, cudaMemcpyAsync(d_dec_d, dec_d, (size_t)n_d * 4, cudaMemcpyHostToDevice, c->stream));
+    ACF_CUDA(c, cudaMemcpyAsync(d_ra_r, ra_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
+    ACF_CUDA(c, cudaMemcpyAsync(d_dec_r, dec_r, (size_t)n_r * 4, cudaMemcpyHostToDevice, c->stream));
+    const int rc2 = correlate_impl(c, d_ra_d, d_dec_d, n_d, d_ra_r, d_dec_r, n_r, w_deg, nbins, d_dd, d_dr, d_rr, d_om);
+    if (rc2) return rc2;
+    ACF_CUDA(c, cudaMemcpyAsync(dd, d_dd, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+    ACF_CUDA(c, cudaMemcpyAsync(dr, d_dr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+    ACF_CUDA(c, cudaMemcpyAsync(rr, d_rr, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+    ACF_CUDA(c, cudaMemcpyAsync(omega, d_om, (size_t)nbins * 8, cudaMemcpyDeviceToHost, c->stream));
+    return ACF_OK;
+  };
+  // with page-locked host buffers the copies can sit in a graph with the kernels (pageable ones
+  // cannot be captured)
+  const void* hp[8] = {ra_d, dec_d, ra_r, dec_r, dd, dr, rr, omega};
+  bool pinned = true;
+  for (const void* q : hp) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+      cudaGetLastError();
+      pinned = false;
+    } else if (at.type != cudaMemoryTypeHost) {
+      pinned = false;
+    }
+  }
+  if (pinned) {
+    CallKey k;
+    k.entry = 3;
+    std::copy(hp, hp + 8, k.p);
+    k.n[0] = n_d;
+    k.n[1] = n_r;
+    k.w = w_deg;
+    k.nbins = nbins;
+    rc = run_graphed(c, k, body);
+  } else {
+    rc = body();
+  }
+  if (rc) return rc;
   ACF_CUDA(c, cudaStreamSynchronize(c->stream));
   return ACF_OK;
 }

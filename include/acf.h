@@ -215,7 +215,8 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    same pointers, sizes, binning, options, stream and workspace) replays a CUDA
  *                    graph of its launches: captured the second time the call comes (its kernels
  *                    run from the graph), launched as one graph from then on; the four most
- *                    recent such calls are kept (default). The results, and what acf_get_info
+ *                    recent such calls are kept (default). acf_correlate_host does the same, its
+ *                    copies included, when every host buffer is page-locked. The results, and what acf_get_info
  *                    reports, are those of the call; the inputs' current contents are read.
  *                    Calls go launch by launch while "kernel_timing" or "inject_launch_error" is
  *                    set, on the legacy default stream (NULL), and while the caller captures the

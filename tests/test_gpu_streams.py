@@ -183,3 +183,35 @@ def test_repeated_calls_replay_a_graph(acf, data):
             ctx.set_option(key, 1 - v)
     finally:
         ctx.close()
+
+
+def test_repeated_host_calls_replay_a_graph_with_page_locked_buffers(acf, data):
+    # acf_correlate_host with page-locked host buffers: the copies join the kernels in the graph;
+    # with pageable ones (which a graph cannot hold) every call runs launch by launch
+    s = torch.cuda.Stream()
+    ctx = acf.Context(0, s)
+    try:
+        c = synth.catalogs(6000, 5000, 10, 30.0, seed=81)  # the fixture's catalogs "a"
+        ref, ref_om = data["a"][1], data["a"][2]
+        host_in = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (c.ra_d, c.dec_d, c.ra_r, c.dec_r)]
+        host_out = [torch.empty(720, dtype=torch.int64).pin_memory() for _ in range(3)] + [
+            torch.empty(720, dtype=torch.float64).pin_memory()]
+        base = ctx.info("graph_replays")
+        for _ in range(4):
+            for o in host_out:
+                o.zero_()
+            acf.acf_correlate_host(ctx.handle, host_in[0], host_in[1], c.n_d, host_in[2], host_in[3], c.n_r, 0.25, 720,
+                                   *host_out)
+            for h, r in zip(host_out[:3], ref):
+                assert np.array_equal(acf.as_uint64(h), r)
+            assert np.allclose(host_out[3].numpy(), ref_om, rtol=0, atol=0, equal_nan=True)
+        assert ctx.info("graph_replays") - base == 3
+        out = (np.empty(720, np.uint64), np.empty(720, np.uint64), np.empty(720, np.uint64), np.empty(720, np.float64))
+        n0 = ctx.info("graph_replays")
+        for _ in range(3):
+            dd, dr, rr, om = ctx.correlate_host(c.ra_d, c.dec_d, c.ra_r, c.dec_r, 0.25, 720, out=out)
+            for h, r in zip((dd, dr, rr), ref):
+                assert np.array_equal(h, r)
+        assert ctx.info("graph_replays") == n0
+    finally:
+        ctx.close()
