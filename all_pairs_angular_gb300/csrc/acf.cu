@@ -60,7 +60,7 @@ struct CallKey {
   const void* io = nullptr;  // acf_correlate_host's device staging
   size_t io_bytes = 0;
   // the options that shape the launches
-  int threads = 0, ctas = 0, method = 0, layout = 0, exact = 0, range_forms = 0, unit_groups = 0;
+  int threads = 0, ctas = 0, method = 0, layout = 0, exact = 0, range_forms = 0, unit_groups = 0, timing = 0;
   long long units_per_launch = 0, exact_queue = 0;
   double exact_below_deg = 0.0;
   bool operator==(const CallKey& o) const {
@@ -68,7 +68,8 @@ struct CallKey {
            nbins == o.nbins && stream == o.stream && ws == o.ws && ws_bytes == o.ws_bytes && io == o.io &&
            io_bytes == o.io_bytes && threads == o.threads &&
            ctas == o.ctas && method == o.method && layout == o.layout && exact == o.exact &&
-           range_forms == o.range_forms && unit_groups == o.unit_groups && units_per_launch == o.units_per_launch &&
+           range_forms == o.range_forms && unit_groups == o.unit_groups && timing == o.timing &&
+           units_per_launch == o.units_per_launch &&
            exact_queue == o.exact_queue && exact_below_deg == o.exact_below_deg;
   }
 };
@@ -80,10 +81,22 @@ struct CallInfo {
 };
 struct CachedGraph {
   CallKey key;
+  cudaGraph_t graph = nullptr;  // kept while its event nodes are rebound on every launch
   cudaGraphExec_t exec = nullptr;
   long long launches = 0;    // kernels in the graph
   unsigned long long used = 0;  // last use (for eviction)
   CallInfo info;             // the captured call's
+  // kernel timing: the graph's event-record nodes and, for each, which of the call's events it is
+  std::vector<std::pair<cudaGraphNode_t, int>> ev_nodes;
+  int ev_count = 0;
+  void release() {
+    if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
+    exec = nullptr;
+    graph = nullptr;
+    ev_nodes.clear();
+    ev_count = 0;
+  }
 };
 constexpr int kGraphSlots = 4;
 
@@ -114,6 +127,7 @@ struct acf_ctx {
   CachedGraph graphs[kGraphSlots];
   unsigned long long graph_clock = 0;
   long long graph_replays = 0;    // calls served by a graph
+  bool capturing = false;         // the library is capturing a call (see run_graphed)
   CallInfo info() const {
     return CallInfo{last_counters, last_qcap, info_grid,  info_threads, info_ctas, info_chunks, info_layout,
                     info_map,      info_entries, info_smem, info_pairs, info_flush, info_groups};
@@ -649,19 +663,23 @@ int histogram_vectors(acf_ctx* c, const CatBufs& ci, long long ni, const CatBufs
     if (ub > 0) ACF_CUDA(c, cudaMemsetAsync(ticket, 0, 8, c->stream));  // ticket and queue slots
     // kernel_timing 1: events around the pair kernel; 2: around the fix-up
     const bool timed = c->opt_timing && c->ev_used + 2 <= (int)c->ev.size();
-    if (timed && c->opt_timing == 1) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
+    // (while the library captures the call, external records: event nodes of the graph)
+    const unsigned rec = c->capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
+    if (timed && c->opt_timing == 1)
+      ACF_CUDA(c, cudaEventRecordWithFlags(c->ev[c->ev_used], c->stream, rec));
     L.fn<<<(unsigned)L.grid, pl.threads, pl.smem, c->stream>>>(p);
     ACF_LAUNCHED(c);
     if (timed && c->opt_timing == 1) {
-      ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
+      ACF_CUDA(c, cudaEventRecordWithFlags(c->ev[c->ev_used + 1], c->stream, rec));
       c->ev_used += 2;
     }
     if (p.exact_mode) {
-      if (timed && c->opt_timing == 2) ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used], c->stream));
+      if (timed && c->opt_timing == 2)
+        ACF_CUDA(c, cudaEventRecordWithFlags(c->ev[c->ev_used], c->stream, rec));
       const int frc = launch_fixup(c, pl, L, p, sc, ci, cj);
       if (frc) return frc;
       if (timed && c->opt_timing == 2) {
-        ACF_CUDA(c, cudaEventRecord(c->ev[c->ev_used + 1], c->stream));
+        ACF_CUDA(c, cudaEventRecordWithFlags(c->ev[c->ev_used + 1], c->stream, rec));
         c->ev_used += 2;
       }
     }
@@ -827,17 +845,20 @@ int histogram_impl(acf_ctx* c, const float* ra, const float* dec, int64_t n, con
   return run_pipeline(c, ra, dec, n, ra2, dec2, nj, sym, pl, L, sc, out);
 }
 
-// Graph replay of repeated calls. A call is eligible when the option is on, neither kernel timing
-// nor launch-error injection is asked for, the context has a stream of its own (the legacy default
-// stream cannot be captured) and the caller is not capturing that stream. The first call with a key
-// runs as usual (and sizes the workspace); when the same key comes again the call is captured into
-// a graph (its kernels do not run while it is captured), instantiated and launched, and later calls
-// with that key launch the graph. The results are those of the call: the graph holds the same
-// launches with the same arguments, and they read the inputs' current contents. run() is the call.
+// Graph replay of repeated calls. A call is eligible when the option is on, no launch-error
+// injection is asked for, the context has a stream of its own (the legacy default stream cannot be
+// captured) and the caller is not capturing that stream. The first call with a key runs as usual
+// (and sizes the workspace); when the same key comes again the call is captured into a graph (its
+// kernels do not run while it is captured), instantiated and launched, and later calls with that
+// key launch the graph. The results are those of the call: the graph holds the same launches with
+// the same arguments, and they read the inputs' current contents. With kernel timing on, the timing
+// events the call records are event nodes of the graph; before every launch they are pointed at the
+// next free events, so acf_kernel_times sees each launch as if the call had run kernel by kernel.
+// run() is the call.
 template <class Run>
 int run_graphed(acf_ctx* c, CallKey key, Run run) {
-  bool eligible = c->opt_graphs && !c->opt_timing && c->inject_launch_error == 0 && c->stream != nullptr &&
-                  c->stream != cudaStreamLegacy && c->stream != cudaStreamPerThread;
+  bool eligible = c->opt_graphs && c->inject_launch_error == 0 && c->stream != nullptr && c->stream != cudaStreamLegacy &&
+                  c->stream != cudaStreamPerThread;
   if (eligible) {
     ACF_CUDA(c, cudaSetDevice(c->device));
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
@@ -853,6 +874,7 @@ int run_graphed(acf_ctx* c, CallKey key, Run run) {
   key.exact = c->opt_exact;
   key.range_forms = c->opt_range_forms;
   key.unit_groups = c->opt_unit_groups;
+  key.timing = c->opt_timing;
   key.units_per_launch = c->opt_units_per_launch;
   key.exact_queue = c->opt_exact_queue;
   key.exact_below_deg = c->opt_exact_below_deg;
@@ -860,14 +882,37 @@ int run_graphed(acf_ctx* c, CallKey key, Run run) {
   key.ws_bytes = c->ws.bytes;
   key.io = c->io.ptr;
   key.io_bytes = c->io.bytes;
+  // launch a cached graph, its timing events (if any) pointed at the next free ones; false when the
+  // timing record is full (the call then runs kernel by kernel, which stops recording)
+  auto launch = [&](CachedGraph& g, int& rc) -> bool {
+    rc = ACF_OK;
+    if (g.ev_count) {
+      if (c->ev_used + g.ev_count > (int)c->ev.size()) return false;
+      for (const auto& nr : g.ev_nodes) {
+        const cudaError_t e = cudaGraphExecEventRecordNodeSetEvent(g.exec, nr.first, c->ev[c->ev_used + nr.second]);
+        if (e != cudaSuccess) {
+          rc = cuda_fail(c, e, "cudaGraphExecEventRecordNodeSetEvent");
+          return true;
+        }
+      }
+    }
+    const cudaError_t e = cudaGraphLaunch(g.exec, c->stream);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(c, e, "cudaGraphLaunch");
+      return true;
+    }
+    c->ev_used += g.ev_count;
+    g.used = ++c->graph_clock;
+    c->kernel_launches += g.launches;
+    ++c->graph_replays;
+    c->set_info(g.info);
+    return true;
+  };
   for (CachedGraph& g : c->graphs)
     if (g.exec && g.key == key) {
-      ACF_CUDA(c, cudaGraphLaunch(g.exec, c->stream));
-      g.used = ++c->graph_clock;
-      c->kernel_launches += g.launches;
-      ++c->graph_replays;
-      c->set_info(g.info);
-      return ACF_OK;
+      int rc = ACF_OK;
+      if (launch(g, rc)) return rc;
+      return run();
     }
   int seen = -1;
   for (int k = 0; k < kGraphSlots; ++k)
@@ -884,34 +929,65 @@ int run_graphed(acf_ctx* c, CallKey key, Run run) {
   }
   c->seen[seen] = CallKey();  // captured once, whatever the outcome
   const long long before = c->kernel_launches;
+  const int ev_start = c->ev_used;
   if (cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
     cudaGetLastError();
     return run();
   }
+  c->capturing = true;
   const int rc = run();
-  cudaGraph_t graph = nullptr;
-  const cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
-  cudaGraphExec_t exec = nullptr;
-  if (rc == ACF_OK && e == cudaSuccess && graph && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) exec = nullptr;
-  if (graph) cudaGraphDestroy(graph);
-  if (!exec) {
+  c->capturing = false;
+  CachedGraph ng;
+  const cudaError_t e = cudaStreamEndCapture(c->stream, &ng.graph);
+  ng.ev_count = c->ev_used - ev_start;
+  c->ev_used = ev_start;  // the captured records did not happen
+  bool ok = rc == ACF_OK && e == cudaSuccess && ng.graph;
+  if (ok && ng.ev_count) {
+    // the event-record nodes, and which of the call's events each one records
+    size_t nn = 0;
+    ok = cudaGraphGetNodes(ng.graph, nullptr, &nn) == cudaSuccess;
+    std::vector<cudaGraphNode_t> nodes(nn);
+    if (ok && nn) ok = cudaGraphGetNodes(ng.graph, nodes.data(), &nn) == cudaSuccess;
+    for (size_t k = 0; ok && k < nn; ++k) {
+      cudaGraphNodeType t;
+      ok = cudaGraphNodeGetType(nodes[k], &t) == cudaSuccess;
+      if (!ok || t != cudaGraphNodeTypeEventRecord) continue;
+      cudaEvent_t ev = nullptr;
+      ok = cudaGraphEventRecordNodeGetEvent(nodes[k], &ev) == cudaSuccess;
+      int rel = -1;
+      for (int i = 0; ok && i < ng.ev_count; ++i)
+        if (c->ev[ev_start + i] == ev) rel = i;
+      ok = ok && rel >= 0;
+      if (ok) ng.ev_nodes.emplace_back(nodes[k], rel);
+    }
+    ok = ok && (int)ng.ev_nodes.size() == ng.ev_count;
+  }
+  if (ok && cudaGraphInstantiate(&ng.exec, ng.graph, 0) != cudaSuccess) ng.exec = nullptr;
+  if (!ok || !ng.exec) {
     // not capturable after all (or the call failed while captured): run it as usual
+    ng.release();
     cudaGetLastError();
     c->kernel_launches = before;
     return run();
   }
+  if (!ng.ev_count) {
+    cudaGraphDestroy(ng.graph);  // nothing to rebind: the instantiated graph is all that is needed
+    ng.graph = nullptr;
+  }
   CachedGraph* slot = &c->graphs[0];
   for (CachedGraph& g : c->graphs)
     if (!g.exec || (slot->exec && g.used < slot->used)) slot = &g;
-  if (slot->exec) cudaGraphExecDestroy(slot->exec);
-  slot->key = key;
-  slot->exec = exec;
-  slot->launches = c->kernel_launches - before;
-  slot->used = ++c->graph_clock;
-  slot->info = c->info();
-  ACF_CUDA(c, cudaGraphLaunch(exec, c->stream));
-  ++c->graph_replays;
-  return ACF_OK;
+  slot->release();
+  ng.key = key;
+  ng.launches = c->kernel_launches - before;
+  ng.info = c->info();
+  c->kernel_launches = before;  // launch() counts them
+  *slot = ng;
+  ng.graph = nullptr;  // (ownership moved to the slot)
+  ng.exec = nullptr;
+  int lrc = ACF_OK;
+  if (launch(*slot, lrc)) return lrc;
+  return run();
 }
 
 }  // namespace
@@ -964,8 +1040,7 @@ void acf_destroy(acf_ctx* c) {
   if (c->ws.ptr) cudaFree(c->ws.ptr);
   if (c->io.ptr) cudaFree(c->io.ptr);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
-  for (CachedGraph& g : c->graphs)
-    if (g.exec) cudaGraphExecDestroy(g.exec);
+  for (CachedGraph& g : c->graphs) g.release();
   delete c;
 }
 

@@ -306,6 +306,7 @@ def run_ours(args, cat, workload, rank, world, local):
         log_dir = os.environ.get("ACF_CLOCK_LOG_DIR", "")
         clock_log = os.path.join(log_dir, f"clocks_rank{rank}.csv") if log_dir and os.path.isdir(log_dir) else None
         launched_before = ctx.info("kernel_launches")
+        replays_before = ctx.info("graph_replays")
         with ClockSampler(local, clock_log) as clk:
             for s in range(args.steps):
                 flush.zero_()                     # evict L2 outside the timed region
@@ -316,6 +317,9 @@ def run_ours(args, cat, workload, rank, world, local):
         torch.cuda.synchronize(dev)
         barrier(world)
     gpu_launches = ctx.info("kernel_launches") - launched_before  # this library's kernels, timed steps only
+    # timed steps the library served from its CUDA graph of the call (option "graphs", default on:
+    # the first warm-up step runs as usual, the second is captured, later ones replay it)
+    graph_steps = ctx.info("graph_replays") - replays_before
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kt = ctx.kernel_times()
     # instructions the algorithm needs per step: one untimed step, reading each call's path counts
@@ -349,27 +353,6 @@ def run_ours(args, cat, workload, rank, world, local):
         ctx.set_option("kernel_timing", 0)
         fixup = {"ms_per_step": sum(ft) / 3, "launches_per_step": len(ft) // 3,
                  "basis": "CUDA events around each fix-up launch, 3 untimed steps"}
-    # the same step replayed from the library's CUDA graph of it (option "graphs"; the timed steps
-    # above launch kernel by kernel, as kernel timing needs): warm-up, capture, then timed replays
-    graph = None
-    with torch.cuda.stream(stream):
-        replays0 = ctx.info("graph_replays")
-        for _ in range(3):
-            step()
-        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for s in range(args.steps):
-            flush.zero_()
-            gev[s][0].record(stream)
-            step()
-            gev[s][1].record(stream)
-        stream.synchronize()
-    gms = [a.elapsed_time(b) for a, b in gev]
-    if ctx.info("graph_replays") - replays0 >= args.steps:
-        graph = {"ms_per_step": statistics.median(gms), "min_ms": min(gms),
-                 "value": world * logical_pairs(cat.n_d, cat.n_r) / (statistics.median(gms) / 1e3) / 1e9,
-                 "unit": UNIT, "basis": "median of the same step replayed from the library's CUDA graph of "
-                                        "its launches, L2 flushed between steps"}
     total_ms = sum(step_ms)
     total_ms_max, = reduce_max([total_ms], world)
     pairs = logical_pairs(cat.n_d, cat.n_r)
@@ -448,7 +431,7 @@ def run_ours(args, cat, workload, rank, world, local):
                     # host-timed, so a host hiccup shows here: the spread of the steps on rank 0
                     "step_ms_stats": {"first": 1e3 * e2e_times[0], "median": 1e3 * statistics.median(e2e_times),
                                       "min": 1e3 * min(e2e_times), "max": 1e3 * max(e2e_times)}},
-            "gpu_launches": gpu_launches, "clocks": clocks, "fixup": fixup, "graph_replay": graph,
+            "gpu_launches": gpu_launches, "clocks": clocks, "fixup": fixup, "graph_replayed_steps": graph_steps,
         }
         print(json.dumps(line), flush=True)
     ctx.close()

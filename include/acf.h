@@ -218,9 +218,11 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    recent such calls are kept (default). acf_correlate_host does the same, its
  *                    copies included, when every host buffer is page-locked. The results, and what acf_get_info
  *                    reports, are those of the call; the inputs' current contents are read.
- *                    Calls go launch by launch while "kernel_timing" or "inject_launch_error" is
- *                    set, on the legacy default stream (NULL), and while the caller captures the
- *                    context's stream. 0 = every call launches its kernels one by one
+ *                    With "kernel_timing" on, every launch the graph holds is timed as if it had
+ *                    been launched by itself. Calls go launch by launch while
+ *                    "inject_launch_error" is set, on the legacy default stream (NULL), and while
+ *                    the caller captures the context's stream. 0 = every call launches its
+ *                    kernels one by one
  *   "workspace_limit"  bytes the context's device workspaces may grow to; a call that needs more
  *                    returns ACF_ERR_NOMEM and leaves the context usable (0 = no limit, default)
  *   "inject_launch_error"  fault injection for tests, on the host only: the n-th kernel launch from

@@ -7,8 +7,8 @@
   and replayed. The replays give the captured call's results.
 - The library's own graph replay of repeated calls (option "graphs"): the same results and launch
   counts as calls launched one by one, the inputs' current contents read, acf_get_info describing
-  the replayed call, and calls launched one by one again when an option changes, kernel timing is
-  on or the option is off.
+  the replayed call, kernel timing recording every replayed launch, and calls launched one by one
+  again when an option changes or the option is off.
 """
 import numpy as np
 import pytest
@@ -171,16 +171,24 @@ def test_repeated_calls_replay_a_graph(acf, data):
         assert ctx.info("graph_replays") == n0 + 2
         check()
 
-        # kernel timing, or the option off: every kernel launched by itself
-        for key, v in (("kernel_timing", 1), ("graphs", 0)):
-            ctx.set_option(key, v)
-            n0 = ctx.info("graph_replays")
+        # kernel timing: a graph of its own (its timing events are nodes of it), and every pair
+        # kernel of every call timed, replays included
+        ctx.set_option("kernel_timing", 1)
+        n0 = ctx.info("graph_replays")
+        for _ in range(4):
             assert call() == launches[0]
             check()
-            assert ctx.info("graph_replays") == n0
-            if key == "kernel_timing":
-                assert len(ctx.kernel_times()) == 3  # DD, DR, RR: every pair kernel timed
-            ctx.set_option(key, 1 - v)
+        assert ctx.info("graph_replays") == n0 + 3
+        kt = ctx.kernel_times()
+        assert len(kt) == 12 and all(x > 0 for x in kt), kt  # DD, DR, RR of four calls
+        ctx.set_option("kernel_timing", 0)
+        # the option off: every kernel launched by itself
+        ctx.set_option("graphs", 0)
+        n0 = ctx.info("graph_replays")
+        assert call() == launches[0]
+        check()
+        assert ctx.info("graph_replays") == n0
+        ctx.set_option("graphs", 1)
     finally:
         ctx.close()
 
