@@ -181,6 +181,15 @@ def test_repeated_calls_replay_a_graph(acf, data):
         assert ctx.info("graph_replays") == n0 + 3
         kt = ctx.kernel_times()
         assert len(kt) == 12 and all(x > 0 for x in kt), kt  # DD, DR, RR of four calls
+        # the same with the fix-ups timed (a graph of its own again)
+        ctx.set_option("kernel_timing", 2)
+        n0 = ctx.info("graph_replays")
+        for _ in range(4):
+            call()
+            check()
+        assert ctx.info("graph_replays") == n0 + 3
+        kt = ctx.kernel_times()
+        assert len(kt) == 12 and all(x > 0 for x in kt), kt
         ctx.set_option("kernel_timing", 0)
         # the option off: every kernel launched by itself
         ctx.set_option("graphs", 0)
