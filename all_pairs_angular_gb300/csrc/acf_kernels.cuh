@@ -970,7 +970,9 @@ __device__ __forceinline__ bool add_pair(const PairParams& p, uint32_t cb, uint3
 // the record need not carry them. The warp's records go to its own region of the queue at its
 // cursor `cur` (the same value in every lane; no atomic), and past the region's end to slots of the
 // spill region (one global counter). Called by every lane. Returns whether the record found a slot;
-// if not, its pairs keep their fp32 bins and are counted as flagged and as overflow.
+// if not, its pairs keep their fp32 bins and are counted as flagged and as overflow. (These per-j
+// records serve the kernels whose flags are rare; the block-shared exact kernel, whose flags are
+// dense, keeps group records instead: see GroupRecord.)
 static_assert(kJT == 128, "a flag record holds four 32-lane ballots");
 __device__ __forceinline__ bool push_record(const PairParams& p, unsigned int region, unsigned int& cur, int r, int j, int pc,
                                             uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3) {
