@@ -561,7 +561,12 @@ int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& 
   // per-j records: one warp per region; group records: enough warps for the batches of groups,
   // as many blocks as are resident at once (they take batches from a ticket)
   const long long ngroups = (p.unit_end - p.unit_begin) * 4;
-  const long long fwarps = pl.grouped ? std::min<long long>((ngroups + kFixupBatch - 1) / kFixupBatch,
+  // group records: kFixupBatch groups per ticket where a lane's 128 pairs of a group hold a flag
+  // more often than not (probability ~ 1 - (1 - 2^(1 - S))^128, S the short chord's fine bits:
+  // 0.87 at 0.01 deg bins), else 32
+  const double prec = 1.0 - std::pow(1.0 - std::ldexp(1.0, 1 - pl.bp.fine_shift_small), 128.0);
+  const int gbatch = prec > 0.5 ? kFixupBatch : 32;
+  const long long fwarps = pl.grouped ? std::min<long long>((ngroups + gbatch - 1) / gbatch,
                                                             (long long)c->num_sms * ACF_FIXUP_MINB * fwpb)
                                       : regions;
   const unsigned fblocks = (unsigned)std::max<long long>(1, (fwarps + fwpb - 1) / fwpb);
@@ -598,11 +603,13 @@ int launch_fixup(acf_ctx* c, const Plan& pl, const Launch& L, const PairParams& 
   else if (level == 1) ACF_FIXUP(M, 1, G); \
   else ACF_FIXUP(M, 0, G);
   if (pl.map == kDirect) {
-    if (pl.grouped) { ACF_FIXUP_LEVELS(kDirect, true) }
-    else { ACF_FIXUP_LEVELS(kDirect, false) }
+    if (!pl.grouped) { ACF_FIXUP_LEVELS(kDirect, 0) }
+    else if (gbatch == kFixupBatch) { ACF_FIXUP_LEVELS(kDirect, kFixupBatch) }
+    else { ACF_FIXUP_LEVELS(kDirect, 32) }
   } else {
-    if (pl.grouped) { ACF_FIXUP_LEVELS(kClamp, true) }
-    else { ACF_FIXUP_LEVELS(kClamp, false) }
+    if (!pl.grouped) { ACF_FIXUP_LEVELS(kClamp, 0) }
+    else if (gbatch == kFixupBatch) { ACF_FIXUP_LEVELS(kClamp, kFixupBatch) }
+    else { ACF_FIXUP_LEVELS(kClamp, 32) }
   }
 #undef ACF_FIXUP_LEVELS
 #undef ACF_FIXUP

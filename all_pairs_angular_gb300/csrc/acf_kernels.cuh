@@ -1687,10 +1687,10 @@ struct FixupParams {
 // (about 1e-13 relative, against a flagged pair's 1e-6 rad window) the pair is redone in fp64.
 // Pairs outside the exact zone (mode 1) keep their fp32 bin; a single-code loop's count that the bias
 // carried one entry up moves back.
-// Per-j records (GROUPED false): the queue holds one region of qbatch records per pair-kernel warp
+// Per-j records (GROUPED 0): the queue holds one region of qbatch records per pair-kernel warp
 // (region g: qused[g] in use), then spill records. Fix-up warp g takes region g, whose records came
 // from one pair-kernel warp in order (consecutive records share an i-set, and mostly a path code),
-// and a share of the spill records. Group records (GROUPED true): warps take batches of 32 groups
+// and a share of the spill records. Group records (GROUPED > 0): warps take batches of GROUPED groups
 // from a ticket.
 // SMEM 2: the double-single tables and per-bin moves in shared memory; 1: the moves only; 0: neither.
 // Shared moves reach delta[] once per block.
@@ -1703,13 +1703,15 @@ constexpr int kFixupThreads = 256;
 #define ACF_FIXUP_PAIRS 2
 #endif
 constexpr int kFixupPairs = ACF_FIXUP_PAIRS;
-// Fix-up of group records: groups per ticket (a batch ends with the warp's last record of it, so
-// smaller batches shorten the launch's tail; measured on fine bins: 4 and 16 groups slower than 8)
+// Fix-up of group records: groups per ticket where nearly every lane holds a record (a batch ends
+// with the warp's last record of it, so smaller batches shorten the launch's tail; measured on fine
+// bins: 4 and 16 groups slower than 8); where records are sparse, batches of 32 groups (so that warps
+// do not spend their time taking tickets for nearly empty batches)
 #ifndef ACF_FIXUP_BATCH
 #define ACF_FIXUP_BATCH 8
 #endif
 constexpr int kFixupBatch = ACF_FIXUP_BATCH;
-template <int MAP, int SMEM, bool GROUPED>
+template <int MAP, int SMEM, int GROUPED>
 __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(const FixupParams f) {
   constexpr int WARPS = kFixupThreads / 32;
   extern __shared__ __align__(16) unsigned char fsm[];
@@ -1897,21 +1899,21 @@ __global__ void __launch_bounds__(kFixupThreads, ACF_FIXUP_MINB) fixup_kernel(co
         if (e[u].w == 0u) pair((int)e[u].x, (int)e[u].y, (int)e[u].z, ah[u], al[u], bh[u], bl[u]);
     }
   };
-  if constexpr (GROUPED) {
-    // batches of kFixupBatch groups from a ticket (the next ticket fetched while a batch is done);
+  if constexpr (GROUPED != 0) {
+    // batches of GROUPED groups from a ticket (the next ticket fetched while a batch is done);
     // in each, lane l takes the records of lane l of the groups whose ballot holds l
     unsigned int bt = 0u;
     if (lane == 0) bt = atomicAdd(f.gticket, 1u);
     bt = __shfl_sync(0xffffffffu, bt, 0);
     while (true) {
-      const unsigned long long g0 = (unsigned long long)kFixupBatch * bt;
+      const unsigned long long g0 = (unsigned long long)GROUPED * bt;
       if (g0 >= f.ngroups) break;
       unsigned int bn = 0u;
       if (lane == 0) bn = atomicAdd(f.gticket, 1u);
-      const unsigned int bal = lane < kFixupBatch && g0 + lane < f.ngroups ? f.gbal[g0 + lane] : 0u;
+      const unsigned int bal = lane < GROUPED && g0 + lane < f.ngroups ? f.gbal[g0 + lane] : 0u;
       unsigned int mine = 0u;  // bit q: group g0 + q holds a record of this lane
 #pragma unroll
-      for (int q = 0; q < kFixupBatch; ++q) mine |= ((__shfl_sync(0xffffffffu, bal, q) >> lane) & 1u) << q;
+      for (int q = 0; q < GROUPED; ++q) mine |= ((__shfl_sync(0xffffffffu, bal, q) >> lane) & 1u) << q;
       bt = __shfl_sync(0xffffffffu, bn, 0);
       rounds([&](uint4& hn, uint4& mn) {
         if (!mine) return false;
