@@ -216,8 +216,9 @@ int acf_pair_bins(acf_ctx *ctx, const float *ra1, const float *dec1, const float
  *                    graph of its launches: captured the second time the call comes (its kernels
  *                    run from the graph), launched as one graph from then on; the four most
  *                    recent such calls are kept (default). acf_correlate_host does the same, its
- *                    copies included, when every host buffer is page-locked. The results, and what acf_get_info
- *                    reports, are those of the call; the inputs' current contents are read.
+ *                    copies included, when every host buffer is page-locked. The results, and
+ *                    what acf_get_info reports, are those of the call; the inputs' current
+ *                    contents are read.
  *                    With "kernel_timing" on, every launch the graph holds is timed as if it had
  *                    been launched by itself. Calls go launch by launch while
  *                    "inject_launch_error" is set, on the legacy default stream (NULL), and while
